@@ -1,0 +1,274 @@
+"""Python binding of the Dust estimator engine (libdust.so, C ABI in include/dust.h).
+
+Argument marshalling only: every step of the estimator runs in the library's
+CUDA kernels.  Tensors are torch CUDA tensors; outputs and workspaces are
+allocated here with torch (device memory is the caller's, as the C ABI
+requires) and their pointers are passed with the current CUDA stream.
+
+There is no CPU path: if libdust.so is missing or cannot be loaded, every call
+raises.  Build it with `python -m activation_perturbation_es_noise_b300.build`.
+"""
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libdust.so")
+
+DUST_OK = 0
+STATUS_NAMES = {0: "DUST_OK", 1: "DUST_ERR_INVALID_ARG", 2: "DUST_ERR_UNSUPPORTED",
+                3: "DUST_ERR_WORKSPACE", 4: "DUST_ERR_CUDA", 5: "DUST_ERR_TIMEOUT",
+                6: "DUST_ERR_DEVICE_RANGE"}
+DUST_F32, DUST_BF16 = 0, 1
+
+# Entry points declared in include/dust.h.
+EXPORTS = ("dust_status_string", "dust_abi_version", "dust_workspace_status",
+           "dust_head_workspace", "dust_head_estimate", "dust_linear_workspace",
+           "dust_linear_estimate", "dust_embed_workspace", "dust_embed_scatter",
+           "dust_philox_fill", "dust_gemm_bf16", "dust_set_kernel_events",
+           "dust_kernel_event_count")
+
+
+class DustError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__("%s returned %s (%s)" % (fn, STATUS_NAMES.get(status, status),
+                                                    _status_string(status)))
+
+
+class DustNoise(ctypes.Structure):
+    _fields_ = [("seed", ctypes.c_uint64), ("layer", ctypes.c_uint32),
+                ("draw0", ctypes.c_uint32), ("num_draws", ctypes.c_uint32),
+                ("token0", ctypes.c_uint32), ("sigma", ctypes.c_float),
+                ("gamma", ctypes.c_float)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_U32 = ctypes.c_uint32
+_SZ = ctypes.c_size_t
+
+
+def lib():
+    """The loaded libdust.so (raises if it is missing)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libdust.so is not built: run "
+                               "`python -m activation_perturbation_es_noise_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        L.dust_status_string.argtypes = [ctypes.c_int]
+        L.dust_status_string.restype = ctypes.c_char_p
+        L.dust_abi_version.restype = ctypes.c_int
+        L.dust_workspace_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int)]
+        L.dust_head_workspace.argtypes = [_I64, _I64, _I64, _U32]
+        L.dust_head_workspace.restype = _SZ
+        L.dust_head_estimate.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, DustNoise,
+                                         _P, _P, _P, _SZ, _P]
+        L.dust_linear_workspace.argtypes = [_I64, _I64, _I64, _I64, _I64, _U32]
+        L.dust_linear_workspace.restype = _SZ
+        L.dust_linear_estimate.argtypes = [_P, _P, _P, ctypes.c_float, _P, _P, _P, _I64, _I64,
+                                           _I64, _I64, _I64, _I64, DustNoise, _P, _P, _P, _SZ,
+                                           _P]
+        L.dust_embed_workspace.argtypes = [_I64, _I64, _I64]
+        L.dust_embed_workspace.restype = _SZ
+        L.dust_embed_scatter.argtypes = [_P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]
+        L.dust_philox_fill.argtypes = [ctypes.c_uint64, _U32, _U32, _I64, _I64, _I64, _P, _P, _P]
+        L.dust_gemm_bf16.argtypes = [_P, ctypes.c_int, _I64, _P, ctypes.c_int, _I64, _I64, _I64,
+                                     _I64, _P, _I64, _P, _SZ, _P]
+        L.dust_set_kernel_events.argtypes = [_P, _P, ctypes.c_int]
+        L.dust_kernel_event_count.restype = ctypes.c_int
+        for name in ("dust_set_kernel_events", "dust_workspace_status", "dust_head_estimate", "dust_linear_estimate",
+                     "dust_embed_scatter", "dust_philox_fill", "dust_gemm_bf16"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _status_string(status):
+    try:
+        return lib().dust_status_string(int(status)).decode()
+    except Exception:  # noqa: BLE001 - only used to decorate an error message
+        return "?"
+
+
+def _check(fn, status):
+    if status != DUST_OK:
+        raise DustError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def _workspace(nbytes, device):
+    # 256-byte aligned by the caching allocator.
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def noise(seed, sigma, K, layer=0, draw0=0, token0=0, gamma=0.0):
+    return DustNoise(seed, layer, draw0, K, token0, sigma, gamma)
+
+
+def workspace_status(ws, stream=None):
+    """Status word the kernels left in a workspace (and clear it)."""
+    out = ctypes.c_int(0)
+    _check("dust_workspace_status", lib().dust_workspace_status(_ptr(ws), _stream(stream),
+                                                                ctypes.byref(out)))
+    return out.value
+
+
+# ----------------------------------------------------------------- head ----
+def head_workspace_bytes(T, V, d, K):
+    return lib().dust_head_workspace(T, V, d, K)
+
+
+def head_estimate(logits, targets, x, sigma, K, seed, layer=0, draw0=0, token0=0,
+                  want_g=True, out=None, ws=None, stream=None):
+    """LM-head estimator on cached logits.  Returns (g_hat or None, G_W, ws)."""
+    _need_cuda(logits, targets, x)
+    T, V = logits.shape
+    d = x.shape[1]
+    dev = logits.device
+    if out is None:
+        g = torch.empty((T, V), dtype=torch.float32, device=dev) if want_g else None
+        G = torch.empty((V, d), dtype=torch.float32, device=dev)
+    else:
+        g, G = out
+    if ws is None:
+        ws = _workspace(head_workspace_bytes(T, V, d, K), dev)
+    xdt = DUST_BF16 if x.dtype == torch.bfloat16 else DUST_F32
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("x must be bf16 or fp32")
+    st = lib().dust_head_estimate(_ptr(logits), _ptr(targets), _ptr(x), xdt, T, V, d,
+                                  noise(seed, sigma, K, layer, draw0, token0), _ptr(g), _ptr(G),
+                                  _ptr(ws), ws.numel(), _stream(stream))
+    _check("dust_head_estimate", st)
+    return g, G, ws
+
+
+# ------------------------------------------------------------- interior ----
+def linear_workspace_bytes(T, d_in, C, d_model, V, K):
+    return lib().dust_linear_workspace(T, d_in, C, d_model, V, K)
+
+
+def linear_estimate(x, y1, W2, ema_decay, W_head, z_clean, targets, seq_len, sigma, gamma, K,
+                    seed, layer=1, draw0=0, token0=0, want_g=True, out=None, ws=None,
+                    stream=None):
+    """Interior linear-layer estimator.  Returns (g_hat or None, G_W1, ws)."""
+    _need_cuda(x, y1, W2, W_head, z_clean, targets)
+    T, d_in = x.shape
+    C = y1.shape[1]
+    d_model = W2.shape[0]
+    V = W_head.shape[0]
+    dev = x.device
+    if out is None:
+        g = torch.empty((T, C), dtype=torch.float32, device=dev) if want_g else None
+        G = torch.empty((C, d_in), dtype=torch.float32, device=dev)
+    else:
+        g, G = out
+    if ws is None:
+        ws = _workspace(linear_workspace_bytes(T, d_in, C, d_model, V, K), dev)
+    st = lib().dust_linear_estimate(_ptr(x), _ptr(y1), _ptr(W2), float(ema_decay), _ptr(W_head),
+                                    _ptr(z_clean), _ptr(targets), T, seq_len, d_in, C, d_model,
+                                    V, noise(seed, sigma, K, layer, draw0, token0, gamma),
+                                    _ptr(g), _ptr(G), _ptr(ws), ws.numel(), _stream(stream))
+    _check("dust_linear_estimate", st)
+    return g, G, ws
+
+
+# ------------------------------------------------------------ embedding ----
+def embed_workspace_bytes(T, d, V):
+    return lib().dust_embed_workspace(T, d, V)
+
+
+def embed_scatter(g_hat, ids, V, want_perm=True, out=None, ws=None, stream=None):
+    """Embedding gradient G_E (V x d) and the stable order of the ids."""
+    _need_cuda(g_hat, ids)
+    T, d = g_hat.shape
+    dev = g_hat.device
+    if out is None:
+        G = torch.empty((V, d), dtype=torch.float32, device=dev)
+        perm = torch.empty(T, dtype=torch.int32, device=dev) if want_perm else None
+    else:
+        G, perm = out
+    if ws is None:
+        ws = _workspace(embed_workspace_bytes(T, d, V), dev)
+    st = lib().dust_embed_scatter(_ptr(g_hat), _ptr(ids), T, d, V, _ptr(G), _ptr(perm),
+                                  _ptr(ws), ws.numel(), _stream(stream))
+    _check("dust_embed_scatter", st)
+    return G, perm, ws
+
+
+# ---------------------------------------------------------- test hooks ----
+def philox_fill(seed, layer, draw, token0, ntok, nchan, device="cuda", stream=None):
+    """(words uint32 as int32 tensor, normals fp32) of one draw, ntok x nchan."""
+    words = torch.empty((ntok, nchan), dtype=torch.int32, device=device)
+    normals = torch.empty((ntok, nchan), dtype=torch.float32, device=device)
+    st = lib().dust_philox_fill(seed, layer, draw, token0, ntok, nchan, _ptr(words),
+                                _ptr(normals), _stream(stream))
+    _check("dust_philox_fill", st)
+    return words, normals
+
+
+def gemm_bf16(A, a_mn, B, b_mn, M, N, K, stream=None):
+    """G (M x N fp32) = sum_k A(m,k) B(n,k) on the tensor cores."""
+    _need_cuda(A, B)
+    G = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    ws = _workspace(256, A.device)
+    st = lib().dust_gemm_bf16(_ptr(A), int(a_mn), A.shape[1], _ptr(B), int(b_mn), B.shape[1],
+                              M, N, K, _ptr(G), N, _ptr(ws), ws.numel(), _stream(stream))
+    _check("dust_gemm_bf16", st)
+    return G
+
+
+class KernelTimer:
+    """Times the dominant kernel of the library's entry points with CUDA events
+    recorded by the library on the kernel's own stream (dust_set_kernel_events).
+
+    with KernelTimer(capacity) as kt:  ... calls ...
+    kt.total_ms() sums the recorded launches (synchronises on the events).
+    """
+
+    def __init__(self, capacity):
+        self.start = [torch.cuda.Event(enable_timing=True) for _ in range(capacity)]
+        self.stop = [torch.cuda.Event(enable_timing=True) for _ in range(capacity)]
+        s = torch.cuda.current_stream()
+        for e in self.start + self.stop:  # create the underlying events
+            e.record(s)
+        torch.cuda.synchronize()
+        self._a0 = (ctypes.c_void_p * capacity)(*[e.cuda_event for e in self.start])
+        self._a1 = (ctypes.c_void_p * capacity)(*[e.cuda_event for e in self.stop])
+        self.capacity = capacity
+        self.count = 0
+
+    def __enter__(self):
+        _check("dust_set_kernel_events",
+               lib().dust_set_kernel_events(self._a0, self._a1, self.capacity))
+        return self
+
+    def __exit__(self, *exc):
+        self.count = lib().dust_kernel_event_count()
+        lib().dust_set_kernel_events(None, None, 0)
+        return False
+
+    def times_ms(self):
+        for e in self.stop[:self.count]:
+            e.synchronize()
+        return [a.elapsed_time(b) for a, b in zip(self.start[:self.count], self.stop[:self.count])]
+
+    def total_ms(self):
+        return float(sum(self.times_ms()))

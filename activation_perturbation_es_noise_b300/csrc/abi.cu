@@ -1,0 +1,103 @@
+// abi.cu -- status strings, the workspace status read-back and the noise
+// regenerator test hook.
+#include "dust_common.cuh"
+#include "internal.h"
+#include "noise.cuh"
+
+namespace dust {
+namespace {
+
+// One thread per (token, channel block of 4): the words and normals of the
+// block, written for the channels below nchan.
+__global__ void philox_fill_kernel(PhiloxKeys keys, uint32_t layer, uint32_t draw,
+                                   uint32_t token0, int64_t ntok, int64_t nchan,
+                                   uint32_t* __restrict__ words, float* __restrict__ normals) {
+    const int64_t nblk = (nchan + 3) / 4;
+    const int64_t n = ntok * nblk;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = i / nblk, j = i - t * nblk;
+        const uint4 w = philox4x32_10(static_cast<uint32_t>(j), token0 + static_cast<uint32_t>(t),
+                                      draw, layer, keys);
+        const float4 a = words_to_normals(w);
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+        const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t c = 4 * j + k;
+            if (c < nchan) {
+                if (words) words[t * nchan + c] = wv[k];
+                if (normals) normals[t * nchan + c] = av[k];
+            }
+        }
+    }
+}
+
+}  // namespace
+
+KernelTimer& kernel_timer() {
+    static KernelTimer t;
+    return t;
+}
+
+}  // namespace dust
+
+using namespace dust;
+
+extern "C" dust_status dust_set_kernel_events(void* const* start_events, void* const* stop_events,
+                                              int capacity) {
+    KernelTimer& k = kernel_timer();
+    if ((start_events == nullptr) != (stop_events == nullptr) || capacity < 0)
+        return DUST_ERR_INVALID_ARG;
+    k.start = start_events;
+    k.stop = stop_events;
+    k.capacity = start_events ? capacity : 0;
+    k.count = 0;
+    return DUST_OK;
+}
+
+extern "C" int dust_kernel_event_count(void) { return kernel_timer().count; }
+
+extern "C" int dust_abi_version(void) { return 100; }
+
+extern "C" const char* dust_status_string(dust_status s) {
+    switch (s) {
+        case DUST_OK: return "ok";
+        case DUST_ERR_INVALID_ARG: return "invalid argument";
+        case DUST_ERR_UNSUPPORTED: return "size not supported";
+        case DUST_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+        case DUST_ERR_CUDA: return "CUDA call failed";
+        case DUST_ERR_TIMEOUT: return "bounded in-kernel wait ran out";
+        case DUST_ERR_DEVICE_RANGE: return "device-side id out of range";
+    }
+    return "unknown status";
+}
+
+extern "C" dust_status dust_workspace_status(void* ws, void* stream, dust_status* status_out) {
+    if (!ws || !status_out || !aligned(ws, 256)) return DUST_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    DUST_CUDA_TRY(cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, s));
+    DUST_CUDA_TRY(cudaStreamSynchronize(s));
+    DUST_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(word), s));
+    *status_out = static_cast<dust_status>(word);
+    return DUST_OK;
+}
+
+extern "C" dust_status dust_philox_fill(uint64_t seed, uint32_t layer, uint32_t draw,
+                                        int64_t token0, int64_t ntok, int64_t nchan,
+                                        uint32_t* words, float* normals, void* stream) {
+    if (ntok < 0 || nchan < 0 || token0 < 0) return DUST_ERR_INVALID_ARG;
+    if (token0 + ntok > (1LL << 32)) return DUST_ERR_INVALID_ARG;
+    if (nchan > (1LL << 34)) return DUST_ERR_UNSUPPORTED;
+    if (ntok == 0 || nchan == 0) return DUST_OK;
+    if (!words && !normals) return DUST_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t n = ntok * ((nchan + 3) / 4);
+    int64_t blocks = ceil_div(n, 256);
+    if (blocks > 148 * 64) blocks = 148 * 64;
+    philox_fill_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        philox_round_keys(seed), layer, draw, static_cast<uint32_t>(token0), ntok, nchan, words,
+        normals);
+    return launch_status();
+}

@@ -1,0 +1,437 @@
+// head.cu -- the LM-head estimator, perturbed on the cached logits.
+//
+// The pages perturb the head's output (the logits) directly and recompute
+// only the cross-entropy, which is cheap enough to give the head a much larger
+// population (laoyaoba.com article, section 机制拆解; Dust translation,
+// hn.213312.xyz, §2.3 干扰与调优).  With gamma = 0 the reward of a token is
+// its own centred loss decrease (§2.2 信用分配), so for draw i and token t
+//
+//   dl_{i,t} = CE(z_t + sigma a_{i,t}) - CE(z_t)
+//            = log sum_v p_{t,v} exp(sigma a_{i,t,v}) - sigma a_{i,t,y_t},
+//
+// with p_t = softmax(z_t) (the lse of the clean logits cancels exactly), and
+//
+//   g_t = -(1/(K sigma)) sum_i c_{i,t} a_{i,t},  c_{i,t} = -(dl_{i,t} - m_t),
+//       = (S1_t - m_t S0_t) / (K sigma),
+//   S1_t = sum_i dl_{i,t} a_{i,t},  S0_t = sum_i a_{i,t},  m_t = mean_i dl_{i,t}.
+//
+// One CTA owns one token (and one chunk of draws when there are too few
+// tokens to fill the GPU).  Its threads hold the token's probabilities and the
+// S1/S0 accumulators of their channels in registers; every draw regenerates
+// the noise of those channels from its counter, reduces sum p e^{sigma a}
+// across the CTA, and folds dl a into the accumulators.  Nothing per draw ever
+// leaves the chip.
+#include "dust_common.cuh"
+#include "internal.h"
+#include "noise.cuh"
+
+namespace dust {
+namespace {
+
+struct HeadArgs {
+    const float* logits;
+    const int32_t* targets;
+    int T, V, nblk, K, Q, chunk;
+    uint32_t draw0, token0, layer;
+    float sig_l2e;  // sigma * log2(e)
+    float sigma;
+    float inv_ks;   // 1 / (K sigma)
+    float* g_hat;   // T x V fp32, may be null
+    __nv_bfloat16* gbf;
+    int64_t ldg;    // row stride of gbf (elements)
+    float* part_s1;  // Q x T x V
+    float* part_s0;
+    float* part_dl;  // Q x T
+    uint32_t* status;
+};
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// Block-wide reductions for the once-per-token softmax (all threads get the
+// same value; the summation order is fixed).
+template <bool ONE_WARP>
+__device__ __forceinline__ float block_sum(float v, float* scratch) {
+    v = warp_sum(v);
+    if (ONE_WARP) return v;
+    const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) scratch[warp] = v;
+    __syncthreads();
+    float s = 0.f;
+    for (int w = 0; w < nw; ++w) s += scratch[w];
+    return s;
+}
+template <bool ONE_WARP>
+__device__ __forceinline__ float block_max(float v, float* scratch) {
+    v = warp_max(v);
+    if (ONE_WARP) return v;
+    const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) scratch[warp] = v;
+    __syncthreads();
+    float s = -INFINITY;
+    for (int w = 0; w < nw; ++w) s = fmaxf(s, scratch[w]);
+    return s;
+}
+
+// NB channel blocks of 4 per thread; ONE_WARP: the CTA is a single warp and
+// all reductions are shuffles.  Otherwise blockDim.x <= 256.
+template <int NB, bool ONE_WARP>
+__global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
+    head_draws_kernel(const HeadArgs A, const PhiloxKeys keys) {
+    __shared__ float red[2][8];
+    __shared__ float red_y[2];
+    __shared__ float scratch[8];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int NT = ONE_WARP ? 32 : static_cast<int>(blockDim.x);
+    const int nw = NT >> 5;
+    const int t = blockIdx.x / A.Q;
+    const int q = blockIdx.x - t * A.Q;
+    const int i_begin = q * A.chunk;
+    const int i_end = min(A.K, i_begin + A.chunk);
+    const int V = A.V;
+    const bool vec = (V & 3) == 0;
+    const float* zrow = A.logits + static_cast<int64_t>(t) * V;
+
+    // Cached logits of this token -> registers; softmax.
+    float p[NB][4];
+    float zmax = -INFINITY;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        const int j = b * NT + tid;
+        if (vec && j < A.nblk) {
+            const float4 z4 = __ldg(reinterpret_cast<const float4*>(zrow) + j);
+            p[b][0] = z4.x; p[b][1] = z4.y; p[b][2] = z4.z; p[b][3] = z4.w;
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int c = 4 * j + k;
+                p[b][k] = (j < A.nblk && c < V) ? __ldg(zrow + c) : -INFINITY;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) zmax = fmaxf(zmax, p[b][k]);
+    }
+    zmax = block_max<ONE_WARP>(zmax, scratch);
+    float zsum = 0.f;
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            p[b][k] = (p[b][k] == -INFINITY) ? 0.f : expf(p[b][k] - zmax);
+            zsum += p[b][k];
+        }
+    zsum = block_sum<ONE_WARP>(zsum, scratch);
+    const float zinv = 1.0f / zsum;
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) p[b][k] *= zinv;
+
+    // Target channel: the thread that owns it supplies sigma a_y every draw.
+    int y = __ldg(A.targets + t);
+    if (y < 0 || y >= V) {
+        if (tid == 0 && q == 0) record_status(A.status, DUST_ERR_DEVICE_RANGE);
+        y = -1;
+    }
+    const int yblk = y >> 2;
+    const bool owner = (y >= 0) && (yblk % NT == tid);
+    const int yb = (y >= 0) ? yblk / NT : 0;
+    const int yc = y & 3;
+    const int ylane = (y >= 0) ? (yblk % NT) & 31 : 0;
+
+    BlockHalf bh[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) bh[b] = philox_block_half(b * NT + tid, A.layer, keys);
+
+    float s1[NB][4], s0[NB][4];
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) s1[b][k] = s0[b][k] = 0.f;
+    float sdl = 0.f;
+    const uint32_t token = A.token0 + static_cast<uint32_t>(t);
+
+#pragma unroll 1
+    for (int i = i_begin; i < i_end; ++i) {
+        const DrawHalf dh = philox_draw_half(A.draw0 + static_cast<uint32_t>(i), token, keys);
+        float a[NB][4];
+        float part = 0.f;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            if (b * NT + tid < A.nblk) {
+                const float4 n = words_to_normals(philox_rest(dh, bh[b], keys));
+                a[b][0] = n.x; a[b][1] = n.y; a[b][2] = n.z; a[b][3] = n.w;
+                part = fmaf(p[b][0], ex2_approx(A.sig_l2e * n.x), part);
+                part = fmaf(p[b][1], ex2_approx(A.sig_l2e * n.y), part);
+                part = fmaf(p[b][2], ex2_approx(A.sig_l2e * n.z), part);
+                part = fmaf(p[b][3], ex2_approx(A.sig_l2e * n.w), part);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) a[b][k] = 0.f;
+            }
+        }
+        float ay = 0.f;
+        if (owner) {
+#pragma unroll
+            for (int b = 0; b < NB; ++b)
+                if (b == yb) ay = yc == 0 ? a[b][0] : yc == 1 ? a[b][1] : yc == 2 ? a[b][2] : a[b][3];
+        }
+        part = warp_sum(part);
+        float S;
+        if (ONE_WARP) {
+            S = part;
+            ay = __shfl_sync(0xFFFFFFFFu, ay, ylane);
+        } else {
+            const int buf = i & 1;
+            if (lane == 0) red[buf][warp] = part;
+            if (owner) red_y[buf] = ay;
+            __syncthreads();
+            S = 0.f;
+            for (int w = 0; w < nw; ++w) S += red[buf][w];
+            ay = (y >= 0) ? red_y[buf] : 0.f;
+        }
+        const float dl = logf(S) - A.sigma * ay;
+        sdl += dl;
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                s1[b][k] = fmaf(dl, a[b][k], s1[b][k]);
+                s0[b][k] += a[b][k];
+            }
+    }
+
+    if (A.Q == 1) {
+        const float mean = sdl / static_cast<float>(A.K);
+        float* grow = A.g_hat ? A.g_hat + static_cast<int64_t>(t) * V : nullptr;
+        __nv_bfloat16* brow = A.gbf + static_cast<int64_t>(t) * A.ldg;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const int j = b * NT + tid;
+            if (j >= A.nblk) continue;
+            float g[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) g[k] = (s1[b][k] - mean * s0[b][k]) * A.inv_ks;
+            if (vec) {
+                if (grow) *reinterpret_cast<float4*>(grow + 4 * j) = make_float4(g[0], g[1], g[2], g[3]);
+                __nv_bfloat162 lo = __floats2bfloat162_rn(g[0], g[1]);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(g[2], g[3]);
+                uint2 pk;
+                pk.x = *reinterpret_cast<uint32_t*>(&lo);
+                pk.y = *reinterpret_cast<uint32_t*>(&hi);
+                *reinterpret_cast<uint2*>(brow + 4 * j) = pk;
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int c = 4 * j + k;
+                    if (c < V) {
+                        if (grow) grow[c] = g[k];
+                        brow[c] = __float2bfloat16_rn(g[k]);
+                    }
+                }
+            }
+        }
+    } else {
+        const int64_t off = (static_cast<int64_t>(q) * A.T + t) * V;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const int j = b * NT + tid;
+            if (j >= A.nblk) continue;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int c = 4 * j + k;
+                if (c < V) {
+                    A.part_s1[off + c] = s1[b][k];
+                    A.part_s0[off + c] = s0[b][k];
+                }
+            }
+        }
+        if (tid == 0) A.part_dl[static_cast<int64_t>(q) * A.T + t] = sdl;
+    }
+}
+
+// Sums the draw-chunk partials in chunk order and forms g (fp32 + bf16 copy).
+__global__ void head_finalize_kernel(const HeadArgs A) {
+    const int t = blockIdx.y;
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= A.V) return;
+    float sdl = 0.f, s1 = 0.f, s0 = 0.f;
+    for (int q = 0; q < A.Q; ++q) {
+        const int64_t off = (static_cast<int64_t>(q) * A.T + t) * A.V + c;
+        sdl += A.part_dl[static_cast<int64_t>(q) * A.T + t];
+        s1 += A.part_s1[off];
+        s0 += A.part_s0[off];
+    }
+    const float mean = sdl / static_cast<float>(A.K);
+    const float g = (s1 - mean * s0) * A.inv_ks;
+    if (A.g_hat) A.g_hat[static_cast<int64_t>(t) * A.V + c] = g;
+    A.gbf[static_cast<int64_t>(t) * A.ldg + c] = __float2bfloat16_rn(g);
+}
+
+struct HeadPlan {
+    int nblk, nb, nt, Q, chunk;
+    bool one_warp;
+    int64_t ldg, ldx;
+    size_t ws_bytes;
+    size_t off_gbf, off_xbf, off_s1, off_s0, off_dl;
+};
+
+constexpr int64_t kMaxV = 8192;
+
+HeadPlan head_plan(int64_t T, int64_t V, int64_t d, uint32_t K) {
+    HeadPlan P{};
+    P.nblk = static_cast<int>(ceil_div(V, 4));
+    if (P.nblk <= 32 * 8) {
+        P.one_warp = true;
+        P.nt = 32;
+        const int need = static_cast<int>(ceil_div(P.nblk, 32));
+        P.nb = need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : 8;
+    } else {
+        P.one_warp = false;
+        P.nb = P.nblk <= 4 * 256 ? 4 : 8;
+        P.nt = static_cast<int>(round_up(ceil_div(P.nblk, P.nb), 32));
+    }
+    // Split the draws when there are too few tokens to fill 148 SMs.
+    const int64_t target = P.one_warp ? 148 * 48 : 148 * 8;
+    int64_t Q = 1;
+    if (T < target) {
+        Q = ceil_div(target, T);
+        const int64_t qmax = K / 16 > 1 ? K / 16 : 1;
+        if (Q > qmax) Q = qmax;
+    }
+    P.chunk = static_cast<int>(ceil_div(K, Q));
+    P.Q = static_cast<int>(ceil_div(K, P.chunk));
+    P.ldg = round_up(V, 8);
+    P.ldx = round_up(d, 8);
+    WsLayout w;
+    w.take(kCtlBytes);
+    P.off_gbf = w.take(static_cast<size_t>(T * P.ldg) * 2);
+    P.off_xbf = w.take(static_cast<size_t>(T * P.ldx) * 2);
+    if (P.Q > 1) {
+        const size_t n = static_cast<size_t>(P.Q) * T * V;
+        P.off_s1 = w.take(n * 4);
+        P.off_s0 = w.take(n * 4);
+        P.off_dl = w.take(static_cast<size_t>(P.Q) * T * 4);
+    }
+    P.ws_bytes = w.used;
+    return P;
+}
+
+template <int NB, bool OW>
+dust_status launch_draws(const HeadPlan& P, const HeadArgs& A, const PhiloxKeys& keys,
+                         int64_t T, cudaStream_t s) {
+    timer_begin(s);
+    head_draws_kernel<NB, OW><<<static_cast<unsigned>(T * P.Q), P.nt, 0, s>>>(A, keys);
+    timer_end(s);
+    return launch_status();
+}
+
+}  // namespace
+}  // namespace dust
+
+using namespace dust;
+
+extern "C" size_t dust_head_workspace(int64_t T, int64_t V, int64_t d, uint32_t K) {
+    if (T < 1 || V < 1 || d < 1 || K < 2) return 0;
+    return head_plan(T, V, d, K).ws_bytes;
+}
+
+extern "C" dust_status dust_head_estimate(const float* logits, const int32_t* targets,
+                                          const void* x, dust_dtype x_dtype, int64_t T,
+                                          int64_t V, int64_t d, dust_noise nz, float* g_hat,
+                                          float* G_W, void* ws, size_t ws_bytes, void* stream) {
+    if (!logits || !targets || !x || !G_W) return DUST_ERR_INVALID_ARG;
+    if (T < 1 || V < 1 || d < 1 || nz.num_draws < 2) return DUST_ERR_INVALID_ARG;
+    if (!(nz.sigma > 0.0f) || !(nz.sigma < INFINITY)) return DUST_ERR_INVALID_ARG;
+    if (x_dtype != DUST_F32 && x_dtype != DUST_BF16) return DUST_ERR_INVALID_ARG;
+    if (V > kMaxV || T > (1LL << 30) || d > (1LL << 30) || nz.num_draws > (1u << 30))
+        return DUST_ERR_UNSUPPORTED;
+    if (static_cast<uint64_t>(nz.token0) + static_cast<uint64_t>(T) > (1ULL << 32))
+        return DUST_ERR_INVALID_ARG;
+    if (static_cast<uint64_t>(nz.draw0) + nz.num_draws > (1ULL << 32)) return DUST_ERR_INVALID_ARG;
+    if ((V % 4 == 0) && (!aligned(logits, 16) || (g_hat && !aligned(g_hat, 16))))
+        return DUST_ERR_INVALID_ARG;
+    const HeadPlan P = head_plan(T, V, d, nz.num_draws);
+    if (!ws || ws_bytes < P.ws_bytes || !aligned(ws, 256)) return DUST_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    DUST_CUDA_TRY(cudaMemsetAsync(ws, 0, kCtlBytes, s));
+
+    HeadArgs A{};
+    A.logits = logits;
+    A.targets = targets;
+    A.T = static_cast<int>(T);
+    A.V = static_cast<int>(V);
+    A.nblk = P.nblk;
+    A.K = static_cast<int>(nz.num_draws);
+    A.Q = P.Q;
+    A.chunk = P.chunk;
+    A.draw0 = nz.draw0;
+    A.token0 = nz.token0;
+    A.layer = nz.layer;
+    A.sigma = nz.sigma;
+    A.sig_l2e = static_cast<float>(static_cast<double>(nz.sigma) * 1.4426950408889634);
+    A.inv_ks = static_cast<float>(1.0 / (static_cast<double>(nz.num_draws) * nz.sigma));
+    A.g_hat = g_hat;
+    A.gbf = reinterpret_cast<__nv_bfloat16*>(w + P.off_gbf);
+    A.ldg = P.ldg;
+    A.status = static_cast<uint32_t*>(ws);
+    if (P.Q > 1) {
+        A.part_s1 = reinterpret_cast<float*>(w + P.off_s1);
+        A.part_s0 = reinterpret_cast<float*>(w + P.off_s0);
+        A.part_dl = reinterpret_cast<float*>(w + P.off_dl);
+    }
+    const PhiloxKeys keys = philox_round_keys(nz.seed);
+
+    dust_status st;
+    if (P.one_warp) {
+        switch (P.nb) {
+            case 1: st = launch_draws<1, true>(P, A, keys, T, s); break;
+            case 2: st = launch_draws<2, true>(P, A, keys, T, s); break;
+            case 4: st = launch_draws<4, true>(P, A, keys, T, s); break;
+            default: st = launch_draws<8, true>(P, A, keys, T, s); break;
+        }
+    } else {
+        st = P.nb == 4 ? launch_draws<4, false>(P, A, keys, T, s)
+                       : launch_draws<8, false>(P, A, keys, T, s);
+    }
+    if (st != DUST_OK) return st;
+    if (P.Q > 1) {
+        dim3 grid(static_cast<unsigned>(ceil_div(V, 128)), static_cast<unsigned>(T));
+        head_finalize_kernel<<<grid, 128, 0, s>>>(A);
+        if ((st = launch_status()) != DUST_OK) return st;
+    }
+
+    // x -> bf16 in a padded layout when needed, then G_W = g^T x.
+    const void* xb = x;
+    int64_t ldx = d;
+    if (x_dtype == DUST_F32 || (d % 8) != 0 || !aligned(x, 16)) {
+        void* xbf = w + P.off_xbf;
+        st = x_dtype == DUST_F32
+                 ? f32_to_bf16_launch(static_cast<const float*>(x), T, d, d, xbf, P.ldx, s)
+                 : bf16_pad_launch(x, T, d, d, xbf, P.ldx, s);
+        if (st != DUST_OK) return st;
+        xb = xbf;
+        ldx = P.ldx;
+    }
+    return gemm_bf16_launch(A.gbf, true, P.ldg, xb, true, ldx, V, d, T, 0, 1, G_W, d,
+                            static_cast<uint32_t*>(ws), s);
+}

@@ -1,0 +1,348 @@
+// interior.cu -- the estimator for an interior linear layer with causal
+// credit.
+//
+// The layer's output y1 = W1 x is perturbed per token, y1 + sigma a, and only
+// the part after it is re-run from cached clean activations (laoyaoba.com
+// article, section 机制拆解; Dust translation, hn.213312.xyz, §2.3).  The fixed
+// downstream is GELU -> W2 -> causal per-sequence EMA -> W_head -> CE.  It is
+// linear after the GELU, so a draw's logits are z_clean + dz with
+//   dh = GELU(y1 + sigma a) - GELU(y1),  du = dh W2^T,
+//   de_t = lam de_{t-1} + (1 - lam) du_t (per sequence),  dz = de W_head^T,
+// and the loss change is dl = CE(z_clean + dz) - CE(z_clean)
+//                           = log(1 + sum_v p_v expm1(dz_v)) - dz_y.
+// Later tokens see earlier perturbations through the EMA, so the reward is
+// the gamma-discounted suffix sum r_t = sum_{s>=t} gamma^(s-t) c_s of the
+// centred loss decrease (Dust translation §2.2 信用分配), and
+// g_t = -(1/(K sigma)) sum_i r_{i,t} a_{i,t}.
+//
+// Pipeline per chunk of nd draws (rows ordered token block of 128, draw,
+// token in block, so that the draws of one token block sit next to each other
+// and share its softmax rows in L2):
+//   dh kernel      noise + GELU difference, split into bf16 hi and lo halves
+//                  A1 = [hi | lo]  (rows x 2C)
+//   GEMM 1         du = A1 [W2 | W2]^T on the tensor cores (fp32)
+//   EMA kernel     de, split into A2 = [hi | lo]  (rows x 2 d_model)
+//   GEMM 2 + CE    dz = A2 [W_head | W_head]^T, reduced in the epilogue to dl
+// then once: centring, the segmented suffix scan, the noise-weighted sum for
+// g (noise regenerated), and G_W1 = g^T x.
+//
+// The split-bf16 operands keep the re-forward within the fp32-level
+// tolerance: a single bf16 rounding of dh or de perturbs the loss changes at
+// the 1e-3 relative level, the hi + lo pair at about 1e-5.
+#include <algorithm>
+
+#include "dust_common.cuh"
+#include "internal.h"
+#include "noise.cuh"
+
+namespace dust {
+namespace {
+
+constexpr int kRowBlock = 128;
+
+__device__ __forceinline__ float gelu_erf(float u) {
+    return 0.5f * u * (1.0f + erff(u * 0.70710678118654752f));
+}
+
+__device__ __forceinline__ void split_bf16(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
+    hi = __float2bfloat16_rn(v);
+    lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
+__device__ __forceinline__ uint2 pack4(__nv_bfloat16 a, __nv_bfloat16 b, __nv_bfloat16 c,
+                                       __nv_bfloat16 d) {
+    __nv_bfloat162 lo = __halves2bfloat162(a, b), hi = __halves2bfloat162(c, d);
+    uint2 r;
+    r.x = *reinterpret_cast<uint32_t*>(&lo);
+    r.y = *reinterpret_cast<uint32_t*>(&hi);
+    return r;
+}
+
+__device__ __forceinline__ int64_t chunk_row(int t, int i, int nd) {
+    return (static_cast<int64_t>(t >> 7) * nd + i) * kRowBlock + (t & 127);
+}
+
+// p = softmax(z) per row, fp32.
+__global__ void softmax_rows_kernel(const float* __restrict__ z, int V, float* __restrict__ p) {
+    __shared__ float red[32];
+    const int64_t t = blockIdx.x;
+    const float* zr = z + t * V;
+    float* pr = p + t * V;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    float m = -INFINITY;
+    for (int v = threadIdx.x; v < V; v += blockDim.x) m = fmaxf(m, zr[v]);
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    m = -INFINITY;
+    for (int w = 0; w < nw; ++w) m = fmaxf(m, red[w]);
+    __syncthreads();
+    float s = 0.f;
+    for (int v = threadIdx.x; v < V; v += blockDim.x) s += expf(zr[v] - m);
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    if (lane == 0) red[warp] = s;
+    __syncthreads();
+    s = 0.f;
+    for (int w = 0; w < nw; ++w) s += red[w];
+    const float inv = 1.0f / s;
+    for (int v = threadIdx.x; v < V; v += blockDim.x) pr[v] = expf(zr[v] - m) * inv;
+}
+
+struct DhArgs {
+    const float* y1;
+    int T, Tp, C, nd;
+    uint32_t draw_first, token0, layer;  // draw_first = draw0 + i0
+    float sigma;
+    __nv_bfloat16* A1;  // rows x 2C
+};
+
+// One thread per (draw in chunk, token, channel block of 4).
+__global__ void interior_dh_kernel(const DhArgs a, const PhiloxKeys keys) {
+    const int nblk = a.C >> 2;
+    const int64_t n = static_cast<int64_t>(a.nd) * a.Tp * nblk;
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int j = static_cast<int>(idx % nblk);
+        const int64_t rest = idx / nblk;
+        const int t = static_cast<int>(rest % a.Tp);
+        const int i = static_cast<int>(rest / a.Tp);
+        __nv_bfloat16* row = a.A1 + chunk_row(t, i, a.nd) * (2 * static_cast<int64_t>(a.C));
+        __nv_bfloat16 h[4], l[4];
+        if (t < a.T) {
+            const float4 nrm = words_to_normals(
+                philox4x32_10(j, a.token0 + t, a.draw_first + i, a.layer, keys));
+            const float4 y = __ldg(reinterpret_cast<const float4*>(a.y1 + static_cast<int64_t>(t) * a.C) + j);
+            split_bf16(gelu_erf(fmaf(a.sigma, nrm.x, y.x)) - gelu_erf(y.x), h[0], l[0]);
+            split_bf16(gelu_erf(fmaf(a.sigma, nrm.y, y.y)) - gelu_erf(y.y), h[1], l[1]);
+            split_bf16(gelu_erf(fmaf(a.sigma, nrm.z, y.z)) - gelu_erf(y.z), h[2], l[2]);
+            split_bf16(gelu_erf(fmaf(a.sigma, nrm.w, y.w)) - gelu_erf(y.w), h[3], l[3]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) h[k] = l[k] = __float2bfloat16_rn(0.f);
+        }
+        *reinterpret_cast<uint2*>(row + 4 * j) = pack4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint2*>(row + a.C + 4 * j) = pack4(l[0], l[1], l[2], l[3]);
+    }
+}
+
+// One thread per (draw in chunk, sequence, channel): the causal EMA down the
+// sequence, written as the split pair [hi | lo].
+__global__ void interior_ema_kernel(const float* __restrict__ du, int nd, int nseq, int seq_len,
+                                    int dm, float lam, __nv_bfloat16* __restrict__ A2) {
+    const int64_t n = static_cast<int64_t>(nd) * nseq * dm;
+    const float one_m = 1.0f - lam;
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int k = static_cast<int>(idx % dm);
+        const int64_t rest = idx / dm;
+        const int s = static_cast<int>(rest % nseq);
+        const int i = static_cast<int>(rest / nseq);
+        float e = 0.f;
+        for (int tt = 0; tt < seq_len; ++tt) {
+            const int t = s * seq_len + tt;
+            const int64_t r = chunk_row(t, i, nd);
+            e = fmaf(lam, e, one_m * du[r * dm + k]);
+            __nv_bfloat16 h, l;
+            split_bf16(e, h, l);
+            A2[r * 2 * dm + k] = h;
+            A2[r * 2 * dm + dm + k] = l;
+        }
+    }
+}
+
+__global__ void draw_mean_kernel(const float* __restrict__ dl, int K, int T, float* __restrict__ m) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    float s = 0.f;
+    for (int i = 0; i < K; ++i) s += dl[static_cast<int64_t>(i) * T + t];
+    m[t] = s / static_cast<float>(K);
+}
+
+// r_{i,t} = c_{i,t} + gamma r_{i,t+1} inside each sequence, c = -(dl - m).
+__global__ void reward_scan_kernel(const float* __restrict__ dl, const float* __restrict__ m,
+                                   int K, int T, int seq_len, float gamma, float* __restrict__ r) {
+    const int nseq = T / seq_len;
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= K * nseq) return;
+    const int i = idx / nseq, s = idx - i * nseq;
+    const int64_t rowoff = static_cast<int64_t>(i) * T;
+    float acc = 0.f;
+    for (int t = (s + 1) * seq_len - 1; t >= s * seq_len; --t) {
+        const float c = -(dl[rowoff + t] - m[t]);
+        acc = fmaf(gamma, acc, c);
+        r[rowoff + t] = acc;
+    }
+}
+
+struct GhatArgs {
+    const float* r;  // K x T
+    int T, C, K;
+    uint32_t draw0, token0, layer;
+    float neg_inv_ks;  // -1 / (K sigma)
+    float* g_hat;      // T x C or null
+    __nv_bfloat16* gbf;  // T x C
+};
+
+// One thread per (token, channel block): g = -(1/(K sigma)) sum_i r a, with
+// the noise regenerated from its counters.
+__global__ void interior_ghat_kernel(const GhatArgs a, const PhiloxKeys keys) {
+    const int nblk = a.C >> 2;
+    const int64_t n = static_cast<int64_t>(a.T) * nblk;
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int j = static_cast<int>(idx % nblk);
+        const int t = static_cast<int>(idx / nblk);
+        const BlockHalf bh = philox_block_half(j, a.layer, keys);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < a.K; ++i) {
+            const float ri = __ldg(a.r + static_cast<int64_t>(i) * a.T + t);
+            const float4 nrm = words_to_normals(
+                philox_rest(philox_draw_half(a.draw0 + i, a.token0 + t, keys), bh, keys));
+            acc.x = fmaf(ri, nrm.x, acc.x);
+            acc.y = fmaf(ri, nrm.y, acc.y);
+            acc.z = fmaf(ri, nrm.z, acc.z);
+            acc.w = fmaf(ri, nrm.w, acc.w);
+        }
+        const float4 g = make_float4(acc.x * a.neg_inv_ks, acc.y * a.neg_inv_ks,
+                                     acc.z * a.neg_inv_ks, acc.w * a.neg_inv_ks);
+        const int64_t off = static_cast<int64_t>(t) * a.C + 4 * j;
+        if (a.g_hat) *reinterpret_cast<float4*>(a.g_hat + off) = g;
+        *reinterpret_cast<uint2*>(a.gbf + off) =
+            pack4(__float2bfloat16_rn(g.x), __float2bfloat16_rn(g.y), __float2bfloat16_rn(g.z),
+                  __float2bfloat16_rn(g.w));
+    }
+}
+
+struct InteriorPlan {
+    int64_t Tp, ldx;
+    int nd;  // draws per chunk
+    size_t off_p, off_a1, off_du, off_a2, off_dl, off_m, off_r, off_gbf, off_xbf, bytes;
+};
+
+InteriorPlan interior_plan(int64_t T, int64_t d_in, int64_t C, int64_t dm, int64_t V, uint32_t K) {
+    InteriorPlan P{};
+    P.Tp = round_up(T, kRowBlock);
+    P.ldx = round_up(d_in, 8);
+    const int64_t ntb = P.Tp / kRowBlock;
+    int64_t nd = ceil_div(148 * 8, ntb);
+    nd = std::max<int64_t>(1, std::min<int64_t>({nd, 16, static_cast<int64_t>(K)}));
+    P.nd = static_cast<int>(nd);
+    const size_t rows = static_cast<size_t>(nd * P.Tp);
+    WsLayout w;
+    w.take(kCtlBytes);
+    P.off_p = w.take(static_cast<size_t>(T * V) * 4);
+    P.off_a1 = w.take(rows * static_cast<size_t>(2 * C) * 2);
+    P.off_du = w.take(rows * static_cast<size_t>(dm) * 4);
+    P.off_a2 = w.take(rows * static_cast<size_t>(2 * dm) * 2);
+    P.off_dl = w.take(static_cast<size_t>(K) * T * 4);
+    P.off_m = w.take(static_cast<size_t>(T) * 4);
+    P.off_r = w.take(static_cast<size_t>(K) * T * 4);
+    P.off_gbf = w.take(static_cast<size_t>(T * C) * 2);
+    P.off_xbf = w.take(static_cast<size_t>(T * P.ldx) * 2);
+    P.bytes = w.used;
+    return P;
+}
+
+unsigned grid_cap(int64_t n, int threads) {
+    int64_t b = ceil_div(n, threads);
+    b = std::min<int64_t>(b, 148 * 32);
+    return static_cast<unsigned>(std::max<int64_t>(b, 1));
+}
+
+}  // namespace
+}  // namespace dust
+
+using namespace dust;
+
+extern "C" size_t dust_linear_workspace(int64_t T, int64_t d_in, int64_t C, int64_t d_model,
+                                        int64_t V, uint32_t K) {
+    if (T < 1 || d_in < 1 || C < 1 || d_model < 1 || V < 1 || K < 2) return 0;
+    return interior_plan(T, d_in, C, d_model, V, K).bytes;
+}
+
+extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, const void* W2,
+                                            float ema_decay, const void* W_head,
+                                            const float* z_clean, const int32_t* targets,
+                                            int64_t T, int64_t seq_len, int64_t d_in, int64_t C,
+                                            int64_t d_model, int64_t V, dust_noise nz,
+                                            float* g_hat, float* G_W1, void* ws, size_t ws_bytes,
+                                            void* stream) {
+    if (!x || !y1 || !W2 || !W_head || !z_clean || !targets || !G_W1) return DUST_ERR_INVALID_ARG;
+    if (T < 1 || seq_len < 1 || T % seq_len != 0 || d_in < 1 || C < 1 || d_model < 1 || V < 1)
+        return DUST_ERR_INVALID_ARG;
+    if (nz.num_draws < 2 || !(nz.sigma > 0.0f) || !(nz.sigma < INFINITY)) return DUST_ERR_INVALID_ARG;
+    if (!(nz.gamma >= 0.0f && nz.gamma <= 1.0f)) return DUST_ERR_INVALID_ARG;
+    if (!(ema_decay >= 0.0f && ema_decay <= 1.0f)) return DUST_ERR_INVALID_ARG;
+    if (C % 64 != 0 || d_model % 64 != 0) return DUST_ERR_UNSUPPORTED;
+    if (T > (1LL << 28) || C > (1LL << 16) || d_model > (1LL << 16) || V > (1LL << 20) ||
+        d_in > (1LL << 20) || nz.num_draws > (1u << 24))
+        return DUST_ERR_UNSUPPORTED;
+    if (static_cast<uint64_t>(nz.token0) + static_cast<uint64_t>(T) > (1ULL << 32) ||
+        static_cast<uint64_t>(nz.draw0) + nz.num_draws > (1ULL << 32))
+        return DUST_ERR_INVALID_ARG;
+    if (!aligned(y1, 16) || !aligned(W2, 16) || !aligned(W_head, 16) || !aligned(z_clean, 16) ||
+        (g_hat && !aligned(g_hat, 16)))
+        return DUST_ERR_INVALID_ARG;
+    const InteriorPlan P = interior_plan(T, d_in, C, d_model, V, nz.num_draws);
+    if (!ws || ws_bytes < P.bytes || !aligned(ws, 256)) return DUST_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    uint32_t* status = static_cast<uint32_t*>(ws);
+    DUST_CUDA_TRY(cudaMemsetAsync(ws, 0, kCtlBytes, s));
+
+    float* p = reinterpret_cast<float*>(w + P.off_p);
+    __nv_bfloat16* A1 = reinterpret_cast<__nv_bfloat16*>(w + P.off_a1);
+    float* du = reinterpret_cast<float*>(w + P.off_du);
+    __nv_bfloat16* A2 = reinterpret_cast<__nv_bfloat16*>(w + P.off_a2);
+    float* dl = reinterpret_cast<float*>(w + P.off_dl);
+    float* mean = reinterpret_cast<float*>(w + P.off_m);
+    float* r = reinterpret_cast<float*>(w + P.off_r);
+    __nv_bfloat16* gbf = reinterpret_cast<__nv_bfloat16*>(w + P.off_gbf);
+    const int K = static_cast<int>(nz.num_draws);
+    const int Ti = static_cast<int>(T), Ci = static_cast<int>(C), dmi = static_cast<int>(d_model);
+    const PhiloxKeys keys = philox_round_keys(nz.seed);
+    dust_status st;
+
+    softmax_rows_kernel<<<static_cast<unsigned>(T), 256, 0, s>>>(z_clean, static_cast<int>(V), p);
+    if ((st = launch_status()) != DUST_OK) return st;
+
+    const int nseq = static_cast<int>(T / seq_len);
+    for (int i0 = 0; i0 < K; i0 += P.nd) {
+        const int nd = std::min(P.nd, K - i0);
+        const int64_t rows = nd * P.Tp;
+        DhArgs da{y1, Ti, static_cast<int>(P.Tp), Ci, nd, nz.draw0 + static_cast<uint32_t>(i0),
+                  nz.token0, nz.layer, nz.sigma, A1};
+        interior_dh_kernel<<<grid_cap(rows * (C / 4), 256), 256, 0, s>>>(da, keys);
+        if ((st = launch_status()) != DUST_OK) return st;
+        st = gemm_bf16_launch(A1, false, 2 * C, W2, false, C, rows, d_model, 2 * C, C,
+                              static_cast<int>(ceil_div(d_model, 256)), du, d_model, status, s);
+        if (st != DUST_OK) return st;
+        if (P.Tp != T)
+            DUST_CUDA_TRY(cudaMemsetAsync(A2, 0, static_cast<size_t>(rows * 2 * d_model) * 2, s));
+        interior_ema_kernel<<<grid_cap(static_cast<int64_t>(nd) * nseq * d_model, 128), 128, 0, s>>>(
+            du, nd, nseq, static_cast<int>(seq_len), dmi, ema_decay, A2);
+        if ((st = launch_status()) != DUST_OK) return st;
+        st = gemm_ce_launch(A2, 2 * d_model, W_head, d_model, rows, V, 2 * d_model, d_model, p,
+                            targets, T, nd, i0, dl, status, s);
+        if (st != DUST_OK) return st;
+    }
+
+    draw_mean_kernel<<<static_cast<unsigned>(ceil_div(T, 256)), 256, 0, s>>>(dl, K, Ti, mean);
+    reward_scan_kernel<<<static_cast<unsigned>(ceil_div(static_cast<int64_t>(K) * nseq, 128)), 128,
+                         0, s>>>(dl, mean, K, Ti, static_cast<int>(seq_len), nz.gamma, r);
+    if ((st = launch_status()) != DUST_OK) return st;
+    GhatArgs ga{r, Ti, Ci, K, nz.draw0, nz.token0, nz.layer,
+                static_cast<float>(-1.0 / (static_cast<double>(K) * nz.sigma)), g_hat, gbf};
+    interior_ghat_kernel<<<grid_cap(T * (C / 4), 256), 256, 0, s>>>(ga, keys);
+    if ((st = launch_status()) != DUST_OK) return st;
+
+    const void* xb = x;
+    int64_t ldx = d_in;
+    if ((d_in % 8) != 0 || !aligned(x, 16)) {
+        void* xbf = w + P.off_xbf;
+        if ((st = bf16_pad_launch(x, T, d_in, d_in, xbf, P.ldx, s)) != DUST_OK) return st;
+        xb = xbf;
+        ldx = P.ldx;
+    }
+    return gemm_bf16_launch(gbf, true, C, xb, true, ldx, C, d_in, T, 0, 1, G_W1, d_in, status, s);
+}

@@ -1,0 +1,97 @@
+// internal.h -- host-side pieces shared by the entry points: workspace
+// carving, CUDA error mapping and the launchers one entry point borrows from
+// another (the outer-product GEMM, the bf16 conversion).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/dust.h"
+
+namespace dust {
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// Offsets of the pieces of a caller-owned workspace; every piece is 256-byte
+// aligned.  The same function computes the layout for the size query and for
+// the call, so the two always agree.
+struct WsLayout {
+    size_t used = 0;
+    size_t take(size_t bytes) {
+        used = static_cast<size_t>(round_up(static_cast<int64_t>(used), 256));
+        const size_t off = used;
+        used += bytes;
+        return off;
+    }
+};
+
+inline bool aligned(const void* p, size_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+#define DUST_CUDA_TRY(expr)                                    \
+    do {                                                       \
+        cudaError_t e_ = (expr);                               \
+        if (e_ != cudaSuccess) {                               \
+            (void)cudaGetLastError();                          \
+            return DUST_ERR_CUDA;                              \
+        }                                                      \
+    } while (0)
+
+// Launch-error check after a kernel launch.
+inline dust_status launch_status() {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? DUST_OK : DUST_ERR_CUDA;
+}
+
+// Optional event pairs around the dominant kernel of each entry point (the
+// benchmark hook of dust_set_kernel_events).
+struct KernelTimer {
+    void* const* start = nullptr;
+    void* const* stop = nullptr;
+    int capacity = 0;
+    int count = 0;
+};
+KernelTimer& kernel_timer();
+inline void timer_begin(cudaStream_t s) {
+    KernelTimer& k = kernel_timer();
+    if (k.start && k.count < k.capacity)
+        cudaEventRecord(static_cast<cudaEvent_t>(k.start[k.count]), s);
+}
+inline void timer_end(cudaStream_t s) {
+    KernelTimer& k = kernel_timer();
+    if (k.stop && k.count < k.capacity) {
+        cudaEventRecord(static_cast<cudaEvent_t>(k.stop[k.count]), s);
+        ++k.count;
+    }
+}
+
+// G[m][n] = sum_k A(m,k) B(n,k) on the tensor cores (bf16 in, fp32 out).
+// a_mn: A stored as K rows of M elements (row stride lda), else M rows of K.
+// b_kmod > 0: B's K index wraps modulo b_kmod.  n_per_cta: 256-column tiles
+// walked by one CTA.
+dust_status gemm_bf16_launch(const void* A, bool a_mn, int64_t lda, const void* B, bool b_mn,
+                             int64_t ldb, int64_t M, int64_t N, int64_t K, int64_t b_kmod,
+                             int n_per_cta, float* G, int64_t ldg, uint32_t* status,
+                             cudaStream_t s);
+
+// Same contraction (both operands K-major) ending in the cross-entropy
+// epilogue: rows ordered (token block of 128, draw, token in block) for
+// ndraw draws starting at draw index i0; writes dl[(i0 + i) T + t] =
+// log sum_v p[t][v] exp(dz_v) - dz_{targets[t]}.
+dust_status gemm_ce_launch(const void* A, int64_t lda, const void* B, int64_t ldb, int64_t M,
+                           int64_t V, int64_t K, int64_t b_kmod, const float* p,
+                           const int32_t* targets, int64_t T, int ndraw, int i0, float* dl,
+                           uint32_t* status, cudaStream_t s);
+
+// rows x cols fp32 (row stride ld_in) -> bf16 (row stride ld_out, padding
+// columns set to zero).
+dust_status f32_to_bf16_launch(const float* in, int64_t rows, int64_t cols, int64_t ld_in,
+                               void* out, int64_t ld_out, cudaStream_t s);
+// bf16 -> bf16 copy into a padded layout.
+dust_status bf16_pad_launch(const void* in, int64_t rows, int64_t cols, int64_t ld_in,
+                            void* out, int64_t ld_out, cudaStream_t s);
+
+}  // namespace dust

@@ -1,0 +1,125 @@
+// noise.cuh -- counter-based Gaussian noise for the activation perturbation
+// y_t + sigma a_t (laoyaoba.com article, section 机制拆解; Dust translation,
+// hn.213312.xyz, §2.2 信用分配).  The pages only say the noise is Gaussian and
+// independent per token and per linear layer; it is regenerated from a
+// counter here so that it is never stored.
+//
+// Generator: Philox4x32-10 as defined by Salmon, Moraes, Dror and Shaw,
+// "Parallel random numbers: as easy as 1, 2, 3" (SC'11).  A round multiplies
+// counter words 0 and 2 by two fixed odd constants into 64-bit products; the
+// next state is (hi(M1 x2) ^ x1 ^ k0, lo(M1 x2), hi(M0 x0) ^ x3 ^ k1,
+// lo(M0 x0)); the key is bumped by the Weyl constants (golden ratio and
+// sqrt(3) - 1 in 32-bit fixed point) after every round.
+//
+// Counter of channel block j (channels 4j .. 4j+3) of token t, draw i, layer
+// L: (j, t, i, L); key (seed low word, seed high word).  Uniform of a word w:
+// ((w >> 9) + 0.5) 2^-23, in [2^-24, 1 - 2^-24].  Box-Muller (Box & Muller,
+// 1958) turns words (0, 1) into channels 4j, 4j+1 and words (2, 3) into
+// 4j+2, 4j+3: rho = sqrt(-2 ln u_even), theta = 2 pi u_odd, (rho cos theta,
+// rho sin theta).
+#pragma once
+
+#include <stdint.h>
+
+namespace dust {
+
+constexpr uint32_t kPhiloxM0 = 0xD2511F53u;
+constexpr uint32_t kPhiloxM1 = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxW0 = 0x9E3779B9u;
+constexpr uint32_t kPhiloxW1 = 0xBB67AE85u;
+
+// Round keys of all ten rounds, computed once on the host and passed as a
+// kernel parameter so that the xors read them from the constant bank.
+struct PhiloxKeys {
+    uint32_t k0[10];
+    uint32_t k1[10];
+};
+
+inline PhiloxKeys philox_round_keys(uint64_t seed) {
+    PhiloxKeys k;
+    uint32_t a = static_cast<uint32_t>(seed & 0xFFFFFFFFu);
+    uint32_t b = static_cast<uint32_t>(seed >> 32);
+    for (int r = 0; r < 10; ++r) {
+        k.k0[r] = a;
+        k.k1[r] = b;
+        a += kPhiloxW0;
+        b += kPhiloxW1;
+    }
+    return k;
+}
+
+__device__ __forceinline__ void philox_round(uint32_t& x0, uint32_t& x1, uint32_t& x2,
+                                             uint32_t& x3, uint32_t k0, uint32_t k1) {
+    const uint64_t p0 = static_cast<uint64_t>(x0) * kPhiloxM0;
+    const uint64_t p1 = static_cast<uint64_t>(x2) * kPhiloxM1;
+    const uint32_t n0 = static_cast<uint32_t>(p1 >> 32) ^ x1 ^ k0;
+    const uint32_t n2 = static_cast<uint32_t>(p0 >> 32) ^ x3 ^ k1;
+    x0 = n0;
+    x1 = static_cast<uint32_t>(p1);
+    x2 = n2;
+    x3 = static_cast<uint32_t>(p0);
+}
+
+// The first round split into its two independent halves.  With the counter
+// (j, t, i, L), the half that multiplies word 0 depends only on the channel
+// block j and the layer, the other only on the draw i and the token t, so
+// kernels compute each half once and reuse it across the other loop.
+struct BlockHalf {  // words 2, 3 after round 1
+    uint32_t x2, x3;
+};
+struct DrawHalf {  // words 0, 1 after round 1
+    uint32_t x0, x1;
+};
+
+__device__ __forceinline__ BlockHalf philox_block_half(uint32_t j, uint32_t layer,
+                                                       const PhiloxKeys& k) {
+    const uint64_t p0 = static_cast<uint64_t>(j) * kPhiloxM0;
+    return {static_cast<uint32_t>(p0 >> 32) ^ layer ^ k.k1[0], static_cast<uint32_t>(p0)};
+}
+
+__device__ __forceinline__ DrawHalf philox_draw_half(uint32_t draw, uint32_t token,
+                                                     const PhiloxKeys& k) {
+    const uint64_t p1 = static_cast<uint64_t>(draw) * kPhiloxM1;
+    return {static_cast<uint32_t>(p1 >> 32) ^ token ^ k.k0[0], static_cast<uint32_t>(p1)};
+}
+
+// Rounds 2..10 from the state after round 1.
+__device__ __forceinline__ uint4 philox_rest(DrawHalf d, BlockHalf b, const PhiloxKeys& k) {
+    uint32_t x0 = d.x0, x1 = d.x1, x2 = b.x2, x3 = b.x3;
+#pragma unroll
+    for (int r = 1; r < 10; ++r) philox_round(x0, x1, x2, x3, k.k0[r], k.k1[r]);
+    return make_uint4(x0, x1, x2, x3);
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t j, uint32_t token, uint32_t draw,
+                                               uint32_t layer, const PhiloxKeys& k) {
+    return philox_rest(philox_draw_half(draw, token, k), philox_block_half(j, layer, k), k);
+}
+
+// ((w >> 9) + 0.5) 2^-23, exactly: the 23 high bits of w as the mantissa of a
+// float in [1, 2), minus (1 - 2^-24).  The difference (2m + 1) 2^-24 has at
+// most 24 significant bits, so the subtraction is exact.
+__device__ __forceinline__ float word_to_uniform(uint32_t w) {
+    const float f = __uint_as_float((w >> 9) | 0x3F800000u);
+    return __fadd_rn(f, -0x1.fffffep-1f);
+}
+
+__device__ __forceinline__ void box_muller(uint32_t w_even, uint32_t w_odd, float& a_cos,
+                                           float& a_sin) {
+    const float u0 = word_to_uniform(w_even);
+    const float u1 = word_to_uniform(w_odd);
+    const float rho = sqrtf(-2.0f * logf(u0));
+    float s, c;
+    sincospif(2.0f * u1, &s, &c);
+    a_cos = rho * c;
+    a_sin = rho * s;
+}
+
+__device__ __forceinline__ float4 words_to_normals(uint4 w) {
+    float4 a;
+    box_muller(w.x, w.y, a.x, a.y);
+    box_muller(w.z, w.w, a.z, a.w);
+    return a;
+}
+
+}  // namespace dust

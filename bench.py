@@ -1,0 +1,501 @@
+#!/usr/bin/env python
+"""Throughput of the Dust estimator engine on B300: perturbed token-evaluations/s.
+
+One step is one call of an estimator entry point over one batch: every step
+of the hot path (noise, perturbed loss, centring/reward, error estimate, outer
+product) runs inside it.  The metric is draws x tokens per second.
+
+Default workload: the LM-head estimator at the pages' batch shape -- 8
+sequences x 2048 tokens, d = 512, vocabulary 4096, K = 64 draws, sigma = 0.05
+(linlog.top article, experimental setup; Dust translation, hn.213312.xyz,
+§3.1).  Inputs are synthetic: Zipf(1.1) targets stand in for FineWeb token
+frequencies; weights are random N(0, 1/fan_in).  The cached logits (256 MB)
+are larger than the 126 MB L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dust|reference]
+                  [--workload head_batch|head_tiny|head_scale|interior|interior_scale|embed_scale]
+
+Under torchrun (N > 1) every rank estimates its own batch (global token
+offset rank * T, so the noise differs per rank) with no collective on the data
+path; rank 0 prints the aggregate over the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (the pages give no implementation to run).
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("perturbed token-evals/sec (draws×tokens/s) on 1 B300; "
+          "% of HBM/tensor roofline")
+UNIT = "token-evals/s"
+N_SM = 148
+SM_MAX_MHZ = 2032.0
+# Algorithmic operation budget of one head element-draw (one noise sample, one
+# perturbed probability term, two accumulator updates), counted in the design
+# notes: Philox 9 + uniform 2 + Box-Muller 3 + CE 2 + accumulators 2 + share
+# of the per-draw reduction 2.
+HEAD_OPS_PER_ELEMENT_DRAW = 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+                "sm_max_mhz": SM_MAX_MHZ}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- workloads ----
+def make_workload(name, device, rank):
+    import torch
+
+    import workloads as W
+    bf = torch.bfloat16
+    dev = lambda a, dt=None: (torch.from_numpy(np.ascontiguousarray(a)).to(device)
+                              if dt is None else torch.from_numpy(np.ascontiguousarray(a)).to(device).to(dt))
+    if name.startswith("head"):
+        p = W.HEAD_PARAMS[name]
+        wl = W.head_workload(p["T"], p["d"], p["V"], p["seq_len"], p["x_bf16"], p["zipf"],
+                             device=str(device))
+        T = p["T"]
+        return {
+            "kind": "head", "name": name, "T": T, "V": p["V"], "d": p["d"], "K": p["K"],
+            "sigma": p["sigma"], "seq_len": p["seq_len"], "token0": rank * T,
+            "host": {"logits": wl["z"], "targets": wl["targets"],
+                     "x": W.bf16_round(wl["x"]) if p["x_bf16"] else wl["x"]},
+            "x_bf16": p["x_bf16"],
+            "dev": {"logits": dev(wl["z"]), "targets": dev(wl["targets"]),
+                    "x": dev(wl["x"], bf) if p["x_bf16"] else dev(wl["x"])},
+        }
+    if name.startswith("interior"):
+        p = W.INTERIOR_PARAMS[name]
+        wl = W.interior_workload(p["T"], p["d_in"], p["C"], p["d_model"], p["V"], p["seq_len"],
+                                 device=str(device))
+        return {
+            "kind": "interior", "name": name, "T": p["T"], "K": p["K"], "sigma": p["sigma"],
+            "gamma": p["gamma"], "seq_len": p["seq_len"], "lam": wl["lam"], "C": p["C"],
+            "d_in": p["d_in"], "d_model": p["d_model"], "V": p["V"], "token0": rank * p["T"],
+            "host": {k: wl[k] for k in ("x", "y1", "W2", "W_head", "z_clean", "targets")},
+            "dev": {"x": dev(wl["x"], bf), "y1": dev(wl["y1"]), "W2": dev(wl["W2"], bf),
+                    "W_head": dev(wl["W_head"], bf), "z_clean": dev(wl["z_clean"]),
+                    "targets": dev(wl["targets"])},
+        }
+    if name == "embed_scale":
+        wl = W.embed_workload()
+        return {"kind": "embed", "name": name, "T": wl["T"], "d": wl["d"], "V": wl["V"], "K": 1,
+                "host": {"g": wl["g"], "ids": wl["ids"]},
+                "dev": {"g": dev(wl["g"]), "ids": dev(wl["ids"])}}
+    raise SystemExit("unknown workload " + name)
+
+
+def make_step(wl, dust):
+    """Returns (step(), evals per step, launches per step) with outputs and
+    workspace allocated once."""
+    import torch
+    d = wl["dev"]
+    if wl["kind"] == "head":
+        T, V, dd, K = wl["T"], wl["V"], wl["d"], wl["K"]
+        g = torch.empty((T, V), dtype=torch.float32, device=d["logits"].device)
+        G = torch.empty((V, dd), dtype=torch.float32, device=g.device)
+        ws = dust._workspace(dust.head_workspace_bytes(T, V, dd, K), g.device)
+
+        def step():
+            dust.head_estimate(d["logits"], d["targets"], d["x"], wl["sigma"], K, 1234, 0, 0,
+                               wl["token0"], out=(g, G), ws=ws)
+        launches = 2 + (0 if wl["x_bf16"] else 1)
+        return step, K * T, launches, ws
+    if wl["kind"] == "interior":
+        T, K = wl["T"], wl["K"]
+        g = torch.empty((T, wl["C"]), dtype=torch.float32, device=d["x"].device)
+        G = torch.empty((wl["C"], wl["d_in"]), dtype=torch.float32, device=g.device)
+        ws = dust._workspace(dust.linear_workspace_bytes(T, wl["d_in"], wl["C"], wl["d_model"],
+                                                          wl["V"], K), g.device)
+
+        def step():
+            dust.linear_estimate(d["x"], d["y1"], d["W2"], wl["lam"], d["W_head"], d["z_clean"],
+                                 d["targets"], wl["seq_len"], wl["sigma"], wl["gamma"], K, 1234,
+                                 1, 0, wl["token0"], out=(g, G), ws=ws)
+        nd = 10
+        chunks = -(-K // nd)
+        return step, K * T, 1 + chunks * 3 + 3 + 1, ws
+    if wl["kind"] == "embed":
+        T, dd, V = wl["T"], wl["d"], wl["V"]
+        G = torch.empty((V, dd), dtype=torch.float32, device=d["g"].device)
+        perm = torch.empty(T, dtype=torch.int32, device=G.device)
+        ws = dust._workspace(dust.embed_workspace_bytes(T, dd, V), G.device)
+
+        def step():
+            dust.embed_scatter(d["g"], d["ids"], V, out=(G, perm), ws=ws)
+        return step, T, 12, ws
+    raise SystemExit("bad workload")
+
+
+def roofline(wl, kernel_ms, traffic):
+    peaks, which = _peaks()
+    if wl["kind"] == "head":
+        ops = HEAD_OPS_PER_ELEMENT_DRAW * wl["T"] * wl["V"] * wl["K"]
+        peak = N_SM * 128 * peaks.get("sm_max_mhz", SM_MAX_MHZ) * 1e6 / 1e12
+        ach = ops / (kernel_ms * 1e-3) / 1e12
+        return {"bound": "alu", "achieved": ach, "peak": peak, "unit": "Tops/s",
+                "frac": ach / peak, "traffic": traffic, "kernel": "head_draws_kernel",
+                "kernel_ms": kernel_ms, "peak_source": "148 SMs x 128 lanes x %.0f MHz (%s clocks)"
+                % (peaks.get("sm_max_mhz", SM_MAX_MHZ), which)}
+    if wl["kind"] == "interior":
+        # GEMM 2 of the re-forward: D draws x T rows x d_model x V, split-bf16 (2x)
+        flops = 2.0 * wl["K"] * wl["T"] * wl["d_model"] * wl["V"] * 2
+        peak = peaks["bf16_tflops_sustained"]
+        ach = flops / (kernel_ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "traffic": traffic, "kernel": "gemm_bf16_kernel<CE>",
+                "kernel_ms": kernel_ms, "peak_source": "bf16_tflops_sustained (%s)" % which}
+    if wl["kind"] == "embed":
+        nbytes = wl["T"] * wl["d"] * 4 + wl["T"] * 4 * 2 + wl["V"] * wl["d"] * 4
+        peak = peaks["hbm_gbs"]
+        ach = nbytes / (kernel_ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                "traffic": traffic, "kernel": "piece_sum_kernel", "kernel_ms": kernel_ms,
+                "peak_source": "hbm_gbs (%s)" % which}
+    return None
+
+
+def load_traffic(wl):
+    """Per-launch DRAM bytes of the dominant kernel from a committed ncu
+    capture, if the capture's kernel source still matches."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(wl["name"])
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    for src in rec.get("sources", []):
+        try:
+            h.update(open(os.path.join(ROOT, src), "rb").read())
+        except OSError:
+            return None
+    if h.hexdigest() != rec.get("sha256"):
+        return None
+    return rec.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------ CPU oracle ----
+def oracle_sample(wl, budget_s=12.0):
+    """The fp64 oracle on a bounded slice of the workload: (evals/s, sample text)."""
+    import oracle
+    h = wl["host"]
+    if wl["kind"] == "head":
+        K = wl["K"]
+
+        def run(n):
+            t0 = time.perf_counter()
+            oracle.head_estimate(h["logits"][:n], h["targets"][:n], h["x"][:n], wl["sigma"], K,
+                                 1234, 0, 0, 0)
+            return time.perf_counter() - t0
+        n = 8
+        dt = run(n)
+        n = int(min(wl["T"], max(8, n * budget_s / max(dt, 1e-3))))
+        dt = run(n)
+        return K * n / dt, "%d of %d tokens, all %d draws, full vocabulary %d" % (
+            n, wl["T"], K, wl["V"])
+    if wl["kind"] == "interior":
+        L = wl["seq_len"]
+
+        def run(k):
+            t0 = time.perf_counter()
+            oracle.linear_estimate(h["x"][:L], h["y1"][:L], h["W2"], wl["lam"], h["W_head"],
+                                   h["z_clean"][:L], h["targets"][:L], L, wl["sigma"],
+                                   wl["gamma"], k, 1234, 1, 0, 0)
+            return time.perf_counter() - t0
+        k = 2
+        dt = run(k)
+        k = int(min(wl["K"], max(2, k * budget_s / max(dt, 1e-3))))
+        dt = run(k)
+        return k * L / dt, "sequence 0 (%d tokens), %d of %d draws" % (L, k, wl["K"])
+    if wl["kind"] == "embed":
+        t0 = time.perf_counter()
+        oracle.embed_scatter(h["g"], h["ids"], wl["V"])
+        dt = time.perf_counter() - t0
+        return wl["T"] / dt, "whole workload (%d tokens)" % wl["T"]
+    return None, ""
+
+
+def config_of(wl, n_gpus):
+    c = {"workload": wl["name"], "tokens": wl["T"], "draws": wl["K"],
+         "l2": "inputs larger than L2 (no flush)", "parallelism": "dp%d" % n_gpus}
+    for k in ("V", "d", "C", "d_in", "d_model", "seq_len", "sigma", "gamma"):
+        if k in wl:
+            c[k] = wl[k]
+    return c
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    wl = make_workload(args.workload, "cpu", 0)
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm-up state; its first call builds the C library
+    import oracle
+    oracle.lib()
+    vals, sample = [], ""
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, sample = oracle_sample(wl, budget_s=max(2.0, 60.0 / max(args.steps, 1)))
+        vals.append(v)
+    elapsed = time.perf_counter() - t0
+    value = float(np.median(vals))
+    cores = os.cpu_count()
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * elapsed / max(args.steps, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference", "config": config_of(wl, args.gpus),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_dust(args):
+    import torch
+    import torch.distributed as dist
+
+    import activation_perturbation_es_noise_b300 as dust
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    dust.lib()
+    wl = make_workload(args.workload, device, rank)
+    step, evals, launches, ws = make_step(wl, dust)
+    for _ in range(max(args.warmup, 3 if args.warmup >= 3 else args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if dust.workspace_status(ws) != 0:
+        raise SystemExit("kernel status word set during warm-up")
+
+    stream = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    timer = dust.KernelTimer(capacity=max(1, args.steps) * 64)
+    barrier()
+    with ClockSampler(local) as clocks:
+        with timer:
+            e0.record(stream)
+            for _ in range(args.steps):
+                step()
+            e1.record(stream)
+        e1.synchronize()
+    barrier()
+    ms = e0.elapsed_time(e1)
+    kernel_ms = timer.total_ms() / max(args.steps, 1)
+    if dust.workspace_status(ws) != 0:
+        raise SystemExit("kernel status word set during the timed steps")
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    value = evals * world * args.steps / (ms_max * 1e-3)
+
+    # End to end through the public API from pinned host buffers: the step's
+    # inputs copied in, the estimator, the weight gradient copied out.
+    e2e = None
+    if not args.no_e2e:
+        host = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory()
+                for k, v in wl["host"].items()}
+        devb = {k: torch.empty(v.shape, dtype=v.dtype, device=device) for k, v in host.items()}
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        if wl["kind"] == "head":
+            T, V, dd, K = wl["T"], wl["V"], wl["d"], wl["K"]
+            g = torch.empty((T, V), dtype=torch.float32, device=device)
+            G = torch.empty((V, dd), dtype=torch.float32, device=device)
+            Gh = torch.empty((V, dd), dtype=torch.float32).pin_memory()
+            wse = dust._workspace(dust.head_workspace_bytes(T, V, dd, K), device)
+
+            def e2e_step():
+                for k in host:
+                    devb[k].copy_(host[k], non_blocking=True)
+                dust.head_estimate(devb["logits"], devb["targets"], devb["x"], wl["sigma"], K,
+                                   1234, 0, 0, wl["token0"], out=(g, G), ws=wse)
+                Gh.copy_(G, non_blocking=True)
+            d2h = Gh.numel() * 4
+        elif wl["kind"] == "interior":
+            T, K = wl["T"], wl["K"]
+            g = torch.empty((T, wl["C"]), dtype=torch.float32, device=device)
+            G = torch.empty((wl["C"], wl["d_in"]), dtype=torch.float32, device=device)
+            Gh = torch.empty(G.shape, dtype=torch.float32).pin_memory()
+            wse = dust._workspace(dust.linear_workspace_bytes(
+                T, wl["d_in"], wl["C"], wl["d_model"], wl["V"], K), device)
+            bf = torch.bfloat16
+            for k in ("x", "W2", "W_head"):
+                host[k] = host[k]  # already exact bf16 values held as fp32
+            devbf = {}
+
+            def e2e_step():
+                for k in host:
+                    devb[k].copy_(host[k], non_blocking=True)
+                for k in ("x", "W2", "W_head"):
+                    devbf[k] = devb[k].to(bf)
+                dust.linear_estimate(devbf["x"], devb["y1"], devbf["W2"], wl["lam"],
+                                     devbf["W_head"], devb["z_clean"], devb["targets"],
+                                     wl["seq_len"], wl["sigma"], wl["gamma"], K, 1234, 1, 0,
+                                     wl["token0"], out=(g, G), ws=wse)
+                Gh.copy_(G, non_blocking=True)
+            d2h = Gh.numel() * 4
+        else:
+            V, dd, T = wl["V"], wl["d"], wl["T"]
+            G = torch.empty((V, dd), dtype=torch.float32, device=device)
+            perm = torch.empty(T, dtype=torch.int32, device=device)
+            Gh = torch.empty((V, dd), dtype=torch.float32).pin_memory()
+            wse = dust._workspace(dust.embed_workspace_bytes(T, dd, V), device)
+
+            def e2e_step():
+                for k in host:
+                    devb[k].copy_(host[k], non_blocking=True)
+                dust.embed_scatter(devb["g"], devb["ids"], V, out=(G, perm), ws=wse)
+                Gh.copy_(G, non_blocking=True)
+            d2h = Gh.numel() * 4
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        barrier()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        f1.record(stream)
+        f1.synchronize()
+        barrier()
+        te = torch.tensor([f0.elapsed_time(f1)], device=device, dtype=torch.float64)
+        if world > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        e2e = {"value": evals * world * args.steps / (float(te.item()) * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, sample = oracle_sample(wl)
+        cpu = {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": sample}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32" if wl["kind"] != "interior" else "f32+bf16x2",
+                "data": "synthetic", "config": config_of(wl, world),
+                "roofline": roofline(wl, kernel_ms, load_traffic(wl)),
+                "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches * args.steps,
+                "clocks": clocks.summary()}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="dust", choices=["dust", "reference"])
+    ap.add_argument("--workload", default="head_batch",
+                    choices=["head_batch", "head_tiny", "head_scale", "interior",
+                             "interior_scale", "embed_scale"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_dust(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

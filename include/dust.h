@@ -1,0 +1,239 @@
+/*
+ * dust.h -- C ABI of the B300 (sm_103a) engine for the Dust virtual-population
+ * gradient estimator ("Dust: Pretraining Transformers Without
+ * Backpropagation", Q Labs).
+ *
+ * The method (Dust translation, hn.213312.xyz, §2.2 信用分配): a linear layer
+ * y_t = W x_t has its output perturbed per token, y_t + sigma a_t with
+ * a_t ~ N(0, I).  For each of K draws the per-token loss is re-evaluated from
+ * cached clean activations; the centred loss decrease c_s of token s gives the
+ * reward r_t = sum_{s>=t} gamma^(s-t) c_s (gamma = 0: own token only); the
+ * error estimate is g_t = -(1/(K sigma)) sum_i r_t^(i) a_t^(i) and the weight
+ * gradient is G_W = sum_t g_t x_t^T.  For an embedding (one-hot input) the
+ * outer product is a scatter-add of g_t into row id_t.  The LM head is
+ * perturbed directly on its cached logits and only the cross-entropy is
+ * recomputed (same page, §2.3 干扰与调优; laoyaoba.com article, section
+ * 机制拆解).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer named as device memory must point to memory of the current
+ *    CUDA device; host pointers are named as such.  Arrays are row-major and
+ *    contiguous.  The caller owns every buffer; the library never allocates,
+ *    frees or synchronises (apart from dust_workspace_status, which reads a
+ *    word back on purpose).  All work is enqueued on `stream` (a cudaStream_t;
+ *    NULL = the legacy default stream).
+ *  - Outputs are overwritten, never accumulated into.  Inputs are not
+ *    modified.
+ *  - Arguments are checked on the host before any launch; a bad argument
+ *    returns an error status and enqueues nothing.  Values that live on the
+ *    device (target ids, embedding ids) are checked by the kernels: an id out
+ *    of range is skipped and recorded in the workspace status word, which
+ *    dust_workspace_status reads back.  No kernel traps or asserts.
+ *  - Every wait inside a kernel is bounded; a wait that runs out records
+ *    DUST_ERR_TIMEOUT in the workspace status word and the kernel returns.
+ *  - Results are deterministic: the same inputs and the same dust_noise give
+ *    bitwise-identical outputs (no floating-point atomics).
+ *  - The workspace (`ws`, `ws_bytes`) is device memory of at least the size
+ *    returned by the matching *_workspace query, 256-byte aligned.  Calls that
+ *    share one workspace must be ordered on the GPU (same stream).
+ */
+#ifndef DUST_H
+#define DUST_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DUST_OK = 0,
+    DUST_ERR_INVALID_ARG = 1,  /* null pointer, bad size, sigma <= 0, ... */
+    DUST_ERR_UNSUPPORTED = 2,  /* a size beyond what the kernels handle   */
+    DUST_ERR_WORKSPACE = 3,    /* workspace null, too small or unaligned  */
+    DUST_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed       */
+    DUST_ERR_TIMEOUT = 5,      /* a bounded in-kernel wait ran out        */
+    DUST_ERR_DEVICE_RANGE = 6  /* a device-side id was out of range       */
+} dust_status;
+
+typedef enum { DUST_F32 = 0, DUST_BF16 = 1 } dust_dtype;
+
+/*
+ * Noise and credit parameters of one estimator call.
+ *
+ * The noise a_{i,t}[c] of draw i, token t, output channel c is regenerated
+ * from a counter, never stored: Philox4x32-10 (Salmon, Moraes, Dror, Shaw,
+ * "Parallel random numbers: as easy as 1, 2, 3", SC'11) of the counter
+ * (c / 4, token0 + t, draw0 + i, layer) under the key (seed low word, seed
+ * high word); each 32-bit word w becomes u = ((w >> 9) + 0.5) * 2^-23 and the
+ * pairs (word 0, word 1), (word 2, word 3) become two normals each by
+ * Box-Muller: rho = sqrt(-2 ln u_even), theta = 2 pi u_odd, channel 4j+2p gets
+ * rho cos theta and 4j+2p+1 gets rho sin theta.  The pages say only that the
+ * noise is Gaussian and independent per token and per layer; the generator and
+ * counter layout are this library's convention.
+ */
+typedef struct {
+    uint64_t seed;
+    uint32_t layer;      /* layer id, the fourth counter word                 */
+    uint32_t draw0;      /* draws are draw0 .. draw0 + num_draws - 1          */
+    uint32_t num_draws;  /* K >= 2 (centring needs two draws)                 */
+    uint32_t token0;     /* global index of the call's first token            */
+    float sigma;         /* noise scale, > 0                                  */
+    float gamma;         /* reward discount in [0, 1]; ignored by the head    */
+} dust_noise;
+
+const char* dust_status_string(dust_status s);
+
+/* Version of this ABI (major * 100 + minor). */
+int dust_abi_version(void);
+
+/*
+ * Reads the workspace status word left by the last call that used `ws`
+ * (waits for `stream` first) into *status_out and clears it.  DUST_OK means no
+ * kernel recorded a device-side error.
+ */
+dust_status dust_workspace_status(void* ws, void* stream, dust_status* status_out);
+
+/* ------------------------------------------------------------------------ */
+/* LM head (configs with gamma = 0)                                          */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes for dust_head_estimate with these sizes. */
+size_t dust_head_workspace(int64_t T, int64_t V, int64_t d, uint32_t K);
+
+/*
+ * LM-head estimator, perturbed directly on the cached logits (Dust
+ * translation §2.3; laoyaoba.com section 机制拆解).
+ *
+ *   logits  device, T x V fp32: the cached clean logits z_t.
+ *   targets device, T int32: next-token ids in [0, V).
+ *   x       device, T x d, dtype x_dtype: the head's input activations.
+ *   g_hat   device, T x V fp32 output, or NULL: the error estimate
+ *           g_t[v] = -(1/(K sigma)) sum_i c_{i,t} a_{i,t}[v], with
+ *           c_{i,t} = -(dl_{i,t} - mean_j dl_{j,t}) and
+ *           dl_{i,t} = CE(z_t + sigma a_{i,t}) - CE(z_t) (natural log, full
+ *           vocabulary).  gamma is not used: the head has no path from one
+ *           token's logits to another token's loss, so r = c.
+ *   G_W     device, V x d fp32 output: sum_t g_t x_t^T, computed from g
+ *           rounded to bf16 and x rounded to bf16, accumulated in fp32.
+ *
+ * Limits: 1 <= V <= 8192, 1 <= d, 1 <= T <= 2^30, 2 <= K <= 2^30,
+ *         token0 + T <= 2^32, draw0 + K <= 2^32.
+ */
+dust_status dust_head_estimate(const float* logits, const int32_t* targets, const void* x,
+                               dust_dtype x_dtype, int64_t T, int64_t V, int64_t d,
+                               dust_noise nz, float* g_hat, float* G_W, void* ws,
+                               size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Interior linear layer with causal credit                                  */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes for dust_linear_estimate with these sizes. */
+size_t dust_linear_workspace(int64_t T, int64_t d_in, int64_t C, int64_t d_model, int64_t V,
+                             uint32_t K);
+
+/*
+ * Interior linear layer y1 = W1 x whose output is perturbed; only the part
+ * after it is re-run, from cached clean activations (laoyaoba.com section
+ * 机制拆解; Dust translation §2.3).  The downstream is fixed:
+ * GELU (exact erf) -> W2 -> causal per-sequence EMA
+ * e_t = ema_decay e_{t-1} + (1 - ema_decay) u_t (e = 0 before each sequence
+ * start) -> W_head -> cross-entropy.  Because W2, the EMA and W_head are
+ * linear, a draw's perturbed logits are z_clean + W_head EMA(W2 dh) with
+ * dh = GELU(y1 + sigma a) - GELU(y1).
+ *
+ *   x       device, T x d_in bf16: the layer input.
+ *   y1      device, T x C fp32: cached clean output of the layer.
+ *   W2      device, d_model x C bf16.
+ *   W_head  device, V x d_model bf16.
+ *   z_clean device, T x V fp32: cached clean logits.
+ *   targets device, T int32 in [0, V).
+ *   seq_len tokens per sequence; T is a multiple of it.  Credit and the EMA
+ *           never cross a sequence boundary.
+ *   g_hat   device, T x C fp32 output, or NULL.
+ *   G_W1    device, C x d_in fp32 output: sum_t g_t x_t^T (g rounded to bf16).
+ *
+ * Reward: r_{i,t} = sum_{s >= t, same sequence} gamma^(s-t) c_{i,s}.
+ */
+dust_status dust_linear_estimate(const void* x, const float* y1, const void* W2,
+                                 float ema_decay, const void* W_head, const float* z_clean,
+                                 const int32_t* targets, int64_t T, int64_t seq_len,
+                                 int64_t d_in, int64_t C, int64_t d_model, int64_t V,
+                                 dust_noise nz, float* g_hat, float* G_W1, void* ws,
+                                 size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Embedding: one-hot input, so the outer product is a scatter-add            */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes for dust_embed_scatter with these sizes. */
+size_t dust_embed_workspace(int64_t T, int64_t d, int64_t V);
+
+/*
+ * Embedding gradient (Dust translation §2.2, last sentences): with one-hot
+ * inputs, sum_t g_t onehot(id_t)^T is the scatter-add G_E[id_t] += g_t.
+ *
+ *   g_hat   device, T x d fp32.
+ *   ids     device, T int32 in [0, V).
+ *   G_E     device, V x d fp32 output, fully overwritten; rows no token hits
+ *           are zero.  Row v is the sum of the g_t with id_t = v, in a fixed
+ *           order that depends only on the ids (bitwise reproducible).
+ *   perm_out device, T int32 output, or NULL: the tokens ordered by
+ *           (id, t) ascending -- a stable sort of the ids.
+ *
+ * Limits: 1 <= V <= 2^24, 1 <= d, 0 <= T < 2^31.
+ */
+dust_status dust_embed_scatter(const float* g_hat, const int32_t* ids, int64_t T, int64_t d,
+                               int64_t V, float* G_E, int32_t* perm_out, void* ws,
+                               size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Test hooks                                                               */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The noise regenerator alone, for tokens token0 .. token0 + ntok - 1 and
+ * channels 0 .. nchan - 1 of one draw (counter layout as in dust_noise).
+ *   words   device, ntok x nchan uint32 output, or NULL: word (c % 4) of the
+ *           Philox block of channel c.
+ *   normals device, ntok x nchan fp32 output, or NULL: the normal of channel c.
+ */
+dust_status dust_philox_fill(uint64_t seed, uint32_t layer, uint32_t draw, int64_t token0,
+                             int64_t ntok, int64_t nchan, uint32_t* words, float* normals,
+                             void* stream);
+
+/*
+ * The outer-product GEMM alone: G[m][n] = sum_k A(m, k) B(n, k) in fp32 from
+ * bf16 operands on the tensor cores.  A is stored M-major (k rows of M
+ * elements, row stride lda elements) when a_mn != 0, else K-major (M rows of
+ * K elements); likewise B with b_mn.  All device; G is M x N fp32 (row stride
+ * ldg).  Strides are multiples of 8 elements; the bases are 16-byte aligned.
+ * `ws` holds the status word (>= 256 bytes).
+ */
+dust_status dust_gemm_bf16(const void* A, int a_mn, int64_t lda, const void* B, int b_mn,
+                           int64_t ldb, int64_t M, int64_t N, int64_t K, float* G, int64_t ldg,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Benchmark hook.  While set, every launch of an entry point's dominant
+ * kernel (the head's draw kernel, the interior layer's re-forward GEMM with
+ * the cross-entropy epilogue, the embedding's piece sums) is bracketed on its
+ * stream by cudaEventRecord(start_events[n]) and cudaEventRecord(
+ * stop_events[n]) for n = 0, 1, ... up to capacity - 1.  The events are the
+ * caller's (created with timing enabled).  Passing NULL arrays turns the hook
+ * off.  The hook is process-wide and not thread-safe: it is for timing runs.
+ * dust_kernel_event_count returns how many pairs were recorded since the last
+ * dust_set_kernel_events.
+ */
+dust_status dust_set_kernel_events(void* const* start_events, void* const* stop_events,
+                                   int capacity);
+int dust_kernel_event_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DUST_H */

@@ -26,3 +26,23 @@ def orc():
     import oracle
     oracle.lib()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def dust():
+    """The engine's Python binding with libdust.so loaded (GPU tests only)."""
+    import torch
+    import activation_perturbation_es_noise_b300 as d
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test collected without a CUDA device")
+    d.lib()
+    return d
+
+
+def to_dev(a, dtype=None):
+    import numpy as np
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.cuda()

@@ -1,0 +1,81 @@
+"""The C-ABI library on the host (no GPU): it loads, exports every entry point
+include/dust.h declares, sizes workspaces, and rejects bad arguments before
+touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import activation_perturbation_es_noise_b300 as dust
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "dust.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dust_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    from activation_perturbation_es_noise_b300 import build
+    build.build()
+    L = dust.lib()
+    names = _declared()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(dust.EXPORTS) == set(names)
+
+
+def test_status_strings():
+    L = dust.lib()
+    for code in range(7):
+        assert L.dust_status_string(code)
+    assert L.dust_abi_version() == 100
+
+
+def test_workspace_sizes_monotone():
+    a = dust.head_workspace_bytes(256, 512, 64, 64)
+    b = dust.head_workspace_bytes(16384, 4096, 512, 64)
+    assert 0 < a < b
+    assert dust.head_workspace_bytes(0, 512, 64, 64) == 0
+    assert dust.head_workspace_bytes(16, 512, 64, 1) == 0
+    assert dust.linear_workspace_bytes(16384, 512, 2048, 512, 4096, 256) > 0
+    assert dust.embed_workspace_bytes(16384, 1536, 4096) > 0
+    assert dust.embed_workspace_bytes(0, 1536, 4096) > 0
+
+
+def test_bad_arguments_rejected_on_host():
+    L = dust.lib()
+    nz = dust.noise(1, 0.05, 4)
+    fake = ctypes.c_void_p(256)
+    # null logits
+    assert L.dust_head_estimate(None, fake, fake, 0, 4, 4, 4, nz, None, fake, fake, 1 << 20,
+                                None) == 1
+    # K < 2
+    assert L.dust_head_estimate(fake, fake, fake, 0, 4, 4, 4, dust.noise(1, 0.05, 1), None, fake,
+                                fake, 1 << 20, None) == 1
+    # workspace too small
+    assert L.dust_head_estimate(fake, fake, fake, 0, 4, 4, 4, nz, None, fake, fake, 16,
+                                None) == 3
+    # V beyond the kernel's register budget
+    assert L.dust_head_estimate(fake, fake, fake, 0, 4, 100000, 4, nz, None, fake, fake,
+                                1 << 20, None) == 2
+    # interior: seq_len must divide T; C must be a multiple of 64
+    nzi = dust.noise(1, 0.02, 4, gamma=0.9)
+    assert L.dust_linear_estimate(fake, fake, fake, 0.9, fake, fake, fake, 100, 30, 8, 64, 64,
+                                  16, nzi, None, fake, fake, 1 << 30, None) == 1
+    assert L.dust_linear_estimate(fake, fake, fake, 0.9, fake, fake, fake, 128, 64, 8, 96, 64,
+                                  16, nzi, None, fake, fake, 1 << 30, None) == 2
+    # gamma outside [0, 1]
+    assert L.dust_linear_estimate(fake, fake, fake, 0.9, fake, fake, fake, 128, 64, 8, 64, 64,
+                                  16, dust.noise(1, 0.02, 4, gamma=1.5), None, fake, fake,
+                                  1 << 30, None) == 1
+    # embedding: null output
+    assert L.dust_embed_scatter(fake, fake, 4, 4, 4, None, None, fake, 1 << 20, None) == 1
+    # philox: negative sizes
+    assert L.dust_philox_fill(1, 0, 0, 0, -1, 4, fake, None, None) == 1
+    # gemm: misaligned leading dimension
+    assert L.dust_gemm_bf16(fake, 0, 7, fake, 0, 8, 4, 4, 4, fake, 4, fake, 256, None) == 1

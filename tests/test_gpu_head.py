@@ -1,0 +1,121 @@
+"""LM-head estimator: CUDA path through the C ABI against the fp64 oracle (GPU).
+
+Tolerances (stated for the estimator): rel-L2 <= 1e-4 on g_hat (fp32 path),
+rel-L2 <= 5e-3 on G_W (bf16 operands, fp32 accumulation).  Sizes span the
+kernel's one-warp and multi-warp CTAs, ragged vocabularies (V not a multiple
+of 4 or 8), ragged d and the draw-split path (few tokens, many draws).
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from conftest import rel_l2, to_dev
+
+pytestmark = pytest.mark.gpu
+
+G_TOL, GW_TOL = 1e-4, 5e-3
+
+
+def _inputs(T, d, V, seed=0, zipf=False):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    Wh = (rng.standard_normal((V, d)) / np.sqrt(d)).astype(np.float32)
+    z = (x.astype(np.float64) @ Wh.astype(np.float64).T).astype(np.float32)
+    y = (W.zipf_ids(seed + 1, T, V) if zipf else rng.integers(0, V, T)).astype(np.int32)
+    return x, z, y
+
+
+def _run(dust, x, z, y, sigma, K, seed, layer=0, draw0=0, token0=0, x_bf16=False):
+    xt = to_dev(x, torch.bfloat16) if x_bf16 else to_dev(x)
+    g, G, ws = dust.head_estimate(to_dev(z), to_dev(y), xt, sigma, K, seed, layer, draw0, token0)
+    torch.cuda.synchronize()
+    assert dust.workspace_status(ws) == 0
+    return g.cpu().numpy(), G.cpu().numpy()
+
+
+def _check(orc, x, z, y, g, G, sigma, K, seed, layer=0, draw0=0, token0=0, x_bf16=False):
+    ref = orc.head_estimate(z, y, x, sigma, K, seed, layer, draw0, token0)
+    eg = rel_l2(g, ref["g"])
+    assert eg <= G_TOL, eg
+    eG = rel_l2(G, ref["G"])
+    assert eG <= GW_TOL, eG
+    return eg, eG
+
+
+def test_head_tiny_config(dust, orc):
+    """The tiny workload: 1 x 256 tokens, d = 64, V = 512, K = 64, sigma = 0.05."""
+    p = W.HEAD_PARAMS["head_tiny"]
+    wl = W.head_workload(p["T"], p["d"], p["V"], p["seq_len"], p["x_bf16"], p["zipf"])
+    g, G = _run(dust, wl["x"], wl["z"], wl["targets"], p["sigma"], p["K"], W.NOISE_SEED)
+    _check(orc, wl["x"], wl["z"], wl["targets"], g, G, p["sigma"], p["K"], W.NOISE_SEED)
+
+
+@pytest.mark.parametrize("T,d,V,K", [
+    (77, 50, 333, 8),      # ragged V (not a multiple of 4), ragged d, one warp
+    (130, 24, 1000, 6),    # V multiple of 8, one-warp NB = 8
+    (64, 512, 4096, 4),    # multi-warp CTA (256 threads)
+    (19, 16, 4100, 3),     # multi-warp, ragged V above 4096 (NB = 8)
+    (5, 8, 7, 2),          # degenerate: 2 blocks, K = 2
+    (8, 64, 512, 512),     # few tokens, many draws: draw chunks + finalize
+])
+def test_head_shapes(dust, orc, T, d, V, K):
+    x, z, y = _inputs(T, d, V, seed=T + V)
+    g, G = _run(dust, x, z, y, 0.05, K, 99, layer=3, draw0=5, token0=1000)
+    _check(orc, x, z, y, g, G, 0.05, K, 99, layer=3, draw0=5, token0=1000)
+
+
+def test_head_bf16_x_and_determinism(dust, orc):
+    x, z, y = _inputs(256, 64, 512, seed=4)
+    xb = W.bf16_round(x)
+    g1, G1 = _run(dust, xb, z, y, 0.05, 16, 7, x_bf16=True)
+    g2, G2 = _run(dust, xb, z, y, 0.05, 16, 7, x_bf16=True)
+    np.testing.assert_array_equal(g1, g2)
+    np.testing.assert_array_equal(G1, G2)
+    _check(orc, xb, z, y, g1, G1, 0.05, 16, 7)
+
+
+def test_head_token_slices_commute(dust):
+    """Noise is keyed by the global token index: tokens [a, b) of a call equal
+    a call on those tokens alone with token0 = a, bit for bit."""
+    x, z, y = _inputs(300, 32, 512, seed=9)
+    g_full, _ = _run(dust, x, z, y, 0.05, 16, 5)
+    g_part, _ = _run(dust, x[100:200], z[100:200], y[100:200], 0.05, 16, 5, token0=100)
+    np.testing.assert_array_equal(g_full[100:200], g_part)
+
+
+def test_head_bad_target_sets_status(dust):
+    x, z, y = _inputs(32, 16, 64, seed=1)
+    y[5] = 64
+    g, G, ws = dust.head_estimate(to_dev(z), to_dev(y), to_dev(x), 0.05, 4, 1)
+    torch.cuda.synchronize()
+    assert dust.workspace_status(ws) == 6  # DUST_ERR_DEVICE_RANGE
+    assert dust.workspace_status(ws) == 0  # read clears it
+
+
+def test_head_invalid_args_raise(dust):
+    x, z, y = _inputs(8, 8, 16)
+    with pytest.raises(dust.DustError):
+        dust.head_estimate(to_dev(z), to_dev(y), to_dev(x), 0.05, 1, 1)   # K < 2
+    with pytest.raises(dust.DustError):
+        dust.head_estimate(to_dev(z), to_dev(y), to_dev(x), -1.0, 4, 1)  # sigma <= 0
+
+
+def test_head_batch_config_sampled(dust, orc):
+    """The pages' batch shape (8 x 2048 tokens, d = 512, V = 4096, K = 64) in the
+    launch configuration the bench times.  g of sampled token ranges against the
+    oracle (g_t depends on token t alone); G_W against a float64 product of the
+    returned g and x, both rounded to bf16 as the kernel's operands are."""
+    p = W.HEAD_PARAMS["head_batch"]
+    wl = W.head_workload(p["T"], p["d"], p["V"], p["seq_len"], p["x_bf16"], p["zipf"])
+    g, G = _run(dust, wl["x"], wl["z"], wl["targets"], p["sigma"], p["K"], W.NOISE_SEED,
+                x_bf16=True)
+    for a in (0, 8191, 16384 - 24):
+        sl = slice(a, a + 24)
+        ref = orc.head_estimate(wl["z"][sl], wl["targets"][sl], wl["x"][sl], p["sigma"], p["K"],
+                                W.NOISE_SEED, 0, 0, a)
+        assert rel_l2(g[sl], ref["g"]) <= G_TOL
+    gb = W.bf16_round(g).astype(np.float64)
+    ref_G = gb.T @ wl["x"].astype(np.float64)
+    # fp32 accumulation of 16384 products inside the tensor cores: ~2e-5
+    assert rel_l2(G, ref_G) <= 1e-4
