@@ -26,7 +26,7 @@ DUST_F32, DUST_BF16 = 0, 1
 EXPORTS = ("dust_status_string", "dust_abi_version", "dust_workspace_status",
            "dust_head_workspace", "dust_head_estimate", "dust_linear_workspace",
            "dust_linear_estimate", "dust_embed_workspace", "dust_embed_scatter",
-           "dust_philox_fill", "dust_gemm_bf16", "dust_set_kernel_events",
+           "dust_embed_scatter_static", "dust_philox_fill", "dust_gemm_bf16", "dust_set_kernel_events",
            "dust_kernel_event_count")
 
 
@@ -75,13 +75,15 @@ def lib():
         L.dust_embed_workspace.argtypes = [_I64, _I64, _I64]
         L.dust_embed_workspace.restype = _SZ
         L.dust_embed_scatter.argtypes = [_P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]
+        L.dust_embed_scatter_static.argtypes = [_P, _P, _I64, _I64, _I64, _P, _P, _P]
         L.dust_philox_fill.argtypes = [ctypes.c_uint64, _U32, _U32, _I64, _I64, _I64, _P, _P, _P]
         L.dust_gemm_bf16.argtypes = [_P, ctypes.c_int, _I64, _P, ctypes.c_int, _I64, _I64, _I64,
                                      _I64, _P, _I64, _P, _SZ, _P]
         L.dust_set_kernel_events.argtypes = [_P, _P, ctypes.c_int]
         L.dust_kernel_event_count.restype = ctypes.c_int
         for name in ("dust_set_kernel_events", "dust_workspace_status", "dust_head_estimate", "dust_linear_estimate",
-                     "dust_embed_scatter", "dust_philox_fill", "dust_gemm_bf16"):
+                     "dust_embed_scatter", "dust_embed_scatter_static", "dust_philox_fill",
+                     "dust_gemm_bf16"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib

@@ -190,6 +190,27 @@ dust_status dust_embed_scatter(const float* g_hat, const int32_t* ids, int64_t T
                                int64_t V, float* G_E, int32_t* perm_out, void* ws,
                                size_t ws_bytes, void* stream);
 
+/*
+ * dust_embed_scatter without a caller-provided workspace, for callers that
+ * cannot allocate device memory where they need the embedding gradient (code
+ * running under a host framework that owns every device allocation, or in a
+ * hook that runs while the caller's memory pool is locked).  The pages have no
+ * counterpart: this is an interface convenience, not a step of the method.
+ *
+ * Same arguments, results and limits as dust_embed_scatter, except that the
+ * scratch is a fixed 32 MiB array inside the library (held on every GPU that
+ * loads the library until the process exits).  Sizes whose workspace
+ * (dust_embed_workspace) exceeds 32 MiB return DUST_ERR_UNSUPPORTED.  The
+ * first call on a device looks up the array's device address, so make it
+ * before any stream capture.  All calls share the array: calls that overlap on
+ * the GPU race, so order them (one stream).  Device-side id errors go to the
+ * shared array's status word and cannot be read back through this call.
+ * Allocates nothing (no cudaMalloc, no allocating library routine).
+ */
+dust_status dust_embed_scatter_static(const float* g_hat, const int32_t* ids, int64_t T,
+                                      int64_t d, int64_t V, float* G_E, int32_t* perm_out,
+                                      void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Test hooks                                                               */
 /* ------------------------------------------------------------------------ */
