@@ -125,23 +125,58 @@ __global__ void interior_dh_kernel(const DhArgs a, const PhiloxKeys keys) {
     }
 }
 
-// One thread per (draw in chunk, sequence, channel): the causal EMA down the
-// sequence, written as the split pair [hi | lo].
-__global__ void interior_ema_kernel(const float* __restrict__ du, int nd, int nseq, int seq_len,
-                                    int dm, float lam, __nv_bfloat16* __restrict__ A2) {
-    const int64_t n = static_cast<int64_t>(nd) * nseq * dm;
+// Causal EMA down each sequence, written as the split pair [hi | lo].
+// One CTA per (draw in chunk, sequence, 32 channels): lane = channel, warp w =
+// the w-th of 16 consecutive token chunks of the sequence.  Each warp runs
+// the recurrence over its chunk from zero and keeps its end state and
+// lam^length; one warp then chains the chunk ends into every chunk's true
+// starting state; each warp reruns its chunk from that state and writes the
+// result.  The recurrence is the sequential one, started at the chained
+// carry.
+constexpr int kEmaWarps = 16;
+
+__global__ void __launch_bounds__(32 * kEmaWarps)
+    interior_ema_kernel(const float* __restrict__ du, int nd, int nseq, int seq_len, int dm,
+                        float lam, __nv_bfloat16* __restrict__ A2) {
+    __shared__ float s_end[kEmaWarps][32];
+    __shared__ float s_pow[kEmaWarps][32];
+    __shared__ float s_carry[kEmaWarps][32];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int ncb = (dm + 31) / 32;
+    const int cb = blockIdx.x % ncb;
+    const int rest = blockIdx.x / ncb;
+    const int s = rest % nseq;
+    const int i = rest / nseq;
+    const int k = cb * 32 + lane;
+    const bool ok = k < dm;
+    const int clen = (seq_len + kEmaWarps - 1) / kEmaWarps;
+    const int t0 = s * seq_len + min(seq_len, w * clen);
+    const int t1 = s * seq_len + min(seq_len, (w + 1) * clen);
     const float one_m = 1.0f - lam;
-    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
-         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int k = static_cast<int>(idx % dm);
-        const int64_t rest = idx / dm;
-        const int s = static_cast<int>(rest % nseq);
-        const int i = static_cast<int>(rest / nseq);
-        float e = 0.f;
-        for (int tt = 0; tt < seq_len; ++tt) {
-            const int t = s * seq_len + tt;
+
+    float e = 0.f, pw = 1.f;
+    if (ok) {
+        for (int t = t0; t < t1; ++t) {
+            e = fmaf(lam, e, one_m * __ldg(du + chunk_row(t, i, nd) * dm + k));
+            pw *= lam;
+        }
+    }
+    s_end[w][lane] = e;
+    s_pow[w][lane] = pw;
+    __syncthreads();
+    if (w == 0) {
+        float c = 0.f;
+        for (int q = 0; q < kEmaWarps; ++q) {
+            s_carry[q][lane] = c;
+            c = fmaf(s_pow[q][lane], c, s_end[q][lane]);
+        }
+    }
+    __syncthreads();
+    if (ok) {
+        e = s_carry[w][lane];
+        for (int t = t0; t < t1; ++t) {
             const int64_t r = chunk_row(t, i, nd);
-            e = fmaf(lam, e, one_m * du[r * dm + k]);
+            e = fmaf(lam, e, one_m * __ldg(du + r * dm + k));
             __nv_bfloat16 h, l;
             split_bf16(e, h, l);
             A2[r * 2 * dm + k] = h;
@@ -215,7 +250,8 @@ __global__ void interior_ghat_kernel(const GhatArgs a, const PhiloxKeys keys) {
 
 struct InteriorPlan {
     int64_t Tp, ldx;
-    int nd;  // draws per chunk
+    int nd;      // draws per chunk
+    bool fused;  // GEMM 1 generates its A operand on chip
     size_t off_p, off_a1, off_du, off_a2, off_dl, off_m, off_r, off_gbf, off_xbf, bytes;
 };
 
@@ -227,11 +263,12 @@ InteriorPlan interior_plan(int64_t T, int64_t d_in, int64_t C, int64_t dm, int64
     int64_t nd = ceil_div(148 * 8, ntb);
     nd = std::max<int64_t>(1, std::min<int64_t>({nd, 16, static_cast<int64_t>(K)}));
     P.nd = static_cast<int>(nd);
+    P.fused = reforward1_supported(C, dm);
     const size_t rows = static_cast<size_t>(nd * P.Tp);
     WsLayout w;
     w.take(kCtlBytes);
     P.off_p = w.take(static_cast<size_t>(T * V) * 4);
-    P.off_a1 = w.take(rows * static_cast<size_t>(2 * C) * 2);
+    P.off_a1 = w.take(P.fused ? 0 : rows * static_cast<size_t>(2 * C) * 2);
     P.off_du = w.take(rows * static_cast<size_t>(dm) * 4);
     P.off_a2 = w.take(rows * static_cast<size_t>(2 * dm) * 2);
     P.off_dl = w.take(static_cast<size_t>(K) * T * 4);
@@ -310,17 +347,26 @@ extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, cons
     for (int i0 = 0; i0 < K; i0 += P.nd) {
         const int nd = std::min(P.nd, K - i0);
         const int64_t rows = nd * P.Tp;
-        DhArgs da{y1, Ti, static_cast<int>(P.Tp), Ci, nd, nz.draw0 + static_cast<uint32_t>(i0),
-                  nz.token0, nz.layer, nz.sigma, A1};
-        interior_dh_kernel<<<grid_cap(rows * (C / 4), 256), 256, 0, s>>>(da, keys);
-        if ((st = launch_status()) != DUST_OK) return st;
-        st = gemm_bf16_launch(A1, false, 2 * C, W2, false, C, rows, d_model, 2 * C, C,
-                              static_cast<int>(ceil_div(d_model, 256)), du, d_model, status, s);
-        if (st != DUST_OK) return st;
+        if (P.fused) {
+            st = reforward1_launch(y1, W2, T, P.Tp, C, d_model, nd,
+                                   nz.draw0 + static_cast<uint32_t>(i0), nz.token0, nz.layer,
+                                   nz.sigma, keys, du, status, s);
+            if (st != DUST_OK) return st;
+        } else {
+            DhArgs da{y1, Ti, static_cast<int>(P.Tp), Ci, nd,
+                      nz.draw0 + static_cast<uint32_t>(i0), nz.token0, nz.layer, nz.sigma, A1};
+            interior_dh_kernel<<<grid_cap(rows * (C / 4), 256), 256, 0, s>>>(da, keys);
+            if ((st = launch_status()) != DUST_OK) return st;
+            st = gemm_bf16_launch(A1, false, 2 * C, W2, false, C, rows, d_model, 2 * C, C,
+                                  static_cast<int>(ceil_div(d_model, 256)), du, d_model, status,
+                                  s);
+            if (st != DUST_OK) return st;
+        }
         if (P.Tp != T)
             DUST_CUDA_TRY(cudaMemsetAsync(A2, 0, static_cast<size_t>(rows * 2 * d_model) * 2, s));
-        interior_ema_kernel<<<grid_cap(static_cast<int64_t>(nd) * nseq * d_model, 128), 128, 0, s>>>(
-            du, nd, nseq, static_cast<int>(seq_len), dmi, ema_decay, A2);
+        interior_ema_kernel<<<static_cast<unsigned>(nd * nseq * ceil_div(d_model, 32)),
+                              32 * kEmaWarps, 0, s>>>(du, nd, nseq, static_cast<int>(seq_len), dmi,
+                                                      ema_decay, A2);
         if ((st = launch_status()) != DUST_OK) return st;
         st = gemm_ce_launch(A2, 2 * d_model, W_head, d_model, rows, V, 2 * d_model, d_model, p,
                             targets, T, nd, i0, dl, status, s);

@@ -96,12 +96,12 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t j, uint32_t token, uint3
     return philox_rest(philox_draw_half(draw, token, k), philox_block_half(j, layer, k), k);
 }
 
-// ((w >> 9) + 0.5) 2^-23, exactly: the 23 high bits of w (w >> 9, taken as
-// the high word of w * 2^23 so that it runs on the multiply-add pipe) as the
-// mantissa of a float in [1, 2), minus (1 - 2^-24).  The difference
-// (2m + 1) 2^-24 has at most 24 significant bits, so the subtraction is exact.
+// ((w >> 9) + 0.5) 2^-23, exactly: the 23 high bits of w as the mantissa of
+// a float in [1, 2), minus (1 - 2^-24).  The difference (2m + 1) 2^-24 has at
+// most 24 significant bits, so the subtraction is exact.  (Shift and or run on
+// the integer ALU, leaving the multiply pipe to Philox.)
 __device__ __forceinline__ float word_to_uniform(uint32_t w) {
-    const float f = __uint_as_float(__umulhi(w, 1u << 23) + 0x3F800000u);
+    const float f = __uint_as_float((w >> 9) | 0x3F800000u);
     return __fadd_rn(f, -0x1.fffffep-1f);
 }
 
@@ -138,37 +138,20 @@ __device__ __forceinline__ float neg2_log_unit(float u) {
 }
 
 // Box-Muller pair from two words: rho = sqrt(-2 ln u_even), theta =
-// 2 pi u_odd; a_cos = rho cos theta, a_sin = rho sin theta.
-//
-// theta is reduced to a quarter turn: v = 4 u_odd, q = nearest integer to v
-// (v is never a half-integer, so the rounding has no ties), y = (pi/2)(v - q)
-// in [-pi/4, pi/4]; sin y and cos y come from short polynomials in y^2
-// (least-squares fits on Chebyshev nodes of sin(y)/y and cos(y), errors below
-// 4e-9 and 6e-11), and theta = y + q pi/2 rotates them by q quarter turns.
+// 2 pi u_odd; a_cos = rho cos theta, a_sin = rho sin theta.  With
+// theta' = 2 pi u_odd - pi in (-pi, pi), cos theta = -cos theta' and
+// sin theta = -sin theta'; sin and cos of theta' come from the hardware
+// approximations (absolute error about 4e-7 on that interval), so the normals
+// are within about 3e-6 of the exact ones at the largest radius (5.77).
 __device__ __forceinline__ void box_muller(uint32_t w_even, uint32_t w_odd, float& a_cos,
                                            float& a_sin) {
     const float x = neg2_log_unit(word_to_uniform(w_even));
-    const float rho = x * rsqrt_approx(x);
-    const float v = 4.0f * word_to_uniform(w_odd);
-    const float t = v + 12582912.0f;  // 1.5 * 2^23: rounds v to an integer
-    const float y = (v - (t - 12582912.0f)) * 1.5707963267948966f;
-    const float z = y * y;
-    float ps = fmaf(z, -0.00019515283f, 0.0083321608f);
-    ps = fmaf(z, ps, -0.16666655f);
-    ps = fmaf(z, ps, 1.0f);
-    const float sy = y * ps;
-    float pc = fmaf(z, 2.4390451e-05f, -0.0013886764f);
-    pc = fmaf(z, pc, 0.041666623f);
-    pc = fmaf(z, pc, -0.5f);
-    const float cy = fmaf(z, pc, 1.0f);
-    const uint32_t q = __float_as_uint(t) & 3u;  // quarter turns, mod 4
-    const bool odd = (q & 1u) != 0u;
-    const float c_abs = odd ? sy : cy;
-    const float s_abs = odd ? cy : sy;
-    // cos theta is negative for q = 1, 2; sin theta for q = 2, 3
-    const uint32_t rb = __float_as_uint(rho);
-    a_cos = __uint_as_float(rb ^ (((q + 1u) & 2u) << 30)) * c_abs;
-    a_sin = __uint_as_float(rb ^ ((q & 2u) << 30)) * s_abs;
+    const float neg_rho = -(x * rsqrt_approx(x));
+    const float th = fmaf(word_to_uniform(w_odd), 6.2831853071795865f, -3.1415926535897932f);
+    float s, c;
+    __sincosf(th, &s, &c);
+    a_cos = neg_rho * c;
+    a_sin = neg_rho * s;
 }
 
 __device__ __forceinline__ float4 words_to_normals(uint4 w) {

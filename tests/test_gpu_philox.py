@@ -1,7 +1,9 @@
 """The CUDA noise regenerator against the oracle's own Philox (GPU).
 
-Words must match bit for bit; normals within 2e-6 absolute (fp32 CUDA logf,
-sqrtf and sincospif against the oracle's float64 Box-Muller).
+Words must match bit for bit; normals within 5e-6 absolute: the kernels' fp32
+Box-Muller (own logarithm to about 1e-7 relative, hardware sin/cos with about
+4e-7 absolute error on (-pi, pi)) against the oracle's float64 one, at radii
+up to sqrt(48 ln 2) = 5.77.
 """
 import numpy as np
 import pytest
@@ -30,7 +32,7 @@ def test_words_bit_exact(dust, orc, seed, layer, draw, token0, ntok, nchan):
 def test_normals_close(dust, orc, seed, layer, draw, token0, ntok, nchan):
     w, a = dust.philox_fill(seed, layer, draw, token0, ntok, nchan)
     ref = orc.noise(seed, layer, draw, token0, ntok, nchan)
-    np.testing.assert_allclose(a.cpu().numpy().astype(np.float64), ref, rtol=0, atol=2e-6)
+    np.testing.assert_allclose(a.cpu().numpy().astype(np.float64), ref, rtol=0, atol=5e-6)
 
 
 def test_large_fill_statistics(dust):
