@@ -116,6 +116,23 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def rank_token0(rank, tokens_per_rank):
+    """Global index of a rank's first token: every rank estimates its own
+    batch, and the noise (keyed by global token) differs between ranks."""
+    return rank * tokens_per_rank
+
+
+def max_over_ranks(value, dist=None):
+    """The slowest rank's value (the job's time); the value itself on one rank."""
+    import torch
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------- workloads ----
 def make_workload(name, device, rank):
     import torch
@@ -131,7 +148,7 @@ def make_workload(name, device, rank):
         T = p["T"]
         return {
             "kind": "head", "name": name, "T": T, "V": p["V"], "d": p["d"], "K": p["K"],
-            "sigma": p["sigma"], "seq_len": p["seq_len"], "token0": rank * T,
+            "sigma": p["sigma"], "seq_len": p["seq_len"], "token0": rank_token0(rank, T),
             "host": {"logits": wl["z"], "targets": wl["targets"],
                      "x": W.bf16_round(wl["x"]) if p["x_bf16"] else wl["x"]},
             "x_bf16": p["x_bf16"],
@@ -145,7 +162,8 @@ def make_workload(name, device, rank):
         return {
             "kind": "interior", "name": name, "T": p["T"], "K": p["K"], "sigma": p["sigma"],
             "gamma": p["gamma"], "seq_len": p["seq_len"], "lam": wl["lam"], "C": p["C"],
-            "d_in": p["d_in"], "d_model": p["d_model"], "V": p["V"], "token0": rank * p["T"],
+            "d_in": p["d_in"], "d_model": p["d_model"], "V": p["V"],
+            "token0": rank_token0(rank, p["T"]),
             "host": {k: wl[k] for k in ("x", "y1", "W2", "W_head", "z_clean", "targets")},
             "dev": {"x": dev(wl["x"], bf), "y1": dev(wl["y1"]), "W2": dev(wl["W2"], bf),
                     "W_head": dev(wl["W_head"], bf), "z_clean": dev(wl["z_clean"]),
@@ -377,10 +395,7 @@ def run_dust(args):
     kernel_ms = timer.total_ms() / max(args.steps, 1)
     if dust.workspace_status(ws) != 0:
         raise SystemExit("kernel status word set during the timed steps")
-    t = torch.tensor([ms], device=device, dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dist if world > 1 else None)
     value = evals * world * args.steps / (ms_max * 1e-3)
 
     # End to end through the public API from pinned host buffers: the step's
@@ -452,10 +467,8 @@ def run_dust(args):
         f1.record(stream)
         f1.synchronize()
         barrier()
-        te = torch.tensor([f0.elapsed_time(f1)], device=device, dtype=torch.float64)
-        if world > 1:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        e2e = {"value": evals * world * args.steps / (float(te.item()) * 1e-3), "unit": UNIT,
+        te = max_over_ranks(f0.elapsed_time(f1), dist if world > 1 else None)
+        e2e = {"value": evals * world * args.steps / (te * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     cpu = None
