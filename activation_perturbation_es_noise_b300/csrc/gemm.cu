@@ -28,6 +28,10 @@
 #include "internal.h"
 
 namespace dust {
+
+bool encode_bf16_2d(CUtensorMap* map, const void* ptr, int64_t inner, int64_t outer,
+                    int64_t stride_elems, uint32_t box_inner, uint32_t box_outer);
+
 namespace {
 
 constexpr int kBM = 128;
@@ -37,8 +41,17 @@ constexpr int kStages = 4;
 constexpr uint32_t kABytes = kBM * kBK * 2;
 constexpr uint32_t kBBytes = kBN * kBK * 2;
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 + 256;
-constexpr int kThreads = 192;
+// The cross-entropy epilogue also stages the softmax rows it needs: two
+// 128 x 32 fp32 tiles (128-byte swizzle), filled by TMA from a seventh warp.
+constexpr uint32_t kPTile = kBM * 32 * 4;
+template <int EPI>
+constexpr uint32_t smem_bytes() {
+    return kStages * kStageBytes + (EPI == 1 ? 2 * kPTile : 0) + 1024 + 256;
+}
+template <int EPI>
+constexpr int threads_of() {
+    return EPI == 1 ? 224 : 192;
+}
 
 enum { EPI_STORE = 0, EPI_CE = 1 };
 
@@ -61,7 +74,7 @@ struct EpiStore {
 // CE(z + dz) - CE(z) because sum_v p_{t,v} = 1.  Summing the small terms
 // e^dz - 1 keeps the fp32 rounding of the sum far below the loss change.
 struct EpiCE {
-    const float* p;  // T x V softmax of the clean logits
+    const float* p;  // T x V softmax of the clean logits (staged by TMA)
     const int32_t* targets;
     float* dl;       // K x T
     int T, V, ndraw, i0;
@@ -88,19 +101,23 @@ __device__ __forceinline__ float expm1_small(float x) {
 }
 
 template <bool A_MN, bool B_MN, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of<EPI>(), 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
-                     const GemmShape sh, const EpiStore es, const EpiCE ec, uint32_t* status) {
+                     const __grid_constant__ CUtensorMap tp, const GemmShape sh,
+                     const EpiStore es, const EpiCE ec, uint32_t* status) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_gen = smem_raw + (base - raw);
-    const uint32_t bars = base + kStages * kStageBytes;
+    const uint32_t pbuf = base + kStages * kStageBytes;  // CE epilogue only
+    const uint32_t bars = pbuf + (EPI == EPI_CE ? 2 * kPTile : 0);
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
     auto accf_bar = [&](int b) { return bars + 8u * (2 * kStages + b); };
     auto acce_bar = [&](int b) { return bars + 8u * (2 * kStages + 2 + b); };
-    const uint32_t tmem_slot = bars + 8u * (2 * kStages + 4);
+    auto pfull_bar = [&](int b) { return bars + 8u * (2 * kStages + 4 + b); };
+    auto pempty_bar = [&](int b) { return bars + 8u * (2 * kStages + 6 + b); };
+    const uint32_t tmem_slot = bars + 8u * (2 * kStages + 8);
     volatile uint32_t* tmem_slot_gen =
         reinterpret_cast<volatile uint32_t*>(base_gen + (tmem_slot - base));
 
@@ -120,10 +137,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
             mbar_init(acce_bar(b), 4);
+            mbar_init(pfull_bar(b), 1);
+            mbar_init(pempty_bar(b), 4);
         }
         mbar_fence_init();
         tma_prefetch_desc(&ta);
         tma_prefetch_desc(&tb);
+        if (EPI == EPI_CE) tma_prefetch_desc(&tp);
     }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
@@ -201,6 +221,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_commit(accf_bar(buf));  // also on failure, so nobody waits forever
             }
         }
+    } else if (warp == 6) {
+        // CE epilogue only: the softmax tile of every 32-column chunk, two
+        // chunks ahead, rows = the tile's 128 tokens.
+        if (EPI == EPI_CE && lane == 0) {
+            const int tok0 = (blockIdx.x / ec.ndraw) * kBM;
+            const int nq = nt_count * (kBN / 32);
+            for (int q = 0; q < nq; ++q) {
+                const int b = q & 1;
+                if (q >= 2 && !mbar_wait(pempty_bar(b), ((q >> 1) - 1) & 1u, status)) break;
+                mbar_arrive_expect_tx(pfull_bar(b), kPTile);
+                const int col = (nt0 + q / (kBN / 32)) * kBN + (q % (kBN / 32)) * 32;
+                tma_load_2d(pbuf + b * kPTile, &tp, col, tok0, pfull_bar(b));
+            }
+        }
     } else {
         // Epilogue warps 2..5; warp w may read TMEM lanes 32 (w % 4) .. + 31.
         const int quarter = warp & 3;
@@ -255,31 +289,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     if (col0 + q < sh.N) drow[col0 + q] = __uint_as_float(r[q]);
                             }
                         }
-                    } else if (ce_valid) {
-                        const float* prow = ec.p + static_cast<int64_t>(ce_t) * ec.V;
-                        if (((ec.V & 3) == 0) && col0 + 32 <= ec.V) {
+                    } else {
+                        // chunk q = j * 8 + c uses p buffer q & 1
+                        const int q = j * (kBN / 32) + c;
+                        const int pb = q & 1;
+                        bool pg = mbar_wait(pfull_bar(pb), (q >> 1) & 1u, status);
+                        pg = __all_sync(0xFFFFFFFFu, pg);
+                        if (pg && ce_valid) {
+                            const uint32_t prow = pbuf + pb * kPTile + rit * 128u;
 #pragma unroll
-                            for (int q = 0; q < 32; q += 4) {
-                                const float4 p4 = __ldg(reinterpret_cast<const float4*>(prow + col0 + q));
-                                const float z0 = __uint_as_float(r[q]), z1 = __uint_as_float(r[q + 1]);
-                                const float z2 = __uint_as_float(r[q + 2]), z3 = __uint_as_float(r[q + 3]);
-                                ce_sum = fmaf(p4.x, expm1_small(z0), ce_sum);
-                                ce_sum = fmaf(p4.y, expm1_small(z1), ce_sum);
-                                ce_sum = fmaf(p4.z, expm1_small(z2), ce_sum);
-                                ce_sum = fmaf(p4.w, expm1_small(z3), ce_sum);
+                            for (int g4 = 0; g4 < 8; ++g4) {
+                                float4 p4;
+                                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                             : "=f"(p4.x), "=f"(p4.y), "=f"(p4.z), "=f"(p4.w)
+                                             : "r"(prow + (((g4 ^ (rit & 7)) & 7u) << 4)));
+                                const int qq = 4 * g4;
+                                ce_sum = fmaf(p4.x, expm1_small(__uint_as_float(r[qq])), ce_sum);
+                                ce_sum = fmaf(p4.y, expm1_small(__uint_as_float(r[qq + 1])), ce_sum);
+                                ce_sum = fmaf(p4.z, expm1_small(__uint_as_float(r[qq + 2])), ce_sum);
+                                ce_sum = fmaf(p4.w, expm1_small(__uint_as_float(r[qq + 3])), ce_sum);
                             }
-                        } else {
-#pragma unroll
-                            for (int q = 0; q < 32; ++q)
-                                if (col0 + q < ec.V)
-                                    ce_sum = fmaf(__ldg(prow + col0 + q),
-                                                  expm1_small(__uint_as_float(r[q])), ce_sum);
                         }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(pempty_bar(pb));
+                        if (!ce_valid) continue;
                         const int yo = ce_y - col0;
                         if (yo >= 0 && yo < 32) {
 #pragma unroll
-                            for (int q = 0; q < 32; ++q)
-                                if (q == yo) ce_zy = __uint_as_float(r[q]);
+                            for (int qq = 0; qq < 32; ++qq)
+                                if (qq == yo) ce_zy = __uint_as_float(r[qq]);
                         }
                     }
                 }
@@ -296,7 +334,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+bool encode_operands(CUtensorMap* ta, CUtensorMap* tb, const void* A, bool a_mn, int64_t lda,
+                     const void* B, bool b_mn, int64_t ldb, int64_t M, int64_t N, int64_t K,
+                     int64_t b_kmod) {
+    const int64_t KB = b_kmod > 0 ? b_kmod : K;
+    bool ok = a_mn ? encode_bf16_2d(ta, A, M, K, lda, 64, kBK)
+                   : encode_bf16_2d(ta, A, K, M, lda, kBK, kBM);
+    ok = ok && (b_mn ? encode_bf16_2d(tb, B, N, KB, ldb, 64, kBK)
+                     : encode_bf16_2d(tb, B, KB, N, ldb, kBK, kBN));
+    return ok;
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+dust_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tp,
+                     const GemmShape& sh, const EpiStore& es, const EpiCE& ec, uint32_t* status,
+                     cudaStream_t s) {
+    auto kern = gemm_bf16_kernel<A_MN, B_MN, EPI>;
+    constexpr uint32_t smem = smem_bytes<EPI>();
+    static bool attr_set = false;
+    if (!attr_set) {
+        DUST_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem)));
+        attr_set = true;
+    }
+    const int ntiles = (sh.N + kBN - 1) / kBN;
+    dim3 grid(static_cast<unsigned>(ceil_div(sh.M, kBM)),
+              static_cast<unsigned>(ceil_div(ntiles, sh.n_per_cta)));
+    kern<<<grid, threads_of<EPI>(), smem, s>>>(ta, tb, tp, sh, es, ec, status);
+    return launch_status();
+}
+
+}  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (fn == nullptr) {
         void* p = nullptr;
@@ -325,36 +395,6 @@ bool encode_bf16_2d(CUtensorMap* map, const void* ptr, int64_t inner, int64_t ou
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
-
-bool encode_operands(CUtensorMap* ta, CUtensorMap* tb, const void* A, bool a_mn, int64_t lda,
-                     const void* B, bool b_mn, int64_t ldb, int64_t M, int64_t N, int64_t K,
-                     int64_t b_kmod) {
-    const int64_t KB = b_kmod > 0 ? b_kmod : K;
-    bool ok = a_mn ? encode_bf16_2d(ta, A, M, K, lda, 64, kBK)
-                   : encode_bf16_2d(ta, A, K, M, lda, kBK, kBM);
-    ok = ok && (b_mn ? encode_bf16_2d(tb, B, N, KB, ldb, 64, kBK)
-                     : encode_bf16_2d(tb, B, KB, N, ldb, kBK, kBN));
-    return ok;
-}
-
-template <bool A_MN, bool B_MN, int EPI>
-dust_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmShape& sh,
-                     const EpiStore& es, const EpiCE& ec, uint32_t* status, cudaStream_t s) {
-    auto kern = gemm_bf16_kernel<A_MN, B_MN, EPI>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        DUST_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(kSmemBytes)));
-        attr_set = true;
-    }
-    const int ntiles = (sh.N + kBN - 1) / kBN;
-    dim3 grid(static_cast<unsigned>(ceil_div(sh.M, kBM)),
-              static_cast<unsigned>(ceil_div(ntiles, sh.n_per_cta)));
-    kern<<<grid, kThreads, kSmemBytes, s>>>(ta, tb, sh, es, ec, status);
-    return launch_status();
-}
-
-}  // namespace
 
 __global__ void f32_to_bf16_kernel(const float* __restrict__ in, int64_t rows, int64_t cols,
                                    int64_t ld_in, __nv_bfloat16* __restrict__ out,
@@ -411,14 +451,14 @@ dust_status gemm_bf16_launch(const void* A, bool a_mn, int64_t lda, const void* 
                  static_cast<int>(b_kmod)};
     EpiStore es{G, ldg};
     EpiCE ec{};
-    if (a_mn && b_mn) return launch_t<true, true, EPI_STORE>(ta, tb, sh, es, ec, status, s);
-    if (a_mn) return launch_t<true, false, EPI_STORE>(ta, tb, sh, es, ec, status, s);
-    if (b_mn) return launch_t<false, true, EPI_STORE>(ta, tb, sh, es, ec, status, s);
-    return launch_t<false, false, EPI_STORE>(ta, tb, sh, es, ec, status, s);
+    if (a_mn && b_mn) return launch_t<true, true, EPI_STORE>(ta, tb, ta, sh, es, ec, status, s);
+    if (a_mn) return launch_t<true, false, EPI_STORE>(ta, tb, ta, sh, es, ec, status, s);
+    if (b_mn) return launch_t<false, true, EPI_STORE>(ta, tb, ta, sh, es, ec, status, s);
+    return launch_t<false, false, EPI_STORE>(ta, tb, ta, sh, es, ec, status, s);
 }
 
 dust_status gemm_ce_launch(const void* A, int64_t lda, const void* B, int64_t ldb, int64_t M,
-                           int64_t V, int64_t K, int64_t b_kmod, const float* p,
+                           int64_t V, int64_t K, int64_t b_kmod, const float* p, int64_t ldp,
                            const int32_t* targets, int64_t T, int ndraw, int i0, float* dl,
                            uint32_t* status, cudaStream_t s) {
     CUtensorMap ta, tb;
@@ -429,8 +469,23 @@ dust_status gemm_ce_launch(const void* A, int64_t lda, const void* B, int64_t ld
                  static_cast<int>(b_kmod)};
     EpiStore es{};
     EpiCE ec{p, targets, dl, static_cast<int>(T), static_cast<int>(V), ndraw, i0};
+    // softmax rows: T x V fp32, row stride ldp (a multiple of 4), 128 x 32 boxes
+    CUtensorMap tp;
+    {
+        auto enc = tensor_map_encoder();
+        if (enc == nullptr) return DUST_ERR_CUDA;
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(T)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldp) * 4};
+        cuuint32_t box[2] = {32, kBM};
+        cuuint32_t estr[2] = {1, 1};
+        if (enc(&tp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(p), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return DUST_ERR_CUDA;
+    }
     timer_begin(s);
-    const dust_status st = launch_t<false, false, EPI_CE>(ta, tb, sh, es, ec, status, s);
+    const dust_status st = launch_t<false, false, EPI_CE>(ta, tb, tp, sh, es, ec, status, s);
     timer_end(s);
     return st;
 }

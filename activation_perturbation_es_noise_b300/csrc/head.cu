@@ -160,6 +160,9 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
     BlockHalf bh[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) bh[b] = philox_block_half(b * NT + tid, A.layer, keys);
+    // Blocks past the vocabulary (only in the last block row) get zero noise;
+    // their probabilities are zero, so they add nothing.
+    const bool full = NB * NT <= A.nblk;
 
     float s1[NB][4], s0[NB][4];
 #pragma unroll
@@ -172,22 +175,32 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
 #pragma unroll 1
     for (int i = i_begin; i < i_end; ++i) {
         const DrawHalf dh = philox_draw_half(A.draw0 + static_cast<uint32_t>(i), token, keys);
+        // All NB blocks advance in lockstep (words, then normals, then the
+        // loss terms) so that their independent chains interleave.
+        uint4 w[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) w[b] = philox_rest(dh, bh[b], keys);
         float a[NB][4];
-        float part = 0.f;
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-            if (b * NT + tid < A.nblk) {
-                const float4 n = words_to_normals(philox_rest(dh, bh[b], keys));
-                a[b][0] = n.x; a[b][1] = n.y; a[b][2] = n.z; a[b][3] = n.w;
-                part = fmaf(p[b][0], ex2_approx(A.sig_l2e * n.x), part);
-                part = fmaf(p[b][1], ex2_approx(A.sig_l2e * n.y), part);
-                part = fmaf(p[b][2], ex2_approx(A.sig_l2e * n.z), part);
-                part = fmaf(p[b][3], ex2_approx(A.sig_l2e * n.w), part);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) a[b][k] = 0.f;
-            }
+            const float4 n = words_to_normals(w[b]);
+            const bool valid = full || (b * NT + tid < A.nblk);
+            a[b][0] = valid ? n.x : 0.f;
+            a[b][1] = valid ? n.y : 0.f;
+            a[b][2] = valid ? n.z : 0.f;
+            a[b][3] = valid ? n.w : 0.f;
         }
+        float pb[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            float q = p[b][0] * ex2_approx(A.sig_l2e * a[b][0]);
+            q = fmaf(p[b][1], ex2_approx(A.sig_l2e * a[b][1]), q);
+            q = fmaf(p[b][2], ex2_approx(A.sig_l2e * a[b][2]), q);
+            pb[b] = fmaf(p[b][3], ex2_approx(A.sig_l2e * a[b][3]), q);
+        }
+        float part = pb[0];
+#pragma unroll
+        for (int b = 1; b < NB; ++b) part += pb[b];
         float ay = 0.f;
         if (owner) {
 #pragma unroll

@@ -62,12 +62,13 @@ __device__ __forceinline__ int64_t chunk_row(int t, int i, int nd) {
     return (static_cast<int64_t>(t >> 7) * nd + i) * kRowBlock + (t & 127);
 }
 
-// p = softmax(z) per row, fp32.
-__global__ void softmax_rows_kernel(const float* __restrict__ z, int V, float* __restrict__ p) {
+// p = softmax(z) per row, fp32, rows ldp apart (padding columns zero).
+__global__ void softmax_rows_kernel(const float* __restrict__ z, int V, int ldp,
+                                    float* __restrict__ p) {
     __shared__ float red[32];
     const int64_t t = blockIdx.x;
     const float* zr = z + t * V;
-    float* pr = p + t * V;
+    float* pr = p + t * ldp;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     float m = -INFINITY;
     for (int v = threadIdx.x; v < V; v += blockDim.x) m = fmaxf(m, zr[v]);
@@ -85,7 +86,7 @@ __global__ void softmax_rows_kernel(const float* __restrict__ z, int V, float* _
     s = 0.f;
     for (int w = 0; w < nw; ++w) s += red[w];
     const float inv = 1.0f / s;
-    for (int v = threadIdx.x; v < V; v += blockDim.x) pr[v] = expf(zr[v] - m) * inv;
+    for (int v = threadIdx.x; v < ldp; v += blockDim.x) pr[v] = v < V ? expf(zr[v] - m) * inv : 0.f;
 }
 
 struct DhArgs {
@@ -218,33 +219,51 @@ struct GhatArgs {
     __nv_bfloat16* gbf;  // T x C
 };
 
-// One thread per (token, channel block): g = -(1/(K sigma)) sum_i r a, with
-// the noise regenerated from its counters.
+// One thread per (token, two channel blocks j and j + C/8): g =
+// -(1/(K sigma)) sum_i r a, with the noise regenerated from its counters.  The
+// two blocks advance in lockstep so that their Philox chains interleave.
 __global__ void interior_ghat_kernel(const GhatArgs a, const PhiloxKeys keys) {
-    const int nblk = a.C >> 2;
-    const int64_t n = static_cast<int64_t>(a.T) * nblk;
+    const int half = a.C >> 3;  // channel blocks per half row
+    const int64_t n = static_cast<int64_t>(a.T) * half;
     for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
          idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int j = static_cast<int>(idx % nblk);
-        const int t = static_cast<int>(idx / nblk);
-        const BlockHalf bh = philox_block_half(j, a.layer, keys);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int i = 0; i < a.K; ++i) {
-            const float ri = __ldg(a.r + static_cast<int64_t>(i) * a.T + t);
-            const float4 nrm = words_to_normals(
-                philox_rest(philox_draw_half(a.draw0 + i, a.token0 + t, keys), bh, keys));
-            acc.x = fmaf(ri, nrm.x, acc.x);
-            acc.y = fmaf(ri, nrm.y, acc.y);
-            acc.z = fmaf(ri, nrm.z, acc.z);
-            acc.w = fmaf(ri, nrm.w, acc.w);
+        const int j0 = static_cast<int>(idx % half);
+        const int t = static_cast<int>(idx / half);
+        const int jb[2] = {j0, j0 + half};
+        BlockHalf bh[2];
+        float4 acc[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            bh[u] = philox_block_half(jb[u], a.layer, keys);
+            acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        const float4 g = make_float4(acc.x * a.neg_inv_ks, acc.y * a.neg_inv_ks,
-                                     acc.z * a.neg_inv_ks, acc.w * a.neg_inv_ks);
-        const int64_t off = static_cast<int64_t>(t) * a.C + 4 * j;
-        if (a.g_hat) *reinterpret_cast<float4*>(a.g_hat + off) = g;
-        *reinterpret_cast<uint2*>(a.gbf + off) =
-            pack4(__float2bfloat16_rn(g.x), __float2bfloat16_rn(g.y), __float2bfloat16_rn(g.z),
-                  __float2bfloat16_rn(g.w));
+        const float* rcol = a.r + t;
+#pragma unroll 2
+        for (int i = 0; i < a.K; ++i) {
+            const float ri = __ldg(rcol + static_cast<int64_t>(i) * a.T);
+            const DrawHalf dh = philox_draw_half(a.draw0 + i, a.token0 + t, keys);
+            uint4 w[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) w[u] = philox_rest(dh, bh[u], keys);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const float4 nrm = words_to_normals(w[u]);
+                acc[u].x = fmaf(ri, nrm.x, acc[u].x);
+                acc[u].y = fmaf(ri, nrm.y, acc[u].y);
+                acc[u].z = fmaf(ri, nrm.z, acc[u].z);
+                acc[u].w = fmaf(ri, nrm.w, acc[u].w);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const float4 g = make_float4(acc[u].x * a.neg_inv_ks, acc[u].y * a.neg_inv_ks,
+                                         acc[u].z * a.neg_inv_ks, acc[u].w * a.neg_inv_ks);
+            const int64_t off = static_cast<int64_t>(t) * a.C + 4 * jb[u];
+            if (a.g_hat) *reinterpret_cast<float4*>(a.g_hat + off) = g;
+            *reinterpret_cast<uint2*>(a.gbf + off) =
+                pack4(__float2bfloat16_rn(g.x), __float2bfloat16_rn(g.y),
+                      __float2bfloat16_rn(g.z), __float2bfloat16_rn(g.w));
+        }
     }
 }
 
@@ -252,7 +271,7 @@ struct InteriorPlan {
     int64_t Tp, ldx;
     int nd;      // draws per chunk
     bool fused;  // GEMM 1 generates its A operand on chip
-    size_t off_p, off_a1, off_du, off_a2, off_dl, off_m, off_r, off_gbf, off_xbf, bytes;
+    size_t off_p, off_h0, off_a1, off_du, off_a2, off_dl, off_m, off_r, off_gbf, off_xbf, bytes;
 };
 
 InteriorPlan interior_plan(int64_t T, int64_t d_in, int64_t C, int64_t dm, int64_t V, uint32_t K) {
@@ -267,7 +286,8 @@ InteriorPlan interior_plan(int64_t T, int64_t d_in, int64_t C, int64_t dm, int64
     const size_t rows = static_cast<size_t>(nd * P.Tp);
     WsLayout w;
     w.take(kCtlBytes);
-    P.off_p = w.take(static_cast<size_t>(T * V) * 4);
+    P.off_p = w.take(static_cast<size_t>(T * round_up(V, 4)) * 4);
+    P.off_h0 = w.take(P.fused ? static_cast<size_t>(T * C) * 4 : 0);
     P.off_a1 = w.take(P.fused ? 0 : rows * static_cast<size_t>(2 * C) * 2);
     P.off_du = w.take(rows * static_cast<size_t>(dm) * 4);
     P.off_a2 = w.take(rows * static_cast<size_t>(2 * dm) * 2);
@@ -340,15 +360,19 @@ extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, cons
     const PhiloxKeys keys = philox_round_keys(nz.seed);
     dust_status st;
 
-    softmax_rows_kernel<<<static_cast<unsigned>(T), 256, 0, s>>>(z_clean, static_cast<int>(V), p);
+    const int64_t ldp = round_up(V, 4);
+    softmax_rows_kernel<<<static_cast<unsigned>(T), 256, 0, s>>>(z_clean, static_cast<int>(V),
+                                                                 static_cast<int>(ldp), p);
     if ((st = launch_status()) != DUST_OK) return st;
+    float* h0 = reinterpret_cast<float*>(w + P.off_h0);
+    if (P.fused && (st = gelu_launch(y1, T * C, h0, s)) != DUST_OK) return st;
 
     const int nseq = static_cast<int>(T / seq_len);
     for (int i0 = 0; i0 < K; i0 += P.nd) {
         const int nd = std::min(P.nd, K - i0);
         const int64_t rows = nd * P.Tp;
         if (P.fused) {
-            st = reforward1_launch(y1, W2, T, P.Tp, C, d_model, nd,
+            st = reforward1_launch(y1, h0, W2, T, P.Tp, C, d_model, nd,
                                    nz.draw0 + static_cast<uint32_t>(i0), nz.token0, nz.layer,
                                    nz.sigma, keys, du, status, s);
             if (st != DUST_OK) return st;
@@ -369,7 +393,7 @@ extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, cons
                                                       ema_decay, A2);
         if ((st = launch_status()) != DUST_OK) return st;
         st = gemm_ce_launch(A2, 2 * d_model, W_head, d_model, rows, V, 2 * d_model, d_model, p,
-                            targets, T, nd, i0, dl, status, s);
+                            ldp, targets, T, nd, i0, dl, status, s);
         if (st != DUST_OK) return st;
     }
 
@@ -379,7 +403,7 @@ extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, cons
     if ((st = launch_status()) != DUST_OK) return st;
     GhatArgs ga{r, Ti, Ci, K, nz.draw0, nz.token0, nz.layer,
                 static_cast<float>(-1.0 / (static_cast<double>(K) * nz.sigma)), g_hat, gbf};
-    interior_ghat_kernel<<<grid_cap(T * (C / 4), 256), 256, 0, s>>>(ga, keys);
+    interior_ghat_kernel<<<grid_cap(T * (C / 8), 256), 256, 0, s>>>(ga, keys);
     if ((st = launch_status()) != DUST_OK) return st;
 
     const void* xb = x;

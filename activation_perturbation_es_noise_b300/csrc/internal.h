@@ -3,6 +3,7 @@
 // another (the outer-product GEMM, the bf16 conversion).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -80,11 +81,28 @@ dust_status gemm_bf16_launch(const void* A, bool a_mn, int64_t lda, const void* 
 // Same contraction (both operands K-major) ending in the cross-entropy
 // epilogue: rows ordered (token block of 128, draw, token in block) for
 // ndraw draws starting at draw index i0; writes dl[(i0 + i) T + t] =
-// log sum_v p[t][v] exp(dz_v) - dz_{targets[t]}.
+// log sum_v p[t][v] exp(dz_v) - dz_{targets[t]}; p has row stride ldp, a
+// multiple of 4.
 dust_status gemm_ce_launch(const void* A, int64_t lda, const void* B, int64_t ldb, int64_t M,
-                           int64_t V, int64_t K, int64_t b_kmod, const float* p,
+                           int64_t V, int64_t K, int64_t b_kmod, const float* p, int64_t ldp,
                            const int32_t* targets, int64_t T, int ndraw, int i0, float* dl,
                            uint32_t* status, cudaStream_t s);
+
+// 2-D bf16 TMA descriptor (inner x outer elements, row stride in elements),
+// 128-byte swizzle, box box_inner x box_outer, zero fill out of range.
+bool encode_bf16_2d(CUtensorMap* map, const void* ptr, int64_t inner, int64_t outer,
+                    int64_t stride_elems, uint32_t box_inner, uint32_t box_outer);
+
+struct PhiloxKeys;
+
+// Interior GEMM 1 with its A operand (the GELU difference of the perturbed
+// output, split bf16) generated on chip: du = dh W2^T for nd draws.
+bool reforward1_supported(int64_t C, int64_t dm);
+dust_status gelu_launch(const float* y, int64_t n, float* h, cudaStream_t s);
+dust_status reforward1_launch(const float* y1, const float* h0, const void* W2, int64_t T, int64_t Tp, int64_t C,
+                              int64_t dm, int nd, uint32_t draw_first, uint32_t token0,
+                              uint32_t layer, float sigma, const PhiloxKeys& keys, float* du,
+                              uint32_t* status, cudaStream_t s);
 
 // rows x cols fp32 (row stride ld_in) -> bf16 (row stride ld_out, padding
 // columns set to zero).

@@ -1,0 +1,269 @@
+// reforward.cu -- the first contraction of the interior layer's re-forward,
+// with its A operand generated on chip.
+//
+// A draw perturbs the layer output y1 and only the part after the layer is
+// re-run (laoyaoba.com article, section 机制拆解; Dust translation,
+// hn.213312.xyz, §2.3).  The first step after the layer is
+//   du = dh W2^T,  dh = GELU(y1 + sigma a) - GELU(y1),
+// with the noise a regenerated from its counter.  Instead of writing dh to
+// memory and reading it back, producer warps compute each 128-token x
+// 64-channel slice of dh, split it into bf16 hi and lo halves and store both
+// straight into shared memory in the 128-byte-swizzled K-major layout the
+// tensor cores read; W2's matching slice arrives by TMA.  One thread issues
+// tcgen05.mma for hi and lo into the same fp32 accumulator in tensor memory
+// (d_model <= 512 columns), so dh never leaves the chip and the noise and GELU
+// arithmetic overlaps the MMAs of the previous slice.
+//
+// Rows are ordered (token block of 128, draw, token in block) like the rest of
+// the interior pipeline; the output du (rows x d_model fp32) feeds the EMA.
+#include "dust_common.cuh"
+#include "internal.h"
+#include "noise.cuh"
+
+namespace dust {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kStages = 2;
+constexpr int kProducerWarps = 16;
+constexpr int kThreads = 32 * (2 + kProducerWarps);
+constexpr uint32_t kATile = kBM * kBK * 2;           // 16 KB per half
+constexpr uint32_t kBTile = 512 * kBK * 2;           // 64 KB: up to 512 rows of W2
+constexpr uint32_t kStageBytes = 2 * kATile + kBTile;  // 96 KB
+constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 + 256;
+
+struct RefArgs {
+    const float* y1;  // T x C
+    const float* h0;  // T x C: GELU(y1)
+    float* du;        // rows x dm
+    int T, C, dm, nd;
+    uint32_t draw_first, token0, layer;
+    float sigma;
+    uint32_t* status;
+};
+
+__device__ __forceinline__ float gelu_erf(float u) {
+    return 0.5f * u * (1.0f + erff(u * 0.70710678118654752f));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void fence_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t b) {
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    reforward1_kernel(const __grid_constant__ CUtensorMap tw2, const RefArgs a,
+                      const PhiloxKeys keys) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* base_gen = smem_raw + (base - raw);
+    const uint32_t bars = base + kStages * kStageBytes;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
+    const uint32_t acc_bar = bars + 16u * kStages;
+    const uint32_t tmem_slot = acc_bar + 8u;
+    volatile uint32_t* tmem_slot_gen =
+        reinterpret_cast<volatile uint32_t*>(base_gen + (tmem_slot - base));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int mt = blockIdx.x;
+    const int tb = mt / a.nd;          // token block
+    const int di = mt - tb * a.nd;     // draw within the chunk
+    const int nk = a.C / kBK;
+    const int ngroups = (a.dm + 255) / 256;
+    const uint32_t b_bytes = static_cast<uint32_t>(ngroups) * 256u * kBK * 2u;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 32 * kProducerWarps + 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(acc_bar, 1);
+        mbar_fence_init();
+        tma_prefetch_desc(&tw2);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot_gen;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % kStages;
+                const uint32_t ph = (kb / kStages) & 1u;
+                if (kb >= kStages && !mbar_wait(empty_bar(s), ph ^ 1u, a.status)) break;
+                mbar_arrive_expect_tx(full_bar(s), b_bytes);
+                const uint32_t b_dst = base + s * kStageBytes + 2 * kATile;
+                for (int g = 0; g < ngroups; ++g)
+                    tma_load_2d(b_dst + g * (256u * kBK * 2u), &tw2, kb * kBK, g * 256, full_bar(s));
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kBM, 256, false, false);
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % kStages;
+                const uint32_t ph = (kb / kStages) & 1u;
+                if (!mbar_wait(full_bar(s), ph, a.status)) break;
+                tc_fence_after();
+                const uint32_t st = base + s * kStageBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint64_t ad = sdesc_sw128(st + h * kATile + kk * 32u, 16u, 1024u);
+                        for (int g = 0; g < ngroups; ++g) {
+                            const uint64_t bd = sdesc_sw128(
+                                st + 2 * kATile + g * (256u * kBK * 2u) + kk * 32u, 16u, 1024u);
+                            umma_bf16(tmem + g * 256, ad, bd, idesc,
+                                      (kb | kk | h) != 0 ? 1u : 0u);
+                        }
+                    }
+                }
+                umma_commit(empty_bar(s));
+            }
+            umma_commit(acc_bar);
+        }
+    } else {
+        // Producers: thread p owns channel block jj = p % 16 of the slice and
+        // rows p / 16 + R m, R = 2 kProducerWarps.
+        const int p = threadIdx.x - 64;
+        const int jj = p & 15;
+        const int r0 = p >> 4;  // 0 .. 2 kProducerWarps - 1
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % kStages;
+            const uint32_t ph = (kb / kStages) & 1u;
+            if (kb >= kStages && !mbar_wait(empty_bar(s), ph ^ 1u, a.status)) break;
+            const uint32_t st = base + s * kStageBytes;
+            const int j = kb * (kBK / 4) + jj;  // global channel block
+            const BlockHalf bhalf = philox_block_half(j, a.layer, keys);
+            constexpr int kRows = kBM / (2 * kProducerWarps);  // rows per thread
+            // Issue the loads of every row first, then the arithmetic.
+            float4 yv[kRows], gv[kRows];
+#pragma unroll
+            for (int m = 0; m < kRows; ++m) {
+                const int t = tb * kBM + r0 + 2 * kProducerWarps * m;
+                if (t < a.T) {
+                    const int64_t e4 = static_cast<int64_t>(t) * (a.C / 4) + j;
+                    yv[m] = __ldg(reinterpret_cast<const float4*>(a.y1) + e4);
+                    gv[m] = __ldg(reinterpret_cast<const float4*>(a.h0) + e4);
+                } else {
+                    yv[m] = gv[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < kRows; ++m) {
+                const int r = r0 + 2 * kProducerWarps * m;
+                const int t = tb * kBM + r;
+                uint32_t hi0 = 0, hi1 = 0, lo0 = 0, lo1 = 0;
+                if (t < a.T) {
+                    const DrawHalf dhalf =
+                        philox_draw_half(a.draw_first + di, a.token0 + t, keys);
+                    const float4 nrm = words_to_normals(philox_rest(dhalf, bhalf, keys));
+                    const float4 y = yv[m], g = gv[m];
+                    const float d0 = gelu_erf(fmaf(a.sigma, nrm.x, y.x)) - g.x;
+                    const float d1 = gelu_erf(fmaf(a.sigma, nrm.y, y.y)) - g.y;
+                    const float d2 = gelu_erf(fmaf(a.sigma, nrm.z, y.z)) - g.z;
+                    const float d3 = gelu_erf(fmaf(a.sigma, nrm.w, y.w)) - g.w;
+                    const float h0 = __bfloat162float(__float2bfloat16_rn(d0));
+                    const float h1 = __bfloat162float(__float2bfloat16_rn(d1));
+                    const float h2 = __bfloat162float(__float2bfloat16_rn(d2));
+                    const float h3 = __bfloat162float(__float2bfloat16_rn(d3));
+                    hi0 = pack_bf16x2(h0, h1);
+                    hi1 = pack_bf16x2(h2, h3);
+                    lo0 = pack_bf16x2(d0 - h0, d1 - h1);
+                    lo1 = pack_bf16x2(d2 - h2, d3 - h3);
+                }
+                // 128-byte swizzle: 16-byte chunk c of row r sits at c ^ (r & 7).
+                const uint32_t off = r * 128u + ((((jj >> 1) ^ (r & 7)) & 7u) << 4) + (jj & 1) * 8u;
+                st_shared_v2(st + off, hi0, hi1);
+                st_shared_v2(st + kATile + off, lo0, lo1);
+            }
+            fence_async_shared();
+            mbar_arrive(full_bar(s));
+        }
+        // Epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31; the first four
+        // producer warps take columns 0..255, the next four 256..511.
+        bool ok = mbar_wait(acc_bar, 0, a.status);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        tc_fence_after();
+        const int quarter = warp & 3;
+        const int g = (warp - 2) >> 2;  // warps 2..9 store, the rest are done
+        if (ok && g < ngroups && g < 2) {
+            const int rit = quarter * 32 + lane;
+            const int64_t row = static_cast<int64_t>(mt) * kBM + rit;
+            float* drow = a.du + row * a.dm;
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+                const int col0 = g * 256 + c * 32;
+                if (col0 >= a.dm) break;
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + col0, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 32; q += 4)
+                    *reinterpret_cast<float4*>(drow + col0 + q) =
+                        make_float4(__uint_as_float(v[q]), __uint_as_float(v[q + 1]),
+                                    __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3]));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+bool reforward1_supported(int64_t C, int64_t dm) {
+    return C % kBK == 0 && dm % 32 == 0 && dm <= 512;
+}
+
+// h0[i] = GELU(y1[i]), the clean activation the perturbed one is compared with.
+__global__ void gelu_kernel(const float* __restrict__ y, int64_t n, float* __restrict__ h) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        h[i] = gelu_erf(y[i]);
+}
+
+dust_status gelu_launch(const float* y, int64_t n, float* h, cudaStream_t s) {
+    int64_t b = ceil_div(n, 256);
+    if (b > 148 * 32) b = 148 * 32;
+    gelu_kernel<<<static_cast<unsigned>(b < 1 ? 1 : b), 256, 0, s>>>(y, n, h);
+    return launch_status();
+}
+
+dust_status reforward1_launch(const float* y1, const float* h0, const void* W2, int64_t T, int64_t Tp, int64_t C,
+                              int64_t dm, int nd, uint32_t draw_first, uint32_t token0,
+                              uint32_t layer, float sigma, const PhiloxKeys& keys, float* du,
+                              uint32_t* status, cudaStream_t s) {
+    CUtensorMap tw2;
+    if (!encode_bf16_2d(&tw2, W2, C, dm, C, kBK, 256)) return DUST_ERR_CUDA;
+    static bool attr_set = false;
+    if (!attr_set) {
+        DUST_CUDA_TRY(cudaFuncSetAttribute(reforward1_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(kSmemBytes)));
+        attr_set = true;
+    }
+    RefArgs a{y1, h0, du, static_cast<int>(T), static_cast<int>(C), static_cast<int>(dm), nd,
+              draw_first, token0, layer, sigma, status};
+    const unsigned grid = static_cast<unsigned>(nd * (Tp / kBM));
+    reforward1_kernel<<<grid, kThreads, kSmemBytes, s>>>(tw2, a, keys);
+    return launch_status();
+}
+
+}  // namespace dust

@@ -320,6 +320,58 @@ def config_of(wl, n_gpus):
     return c
 
 
+def run_head_sweep(args):
+    """The tiny head workload at K = 64 .. 16384: token-evals/s per K and the
+    cosine of G_W with the analytic head gradient sum_t (softmax(z_t) -
+    onehot(y_t)) x_t^T, next to the closed-form prediction 1/sqrt(1 + c/K)
+    (the law cos(K) = c_max / sqrt(1 + c/K) the pages fit, Dust translation
+    §4.2).  One JSON line per K."""
+    import torch
+
+    import activation_perturbation_es_noise_b300 as dust
+    import workloads as W
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    p = W.HEAD_PARAMS["head_tiny"]
+    wl = W.head_workload(p["T"], p["d"], p["V"], p["seq_len"], p["x_bf16"], p["zipf"])
+    z64 = wl["z"].astype(np.float64)
+    pr = np.exp(z64 - z64.max(1, keepdims=True))
+    pr /= pr.sum(1, keepdims=True)
+    g = pr.copy()
+    g[np.arange(p["T"]), wl["targets"]] -= 1.0
+    x64 = wl["x"].astype(np.float64)
+    G = g.T @ x64
+    c_pred = float(((x64 ** 2).sum(1) * (p["V"] + 1) * (g ** 2).sum(1)).sum() / (G ** 2).sum())
+    zt = torch.from_numpy(wl["z"]).to(dev)
+    yt = torch.from_numpy(wl["targets"]).to(dev)
+    xt = torch.from_numpy(wl["x"]).to(dev)
+    for K in W.HEAD_SWEEP_K:
+        gh = torch.empty((p["T"], p["V"]), dtype=torch.float32, device=dev)
+        Gw = torch.empty((p["V"], p["d"]), dtype=torch.float32, device=dev)
+        ws = dust._workspace(dust.head_workspace_bytes(p["T"], p["V"], p["d"], K), dev)
+        step = lambda: dust.head_estimate(zt, yt, xt, p["sigma"], K, W.NOISE_SEED, out=(gh, Gw),
+                                          ws=ws)
+        for _ in range(max(3, args.warmup)):
+            step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        e1.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        Gk = Gw.double().cpu().numpy()
+        cos = float((Gk * G).sum() / np.linalg.norm(Gk) / np.linalg.norm(G))
+        print(json.dumps({"metric": METRIC, "value": K * p["T"] / (ms * 1e-3), "unit": UNIT,
+                          "workload": "head_sweep", "draws": K, "ms_per_step": ms,
+                          "cosine_vs_analytic": cos,
+                          "cosine_predicted": 1.0 / np.sqrt(1.0 + c_pred / K),
+                          "c_pred": c_pred}), flush=True)
+    return 0
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -501,12 +553,14 @@ def main():
     ap.add_argument("--impl", default="dust", choices=["dust", "reference"])
     ap.add_argument("--workload", default="head_batch",
                     choices=["head_batch", "head_tiny", "head_scale", "interior",
-                             "interior_scale", "embed_scale"])
+                             "interior_scale", "embed_scale", "head_sweep"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "head_sweep":
+        return run_head_sweep(args)
     return run_dust(args)
 
 

@@ -55,6 +55,7 @@ def _ref(orc, d, sigma, gamma, K, seed, layer=1, draw0=0, token0=0):
     (256, 256, 32, 256, 128, 512, 8, 0.0),   # gamma = 0: own token only
     (200, 100, 40, 64, 64, 300, 6, 1.0),      # ragged T (pads to 256), ragged V, gamma = 1
     (384, 64, 8, 192, 192, 130, 20, 0.5),     # several chunks of draws, 6 sequences
+    (256, 128, 16, 128, 576, 64, 4, 0.95),    # d_model > 512: GEMM 1 from a staged A operand
 ])
 def test_interior_shapes(dust, orc, T, seq_len, d_in, C, dm, V, K, gamma):
     d = _inputs(T, d_in, C, dm, V, seq_len, seed=T + C)
