@@ -191,22 +191,29 @@ __global__ void piece_table_kernel(const uint32_t* __restrict__ seg, const uint3
 }
 
 // One CTA per piece: rows g[perm[start .. start+len)] summed in that order.
+// The piece's token indices are staged in shared memory first, so the row
+// loads of a thread do not wait on index loads and can all be in flight.
 template <bool VEC>
 __global__ void piece_sum_kernel(const float* __restrict__ g, const int32_t* __restrict__ perm,
                                  const Piece* __restrict__ table, const uint32_t* __restrict__ poff,
                                  int V, int d, float* __restrict__ G_E, float* __restrict__ partial) {
+    __shared__ int32_t rows[kPiece];
     const int npieces = static_cast<int>(poff[V]);
     for (int pi = blockIdx.x; pi < npieces; pi += gridDim.x) {
         const Piece pc = table[pi];
+        __syncthreads();
+        if (threadIdx.x < pc.len) rows[threadIdx.x] = __ldg(perm + pc.start + threadIdx.x);
+        __syncthreads();
         float* dst = pc.multi ? partial + static_cast<int64_t>(pi) * d
                               : G_E + static_cast<int64_t>(pc.v) * d;
         if (VEC) {
             const int d4 = d >> 2;
             for (int c = threadIdx.x; c < d4; c += blockDim.x) {
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
                 for (int r = 0; r < pc.len; ++r) {
-                    const int t = __ldg(perm + pc.start + r);
-                    const float4 x = __ldg(reinterpret_cast<const float4*>(g + static_cast<int64_t>(t) * d) + c);
+                    const float4 x = __ldg(reinterpret_cast<const float4*>(
+                                               g + static_cast<int64_t>(rows[r]) * d) + c);
                     acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
                 }
                 reinterpret_cast<float4*>(dst)[c] = acc;
@@ -214,10 +221,8 @@ __global__ void piece_sum_kernel(const float* __restrict__ g, const int32_t* __r
         } else {
             for (int c = threadIdx.x; c < d; c += blockDim.x) {
                 float acc = 0.f;
-                for (int r = 0; r < pc.len; ++r) {
-                    const int t = __ldg(perm + pc.start + r);
-                    acc += __ldg(g + static_cast<int64_t>(t) * d + c);
-                }
+#pragma unroll 8
+                for (int r = 0; r < pc.len; ++r) acc += __ldg(g + static_cast<int64_t>(rows[r]) * d + c);
                 dst[c] = acc;
             }
         }

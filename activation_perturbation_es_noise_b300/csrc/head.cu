@@ -51,6 +51,12 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// ln S for S > 0 (S is a probability-weighted mean of exp(sigma a), near 1):
+// the same exponent split and atanh series as the noise generator's log.
+__device__ __forceinline__ float log_pos(float S) {
+    return -0.5f * neg2_log_unit(S);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
@@ -160,9 +166,6 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
     BlockHalf bh[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) bh[b] = philox_block_half(b * NT + tid, A.layer, keys);
-    // Blocks past the vocabulary (only in the last block row) get zero noise;
-    // their probabilities are zero, so they add nothing.
-    const bool full = NB * NT <= A.nblk;
 
     float s1[NB][4], s0[NB][4];
 #pragma unroll
@@ -180,15 +183,17 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
         uint4 w[NB];
 #pragma unroll
         for (int b = 0; b < NB; ++b) w[b] = philox_rest(dh, bh[b], keys);
+        // Blocks past the vocabulary (only in the last block row) carry real
+        // noise of unused counters; their probabilities are zero and their
+        // accumulators are never written, so they change nothing.
         float a[NB][4];
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             const float4 n = words_to_normals(w[b]);
-            const bool valid = full || (b * NT + tid < A.nblk);
-            a[b][0] = valid ? n.x : 0.f;
-            a[b][1] = valid ? n.y : 0.f;
-            a[b][2] = valid ? n.z : 0.f;
-            a[b][3] = valid ? n.w : 0.f;
+            a[b][0] = n.x;
+            a[b][1] = n.y;
+            a[b][2] = n.z;
+            a[b][3] = n.w;
         }
         float pb[NB];
 #pragma unroll
@@ -221,7 +226,7 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
             for (int w = 0; w < nw; ++w) S += red[buf][w];
             ay = (y >= 0) ? red_y[buf] : 0.f;
         }
-        const float dl = logf(S) - A.sigma * ay;
+        const float dl = log_pos(S) - A.sigma * ay;
         sdl += dl;
 #pragma unroll
         for (int b = 0; b < NB; ++b)

@@ -117,7 +117,8 @@ __device__ __forceinline__ float rsqrt_approx(float x) {
     return y;
 }
 
-// -2 ln u for u in [2^-24, 1 - 2^-24].  u = 2^k f with f in [sqrt(1/2),
+// -2 ln u for a positive normal float u (the noise uses u in [2^-24, 1)).
+// u = 2^k f with f in [sqrt(1/2),
 // sqrt(2)) (k from the exponent field, f by moving the exponent), and
 // ln f = 2 atanh(s), s = (f - 1) / (f + 1), |s| <= 3 - 2 sqrt(2).  atanh(s)/s
 // is the series 1 + s^2/3 + s^4/5 + ... ; its first four terms, refitted for
