@@ -119,3 +119,37 @@ def test_head_batch_config_sampled(dust, orc):
     ref_G = gb.T @ wl["x"].astype(np.float64)
     # fp32 accumulation of 16384 products inside the tensor cores: ~2e-5
     assert rel_l2(G, ref_G) <= 1e-4
+
+
+def test_head_sweep_largest_population_sampled(dust, orc):
+    """The tiny workload at the sweep's largest population, K = 16384 (draw
+    chunks split over many CTAs and summed in order): g of sampled tokens
+    against the oracle, G_W against the product of the returned g and x."""
+    p = W.HEAD_PARAMS["head_tiny"]
+    wl = W.head_workload(p["T"], p["d"], p["V"], p["seq_len"], p["x_bf16"], p["zipf"])
+    K = W.HEAD_SWEEP_K[-1]
+    g, G = _run(dust, wl["x"], wl["z"], wl["targets"], p["sigma"], K, W.NOISE_SEED)
+    for a in (0, 131, 248):
+        sl = slice(a, a + 8)
+        ref = orc.head_estimate(wl["z"][sl], wl["targets"][sl], wl["x"][sl], p["sigma"], K,
+                                W.NOISE_SEED, 0, 0, a)
+        assert rel_l2(g[sl], ref["g"]) <= G_TOL
+    ref_G = W.bf16_round(g).astype(np.float64).T @ W.bf16_round(wl["x"]).astype(np.float64)
+    assert rel_l2(G, ref_G) <= 1e-4
+
+
+def test_head_scale_config_sampled(dust, orc):
+    """The scale workload's head: 8 x 2048 tokens, d = 1536, V = 4096, K = 4096."""
+    p = W.HEAD_PARAMS["head_scale"]
+    wl = W.head_workload(p["T"], p["d"], p["V"], p["seq_len"], p["x_bf16"], p["zipf"],
+                         device="cuda")
+    g, G = _run(dust, wl["x"], wl["z"], wl["targets"], p["sigma"], p["K"], W.NOISE_SEED,
+                x_bf16=True)
+    for a in (5, 12000):
+        sl = slice(a, a + 4)
+        ref = orc.head_estimate(wl["z"][sl], wl["targets"][sl], wl["x"][sl], p["sigma"], p["K"],
+                                W.NOISE_SEED, 0, 0, a)
+        assert rel_l2(g[sl], ref["g"]) <= G_TOL
+    gb = torch.from_numpy(W.bf16_round(g)).cuda().double()
+    ref_G = (gb.T @ torch.from_numpy(wl["x"]).cuda().double()).cpu().numpy()
+    assert rel_l2(G, ref_G) <= 1e-4

@@ -85,3 +85,39 @@ def test_interior_sequences_independent(dust):
     g_part, _ = _run(dust, part, 0.02, 0.95, 8, 5, token0=256)
     # centring is per token over the same draws, so this holds exactly
     np.testing.assert_array_equal(g_full[256:384], g_part)
+
+
+def _full(name, K):
+    p = dict(W.INTERIOR_PARAMS[name])
+    wl = W.interior_workload(p["T"], p["d_in"], p["C"], p["d_model"], p["V"], p["seq_len"],
+                             device="cuda")
+    d = dict(x=wl["x"], y1=wl["y1"], W2=wl["W2"], WH=wl["W_head"], z=wl["z_clean"],
+             y=wl["targets"], lam=wl["lam"], seq_len=p["seq_len"])
+    return p, d
+
+
+def _seq(d, s, L):
+    out = dict(d)
+    for k in ("x", "y1", "z", "y"):
+        out[k] = d[k][s * L:(s + 1) * L]
+    return out
+
+
+@pytest.mark.parametrize("name,K,seqs", [("interior", 12, (0, 7)), ("interior_scale", 2, (3,))])
+def test_interior_full_size_sequences(dust, orc, name, K, seqs):
+    """The full token count and widths of the interior workloads (8 x 2048
+    tokens; 512 -> 2048 with d_model 512, and 1536 -> 6144 with d_model 1536,
+    which takes the staged GEMM 1), with fewer draws so that the oracle can
+    redo whole sequences: sequences never exchange credit, and the centring is
+    per token over the same draws, so a sequence's rows of g equal the oracle
+    run on that sequence alone with its token offset."""
+    p, d = _full(name, K)
+    g, G = _run(dust, d, p["sigma"], p["gamma"], K, W.NOISE_SEED)
+    L = p["seq_len"]
+    for s in seqs:
+        ref = _ref(orc, _seq(d, s, L), p["sigma"], p["gamma"], K, W.NOISE_SEED, token0=s * L)
+        eg = rel_l2(g[s * L:(s + 1) * L], ref["g"])
+        assert eg <= G_TOL, (s, eg)
+    gb = torch.from_numpy(W.bf16_round(g)).cuda().double()
+    ref_G = (gb.T @ torch.from_numpy(d["x"]).cuda().double()).cpu().numpy()
+    assert rel_l2(G, ref_G) <= 1e-4
