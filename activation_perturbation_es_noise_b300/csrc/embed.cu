@@ -230,17 +230,31 @@ __global__ void piece_sum_kernel(const float* __restrict__ g, const int32_t* __r
 }
 
 // Rows with no token -> 0; rows with several pieces -> sum of partials in
-// piece order; rows with one piece are already final.
+// piece order; rows with one piece are already final.  One thread per
+// (row, column group of 4), flat over the table.
+template <bool VEC>
 __global__ void rows_finish_kernel(const uint32_t* __restrict__ poff, int V, int d,
                                    const float* __restrict__ partial, float* __restrict__ G_E) {
-    for (int v = blockIdx.x; v < V; v += gridDim.x) {
-        const uint32_t p0 = poff[v], np = poff[v + 1] - p0;
+    const int w = VEC ? d >> 2 : d;  // items per row
+    const int64_t n = static_cast<int64_t>(V) * w;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int v = static_cast<int>(i / w);
+        const int c = static_cast<int>(i - static_cast<int64_t>(v) * w);
+        const uint32_t p0 = __ldg(poff + v), np = __ldg(poff + v + 1) - p0;
         if (np == 1) continue;
-        float* row = G_E + static_cast<int64_t>(v) * d;
-        for (int c = threadIdx.x; c < d; c += blockDim.x) {
+        if (VEC) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (uint32_t k = 0; k < np; ++k) {
+                const float4 x = __ldg(reinterpret_cast<const float4*>(
+                                           partial + static_cast<int64_t>(p0 + k) * d) + c);
+                acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+            }
+            reinterpret_cast<float4*>(G_E + static_cast<int64_t>(v) * d)[c] = acc;
+        } else {
             float acc = 0.f;
-            for (uint32_t k = 0; k < np; ++k) acc += partial[static_cast<int64_t>(p0 + k) * d + c];
-            row[c] = acc;
+            for (uint32_t k = 0; k < np; ++k) acc += __ldg(partial + static_cast<int64_t>(p0 + k) * d + c);
+            G_E[static_cast<int64_t>(v) * d + c] = acc;
         }
     }
 }
@@ -355,8 +369,14 @@ extern "C" dust_status dust_embed_scatter(const float* g_hat, const int32_t* ids
                                                           G_E, part);
     timer_end(s);
     if ((st = launch_status()) != DUST_OK) return st;
-    rows_finish_kernel<<<static_cast<unsigned>(std::min<int64_t>(V, 148 * 64)), 256, 0, s>>>(
-        poff, Vi, di, part, G_E);
+    {
+        const int64_t items = V * (vec ? d / 4 : d);
+        const unsigned fb = static_cast<unsigned>(std::min<int64_t>(ceil_div(items, 256), 148 * 32));
+        if (vec)
+            rows_finish_kernel<true><<<fb, 256, 0, s>>>(poff, Vi, di, part, G_E);
+        else
+            rows_finish_kernel<false><<<fb, 256, 0, s>>>(poff, Vi, di, part, G_E);
+    }
     if ((st = launch_status()) != DUST_OK) return st;
     if (perm_out) DUST_CUDA_TRY(cudaMemcpyAsync(perm_out, v0, static_cast<size_t>(T) * 4,
                                                 cudaMemcpyDeviceToDevice, s));

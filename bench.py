@@ -448,6 +448,30 @@ def run_dust(args):
     if dust.workspace_status(ws) != 0:
         raise SystemExit("kernel status word set during the timed steps")
     ms_max = max_over_ranks(ms, dist if world > 1 else None)
+
+    # Optional: the same step captured once in a CUDA graph and replayed, which
+    # removes the host's launch gaps between the call's kernels.
+    graph = None
+    if args.graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg):
+            step()
+        cg.replay()
+        torch.cuda.synchronize()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            cg.replay()
+        g1.record(stream)
+        g1.synchronize()
+        gms = g0.elapsed_time(g1) / args.steps
+        graph = {"ms_per_step": gms, "value": evals * world / (gms * 1e-3), "unit": UNIT}
     value = evals * world * args.steps / (ms_max * 1e-3)
 
     # End to end through the public API from pinned host buffers: the step's
@@ -536,7 +560,7 @@ def run_dust(args):
                 "dtype": "f32" if wl["kind"] != "interior" else "f32+bf16x2",
                 "data": "synthetic", "config": config_of(wl, world),
                 "roofline": roofline(wl, kernel_ms, load_traffic(wl)),
-                "cpu_baseline": cpu, "e2e": e2e,
+                "cpu_baseline": cpu, "e2e": e2e, "graph": graph,
                 "gpu_launches": launches * args.steps,
                 "clocks": clocks.summary()}
         print(json.dumps(line), flush=True)
@@ -556,6 +580,8 @@ def main():
                              "interior_scale", "embed_scale", "head_sweep"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step captured in a CUDA graph")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
