@@ -278,9 +278,17 @@ InteriorPlan interior_plan(int64_t T, int64_t d_in, int64_t C, int64_t dm, int64
     InteriorPlan P{};
     P.Tp = round_up(T, kRowBlock);
     P.ldx = round_up(d_in, 8);
+    // Draws per chunk: at least eight 128-row tiles per SM, and where the
+    // count allows, a chunk of nd x (token blocks) tiles that is a whole
+    // number of waves over the 148 SMs.
     const int64_t ntb = P.Tp / kRowBlock;
     int64_t nd = ceil_div(148 * 8, ntb);
-    nd = std::max<int64_t>(1, std::min<int64_t>({nd, 16, static_cast<int64_t>(K)}));
+    for (int64_t c = nd; c <= std::min<int64_t>(64, 4 * nd); ++c)
+        if ((c * ntb) % 148 == 0) {
+            nd = c;
+            break;
+        }
+    nd = std::max<int64_t>(1, std::min<int64_t>({nd, 64, static_cast<int64_t>(K)}));
     P.nd = static_cast<int>(nd);
     P.fused = reforward1_supported(C, dm);
     const size_t rows = static_cast<size_t>(nd * P.Tp);

@@ -168,6 +168,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int p = threadIdx.x - 64;
         const int jj = p & 15;
         const int r0 = p >> 4;  // 0 .. 2 kProducerWarps - 1
+        constexpr int kRows = kBM / (2 * kProducerWarps);  // rows per thread
+        // The (draw, token) half of Philox's first round is the same for every
+        // slice of a row: computed once per tile.
+        DrawHalf dhalf[kRows];
+#pragma unroll
+        for (int m = 0; m < kRows; ++m)
+            dhalf[m] = philox_draw_half(a.draw_first + di,
+                                        a.token0 + tb * kBM + r0 + 2 * kProducerWarps * m, keys);
         for (int kb = 0; kb < nk; ++kb) {
             const int s = kb % kStages;
             const uint32_t ph = (kb / kStages) & 1u;
@@ -175,7 +183,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t st = base + s * kStageBytes;
             const int j = kb * (kBK / 4) + jj;  // global channel block
             const BlockHalf bhalf = philox_block_half(j, a.layer, keys);
-            constexpr int kRows = kBM / (2 * kProducerWarps);  // rows per thread
             // Issue the loads of every row first, then the arithmetic.
             float4 yv[kRows], gv[kRows];
 #pragma unroll
@@ -195,9 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int t = tb * kBM + r;
                 uint32_t hi0 = 0, hi1 = 0, lo0 = 0, lo1 = 0;
                 if (t < a.T) {
-                    const DrawHalf dhalf =
-                        philox_draw_half(a.draw_first + di, a.token0 + t, keys);
-                    const float4 nrm = words_to_normals(philox_rest(dhalf, bhalf, keys));
+                    const float4 nrm = words_to_normals(philox_rest(dhalf[m], bhalf, keys));
                     const float4 y = yv[m], g = gv[m];
                     const float d0 = gelu_erf(fmaf(a.sigma, nrm.x, y.x)) - g.x;
                     const float d1 = gelu_erf(fmaf(a.sigma, nrm.y, y.y)) - g.y;

@@ -204,9 +204,20 @@ def make_step(wl, dust):
             dust.linear_estimate(d["x"], d["y1"], d["W2"], wl["lam"], d["W_head"], d["z_clean"],
                                  d["targets"], wl["seq_len"], wl["sigma"], wl["gamma"], K, 1234,
                                  1, 0, wl["token0"], out=(g, G), ws=ws)
-        nd = 10
+        # draws per chunk as the library plans them: >= 8 tiles per SM, a
+        # whole number of waves over 148 SMs where possible
+        ntb = -(-T // 128)
+        nd = -(-1184 // ntb)
+        for c in range(nd, min(64, 4 * nd) + 1):
+            if (c * ntb) % 148 == 0:
+                nd = c
+                break
+        nd = max(1, min(nd, 64, K))
         chunks = -(-K // nd)
-        return step, K * T, 1 + chunks * 3 + 3 + 1, ws
+        fused = wl["C"] % 64 == 0 and wl["d_model"] <= 512
+        per_chunk = 3 if fused else 4
+        # softmax (+ clean GELU when fused), per chunk, mean + scan + g, outer product
+        return step, K * T, (2 if fused else 1) + chunks * per_chunk + 3 + 1, ws
     if wl["kind"] == "embed":
         T, dd, V = wl["T"], wl["d"], wl["V"]
         G = torch.empty((V, dd), dtype=torch.float32, device=d["g"].device)
