@@ -34,15 +34,13 @@
 #include "dust_common.cuh"
 #include "internal.h"
 #include "noise.cuh"
+#include "gelu.cuh"
 
 namespace dust {
 namespace {
 
 constexpr int kRowBlock = 128;
 
-__device__ __forceinline__ float gelu_erf(float u) {
-    return 0.5f * u * (1.0f + erff(u * 0.70710678118654752f));
-}
 
 __device__ __forceinline__ void split_bf16(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
     hi = __float2bfloat16_rn(v);
@@ -91,6 +89,7 @@ __global__ void softmax_rows_kernel(const float* __restrict__ z, int V, int ldp,
 
 struct DhArgs {
     const float* y1;
+    const float* h0;  // GELU(y1), same function as below
     int T, Tp, C, nd;
     uint32_t draw_first, token0, layer;  // draw_first = draw0 + i0
     float sigma;
@@ -112,11 +111,13 @@ __global__ void interior_dh_kernel(const DhArgs a, const PhiloxKeys keys) {
         if (t < a.T) {
             const float4 nrm = words_to_normals(
                 philox4x32_10(j, a.token0 + t, a.draw_first + i, a.layer, keys));
-            const float4 y = __ldg(reinterpret_cast<const float4*>(a.y1 + static_cast<int64_t>(t) * a.C) + j);
-            split_bf16(gelu_erf(fmaf(a.sigma, nrm.x, y.x)) - gelu_erf(y.x), h[0], l[0]);
-            split_bf16(gelu_erf(fmaf(a.sigma, nrm.y, y.y)) - gelu_erf(y.y), h[1], l[1]);
-            split_bf16(gelu_erf(fmaf(a.sigma, nrm.z, y.z)) - gelu_erf(y.z), h[2], l[2]);
-            split_bf16(gelu_erf(fmaf(a.sigma, nrm.w, y.w)) - gelu_erf(y.w), h[3], l[3]);
+            const int64_t e4 = static_cast<int64_t>(t) * (a.C / 4) + j;
+            const float4 y = __ldg(reinterpret_cast<const float4*>(a.y1) + e4);
+            const float4 g = __ldg(reinterpret_cast<const float4*>(a.h0) + e4);
+            split_bf16(gelu_as(fmaf(a.sigma, nrm.x, y.x)) - g.x, h[0], l[0]);
+            split_bf16(gelu_as(fmaf(a.sigma, nrm.y, y.y)) - g.y, h[1], l[1]);
+            split_bf16(gelu_as(fmaf(a.sigma, nrm.z, y.z)) - g.z, h[2], l[2]);
+            split_bf16(gelu_as(fmaf(a.sigma, nrm.w, y.w)) - g.w, h[3], l[3]);
         } else {
 #pragma unroll
             for (int k = 0; k < 4; ++k) h[k] = l[k] = __float2bfloat16_rn(0.f);
@@ -295,7 +296,7 @@ InteriorPlan interior_plan(int64_t T, int64_t d_in, int64_t C, int64_t dm, int64
     WsLayout w;
     w.take(kCtlBytes);
     P.off_p = w.take(static_cast<size_t>(T * round_up(V, 4)) * 4);
-    P.off_h0 = w.take(P.fused ? static_cast<size_t>(T * C) * 4 : 0);
+    P.off_h0 = w.take(static_cast<size_t>(T * C) * 4);
     P.off_a1 = w.take(P.fused ? 0 : rows * static_cast<size_t>(2 * C) * 2);
     P.off_du = w.take(rows * static_cast<size_t>(dm) * 4);
     P.off_a2 = w.take(rows * static_cast<size_t>(2 * dm) * 2);
@@ -373,7 +374,7 @@ extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, cons
                                                                  static_cast<int>(ldp), p);
     if ((st = launch_status()) != DUST_OK) return st;
     float* h0 = reinterpret_cast<float*>(w + P.off_h0);
-    if (P.fused && (st = gelu_launch(y1, T * C, h0, s)) != DUST_OK) return st;
+    if ((st = gelu_launch(y1, T * C, h0, s)) != DUST_OK) return st;
 
     const int nseq = static_cast<int>(T / seq_len);
     for (int i0 = 0; i0 < K; i0 += P.nd) {
@@ -385,7 +386,7 @@ extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, cons
                                    nz.sigma, keys, du, status, s);
             if (st != DUST_OK) return st;
         } else {
-            DhArgs da{y1, Ti, static_cast<int>(P.Tp), Ci, nd,
+            DhArgs da{y1, h0, Ti, static_cast<int>(P.Tp), Ci, nd,
                       nz.draw0 + static_cast<uint32_t>(i0), nz.token0, nz.layer, nz.sigma, A1};
             interior_dh_kernel<<<grid_cap(rows * (C / 4), 256), 256, 0, s>>>(da, keys);
             if ((st = launch_status()) != DUST_OK) return st;

@@ -138,6 +138,30 @@ __device__ __forceinline__ float neg2_log_unit(float u) {
     return fmaf(s * p, -4.0f, kf * -1.3862943611198906f);  // -2 k ln 2 - 4 s p
 }
 
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// -2 ln u for the uniforms of the noise, u in [2^-24, 1 - 2^-24].  Near 1
+// (v = 1 - u < 1/10, exact since u > 1/2) the series -ln(1 - v) = v + v^2/2
+// + ... + v^6/6 (truncation below 2e-8 relative); elsewhere the hardware
+// log2, whose absolute error (about 1e-7) is at most 1e-6 relative there
+// because |ln u| >= 0.105.  Both are computed and one is selected, so lanes
+// do not diverge.
+__device__ __forceinline__ float neg2_log_uniform(float u) {
+    const float v = 1.0f - u;
+    float q = fmaf(v, 1.0f / 6.0f, 0.2f);
+    q = fmaf(v, q, 0.25f);
+    q = fmaf(v, q, 1.0f / 3.0f);
+    q = fmaf(v, q, 0.5f);
+    q = fmaf(v, q, 1.0f);
+    const float near1 = (2.0f * v) * q;
+    const float far = lg2_approx(u) * -1.3862943611198906f;  // -2 ln 2 log2 u
+    return v < 0.1f ? near1 : far;
+}
+
 // Box-Muller pair from two words: rho = sqrt(-2 ln u_even), theta =
 // 2 pi u_odd; a_cos = rho cos theta, a_sin = rho sin theta.  With
 // theta' = 2 pi u_odd - pi in (-pi, pi), cos theta = -cos theta' and
@@ -146,7 +170,7 @@ __device__ __forceinline__ float neg2_log_unit(float u) {
 // are within about 3e-6 of the exact ones at the largest radius (5.77).
 __device__ __forceinline__ void box_muller(uint32_t w_even, uint32_t w_odd, float& a_cos,
                                            float& a_sin) {
-    const float x = neg2_log_unit(word_to_uniform(w_even));
+    const float x = neg2_log_uniform(word_to_uniform(w_even));
     const float neg_rho = -(x * rsqrt_approx(x));
     const float th = fmaf(word_to_uniform(w_odd), 6.2831853071795865f, -3.1415926535897932f);
     float s, c;

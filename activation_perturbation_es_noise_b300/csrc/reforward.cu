@@ -19,6 +19,7 @@
 #include "dust_common.cuh"
 #include "internal.h"
 #include "noise.cuh"
+#include "gelu.cuh"
 
 namespace dust {
 namespace {
@@ -42,35 +43,6 @@ struct RefArgs {
     float sigma;
     uint32_t* status;
 };
-
-__device__ __forceinline__ float ex2a(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// erf by the rational-exponential approximation of Abramowitz & Stegun,
-// Handbook of Mathematical Functions, 7.1.26 (after Hastings):
-// erf(x) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-x^2),
-// t = 1 / (1 + p x) for x >= 0, odd extension; |error| < 1.5e-7.  One form on
-// the whole line, so lanes do not diverge.  The clean GELU(y1) is computed
-// with the same function, so its smooth error largely cancels in the
-// difference GELU(y1 + sigma a) - GELU(y1) (about 4e-7 relative, float64 model).
-__device__ __forceinline__ float erf_as(float x) {
-    const float ax = fabsf(x);
-    const float t = rcp_approx(fmaf(0.3275911f, ax, 1.0f));
-    float q = fmaf(t, 1.061405429f, -1.453152027f);
-    q = fmaf(t, q, 1.421413741f);
-    q = fmaf(t, q, -0.284496736f);
-    q = fmaf(t, q, 0.254829592f);
-    const float e = ex2a(ax * (ax * -1.4426950408889634f));
-    return copysignf(fmaf(-q * t, e, 1.0f), x);
-}
-
-// GELU(u) = u Phi(u) = u (1 + erf(u / sqrt 2)) / 2.
-__device__ __forceinline__ float gelu_erf(float u) {
-    return u * fmaf(0.5f, erf_as(u * 0.70710678118654752f), 0.5f);
-}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -204,10 +176,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (t < a.T) {
                     const float4 nrm = words_to_normals(philox_rest(dhalf[m], bhalf, keys));
                     const float4 y = yv[m], g = gv[m];
-                    const float d0 = gelu_erf(fmaf(a.sigma, nrm.x, y.x)) - g.x;
-                    const float d1 = gelu_erf(fmaf(a.sigma, nrm.y, y.y)) - g.y;
-                    const float d2 = gelu_erf(fmaf(a.sigma, nrm.z, y.z)) - g.z;
-                    const float d3 = gelu_erf(fmaf(a.sigma, nrm.w, y.w)) - g.w;
+                    const float d0 = gelu_as(fmaf(a.sigma, nrm.x, y.x)) - g.x;
+                    const float d1 = gelu_as(fmaf(a.sigma, nrm.y, y.y)) - g.y;
+                    const float d2 = gelu_as(fmaf(a.sigma, nrm.z, y.z)) - g.z;
+                    const float d3 = gelu_as(fmaf(a.sigma, nrm.w, y.w)) - g.w;
                     const float h0 = __bfloat162float(__float2bfloat16_rn(d0));
                     const float h1 = __bfloat162float(__float2bfloat16_rn(d1));
                     const float h2 = __bfloat162float(__float2bfloat16_rn(d2));
@@ -266,7 +238,7 @@ bool reforward1_supported(int64_t C, int64_t dm) {
 __global__ void gelu_kernel(const float* __restrict__ y, int64_t n, float* __restrict__ h) {
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-        h[i] = gelu_erf(y[i]);
+        h[i] = gelu_as(y[i]);
 }
 
 dust_status gelu_launch(const float* y, int64_t n, float* h, cudaStream_t s) {
