@@ -158,7 +158,19 @@ __global__ void __launch_bounds__(32 * kEmaWarps)
 
     float e = 0.f, pw = 1.f;
     if (ok) {
-        for (int t = t0; t < t1; ++t) {
+        // loads of 8 tokens issued together, then the 8 dependent steps
+        int t = t0;
+        for (; t + 8 <= t1; t += 8) {
+            float u[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) u[q] = __ldg(du + chunk_row(t + q, i, nd) * dm + k);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                e = fmaf(lam, e, one_m * u[q]);
+                pw *= lam;
+            }
+        }
+        for (; t < t1; ++t) {
             e = fmaf(lam, e, one_m * __ldg(du + chunk_row(t, i, nd) * dm + k));
             pw *= lam;
         }
@@ -176,7 +188,22 @@ __global__ void __launch_bounds__(32 * kEmaWarps)
     __syncthreads();
     if (ok) {
         e = s_carry[w][lane];
-        for (int t = t0; t < t1; ++t) {
+        int t = t0;
+        for (; t + 8 <= t1; t += 8) {
+            float u[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) u[q] = __ldg(du + chunk_row(t + q, i, nd) * dm + k);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int64_t r = chunk_row(t + q, i, nd);
+                e = fmaf(lam, e, one_m * u[q]);
+                __nv_bfloat16 h, l;
+                split_bf16(e, h, l);
+                A2[r * 2 * dm + k] = h;
+                A2[r * 2 * dm + dm + k] = l;
+            }
+        }
+        for (; t < t1; ++t) {
             const int64_t r = chunk_row(t, i, nd);
             e = fmaf(lam, e, one_m * __ldg(du + r * dm + k));
             __nv_bfloat16 h, l;
