@@ -27,7 +27,7 @@ EXPORTS = ("dust_status_string", "dust_abi_version", "dust_workspace_status",
            "dust_head_workspace", "dust_head_estimate", "dust_linear_workspace",
            "dust_linear_estimate", "dust_embed_workspace", "dust_embed_scatter",
            "dust_embed_scatter_static", "dust_philox_fill", "dust_gemm_bf16", "dust_set_kernel_events",
-           "dust_kernel_event_count")
+           "dust_kernel_event_count", "dust_wait_selftest")
 
 
 class DustError(RuntimeError):
@@ -80,8 +80,9 @@ def lib():
         L.dust_gemm_bf16.argtypes = [_P, ctypes.c_int, _I64, _P, ctypes.c_int, _I64, _I64, _I64,
                                      _I64, _P, _I64, _P, _SZ, _P]
         L.dust_set_kernel_events.argtypes = [_P, _P, ctypes.c_int]
+        L.dust_wait_selftest.argtypes = [_P, ctypes.c_uint64, _P]
         L.dust_kernel_event_count.restype = ctypes.c_int
-        for name in ("dust_set_kernel_events", "dust_workspace_status", "dust_head_estimate", "dust_linear_estimate",
+        for name in ("dust_set_kernel_events", "dust_wait_selftest", "dust_workspace_status", "dust_head_estimate", "dust_linear_estimate",
                      "dust_embed_scatter", "dust_embed_scatter_static", "dust_philox_fill",
                      "dust_gemm_bf16"):
             getattr(L, name).restype = ctypes.c_int
@@ -224,6 +225,13 @@ def philox_fill(seed, layer, draw, token0, ntok, nchan, device="cuda", stream=No
                                 _ptr(normals), _stream(stream))
     _check("dust_philox_fill", st)
     return words, normals
+
+
+def wait_selftest(limit_ns, stream=None):
+    """Run the bounded-wait check; returns the status word it left."""
+    ws = _workspace(256, torch.device("cuda"))
+    _check("dust_wait_selftest", lib().dust_wait_selftest(_ptr(ws), int(limit_ns), _stream(stream)))
+    return workspace_status(ws, stream)
 
 
 def gemm_bf16(A, a_mn, B, b_mn, M, N, K, stream=None):

@@ -33,6 +33,21 @@ __global__ void philox_fill_kernel(PhiloxKeys keys, uint32_t layer, uint32_t dra
     }
 }
 
+// Waits on an mbarrier that nothing arrives at, with the caller's limit, the
+// way every pipeline wait in the library is bounded; records
+// DUST_ERR_TIMEOUT when the limit runs out and returns.
+__global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) (void)mbar_wait(b, 0, status, limit_ns);
+    __syncthreads();
+}
+
 }  // namespace
 
 KernelTimer& kernel_timer() {
@@ -57,6 +72,15 @@ extern "C" dust_status dust_set_kernel_events(void* const* start_events, void* c
 }
 
 extern "C" int dust_kernel_event_count(void) { return kernel_timer().count; }
+
+extern "C" dust_status dust_wait_selftest(void* ws, uint64_t limit_ns, void* stream) {
+    if (!ws || !aligned(ws, 256)) return DUST_ERR_WORKSPACE;
+    if (limit_ns == 0 || limit_ns > 1000000000ull) return DUST_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DUST_CUDA_TRY(cudaMemsetAsync(ws, 0, kCtlBytes, s));
+    wait_selftest_kernel<<<1, 32, 0, s>>>(static_cast<uint32_t*>(ws), limit_ns);
+    return launch_status();
+}
 
 extern "C" int dust_abi_version(void) { return 100; }
 

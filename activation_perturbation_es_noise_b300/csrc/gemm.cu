@@ -59,6 +59,7 @@ struct GemmShape {
     int M, N, K;
     int n_per_cta;
     int b_kmod;
+    int n_fastest;  // grid.x walks N tiles (CTAs sharing an A tile run together)
 };
 
 struct EpiStore {
@@ -123,9 +124,10 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * kBM;
+    const int mtile = sh.n_fastest ? blockIdx.y : blockIdx.x;
+    const int m0 = mtile * kBM;
     const int ntiles = (sh.N + kBN - 1) / kBN;
-    const int nt0 = blockIdx.y * sh.n_per_cta;
+    const int nt0 = (sh.n_fastest ? blockIdx.x : blockIdx.y) * sh.n_per_cta;
     const int nt_count = min(sh.n_per_cta, ntiles - nt0);
     const int nk = (sh.K + kBK - 1) / kBK;
 
@@ -358,8 +360,9 @@ dust_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtenso
         attr_set = true;
     }
     const int ntiles = (sh.N + kBN - 1) / kBN;
-    dim3 grid(static_cast<unsigned>(ceil_div(sh.M, kBM)),
-              static_cast<unsigned>(ceil_div(ntiles, sh.n_per_cta)));
+    const unsigned gm = static_cast<unsigned>(ceil_div(sh.M, kBM));
+    const unsigned gn = static_cast<unsigned>(ceil_div(ntiles, sh.n_per_cta));
+    const dim3 grid = sh.n_fastest ? dim3(gn, gm) : dim3(gm, gn);
     kern<<<grid, threads_of<EPI>(), smem, s>>>(ta, tb, tp, sh, es, ec, status);
     return launch_status();
 }
@@ -447,8 +450,11 @@ dust_status gemm_bf16_launch(const void* A, bool a_mn, int64_t lda, const void* 
     CUtensorMap ta, tb;
     if (!encode_operands(&ta, &tb, A, a_mn, lda, B, b_mn, ldb, M, N, K, b_kmod))
         return DUST_ERR_CUDA;
+    // One N tile per CTA, N tiles of the same A tile launched together, when
+    // the caller asks for a single tile per CTA: the A tile is then read from
+    // HBM once and served from L2 to its neighbours.
     GemmShape sh{static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), n_per_cta,
-                 static_cast<int>(b_kmod)};
+                 static_cast<int>(b_kmod), n_per_cta == 1 ? 1 : 0};
     EpiStore es{G, ldg};
     EpiCE ec{};
     if (a_mn && b_mn) return launch_t<true, true, EPI_STORE>(ta, tb, ta, sh, es, ec, status, s);
@@ -466,7 +472,7 @@ dust_status gemm_ce_launch(const void* A, int64_t lda, const void* B, int64_t ld
         return DUST_ERR_CUDA;
     const int ntiles = static_cast<int>(ceil_div(V, kBN));
     GemmShape sh{static_cast<int>(M), static_cast<int>(V), static_cast<int>(K), ntiles,
-                 static_cast<int>(b_kmod)};
+                 static_cast<int>(b_kmod), 0};
     EpiStore es{};
     EpiCE ec{p, targets, dl, static_cast<int>(T), static_cast<int>(V), ndraw, i0};
     // softmax rows: T x V fp32, row stride ldp (a multiple of 4), 128 x 32 boxes

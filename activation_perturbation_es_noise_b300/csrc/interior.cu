@@ -299,7 +299,7 @@ struct InteriorPlan {
     int64_t Tp, ldx;
     int nd;      // draws per chunk
     bool fused;  // GEMM 1 generates its A operand on chip
-    size_t off_p, off_h0, off_a1, off_du, off_a2, off_dl, off_m, off_r, off_gbf, off_xbf, bytes;
+    size_t off_p, off_h0, off_coef, off_a1, off_du, off_a2, off_dl, off_m, off_r, off_gbf, off_xbf, bytes;
 };
 
 InteriorPlan interior_plan(int64_t T, int64_t d_in, int64_t C, int64_t dm, int64_t V, uint32_t K) {
@@ -324,6 +324,7 @@ InteriorPlan interior_plan(int64_t T, int64_t d_in, int64_t C, int64_t dm, int64
     w.take(kCtlBytes);
     P.off_p = w.take(static_cast<size_t>(T * round_up(V, 4)) * 4);
     P.off_h0 = w.take(static_cast<size_t>(T * C) * 4);
+    P.off_coef = w.take(P.fused ? static_cast<size_t>(T * C) * 16 : 0);
     P.off_a1 = w.take(P.fused ? 0 : rows * static_cast<size_t>(2 * C) * 2);
     P.off_du = w.take(rows * static_cast<size_t>(dm) * 4);
     P.off_a2 = w.take(rows * static_cast<size_t>(2 * dm) * 2);
@@ -402,13 +403,18 @@ extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, cons
     if ((st = launch_status()) != DUST_OK) return st;
     float* h0 = reinterpret_cast<float*>(w + P.off_h0);
     if ((st = gelu_launch(y1, T * C, h0, s)) != DUST_OK) return st;
+    // Small sigma: GELU(y1 + d) - GELU(y1) by its fourth-order Taylor
+    // polynomial in d (coefficients once per call), exact form otherwise.
+    const bool taylor = P.fused && 5.77 * nz.sigma <= 0.15;
+    void* coef = w + P.off_coef;
+    if (taylor && (st = gelu_taylor_launch(y1, T * C, coef, s)) != DUST_OK) return st;
 
     const int nseq = static_cast<int>(T / seq_len);
     for (int i0 = 0; i0 < K; i0 += P.nd) {
         const int nd = std::min(P.nd, K - i0);
         const int64_t rows = nd * P.Tp;
         if (P.fused) {
-            st = reforward1_launch(y1, h0, W2, T, P.Tp, C, d_model, nd,
+            st = reforward1_launch(y1, h0, coef, taylor, W2, T, P.Tp, C, d_model, nd,
                                    nz.draw0 + static_cast<uint32_t>(i0), nz.token0, nz.layer,
                                    nz.sigma, keys, du, status, s);
             if (st != DUST_OK) return st;
@@ -417,9 +423,8 @@ extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, cons
                       nz.draw0 + static_cast<uint32_t>(i0), nz.token0, nz.layer, nz.sigma, A1};
             interior_dh_kernel<<<grid_cap(rows * (C / 4), 256), 256, 0, s>>>(da, keys);
             if ((st = launch_status()) != DUST_OK) return st;
-            st = gemm_bf16_launch(A1, false, 2 * C, W2, false, C, rows, d_model, 2 * C, C,
-                                  static_cast<int>(ceil_div(d_model, 256)), du, d_model, status,
-                                  s);
+            st = gemm_bf16_launch(A1, false, 2 * C, W2, false, C, rows, d_model, 2 * C, C, 1, du,
+                                  d_model, status, s);
             if (st != DUST_OK) return st;
         }
         if (P.Tp != T)

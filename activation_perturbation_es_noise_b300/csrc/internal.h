@@ -99,7 +99,10 @@ struct PhiloxKeys;
 // output, split bf16) generated on chip: du = dh W2^T for nd draws.
 bool reforward1_supported(int64_t C, int64_t dm);
 dust_status gelu_launch(const float* y, int64_t n, float* h, cudaStream_t s);
-dust_status reforward1_launch(const float* y1, const float* h0, const void* W2, int64_t T, int64_t Tp, int64_t C,
+// Taylor coefficients (4 per channel, T x C/4 x 4 float4) of the GELU difference.
+dust_status gelu_taylor_launch(const float* y, int64_t n, void* coef, cudaStream_t s);
+dust_status reforward1_launch(const float* y1, const float* h0, const void* coef, bool taylor,
+                              const void* W2, int64_t T, int64_t Tp, int64_t C,
                               int64_t dm, int nd, uint32_t draw_first, uint32_t token0,
                               uint32_t layer, float sigma, const PhiloxKeys& keys, float* du,
                               uint32_t* status, cudaStream_t s);

@@ -487,76 +487,90 @@ def run_dust(args):
 
     # End to end through the public API from pinned host buffers: the step's
     # inputs copied in, the estimator, the weight gradient copied out.
+    # End to end through the public API from pinned host buffers: each step
+    # copies its inputs in, runs the estimator and copies G_W back.  The
+    # copies of step i + 1 run on a second stream into a second set of device
+    # buffers while step i computes, as a batch stream would be fed.
     e2e = None
     if not args.no_e2e:
-        host = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory()
-                for k, v in wl["host"].items()}
-        devb = {k: torch.empty(v.shape, dtype=v.dtype, device=device) for k, v in host.items()}
+        bf = torch.bfloat16
+        as_bf16 = {"interior": ("x", "W2", "W_head"), "head": ("x",) if wl.get("x_bf16") else (),
+                   "embed": ()}[wl["kind"]]
+        host = {}
+        for k, v in wl["host"].items():
+            t = torch.from_numpy(np.ascontiguousarray(v))
+            host[k] = (t.to(bf) if k in as_bf16 else t).pin_memory()
+        sets = [{k: torch.empty(v.shape, dtype=v.dtype, device=device) for k, v in host.items()}
+                for _ in range(2)]
         h2d = sum(v.numel() * v.element_size() for v in host.values())
         if wl["kind"] == "head":
             T, V, dd, K = wl["T"], wl["V"], wl["d"], wl["K"]
             g = torch.empty((T, V), dtype=torch.float32, device=device)
             G = torch.empty((V, dd), dtype=torch.float32, device=device)
-            Gh = torch.empty((V, dd), dtype=torch.float32).pin_memory()
             wse = dust._workspace(dust.head_workspace_bytes(T, V, dd, K), device)
 
-            def e2e_step():
-                for k in host:
-                    devb[k].copy_(host[k], non_blocking=True)
-                dust.head_estimate(devb["logits"], devb["targets"], devb["x"], wl["sigma"], K,
-                                   1234, 0, 0, wl["token0"], out=(g, G), ws=wse)
-                Gh.copy_(G, non_blocking=True)
-            d2h = Gh.numel() * 4
+            def call(d):
+                dust.head_estimate(d["logits"], d["targets"], d["x"], wl["sigma"], K, 1234, 0, 0,
+                                   wl["token0"], out=(g, G), ws=wse)
         elif wl["kind"] == "interior":
             T, K = wl["T"], wl["K"]
             g = torch.empty((T, wl["C"]), dtype=torch.float32, device=device)
             G = torch.empty((wl["C"], wl["d_in"]), dtype=torch.float32, device=device)
-            Gh = torch.empty(G.shape, dtype=torch.float32).pin_memory()
             wse = dust._workspace(dust.linear_workspace_bytes(
                 T, wl["d_in"], wl["C"], wl["d_model"], wl["V"], K), device)
-            bf = torch.bfloat16
-            for k in ("x", "W2", "W_head"):
-                host[k] = host[k]  # already exact bf16 values held as fp32
-            devbf = {}
 
-            def e2e_step():
-                for k in host:
-                    devb[k].copy_(host[k], non_blocking=True)
-                for k in ("x", "W2", "W_head"):
-                    devbf[k] = devb[k].to(bf)
-                dust.linear_estimate(devbf["x"], devb["y1"], devbf["W2"], wl["lam"],
-                                     devbf["W_head"], devb["z_clean"], devb["targets"],
-                                     wl["seq_len"], wl["sigma"], wl["gamma"], K, 1234, 1, 0,
-                                     wl["token0"], out=(g, G), ws=wse)
-                Gh.copy_(G, non_blocking=True)
-            d2h = Gh.numel() * 4
+            def call(d):
+                dust.linear_estimate(d["x"], d["y1"], d["W2"], wl["lam"], d["W_head"],
+                                     d["z_clean"], d["targets"], wl["seq_len"], wl["sigma"],
+                                     wl["gamma"], K, 1234, 1, 0, wl["token0"], out=(g, G),
+                                     ws=wse)
         else:
             V, dd, T = wl["V"], wl["d"], wl["T"]
             G = torch.empty((V, dd), dtype=torch.float32, device=device)
             perm = torch.empty(T, dtype=torch.int32, device=device)
-            Gh = torch.empty((V, dd), dtype=torch.float32).pin_memory()
             wse = dust._workspace(dust.embed_workspace_bytes(T, dd, V), device)
 
-            def e2e_step():
+            def call(d):
+                dust.embed_scatter(d["g"], d["ids"], V, out=(G, perm), ws=wse)
+        Gh = torch.empty(G.shape, dtype=torch.float32).pin_memory()
+        d2h = Gh.numel() * 4
+        copy_s = torch.cuda.Stream(device=device)
+        used = [torch.cuda.Event() for _ in range(2)]
+        copied = [torch.cuda.Event() for _ in range(2)]
+
+        def copy_in(b):
+            with torch.cuda.stream(copy_s):
+                copy_s.wait_event(used[b])
                 for k in host:
-                    devb[k].copy_(host[k], non_blocking=True)
-                dust.embed_scatter(devb["g"], devb["ids"], V, out=(G, perm), ws=wse)
+                    sets[b][k].copy_(host[k], non_blocking=True)
+                copied[b].record(copy_s)
+
+        def run(n, start_event=None):
+            if start_event is not None:
+                copy_s.wait_event(start_event)
+            copy_in(0)
+            for i in range(n):
+                if i + 1 < n:
+                    copy_in((i + 1) % 2)
+                stream.wait_event(copied[i % 2])
+                call(sets[i % 2])
+                used[i % 2].record(stream)
                 Gh.copy_(G, non_blocking=True)
-            d2h = Gh.numel() * 4
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
+
+        run(max(2, args.warmup))
+        torch.cuda.synchronize()
         barrier()
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
         f0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        run(args.steps, f0)
         f1.record(stream)
         f1.synchronize()
         barrier()
         te = max_over_ranks(f0.elapsed_time(f1), dist if world > 1 else None)
         e2e = {"value": evals * world * args.steps / (te * 1e-3), "unit": UNIT,
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "overlap": "inputs of step i+1 copied on a second stream during step i"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -121,3 +121,13 @@ def test_interior_full_size_sequences(dust, orc, name, K, seqs):
     gb = torch.from_numpy(W.bf16_round(g)).cuda().double()
     ref_G = (gb.T @ torch.from_numpy(d["x"]).cuda().double()).cpu().numpy()
     assert rel_l2(G, ref_G) <= 1e-4
+
+
+def test_interior_exact_gelu_path(dust, orc):
+    """sigma = 0.05 (5.77 sigma > 0.15): GEMM 1's producers evaluate the GELU
+    difference directly instead of by its Taylor polynomial."""
+    d = _inputs(256, 64, 128, 64, 256, 128, seed=21)
+    g, G = _run(dust, d, 0.05, 0.95, 8, 77)
+    ref = _ref(orc, d, 0.05, 0.95, 8, 77)
+    assert rel_l2(g, ref["g"]) <= G_TOL
+    assert rel_l2(G, ref["G"]) <= GW_TOL
