@@ -89,41 +89,68 @@ __global__ void softmax_rows_kernel(const float* __restrict__ z, int V, int ldp,
 
 struct DhArgs {
     const float* y1;
-    const float* h0;  // GELU(y1), same function as below
+    const float* h0;      // GELU(y1), same function as below
+    const float4* coef;   // Taylor coefficients of the GELU difference
+    int taylor;
     int T, Tp, C, nd;
     uint32_t draw_first, token0, layer;  // draw_first = draw0 + i0
     float sigma;
     __nv_bfloat16* A1;  // rows x 2C
 };
 
-// One thread per (draw in chunk, token, channel block of 4).
+// One thread per (token, channel block of 4), looping over the chunk's draws:
+// the clean activations (or the Taylor coefficients of the GELU difference)
+// are read once and reused for every draw; the A1 rows of one draw are written
+// by consecutive threads.
 __global__ void interior_dh_kernel(const DhArgs a, const PhiloxKeys keys) {
     const int nblk = a.C >> 2;
-    const int64_t n = static_cast<int64_t>(a.nd) * a.Tp * nblk;
+    const int64_t n = static_cast<int64_t>(a.Tp) * nblk;
     for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
          idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int j = static_cast<int>(idx % nblk);
-        const int64_t rest = idx / nblk;
-        const int t = static_cast<int>(rest % a.Tp);
-        const int i = static_cast<int>(rest / a.Tp);
-        __nv_bfloat16* row = a.A1 + chunk_row(t, i, a.nd) * (2 * static_cast<int64_t>(a.C));
-        __nv_bfloat16 h[4], l[4];
-        if (t < a.T) {
-            const float4 nrm = words_to_normals(
-                philox4x32_10(j, a.token0 + t, a.draw_first + i, a.layer, keys));
-            const int64_t e4 = static_cast<int64_t>(t) * (a.C / 4) + j;
-            const float4 y = __ldg(reinterpret_cast<const float4*>(a.y1) + e4);
-            const float4 g = __ldg(reinterpret_cast<const float4*>(a.h0) + e4);
-            split_bf16(gelu_as(fmaf(a.sigma, nrm.x, y.x)) - g.x, h[0], l[0]);
-            split_bf16(gelu_as(fmaf(a.sigma, nrm.y, y.y)) - g.y, h[1], l[1]);
-            split_bf16(gelu_as(fmaf(a.sigma, nrm.z, y.z)) - g.z, h[2], l[2]);
-            split_bf16(gelu_as(fmaf(a.sigma, nrm.w, y.w)) - g.w, h[3], l[3]);
-        } else {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) h[k] = l[k] = __float2bfloat16_rn(0.f);
+        const int t = static_cast<int>(idx / nblk);
+        const bool valid = t < a.T;
+        const int64_t e4 = static_cast<int64_t>(valid ? t : 0) * (a.C / 4) + j;
+        float4 y = make_float4(0.f, 0.f, 0.f, 0.f), g = y, c1 = y, c2 = y, c3 = y, c4 = y;
+        if (valid) {
+            if (a.taylor) {
+                const float4* cp = a.coef + e4 * 4;
+                c1 = __ldg(cp); c2 = __ldg(cp + 1); c3 = __ldg(cp + 2); c4 = __ldg(cp + 3);
+            } else {
+                y = __ldg(reinterpret_cast<const float4*>(a.y1) + e4);
+                g = __ldg(reinterpret_cast<const float4*>(a.h0) + e4);
+            }
         }
-        *reinterpret_cast<uint2*>(row + 4 * j) = pack4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint2*>(row + a.C + 4 * j) = pack4(l[0], l[1], l[2], l[3]);
+        const BlockHalf bh = philox_block_half(j, a.layer, keys);
+        for (int i = 0; i < a.nd; ++i) {
+            __nv_bfloat16* row = a.A1 + chunk_row(t, i, a.nd) * (2 * static_cast<int64_t>(a.C));
+            __nv_bfloat16 h[4], l[4];
+            if (valid) {
+                const float4 nrm = words_to_normals(
+                    philox_rest(philox_draw_half(a.draw_first + i, a.token0 + t, keys), bh, keys));
+                float d[4];
+                if (a.taylor) {
+                    const float e[4] = {a.sigma * nrm.x, a.sigma * nrm.y, a.sigma * nrm.z,
+                                        a.sigma * nrm.w};
+                    d[0] = e[0] * fmaf(e[0], fmaf(e[0], fmaf(e[0], c4.x, c3.x), c2.x), c1.x);
+                    d[1] = e[1] * fmaf(e[1], fmaf(e[1], fmaf(e[1], c4.y, c3.y), c2.y), c1.y);
+                    d[2] = e[2] * fmaf(e[2], fmaf(e[2], fmaf(e[2], c4.z, c3.z), c2.z), c1.z);
+                    d[3] = e[3] * fmaf(e[3], fmaf(e[3], fmaf(e[3], c4.w, c3.w), c2.w), c1.w);
+                } else {
+                    d[0] = gelu_as(fmaf(a.sigma, nrm.x, y.x)) - g.x;
+                    d[1] = gelu_as(fmaf(a.sigma, nrm.y, y.y)) - g.y;
+                    d[2] = gelu_as(fmaf(a.sigma, nrm.z, y.z)) - g.z;
+                    d[3] = gelu_as(fmaf(a.sigma, nrm.w, y.w)) - g.w;
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) split_bf16(d[k], h[k], l[k]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) h[k] = l[k] = __float2bfloat16_rn(0.f);
+            }
+            *reinterpret_cast<uint2*>(row + 4 * j) = pack4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint2*>(row + a.C + 4 * j) = pack4(l[0], l[1], l[2], l[3]);
+        }
     }
 }
 
@@ -324,7 +351,7 @@ InteriorPlan interior_plan(int64_t T, int64_t d_in, int64_t C, int64_t dm, int64
     w.take(kCtlBytes);
     P.off_p = w.take(static_cast<size_t>(T * round_up(V, 4)) * 4);
     P.off_h0 = w.take(static_cast<size_t>(T * C) * 4);
-    P.off_coef = w.take(P.fused ? static_cast<size_t>(T * C) * 16 : 0);
+    P.off_coef = w.take(P.fused ? 0 : static_cast<size_t>(T * C) * 16);
     P.off_a1 = w.take(P.fused ? 0 : rows * static_cast<size_t>(2 * C) * 2);
     P.off_du = w.take(rows * static_cast<size_t>(dm) * 4);
     P.off_a2 = w.take(rows * static_cast<size_t>(2 * dm) * 2);
@@ -403,9 +430,13 @@ extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, cons
     if ((st = launch_status()) != DUST_OK) return st;
     float* h0 = reinterpret_cast<float*>(w + P.off_h0);
     if ((st = gelu_launch(y1, T * C, h0, s)) != DUST_OK) return st;
-    // Small sigma: GELU(y1 + d) - GELU(y1) by its fourth-order Taylor
-    // polynomial in d (coefficients once per call), exact form otherwise.
-    const bool taylor = P.fused && 5.77 * nz.sigma <= 0.15;
+    // Staged A operand (d_model > 512), small sigma: GELU(y1 + d) - GELU(y1)
+    // by its fourth-order Taylor polynomial in d, coefficients once per call
+    // and read once per element for all draws of a chunk.  GEMM 1 with the A
+    // operand on chip evaluates the difference directly: there the
+    // coefficients would be read once per draw, which costs more than the
+    // GELU (measured).
+    const bool taylor = !P.fused && 5.77 * nz.sigma <= 0.15;
     void* coef = w + P.off_coef;
     if (taylor && (st = gelu_taylor_launch(y1, T * C, coef, s)) != DUST_OK) return st;
 
@@ -419,9 +450,10 @@ extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, cons
                                    nz.sigma, keys, du, status, s);
             if (st != DUST_OK) return st;
         } else {
-            DhArgs da{y1, h0, Ti, static_cast<int>(P.Tp), Ci, nd,
-                      nz.draw0 + static_cast<uint32_t>(i0), nz.token0, nz.layer, nz.sigma, A1};
-            interior_dh_kernel<<<grid_cap(rows * (C / 4), 256), 256, 0, s>>>(da, keys);
+            DhArgs da{y1, h0, static_cast<const float4*>(coef), taylor ? 1 : 0, Ti,
+                      static_cast<int>(P.Tp), Ci, nd, nz.draw0 + static_cast<uint32_t>(i0),
+                      nz.token0, nz.layer, nz.sigma, A1};
+            interior_dh_kernel<<<grid_cap(P.Tp * (C / 4), 256), 256, 0, s>>>(da, keys);
             if ((st = launch_status()) != DUST_OK) return st;
             st = gemm_bf16_launch(A1, false, 2 * C, W2, false, C, rows, d_model, 2 * C, C, 1, du,
                                   d_model, status, s);

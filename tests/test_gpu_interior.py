@@ -123,10 +123,12 @@ def test_interior_full_size_sequences(dust, orc, name, K, seqs):
     assert rel_l2(G, ref_G) <= 1e-4
 
 
-def test_interior_exact_gelu_path(dust, orc):
-    """sigma = 0.05 (5.77 sigma > 0.15): GEMM 1's producers evaluate the GELU
-    difference directly instead of by its Taylor polynomial."""
-    d = _inputs(256, 64, 128, 64, 256, 128, seed=21)
+@pytest.mark.parametrize("dm", [64, 576])
+def test_interior_exact_gelu_path(dust, orc, dm):
+    """sigma = 0.05 (5.77 sigma > 0.15): the GELU difference is evaluated
+    directly instead of by its Taylor polynomial, in GEMM 1's producers
+    (d_model 64) and in the staged A operand (d_model 576)."""
+    d = _inputs(256, 64, 128, dm, 256, 128, seed=21)
     g, G = _run(dust, d, 0.05, 0.95, 8, 77)
     ref = _ref(orc, d, 0.05, 0.95, 8, 77)
     assert rel_l2(g, ref["g"]) <= G_TOL
