@@ -60,8 +60,17 @@ __global__ void __launch_bounds__(kChunk)
 }
 
 // Exclusive prefix sum of n words in one CTA of 1024 threads; out[n] = total.
+// Block 1 of a two-block launch scans (in2, out2) instead, with each word w
+// taken as ceil(w / kPiece) when pieces2 is set (the pieces of each id).
 __global__ void __launch_bounds__(1024)
-    exclusive_scan_kernel(const uint32_t* __restrict__ in, uint32_t* __restrict__ out, int64_t n) {
+    exclusive_scan_kernel(const uint32_t* __restrict__ in, uint32_t* __restrict__ out, int64_t n,
+                          const uint32_t* __restrict__ in2 = nullptr,
+                          uint32_t* __restrict__ out2 = nullptr, int pieces2 = 0) {
+    const bool second = blockIdx.x == 1;
+    if (second) {
+        in = in2;
+        out = out2;
+    }
     __shared__ uint32_t wsum[32];
     __shared__ uint32_t carry_s;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -74,6 +83,7 @@ __global__ void __launch_bounds__(1024)
         for (int k = 0; k < 4; ++k) {
             const int64_t i = base + 4 * tid + k;
             v[k] = i < n ? in[i] : 0u;
+            if (second && pieces2) v[k] = (v[k] + kPiece - 1) / kPiece;
             local += v[k];
         }
         uint32_t incl = local;
@@ -165,12 +175,6 @@ __global__ void key_counts_kernel(const uint32_t* __restrict__ keys, int T, int 
     counts[key] = static_cast<uint32_t>(e - k);
 }
 
-__global__ void piece_counts_kernel(const uint32_t* __restrict__ counts, int V,
-                                    uint32_t* __restrict__ npieces) {
-    const int v = blockIdx.x * blockDim.x + threadIdx.x;
-    if (v < V) npieces[v] = (counts[v] + kPiece - 1) / kPiece;
-}
-
 struct Piece {
     int32_t v, start, len, multi;
 };
@@ -230,31 +234,29 @@ __global__ void piece_sum_kernel(const float* __restrict__ g, const int32_t* __r
 }
 
 // Rows with no token -> 0; rows with several pieces -> sum of partials in
-// piece order; rows with one piece are already final.  One thread per
-// (row, column group of 4), flat over the table.
+// piece order; rows with one piece are already final.  blockIdx.y = row.
 template <bool VEC>
 __global__ void rows_finish_kernel(const uint32_t* __restrict__ poff, int V, int d,
                                    const float* __restrict__ partial, float* __restrict__ G_E) {
-    const int w = VEC ? d >> 2 : d;  // items per row
-    const int64_t n = static_cast<int64_t>(V) * w;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int v = static_cast<int>(i / w);
-        const int c = static_cast<int>(i - static_cast<int64_t>(v) * w);
+    for (int v = blockIdx.y; v < V; v += gridDim.y) {
         const uint32_t p0 = __ldg(poff + v), np = __ldg(poff + v + 1) - p0;
         if (np == 1) continue;
-        if (VEC) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (uint32_t k = 0; k < np; ++k) {
-                const float4 x = __ldg(reinterpret_cast<const float4*>(
-                                           partial + static_cast<int64_t>(p0 + k) * d) + c);
-                acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+        const int w = VEC ? d >> 2 : d;
+        for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < w; c += gridDim.x * blockDim.x) {
+            if (VEC) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (uint32_t k = 0; k < np; ++k) {
+                    const float4 x = __ldg(reinterpret_cast<const float4*>(
+                                               partial + static_cast<int64_t>(p0 + k) * d) + c);
+                    acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+                }
+                reinterpret_cast<float4*>(G_E + static_cast<int64_t>(v) * d)[c] = acc;
+            } else {
+                float acc = 0.f;
+                for (uint32_t k = 0; k < np; ++k)
+                    acc += __ldg(partial + static_cast<int64_t>(p0 + k) * d + c);
+                G_E[static_cast<int64_t>(v) * d + c] = acc;
             }
-            reinterpret_cast<float4*>(G_E + static_cast<int64_t>(v) * d)[c] = acc;
-        } else {
-            float acc = 0.f;
-            for (uint32_t k = 0; k < np; ++k) acc += __ldg(partial + static_cast<int64_t>(p0 + k) * d + c);
-            G_E[static_cast<int64_t>(v) * d + c] = acc;
         }
     }
 }
@@ -262,7 +264,7 @@ __global__ void rows_finish_kernel(const uint32_t* __restrict__ poff, int V, int
 struct EmbedPlan {
     int nchunks, passes;
     int64_t np_max;
-    size_t off_k0, off_v0, off_k1, off_v1, off_hist, off_offs, off_cnt, off_seg, off_np, off_poff,
+    size_t off_k0, off_v0, off_k1, off_v1, off_hist, off_offs, off_cnt, off_seg, off_poff,
         off_table, off_part, bytes;
 };
 
@@ -285,7 +287,6 @@ EmbedPlan embed_plan(int64_t T, int64_t d, int64_t V) {
     P.off_offs = w.take((static_cast<size_t>(256) * P.nchunks + 1) * 4);
     P.off_cnt = w.take(Vn * 4);
     P.off_seg = w.take(Vn * 4);
-    P.off_np = w.take(Vn * 4);
     P.off_poff = w.take(Vn * 4);
     P.off_table = w.take(static_cast<size_t>(P.np_max) * sizeof(Piece));
     P.off_part = w.take(static_cast<size_t>(P.np_max) * static_cast<size_t>(d) * 4);
@@ -328,7 +329,6 @@ extern "C" dust_status dust_embed_scatter(const float* g_hat, const int32_t* ids
     uint32_t* offs = reinterpret_cast<uint32_t*>(w + P.off_offs);
     uint32_t* cnt = reinterpret_cast<uint32_t*>(w + P.off_cnt);
     uint32_t* seg = reinterpret_cast<uint32_t*>(w + P.off_seg);
-    uint32_t* np = reinterpret_cast<uint32_t*>(w + P.off_np);
     uint32_t* poff = reinterpret_cast<uint32_t*>(w + P.off_poff);
     Piece* table = reinterpret_cast<Piece*>(w + P.off_table);
     float* part = reinterpret_cast<float*>(w + P.off_part);
@@ -339,9 +339,13 @@ extern "C" dust_status dust_embed_scatter(const float* g_hat, const int32_t* ids
     if ((st = launch_status()) != DUST_OK) return st;
     for (int pass = 0; pass < P.passes; ++pass) {
         const int shift = 8 * pass;
+        // the last pass writes the permutation straight into perm_out
+        int32_t* vout = (pass == P.passes - 1 && perm_out) ? perm_out : v1;
         radix_hist_kernel<<<P.nchunks, kChunk, 0, s>>>(k0, Ti, shift, P.nchunks, hist);
         exclusive_scan_kernel<<<1, 1024, 0, s>>>(hist, offs, static_cast<int64_t>(256) * P.nchunks);
-        radix_scatter_kernel<<<P.nchunks, kChunk, 0, s>>>(k0, v0, Ti, shift, P.nchunks, offs, k1, v1);
+        radix_scatter_kernel<<<P.nchunks, kChunk, 0, s>>>(k0, v0, Ti, shift, P.nchunks, offs, k1,
+                                                          vout);
+        if (vout != v1) v1 = vout;
         if ((st = launch_status()) != DUST_OK) return st;
         uint32_t* tk = k0; k0 = k1; k1 = tk;
         int32_t* tv = v0; v0 = v1; v1 = tv;
@@ -349,36 +353,35 @@ extern "C" dust_status dust_embed_scatter(const float* g_hat, const int32_t* ids
     // k0/v0 now hold the sorted keys and the permutation.
     DUST_CUDA_TRY(cudaMemsetAsync(cnt, 0, static_cast<size_t>(V + 1) * 4, s));
     key_counts_kernel<<<tb, 256, 0, s>>>(k0, Ti, Vi, cnt);
-    exclusive_scan_kernel<<<1, 1024, 0, s>>>(cnt, seg, V);
+    // segment starts and piece offsets in one launch
+    exclusive_scan_kernel<<<2, 1024, 0, s>>>(cnt, seg, V, cnt, poff, 1);
     const unsigned vb = static_cast<unsigned>(ceil_div(V, 256));
-    piece_counts_kernel<<<vb, 256, 0, s>>>(cnt, Vi, np);
-    exclusive_scan_kernel<<<1, 1024, 0, s>>>(np, poff, V);
     piece_table_kernel<<<vb, 256, 0, s>>>(seg, cnt, poff, Vi, table);
     if ((st = launch_status()) != DUST_OK) return st;
     // Pieces are at most np_max; launch enough CTAs to cover the usual count
     // and let the grid-stride loop take the rest.
     const bool vec = (d % 4 == 0) && aligned(g_hat, 16) && aligned(G_E, 16);
+    // one CTA per piece
     const int threads = static_cast<int>(std::min<int64_t>(256, round_up(vec ? d / 4 : d, 32)));
     const unsigned pgrid = static_cast<unsigned>(std::min<int64_t>(P.np_max, 148 * 64));
     timer_begin(s);
     if (vec)
-        piece_sum_kernel<true><<<pgrid, threads, 0, s>>>(g_hat, v0, table, poff, Vi, di,
-                                                         G_E, part);
+        piece_sum_kernel<true><<<pgrid, threads, 0, s>>>(g_hat, v0, table, poff, Vi, di, G_E,
+                                                         part);
     else
-        piece_sum_kernel<false><<<pgrid, threads, 0, s>>>(g_hat, v0, table, poff, Vi, di,
-                                                          G_E, part);
+        piece_sum_kernel<false><<<pgrid, threads, 0, s>>>(g_hat, v0, table, poff, Vi, di, G_E,
+                                                          part);
     timer_end(s);
     if ((st = launch_status()) != DUST_OK) return st;
     {
-        const int64_t items = V * (vec ? d / 4 : d);
-        const unsigned fb = static_cast<unsigned>(std::min<int64_t>(ceil_div(items, 256), 148 * 32));
+        const int64_t w = vec ? d / 4 : d;
+        const dim3 fg(static_cast<unsigned>(ceil_div(w, 128)),
+                      static_cast<unsigned>(std::min<int64_t>(V, 65535)));
         if (vec)
-            rows_finish_kernel<true><<<fb, 256, 0, s>>>(poff, Vi, di, part, G_E);
+            rows_finish_kernel<true><<<fg, 128, 0, s>>>(poff, Vi, di, part, G_E);
         else
-            rows_finish_kernel<false><<<fb, 256, 0, s>>>(poff, Vi, di, part, G_E);
+            rows_finish_kernel<false><<<fg, 128, 0, s>>>(poff, Vi, di, part, G_E);
     }
     if ((st = launch_status()) != DUST_OK) return st;
-    if (perm_out) DUST_CUDA_TRY(cudaMemcpyAsync(perm_out, v0, static_cast<size_t>(T) * 4,
-                                                cudaMemcpyDeviceToDevice, s));
     return DUST_OK;
 }

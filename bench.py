@@ -444,17 +444,23 @@ def run_dust(args):
     stream = torch.cuda.current_stream()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    timer = dust.KernelTimer(capacity=max(1, args.steps) * 64)
     barrier()
     with ClockSampler(local) as clocks:
-        with timer:
-            e0.record(stream)
-            for _ in range(args.steps):
-                step()
-            e1.record(stream)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
         e1.synchronize()
     barrier()
     ms = e0.elapsed_time(e1)
+    # The dominant kernel's launches, timed in a second pass of the same steps
+    # by events the library records around them on their stream (kept out of
+    # the timed region above, where they would add host work per launch).
+    timer = dust.KernelTimer(capacity=max(1, args.steps) * 64)
+    with timer:
+        for _ in range(args.steps):
+            step()
+    torch.cuda.synchronize()
     kernel_ms = timer.total_ms() / max(args.steps, 1)
     if dust.workspace_status(ws) != 0:
         raise SystemExit("kernel status word set during the timed steps")
