@@ -239,6 +239,15 @@ dust_status dust_gemm_bf16(const void* A, int a_mn, int64_t lda, const void* B, 
                            void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Failure-path check of the bounded waits: a one-warp kernel waits on a
+ * barrier that nothing arrives at, gives up after limit_ns (1 .. 1e9) and
+ * records DUST_ERR_TIMEOUT in the status word of `ws` (>= 256 bytes), exactly
+ * as a stalled pipeline inside the estimators would.  Read it back with
+ * dust_workspace_status.
+ */
+dust_status dust_wait_selftest(void* ws, uint64_t limit_ns, void* stream);
+
+/*
  * Benchmark hook.  While set, every launch of an entry point's dominant
  * kernel (the head's draw kernel, the interior layer's re-forward GEMM with
  * the cross-entropy epilogue, the embedding's piece sums) is bracketed on its

@@ -70,3 +70,14 @@ def test_embed_bad_id_sets_status(dust):
     G, perm, st = _run(dust, g, ids, 10)
     assert st == 6
     assert G[3].sum() == 0 and G[4].sum() == 4
+
+
+def test_embed_without_perm_output(dust):
+    """perm_out = NULL gives the same rows as the call that returns it."""
+    rng = np.random.default_rng(4)
+    g = rng.standard_normal((700, 12)).astype(np.float32)
+    ids = W.zipf_ids(2, 700, 90)
+    G1, _, _ = dust.embed_scatter(to_dev(g), to_dev(ids), 90, want_perm=False)
+    G2, _, _ = dust.embed_scatter(to_dev(g), to_dev(ids), 90)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(G1.cpu().numpy(), G2.cpu().numpy())

@@ -153,3 +153,13 @@ def test_head_scale_config_sampled(dust, orc):
     gb = torch.from_numpy(W.bf16_round(g)).cuda().double()
     ref_G = (gb.T @ torch.from_numpy(wl["x"]).cuda().double()).cpu().numpy()
     assert rel_l2(G, ref_G) <= 1e-4
+
+
+def test_head_without_g_output(dust, orc):
+    """g_hat = NULL: only G_W is produced, identical to the call that also
+    returns g."""
+    x, z, y = _inputs(64, 32, 512, seed=12)
+    _, G1, _ = dust.head_estimate(to_dev(z), to_dev(y), to_dev(x), 0.05, 8, 3, want_g=False)
+    g2, G2, _ = dust.head_estimate(to_dev(z), to_dev(y), to_dev(x), 0.05, 8, 3)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(G1.cpu().numpy(), G2.cpu().numpy())
