@@ -33,9 +33,8 @@ struct HeadArgs {
     const int32_t* targets;
     int T, V, nblk, K, Q, chunk;
     uint32_t draw0, token0, layer;
-    float sig_l2e;  // sigma * log2(e)
-    float sigma;
-    float inv_ks;   // 1 / (K sigma)
+    float sig_l2e;  // s = sigma * log2(e): the kernel works with b = s a
+    float g_scale;  // 1 / (K sigma s): turns the b-scaled sums into g
     float* g_hat;   // T x V fp32, may be null
     __nv_bfloat16* gbf;
     int64_t ldg;    // row stride of gbf (elements)
@@ -107,7 +106,7 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int NT = ONE_WARP ? 32 : static_cast<int>(blockDim.x);
-    const int nw = NT >> 5;
+    if (!ONE_WARP && tid < 16) red[tid >> 3][tid & 7] = 0.f;  // slots of absent warps
     const int t = blockIdx.x / A.Q;
     const int q = blockIdx.x - t * A.Q;
     const int i_begin = q * A.chunk;
@@ -185,11 +184,13 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
         for (int b = 0; b < NB; ++b) w[b] = philox_rest(dh, bh[b], keys);
         // Blocks past the vocabulary (only in the last block row) carry real
         // noise of unused counters; their probabilities are zero and their
-        // accumulators are never written, so they change nothing.
+        // accumulators are never written, so they change nothing.  a holds
+        // b = s a: exp(sigma a) = 2^b, and the accumulators are rescaled once
+        // at the end.
         float a[NB][4];
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-            const float4 n = words_to_normals(w[b]);
+            const float4 n = words_to_normals(w[b], A.sig_l2e);
             a[b][0] = n.x;
             a[b][1] = n.y;
             a[b][2] = n.z;
@@ -198,10 +199,10 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
         float pb[NB];
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-            float q = p[b][0] * ex2_approx(A.sig_l2e * a[b][0]);
-            q = fmaf(p[b][1], ex2_approx(A.sig_l2e * a[b][1]), q);
-            q = fmaf(p[b][2], ex2_approx(A.sig_l2e * a[b][2]), q);
-            pb[b] = fmaf(p[b][3], ex2_approx(A.sig_l2e * a[b][3]), q);
+            float q = p[b][0] * ex2_approx(a[b][0]);
+            q = fmaf(p[b][1], ex2_approx(a[b][1]), q);
+            q = fmaf(p[b][2], ex2_approx(a[b][2]), q);
+            pb[b] = fmaf(p[b][3], ex2_approx(a[b][3]), q);
         }
         float part = pb[0];
 #pragma unroll
@@ -222,11 +223,16 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
             if (lane == 0) red[buf][warp] = part;
             if (owner) red_y[buf] = ay;
             __syncthreads();
-            S = 0.f;
-            for (int w = 0; w < nw; ++w) S += red[buf][w];
+            // Eight warp partials (absent warps read zero), summed by a
+            // butterfly over lanes 0..7: every lane forms the same sum.
+            S = red[buf][lane & 7];
+            S += __shfl_xor_sync(0xFFFFFFFFu, S, 1);
+            S += __shfl_xor_sync(0xFFFFFFFFu, S, 2);
+            S += __shfl_xor_sync(0xFFFFFFFFu, S, 4);
             ay = (y >= 0) ? red_y[buf] : 0.f;
         }
-        const float dl = log_pos(S) - A.sigma * ay;
+        // sigma a_y = b_y ln 2.
+        const float dl = fmaf(ay, -0.69314718055994531f, log_pos(S));
         sdl += dl;
 #pragma unroll
         for (int b = 0; b < NB; ++b)
@@ -247,7 +253,7 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
             if (j >= A.nblk) continue;
             float g[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) g[k] = (s1[b][k] - mean * s0[b][k]) * A.inv_ks;
+            for (int k = 0; k < 4; ++k) g[k] = (s1[b][k] - mean * s0[b][k]) * A.g_scale;
             if (vec) {
                 if (grow) *reinterpret_cast<float4*>(grow + 4 * j) = make_float4(g[0], g[1], g[2], g[3]);
                 __nv_bfloat162 lo = __floats2bfloat162_rn(g[0], g[1]);
@@ -299,7 +305,7 @@ __global__ void head_finalize_kernel(const HeadArgs A) {
         s0 += A.part_s0[off];
     }
     const float mean = sdl / static_cast<float>(A.K);
-    const float g = (s1 - mean * s0) * A.inv_ks;
+    const float g = (s1 - mean * s0) * A.g_scale;
     if (A.g_hat) A.g_hat[static_cast<int64_t>(t) * A.V + c] = g;
     A.gbf[static_cast<int64_t>(t) * A.ldg + c] = __float2bfloat16_rn(g);
 }
@@ -405,9 +411,10 @@ extern "C" dust_status dust_head_estimate(const float* logits, const int32_t* ta
     A.draw0 = nz.draw0;
     A.token0 = nz.token0;
     A.layer = nz.layer;
-    A.sigma = nz.sigma;
-    A.sig_l2e = static_cast<float>(static_cast<double>(nz.sigma) * 1.4426950408889634);
-    A.inv_ks = static_cast<float>(1.0 / (static_cast<double>(nz.num_draws) * nz.sigma));
+    const double s_l2e = static_cast<double>(nz.sigma) * 1.4426950408889634;
+    A.sig_l2e = static_cast<float>(s_l2e);
+    A.g_scale = static_cast<float>(
+        1.0 / (static_cast<double>(nz.num_draws) * nz.sigma * static_cast<double>(A.sig_l2e)));
     A.g_hat = g_hat;
     A.gbf = reinterpret_cast<__nv_bfloat16*>(w + P.off_gbf);
     A.ldg = P.ldg;

@@ -145,33 +145,29 @@ __device__ __forceinline__ float lg2_approx(float x) {
 }
 
 // -2 ln u for the uniforms of the noise, u in [2^-24, 1 - 2^-24].  Near 1
-// (v = 1 - u < 1/10, exact since u > 1/2) the series -ln(1 - v) = v + v^2/2
-// + ... + v^6/6 (truncation below 2e-8 relative); elsewhere the hardware
-// log2, whose absolute error (about 1e-7) is at most 1e-6 relative there
-// because |ln u| >= 0.105.  Both are computed and one is selected, so lanes
-// do not diverge.
+// (v = 1 - u < 1/50, exact since u > 1/2) the series -ln(1 - v) = v + v^2/2
+// + v^3/3 (the dropped terms are below 2.1e-6 of the sum); elsewhere the
+// hardware log2, whose absolute error (about 3e-7 in -2 ln u) moves the radius
+// by at most 1e-6 because the radius is at least 0.2 there.  Both are
+// computed and one is selected, so lanes do not diverge.
 __device__ __forceinline__ float neg2_log_uniform(float u) {
     const float v = 1.0f - u;
-    float q = fmaf(v, 1.0f / 6.0f, 0.2f);
-    q = fmaf(v, q, 0.25f);
-    q = fmaf(v, q, 1.0f / 3.0f);
-    q = fmaf(v, q, 0.5f);
-    q = fmaf(v, q, 1.0f);
-    const float near1 = (2.0f * v) * q;
+    const float near1 = v * fmaf(v, fmaf(v, 2.0f / 3.0f, 1.0f), 2.0f);
     const float far = lg2_approx(u) * -1.3862943611198906f;  // -2 ln 2 log2 u
-    return v < 0.1f ? near1 : far;
+    return v < 0.02f ? near1 : far;
 }
 
 // Box-Muller pair from two words: rho = sqrt(-2 ln u_even), theta =
-// 2 pi u_odd; a_cos = rho cos theta, a_sin = rho sin theta.  With
+// 2 pi u_odd; a_cos = rho cos theta, a_sin = rho sin theta, both multiplied by
+// `scale` (a kernel that only ever uses s a folds s into the radius).  With
 // theta' = 2 pi u_odd - pi in (-pi, pi), cos theta = -cos theta' and
 // sin theta = -sin theta'; sin and cos of theta' come from the hardware
 // approximations (absolute error about 4e-7 on that interval), so the normals
 // are within about 3e-6 of the exact ones at the largest radius (5.77).
 __device__ __forceinline__ void box_muller(uint32_t w_even, uint32_t w_odd, float& a_cos,
-                                           float& a_sin) {
+                                           float& a_sin, float scale = 1.0f) {
     const float x = neg2_log_uniform(word_to_uniform(w_even));
-    const float neg_rho = -(x * rsqrt_approx(x));
+    const float neg_rho = (x * rsqrt_approx(x)) * -scale;
     const float th = fmaf(word_to_uniform(w_odd), 6.2831853071795865f, -3.1415926535897932f);
     float s, c;
     __sincosf(th, &s, &c);
@@ -179,10 +175,10 @@ __device__ __forceinline__ void box_muller(uint32_t w_even, uint32_t w_odd, floa
     a_sin = neg_rho * s;
 }
 
-__device__ __forceinline__ float4 words_to_normals(uint4 w) {
+__device__ __forceinline__ float4 words_to_normals(uint4 w, float scale = 1.0f) {
     float4 a;
-    box_muller(w.x, w.y, a.x, a.y);
-    box_muller(w.z, w.w, a.z, a.w);
+    box_muller(w.x, w.y, a.x, a.y, scale);
+    box_muller(w.z, w.w, a.z, a.w, scale);
     return a;
 }
 
