@@ -161,6 +161,7 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
     const int yb = (y >= 0) ? yblk / NT : 0;
     const int yc = y & 3;
     const int ylane = (y >= 0) ? (yblk % NT) & 31 : 0;
+    const bool ywarp = (y >= 0) && (((yblk % NT) >> 5) == warp);
 
     BlockHalf bh[NB];
 #pragma unroll
@@ -208,7 +209,7 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
 #pragma unroll
         for (int b = 1; b < NB; ++b) part += pb[b];
         float ay = 0.f;
-        if (owner) {
+        if (ywarp) {  // warp-uniform: only the warp that holds the target's block
 #pragma unroll
             for (int b = 0; b < NB; ++b)
                 if (b == yb) ay = yc == 0 ? a[b][0] : yc == 1 ? a[b][1] : yc == 2 ? a[b][2] : a[b][3];
