@@ -441,13 +441,17 @@ extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, cons
     if (taylor && (st = gelu_taylor_launch(y1, T * C, coef, s)) != DUST_OK) return st;
 
     const int nseq = static_cast<int>(T / seq_len);
+    const bool fuse_ema = P.fused && seq_len % kRowBlock == 0 && P.Tp == T;
     for (int i0 = 0; i0 < K; i0 += P.nd) {
         const int nd = std::min(P.nd, K - i0);
         const int64_t rows = nd * P.Tp;
         if (P.fused) {
+            // Whole token blocks per sequence: the EMA runs in GEMM 1's
+            // epilogue, one CTA walking a sequence's blocks for one draw.
             st = reforward1_launch(y1, h0, coef, taylor, W2, T, P.Tp, C, d_model, nd,
                                    nz.draw0 + static_cast<uint32_t>(i0), nz.token0, nz.layer,
-                                   nz.sigma, keys, du, status, s);
+                                   nz.sigma, keys, du, fuse_ema ? A2 : nullptr, seq_len,
+                                   ema_decay, status, s);
             if (st != DUST_OK) return st;
         } else {
             DhArgs da{y1, h0, static_cast<const float4*>(coef), taylor ? 1 : 0, Ti,
@@ -459,12 +463,15 @@ extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, cons
                                   d_model, status, s);
             if (st != DUST_OK) return st;
         }
-        if (P.Tp != T)
-            DUST_CUDA_TRY(cudaMemsetAsync(A2, 0, static_cast<size_t>(rows * 2 * d_model) * 2, s));
-        interior_ema_kernel<<<static_cast<unsigned>(nd * nseq * ceil_div(d_model, 32)),
-                              32 * kEmaWarps, 0, s>>>(du, nd, nseq, static_cast<int>(seq_len), dmi,
-                                                      ema_decay, A2);
-        if ((st = launch_status()) != DUST_OK) return st;
+        if (!fuse_ema) {
+            if (P.Tp != T)
+                DUST_CUDA_TRY(
+                    cudaMemsetAsync(A2, 0, static_cast<size_t>(rows * 2 * d_model) * 2, s));
+            interior_ema_kernel<<<static_cast<unsigned>(nd * nseq * ceil_div(d_model, 32)),
+                                  32 * kEmaWarps, 0, s>>>(du, nd, nseq, static_cast<int>(seq_len),
+                                                          dmi, ema_decay, A2);
+            if ((st = launch_status()) != DUST_OK) return st;
+        }
         st = gemm_ce_launch(A2, 2 * d_model, W_head, d_model, rows, V, 2 * d_model, d_model, p,
                             ldp, targets, T, nd, i0, dl, status, s);
         if (st != DUST_OK) return st;

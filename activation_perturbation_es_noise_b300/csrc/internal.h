@@ -96,7 +96,9 @@ bool encode_bf16_2d(CUtensorMap* map, const void* ptr, int64_t inner, int64_t ou
 struct PhiloxKeys;
 
 // Interior GEMM 1 with its A operand (the GELU difference of the perturbed
-// output, split bf16) generated on chip: du = dh W2^T for nd draws.
+// output, split bf16) generated on chip: du = dh W2^T for nd draws.  With A2
+// non-null (seq_len a multiple of 128, T = Tp) the epilogue also runs the
+// per-sequence EMA and writes A2 = [hi | lo] of de instead of du.
 bool reforward1_supported(int64_t C, int64_t dm);
 dust_status gelu_launch(const float* y, int64_t n, float* h, cudaStream_t s);
 // Taylor coefficients (4 per channel, T x C/4 x 4 float4) of the GELU difference.
@@ -105,7 +107,8 @@ dust_status reforward1_launch(const float* y1, const float* h0, const void* coef
                               const void* W2, int64_t T, int64_t Tp, int64_t C,
                               int64_t dm, int nd, uint32_t draw_first, uint32_t token0,
                               uint32_t layer, float sigma, const PhiloxKeys& keys, float* du,
-                              uint32_t* status, cudaStream_t s);
+                              void* A2, int64_t seq_len, float lam, uint32_t* status,
+                              cudaStream_t s);
 
 // rows x cols fp32 (row stride ld_in) -> bf16 (row stride ld_out, padding
 // columns set to zero).

@@ -39,8 +39,12 @@ struct RefArgs {
     const float* h0;  // T x C: GELU(y1) (exact path)
     const float4* coef;  // T x C/4 x 4: Taylor coefficients of the GELU difference
     int taylor;          // use the Taylor form (small sigma)
-    float* du;        // rows x dm
+    float* du;        // rows x dm (plain epilogue)
+    __nv_bfloat16* A2;  // rows x 2 dm: [hi | lo] of the EMA output (EMA epilogue)
     int T, C, dm, nd;
+    int ema;    // 1: work item = (sequence, draw), EMA in the epilogue
+    int tiles;  // token blocks per sequence (EMA epilogue)
+    float lam;  // EMA decay
     uint32_t draw_first, token0, layer;
     float sigma;
     uint32_t* status;
@@ -59,10 +63,37 @@ __device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
 }
 
+// Named barrier over the 128 threads of one epilogue column group.
+__device__ __forceinline__ void group_sync(int id) {
+    asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
+}
+
+// True on every producer thread iff `ok` holds on all of them (barrier 5 over
+// the producer warps only).
+__device__ __forceinline__ bool producers_all(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n"
+        " bar.red.and.pred p, 5, %2, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(r)
+        : "r"(ok ? 1u : 0u), "n"(32 * kProducerWarps)
+        : "memory");
+    return r != 0;
+}
+
+// Barrier 6 over the producer warps only.
+__device__ __forceinline__ void producers_sync() {
+    asm volatile("bar.sync 6, %0;" ::"n"(32 * kProducerWarps) : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     reforward1_kernel(const __grid_constant__ CUtensorMap tw2, const RefArgs a,
                       const PhiloxKeys keys) {
     extern __shared__ uint8_t smem_raw[];
+    // EMA epilogue: end values of each quarter's walk from zero (two chunk
+    // parities) and the carry into the next tile (two tile parities).
+    __shared__ float s_end[2][4][4][32];
+    __shared__ float s_carry[2][512];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_gen = smem_raw + (base - raw);
@@ -70,18 +101,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
     const uint32_t acc_bar = bars + 16u * kStages;
-    const uint32_t tmem_slot = acc_bar + 8u;
+    const uint32_t tmem_empty = acc_bar + 8u;
+    const uint32_t tmem_slot = acc_bar + 16u;
     volatile uint32_t* tmem_slot_gen =
         reinterpret_cast<volatile uint32_t*>(base_gen + (tmem_slot - base));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int mt = blockIdx.x;
-    const int tb = mt / a.nd;          // token block
-    const int di = mt - tb * a.nd;     // draw within the chunk
     const int nk = a.C / kBK;
     const int ngroups = (a.dm + 255) / 256;
     const uint32_t b_bytes = static_cast<uint32_t>(ngroups) * 256u * kBK * 2u;
+    // Work item: one 128-row tile, or (EMA epilogue) the `tiles` token blocks
+    // of one sequence for one draw, in token order.
+    const int ntiles = a.ema ? a.tiles : 1;
+    const int di = static_cast<int>(blockIdx.x) % a.nd;
+    const int tb0 = a.ema ? (static_cast<int>(blockIdx.x) / a.nd) * a.tiles
+                          : static_cast<int>(blockIdx.x) / a.nd;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -89,9 +124,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(empty_bar(s), 1);
         }
         mbar_init(acc_bar, 1);
+        mbar_init(tmem_empty, kProducerWarps);
         mbar_fence_init();
         tma_prefetch_desc(&tw2);
     }
+    for (int i = threadIdx.x; i < 512; i += blockDim.x) s_carry[0][i] = 0.f;
     if (warp == 1) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
     __syncthreads();
@@ -100,41 +137,63 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % kStages;
-                const uint32_t ph = (kb / kStages) & 1u;
-                if (kb >= kStages && !mbar_wait(empty_bar(s), ph ^ 1u, a.status)) break;
-                mbar_arrive_expect_tx(full_bar(s), b_bytes);
-                const uint32_t b_dst = base + s * kStageBytes + 2 * kATile;
-                for (int g = 0; g < ngroups; ++g)
-                    tma_load_2d(b_dst + g * (256u * kBK * 2u), &tw2, kb * kBK, g * 256, full_bar(s));
+            int it = 0;
+            for (int k = 0; k < ntiles; ++k) {
+                bool ok = true;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (it >= kStages && !mbar_wait(empty_bar(s), ph ^ 1u, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(s), b_bytes);
+                    const uint32_t b_dst = base + s * kStageBytes + 2 * kATile;
+                    for (int g = 0; g < ngroups; ++g)
+                        tma_load_2d(b_dst + g * (256u * kBK * 2u), &tw2, kb * kBK, g * 256,
+                                    full_bar(s));
+                }
+                if (!ok) break;
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(kBM, 256, false, false);
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % kStages;
-                const uint32_t ph = (kb / kStages) & 1u;
-                if (!mbar_wait(full_bar(s), ph, a.status)) break;
-                tc_fence_after();
-                const uint32_t st = base + s * kStageBytes;
+            int it = 0;
+            bool ok = true;
+            for (int k = 0; k < ntiles && ok; ++k) {
+                // The accumulator is reused: wait until the previous tile's
+                // epilogue has read it.
+                if (k > 0) {
+                    if (!mbar_wait(tmem_empty, (k - 1) & 1, a.status)) break;
+                    tc_fence_after();
+                }
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (!mbar_wait(full_bar(s), ph, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t st = base + s * kStageBytes;
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint64_t ad = sdesc_sw128(st + h * kATile + kk * 32u, 16u, 1024u);
-                        for (int g = 0; g < ngroups; ++g) {
-                            const uint64_t bd = sdesc_sw128(
-                                st + 2 * kATile + g * (256u * kBK * 2u) + kk * 32u, 16u, 1024u);
-                            umma_bf16(tmem + g * 256, ad, bd, idesc,
-                                      (kb | kk | h) != 0 ? 1u : 0u);
+                        for (int h = 0; h < 2; ++h) {
+                            const uint64_t ad = sdesc_sw128(st + h * kATile + kk * 32u, 16u, 1024u);
+                            for (int g = 0; g < ngroups; ++g) {
+                                const uint64_t bd = sdesc_sw128(
+                                    st + 2 * kATile + g * (256u * kBK * 2u) + kk * 32u, 16u, 1024u);
+                                umma_bf16(tmem + g * 256, ad, bd, idesc,
+                                          (kb | kk | h) != 0 ? 1u : 0u);
+                            }
                         }
                     }
+                    umma_commit(empty_bar(s));
                 }
-                umma_commit(empty_bar(s));
+                if (ok) umma_commit(acc_bar);
             }
-            umma_commit(acc_bar);
         }
     } else {
         // Producers: thread p owns channel block jj = p % 16 of the slice and
@@ -143,122 +202,204 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int jj = p & 15;
         const int r0 = p >> 4;  // 0 .. 2 kProducerWarps - 1
         constexpr int kRows = kBM / (2 * kProducerWarps);  // rows per thread
-        // The (draw, token) half of Philox's first round is the same for every
-        // slice of a row: computed once per tile.
-        DrawHalf dhalf[kRows];
+        // EMA epilogue constants: 1 - lam and lam^32 (one quarter of a tile).
+        const float one_m = 1.0f - a.lam;
+        float l32 = a.lam;
 #pragma unroll
-        for (int m = 0; m < kRows; ++m)
-            dhalf[m] = philox_draw_half(a.draw_first + di,
-                                        a.token0 + tb * kBM + r0 + 2 * kProducerWarps * m, keys);
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % kStages;
-            const uint32_t ph = (kb / kStages) & 1u;
-            if (kb >= kStages && !mbar_wait(empty_bar(s), ph ^ 1u, a.status)) break;
-            const uint32_t st = base + s * kStageBytes;
-            const int j = kb * (kBK / 4) + jj;  // global channel block
-            const BlockHalf bhalf = philox_block_half(j, a.layer, keys);
-            if (a.taylor) {
-                // dh = d (c1 + d (c2 + d (c3 + d c4))), d = sigma a, per channel.
+        for (int i = 0; i < 5; ++i) l32 *= l32;
+
+        bool ok = true;
+        int it = 0;
+        for (int k = 0; k < ntiles; ++k) {
+            const int tb = tb0 + k;
+            const int mt = tb * a.nd + di;
+            // The (draw, token) half of Philox's first round is the same for
+            // every slice of a row: computed once per tile.
+            DrawHalf dhalf[kRows];
 #pragma unroll
-                for (int m = 0; m < kRows; ++m) {
-                    const int r = r0 + 2 * kProducerWarps * m;
-                    const int t = tb * kBM + r;
-                    uint32_t hi0 = 0, hi1 = 0, lo0 = 0, lo1 = 0;
-                    if (t < a.T) {
-                        const float4* cp = a.coef + (static_cast<int64_t>(t) * (a.C / 4) + j) * 4;
-                        const float4 c1 = __ldg(cp), c2 = __ldg(cp + 1);
-                        const float4 c3 = __ldg(cp + 2), c4 = __ldg(cp + 3);
-                        const float4 nrm = words_to_normals(philox_rest(dhalf[m], bhalf, keys));
-                        const float e0 = a.sigma * nrm.x, e1 = a.sigma * nrm.y;
-                        const float e2 = a.sigma * nrm.z, e3 = a.sigma * nrm.w;
-                        const float d0 = e0 * fmaf(e0, fmaf(e0, fmaf(e0, c4.x, c3.x), c2.x), c1.x);
-                        const float d1 = e1 * fmaf(e1, fmaf(e1, fmaf(e1, c4.y, c3.y), c2.y), c1.y);
-                        const float d2 = e2 * fmaf(e2, fmaf(e2, fmaf(e2, c4.z, c3.z), c2.z), c1.z);
-                        const float d3 = e3 * fmaf(e3, fmaf(e3, fmaf(e3, c4.w, c3.w), c2.w), c1.w);
-                        const float h0 = __bfloat162float(__float2bfloat16_rn(d0));
-                        const float h1 = __bfloat162float(__float2bfloat16_rn(d1));
-                        const float h2 = __bfloat162float(__float2bfloat16_rn(d2));
-                        const float h3 = __bfloat162float(__float2bfloat16_rn(d3));
-                        hi0 = pack_bf16x2(h0, h1);
-                        hi1 = pack_bf16x2(h2, h3);
-                        lo0 = pack_bf16x2(d0 - h0, d1 - h1);
-                        lo1 = pack_bf16x2(d2 - h2, d3 - h3);
+            for (int m = 0; m < kRows; ++m)
+                dhalf[m] = philox_draw_half(a.draw_first + di,
+                                            a.token0 + tb * kBM + r0 + 2 * kProducerWarps * m, keys);
+            for (int kb = 0; kb < nk; ++kb, ++it) {
+                if (!ok) continue;
+                const int s = it % kStages;
+                const uint32_t ph = (it / kStages) & 1u;
+                if (it >= kStages && !mbar_wait(empty_bar(s), ph ^ 1u, a.status)) {
+                    ok = false;
+                    continue;
+                }
+                const uint32_t st = base + s * kStageBytes;
+                const int j = kb * (kBK / 4) + jj;  // global channel block
+                const BlockHalf bhalf = philox_block_half(j, a.layer, keys);
+                if (a.taylor) {
+                    // dh = d (c1 + d (c2 + d (c3 + d c4))), d = sigma a, per channel.
+#pragma unroll
+                    for (int m = 0; m < kRows; ++m) {
+                        const int r = r0 + 2 * kProducerWarps * m;
+                        const int t = tb * kBM + r;
+                        uint32_t hi0 = 0, hi1 = 0, lo0 = 0, lo1 = 0;
+                        if (t < a.T) {
+                            const float4* cp =
+                                a.coef + (static_cast<int64_t>(t) * (a.C / 4) + j) * 4;
+                            const float4 c1 = __ldg(cp), c2 = __ldg(cp + 1);
+                            const float4 c3 = __ldg(cp + 2), c4 = __ldg(cp + 3);
+                            const float4 nrm =
+                                words_to_normals(philox_rest(dhalf[m], bhalf, keys));
+                            const float e0 = a.sigma * nrm.x, e1 = a.sigma * nrm.y;
+                            const float e2 = a.sigma * nrm.z, e3 = a.sigma * nrm.w;
+                            const float d0 = e0 * fmaf(e0, fmaf(e0, fmaf(e0, c4.x, c3.x), c2.x), c1.x);
+                            const float d1 = e1 * fmaf(e1, fmaf(e1, fmaf(e1, c4.y, c3.y), c2.y), c1.y);
+                            const float d2 = e2 * fmaf(e2, fmaf(e2, fmaf(e2, c4.z, c3.z), c2.z), c1.z);
+                            const float d3 = e3 * fmaf(e3, fmaf(e3, fmaf(e3, c4.w, c3.w), c2.w), c1.w);
+                            const float h0 = __bfloat162float(__float2bfloat16_rn(d0));
+                            const float h1 = __bfloat162float(__float2bfloat16_rn(d1));
+                            const float h2 = __bfloat162float(__float2bfloat16_rn(d2));
+                            const float h3 = __bfloat162float(__float2bfloat16_rn(d3));
+                            hi0 = pack_bf16x2(h0, h1);
+                            hi1 = pack_bf16x2(h2, h3);
+                            lo0 = pack_bf16x2(d0 - h0, d1 - h1);
+                            lo1 = pack_bf16x2(d2 - h2, d3 - h3);
+                        }
+                        const uint32_t off =
+                            r * 128u + ((((jj >> 1) ^ (r & 7)) & 7u) << 4) + (jj & 1) * 8u;
+                        st_shared_v2(st + off, hi0, hi1);
+                        st_shared_v2(st + kATile + off, lo0, lo1);
                     }
-                    const uint32_t off =
-                        r * 128u + ((((jj >> 1) ^ (r & 7)) & 7u) << 4) + (jj & 1) * 8u;
-                    st_shared_v2(st + off, hi0, hi1);
-                    st_shared_v2(st + kATile + off, lo0, lo1);
+                } else {
+                    // Issue the loads of every row first, then the arithmetic.
+                    float4 yv[kRows], gv[kRows];
+#pragma unroll
+                    for (int m = 0; m < kRows; ++m) {
+                        const int t = tb * kBM + r0 + 2 * kProducerWarps * m;
+                        if (t < a.T) {
+                            const int64_t e4 = static_cast<int64_t>(t) * (a.C / 4) + j;
+                            yv[m] = __ldg(reinterpret_cast<const float4*>(a.y1) + e4);
+                            gv[m] = __ldg(reinterpret_cast<const float4*>(a.h0) + e4);
+                        } else {
+                            yv[m] = gv[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                    }
+#pragma unroll
+                    for (int m = 0; m < kRows; ++m) {
+                        const int r = r0 + 2 * kProducerWarps * m;
+                        const int t = tb * kBM + r;
+                        uint32_t hi0 = 0, hi1 = 0, lo0 = 0, lo1 = 0;
+                        if (t < a.T) {
+                            const float4 nrm =
+                                words_to_normals(philox_rest(dhalf[m], bhalf, keys));
+                            const float4 y = yv[m], g = gv[m];
+                            const float d0 = gelu_as(fmaf(a.sigma, nrm.x, y.x)) - g.x;
+                            const float d1 = gelu_as(fmaf(a.sigma, nrm.y, y.y)) - g.y;
+                            const float d2 = gelu_as(fmaf(a.sigma, nrm.z, y.z)) - g.z;
+                            const float d3 = gelu_as(fmaf(a.sigma, nrm.w, y.w)) - g.w;
+                            const float h0 = __bfloat162float(__float2bfloat16_rn(d0));
+                            const float h1 = __bfloat162float(__float2bfloat16_rn(d1));
+                            const float h2 = __bfloat162float(__float2bfloat16_rn(d2));
+                            const float h3 = __bfloat162float(__float2bfloat16_rn(d3));
+                            hi0 = pack_bf16x2(h0, h1);
+                            hi1 = pack_bf16x2(h2, h3);
+                            lo0 = pack_bf16x2(d0 - h0, d1 - h1);
+                            lo1 = pack_bf16x2(d2 - h2, d3 - h3);
+                        }
+                        // 128-byte swizzle: 16-byte chunk c of row r sits at c ^ (r & 7).
+                        const uint32_t off =
+                            r * 128u + ((((jj >> 1) ^ (r & 7)) & 7u) << 4) + (jj & 1) * 8u;
+                        st_shared_v2(st + off, hi0, hi1);
+                        st_shared_v2(st + kATile + off, lo0, lo1);
+                    }
                 }
                 fence_async_shared();
                 mbar_arrive(full_bar(s));
-                continue;
             }
-            // Issue the loads of every row first, then the arithmetic.
-            float4 yv[kRows], gv[kRows];
-#pragma unroll
-            for (int m = 0; m < kRows; ++m) {
-                const int t = tb * kBM + r0 + 2 * kProducerWarps * m;
-                if (t < a.T) {
-                    const int64_t e4 = static_cast<int64_t>(t) * (a.C / 4) + j;
-                    yv[m] = __ldg(reinterpret_cast<const float4*>(a.y1) + e4);
-                    gv[m] = __ldg(reinterpret_cast<const float4*>(a.h0) + e4);
-                } else {
-                    yv[m] = gv[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            }
-#pragma unroll
-            for (int m = 0; m < kRows; ++m) {
-                const int r = r0 + 2 * kProducerWarps * m;
-                const int t = tb * kBM + r;
-                uint32_t hi0 = 0, hi1 = 0, lo0 = 0, lo1 = 0;
-                if (t < a.T) {
-                    const float4 nrm = words_to_normals(philox_rest(dhalf[m], bhalf, keys));
-                    const float4 y = yv[m], g = gv[m];
-                    const float d0 = gelu_as(fmaf(a.sigma, nrm.x, y.x)) - g.x;
-                    const float d1 = gelu_as(fmaf(a.sigma, nrm.y, y.y)) - g.y;
-                    const float d2 = gelu_as(fmaf(a.sigma, nrm.z, y.z)) - g.z;
-                    const float d3 = gelu_as(fmaf(a.sigma, nrm.w, y.w)) - g.w;
-                    const float h0 = __bfloat162float(__float2bfloat16_rn(d0));
-                    const float h1 = __bfloat162float(__float2bfloat16_rn(d1));
-                    const float h2 = __bfloat162float(__float2bfloat16_rn(d2));
-                    const float h3 = __bfloat162float(__float2bfloat16_rn(d3));
-                    hi0 = pack_bf16x2(h0, h1);
-                    hi1 = pack_bf16x2(h2, h3);
-                    lo0 = pack_bf16x2(d0 - h0, d1 - h1);
-                    lo1 = pack_bf16x2(d2 - h2, d3 - h3);
-                }
-                // 128-byte swizzle: 16-byte chunk c of row r sits at c ^ (r & 7).
-                const uint32_t off = r * 128u + ((((jj >> 1) ^ (r & 7)) & 7u) << 4) + (jj & 1) * 8u;
-                st_shared_v2(st + off, hi0, hi1);
-                st_shared_v2(st + kATile + off, lo0, lo1);
-            }
-            fence_async_shared();
-            mbar_arrive(full_bar(s));
-        }
-        // Epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31; the first four
-        // producer warps take columns 0..255, the next four 256..511.
-        bool ok = mbar_wait(acc_bar, 0, a.status);
-        ok = __all_sync(0xFFFFFFFFu, ok);
-        tc_fence_after();
-        const int quarter = warp & 3;
-        const int g = (warp - 2) >> 2;  // warps 2..9 store, the rest are done
-        if (ok && g < ngroups && g < 2) {
+            if (ok) ok = mbar_wait(acc_bar, static_cast<uint32_t>(k & 1), a.status);
+            // Every producer thread takes the same branch from here on, so the
+            // group barriers of the epilogue are reached by all or by none.
+            if (!producers_all(ok)) break;
+            tc_fence_after();
+            // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (rows of the tile).
+            const int quarter = warp & 3;
             const int rit = quarter * 32 + lane;
             const int64_t row = static_cast<int64_t>(mt) * kBM + rit;
-            float* drow = a.du + row * a.dm;
-#pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
-                const int col0 = g * 256 + c * 32;
-                if (col0 >= a.dm) break;
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + col0, v);
-                tmem_wait_ld();
+            if (a.ema) {
+                // de_t = lam de_{t-1} + (1 - lam) du_t along the tile's rows,
+                // started from the previous tile's last row; kept as
+                // f_t = de_t / (1 - lam) = lam f_{t-1} + du_t.  Column group cg
+                // (four warps, one per quarter of the rows) takes 32-column
+                // chunks cg, cg + 4, ...  Each warp stages its 32 x 32 block
+                // in shared memory (the A operand buffers, idle until every
+                // producer has left the epilogue), then lane j walks column j:
+                // once from zero for the quarter's end value, and, once the
+                // quarters' end values have given it its carry in, again from
+                // that carry, writing A2 = [hi | lo] a row at a time.
+                const int cg = (warp - 2) >> 2;
+                const int wp = warp - 2;
+                const int par = k & 1;
+                float* sc = reinterpret_cast<float*>(base_gen + (wp >> 3) * kStageBytes +
+                                                     (wp & 7) * 4096);
+                // Row r, 16-byte piece i of the block sits at piece i ^ (r & 7).
+                int off[8];
 #pragma unroll
-                for (int q = 0; q < 32; q += 4)
-                    *reinterpret_cast<float4*>(drow + col0 + q) =
-                        make_float4(__uint_as_float(v[q]), __uint_as_float(v[q + 1]),
-                                    __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3]));
+                for (int c8 = 0; c8 < 8; ++c8) off[c8] = (((lane >> 2) ^ c8) << 2) + (lane & 3);
+                const int64_t row0 = static_cast<int64_t>(mt) * kBM + quarter * 32;
+                for (int c = cg, n = 0; c < (a.dm >> 5); c += 4, ++n) {
+                    const int col0 = c * 32;
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + col0, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        *reinterpret_cast<float4*>(sc + lane * 32 + ((i ^ (lane & 7)) << 2)) =
+                            make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                        __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                    __syncwarp();
+                    float f = 0.f;
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) f = fmaf(a.lam, f, sc[r * 32 + off[r & 7]]);
+                    s_end[n & 1][cg][quarter][lane] = f;
+                    group_sync(1 + cg);
+                    float cin = s_carry[par][col0 + lane];
+                    for (int qq = 0; qq < quarter; ++qq)
+                        cin = fmaf(l32, cin, s_end[n & 1][cg][qq][lane]);
+                    if (quarter == 3) s_carry[par ^ 1][col0 + lane] = fmaf(l32, cin, f);
+                    __nv_bfloat16* out = a.A2 + row0 * (2 * a.dm) + col0 + lane;
+                    f = cin;
+#pragma unroll 8
+                    for (int r = 0; r < 32; ++r) {
+                        f = fmaf(a.lam, f, sc[r * 32 + off[r & 7]]);
+                        const float e = one_m * f;
+                        const __nv_bfloat16 hi = __float2bfloat16_rn(e);
+                        out[0] = hi;
+                        out[a.dm] = __float2bfloat16_rn(e - __bfloat162float(hi));
+                        out += 2 * a.dm;
+                    }
+                    __syncwarp();
+                }
+            } else {
+                // du rows: the first four producer warps take columns 0..255,
+                // the next four 256..511.
+                const int g = (warp - 2) >> 2;
+                if (g < ngroups && g < 2) {
+                    float* drow = a.du + row * a.dm;
+#pragma unroll 1
+                    for (int c = 0; c < 8; ++c) {
+                        const int col0 = g * 256 + c * 32;
+                        if (col0 >= a.dm) break;
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + col0, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int q = 0; q < 32; q += 4)
+                            *reinterpret_cast<float4*>(drow + col0 + q) =
+                                make_float4(__uint_as_float(v[q]), __uint_as_float(v[q + 1]),
+                                            __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3]));
+                    }
+                }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tmem_empty);
+            // The next tile's A operand overwrites the staging blocks.
+            if (a.ema) producers_sync();
         }
     }
     tc_fence_before();
@@ -331,7 +472,8 @@ dust_status reforward1_launch(const float* y1, const float* h0, const void* coef
                               const void* W2, int64_t T, int64_t Tp, int64_t C,
                               int64_t dm, int nd, uint32_t draw_first, uint32_t token0,
                               uint32_t layer, float sigma, const PhiloxKeys& keys, float* du,
-                              uint32_t* status, cudaStream_t s) {
+                              void* A2, int64_t seq_len, float lam, uint32_t* status,
+                              cudaStream_t s) {
     CUtensorMap tw2;
     if (!encode_bf16_2d(&tw2, W2, C, dm, C, kBK, 256)) return DUST_ERR_CUDA;
     static bool attr_set = false;
@@ -341,9 +483,28 @@ dust_status reforward1_launch(const float* y1, const float* h0, const void* coef
                                            static_cast<int>(kSmemBytes)));
         attr_set = true;
     }
-    RefArgs a{y1, h0, static_cast<const float4*>(coef), taylor ? 1 : 0, du, static_cast<int>(T), static_cast<int>(C), static_cast<int>(dm), nd,
-              draw_first, token0, layer, sigma, status};
-    const unsigned grid = static_cast<unsigned>(nd * (Tp / kBM));
+    const bool ema = A2 != nullptr;
+    if (ema && (seq_len % kBM != 0 || Tp != T)) return DUST_ERR_UNSUPPORTED;
+    RefArgs a{};
+    a.y1 = y1;
+    a.h0 = h0;
+    a.coef = static_cast<const float4*>(coef);
+    a.taylor = taylor ? 1 : 0;
+    a.du = du;
+    a.A2 = static_cast<__nv_bfloat16*>(A2);
+    a.T = static_cast<int>(T);
+    a.C = static_cast<int>(C);
+    a.dm = static_cast<int>(dm);
+    a.nd = nd;
+    a.ema = ema ? 1 : 0;
+    a.tiles = ema ? static_cast<int>(seq_len / kBM) : 1;
+    a.lam = lam;
+    a.draw_first = draw_first;
+    a.token0 = token0;
+    a.layer = layer;
+    a.sigma = sigma;
+    a.status = status;
+    const unsigned grid = static_cast<unsigned>(ema ? nd * (T / seq_len) : nd * (Tp / kBM));
     reforward1_kernel<<<grid, kThreads, kSmemBytes, s>>>(tw2, a, keys);
     return launch_status();
 }

@@ -215,7 +215,8 @@ def make_step(wl, dust):
         nd = max(1, min(nd, 64, K))
         chunks = -(-K // nd)
         fused = wl["C"] % 64 == 0 and wl["d_model"] <= 512
-        per_chunk = 3 if fused else 4
+        # GEMM 1 (+ EMA in its epilogue for whole token blocks per sequence), GEMM 2
+        per_chunk = (2 if wl["seq_len"] % 128 == 0 else 3) if fused else 4
         # softmax (+ clean GELU when fused), per chunk, mean + scan + g, outer product
         return step, K * T, (2 if fused else 1) + chunks * per_chunk + 3 + 1, ws
     if wl["kind"] == "embed":

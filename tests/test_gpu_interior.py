@@ -56,6 +56,7 @@ def _ref(orc, d, sigma, gamma, K, seed, layer=1, draw0=0, token0=0):
     (200, 100, 40, 64, 64, 300, 6, 1.0),      # ragged T (pads to 256), ragged V, gamma = 1
     (384, 64, 8, 192, 192, 130, 20, 0.5),     # several chunks of draws, 6 sequences
     (256, 128, 16, 128, 576, 64, 4, 0.95),    # d_model > 512: GEMM 1 from a staged A operand
+    (768, 384, 16, 128, 192, 256, 70, 0.9),   # EMA carried over 3 blocks, 6 column chunks, 2 draw chunks
 ])
 def test_interior_shapes(dust, orc, T, seq_len, d_in, C, dm, V, K, gamma):
     d = _inputs(T, d_in, C, dm, V, seq_len, seed=T + C)
