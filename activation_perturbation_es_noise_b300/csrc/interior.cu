@@ -23,6 +23,9 @@
 //   GEMM 1         du = A1 [W2 | W2]^T on the tensor cores (fp32)
 //   EMA kernel     de, split into A2 = [hi | lo]  (rows x 2 d_model)
 //   GEMM 2 + CE    dz = A2 [W_head | W_head]^T, reduced in the epilogue to dl
+// For d_model <= 512 the first three are one kernel (reforward.cu): GEMM 1
+// generates A1 in shared memory and, when every sequence is whole 128-token
+// blocks, runs the EMA in its epilogue and writes A2 directly.
 // then once: centring, the segmented suffix scan, the noise-weighted sum for
 // g (noise regenerated), and G_W1 = g^T x.
 //
