@@ -250,7 +250,10 @@ def roofline(wl, kernel_ms, traffic):
                 "frac": ach / peak, "traffic": traffic, "kernel": "gemm_bf16_kernel<CE>",
                 "kernel_ms": kernel_ms, "peak_source": "bf16_tflops_sustained (%s)" % which}
     if wl["kind"] == "embed":
-        nbytes = wl["T"] * wl["d"] * 4 + wl["T"] * 4 * 2 + wl["V"] * wl["d"] * 4
+        # what piece_sum itself must move: every g row once and each token's id
+        # and permutation entry (the G_E rows are written partly by it, partly
+        # by the finish kernel)
+        nbytes = wl["T"] * wl["d"] * 4 + wl["T"] * 4 * 2
         peak = peaks["hbm_gbs"]
         ach = nbytes / (kernel_ms * 1e-3) / 1e9
         return {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
@@ -459,6 +462,10 @@ def run_dust(args):
     # the timed region above, where they would add host work per launch).
     timer = dust.KernelTimer(capacity=max(1, args.steps) * 64)
     with timer:
+        # A bounded spin (about 0.5 ms per step) first, so that the host has
+        # queued the steps' launches before the GPU reaches them: the events
+        # then bracket the kernel alone, not host gaps between small launches.
+        torch.cuda._sleep(1_000_000 * max(1, args.steps))
         for _ in range(args.steps):
             step()
     torch.cuda.synchronize()

@@ -13,6 +13,13 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "slow: long CPU test")
 
 
+def parity(**errors):
+    """Prints the measured errors of a parity check on one line (shown with
+    pytest -s), so that a run reports the margins, not only pass/fail."""
+    name = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    print("PARITY %s %s" % (name, " ".join("%s=%.3e" % kv for kv in errors.items())))
+
+
 def rel_l2(a, b):
     import numpy as np
     a = np.asarray(a, np.float64)

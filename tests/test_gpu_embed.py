@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import workloads as W
-from conftest import rel_l2, to_dev
+from conftest import rel_l2, to_dev, parity
 
 pytestmark = pytest.mark.gpu
 
@@ -40,7 +40,9 @@ def test_embed_shapes(dust, orc, T, d, V, kind):
     assert st == 0
     ref_perm, ref_G = orc.embed_scatter(g, ids, V)
     np.testing.assert_array_equal(perm, ref_perm)
-    assert rel_l2(G, ref_G) <= 1e-5
+    e = rel_l2(G, ref_G)
+    assert e <= 1e-5
+    parity(G_E=e)
 
 
 def test_embed_scale_config(dust, orc):

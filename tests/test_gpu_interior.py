@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import workloads as W
-from conftest import rel_l2, to_dev
+from conftest import rel_l2, to_dev, parity
 
 pytestmark = pytest.mark.gpu
 
@@ -65,6 +65,7 @@ def test_interior_shapes(dust, orc, T, seq_len, d_in, C, dm, V, K, gamma):
     eg, eG = rel_l2(g, ref["g"]), rel_l2(G, ref["G"])
     assert eg <= G_TOL, eg
     assert eG <= GW_TOL, eG
+    parity(g=eg, G_W=eG)
 
 
 def test_interior_deterministic(dust):
@@ -115,13 +116,17 @@ def test_interior_full_size_sequences(dust, orc, name, K, seqs):
     p, d = _full(name, K)
     g, G = _run(dust, d, p["sigma"], p["gamma"], K, W.NOISE_SEED)
     L = p["seq_len"]
+    worst = 0.0
     for s in seqs:
         ref = _ref(orc, _seq(d, s, L), p["sigma"], p["gamma"], K, W.NOISE_SEED, token0=s * L)
         eg = rel_l2(g[s * L:(s + 1) * L], ref["g"])
         assert eg <= G_TOL, (s, eg)
+        worst = max(worst, eg)
     gb = torch.from_numpy(W.bf16_round(g)).cuda().double()
     ref_G = (gb.T @ torch.from_numpy(d["x"]).cuda().double()).cpu().numpy()
-    assert rel_l2(G, ref_G) <= 1e-4
+    eG = rel_l2(G, ref_G)
+    assert eG <= 1e-4
+    parity(g_sequences=worst, G_W_vs_g_x=eG)
 
 
 @pytest.mark.parametrize("dm", [64, 576])
