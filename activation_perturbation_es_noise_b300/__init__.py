@@ -27,7 +27,8 @@ EXPORTS = ("dust_status_string", "dust_abi_version", "dust_workspace_status",
            "dust_head_workspace", "dust_head_estimate", "dust_linear_workspace",
            "dust_linear_estimate", "dust_embed_workspace", "dust_embed_scatter",
            "dust_embed_scatter_static", "dust_philox_fill", "dust_gemm_bf16", "dust_set_kernel_events",
-           "dust_kernel_event_count", "dust_wait_selftest")
+           "dust_kernel_event_count", "dust_wait_selftest", "dust_sgd_step", "dust_adam_step",
+           "dust_head_backprop_workspace", "dust_head_backprop")
 
 
 class DustError(RuntimeError):
@@ -82,9 +83,17 @@ def lib():
         L.dust_set_kernel_events.argtypes = [_P, _P, ctypes.c_int]
         L.dust_wait_selftest.argtypes = [_P, ctypes.c_uint64, _P]
         L.dust_kernel_event_count.restype = ctypes.c_int
-        for name in ("dust_set_kernel_events", "dust_wait_selftest", "dust_workspace_status", "dust_head_estimate", "dust_linear_estimate",
-                     "dust_embed_scatter", "dust_embed_scatter_static", "dust_philox_fill",
-                     "dust_gemm_bf16"):
+        _F = ctypes.c_float
+        L.dust_sgd_step.argtypes = [_P, _P, _P, _I64, _F, _F, _F, _P, _P]
+        L.dust_adam_step.argtypes = [_P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _I64, _P, _P]
+        L.dust_head_backprop_workspace.argtypes = [_I64, _I64, _I64]
+        L.dust_head_backprop_workspace.restype = _SZ
+        L.dust_head_backprop.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _P, _P, _P,
+                                         _SZ, _P]
+        for name in ("dust_set_kernel_events", "dust_wait_selftest", "dust_workspace_status",
+                     "dust_head_estimate", "dust_linear_estimate", "dust_embed_scatter",
+                     "dust_embed_scatter_static", "dust_philox_fill", "dust_gemm_bf16",
+                     "dust_sgd_step", "dust_adam_step", "dust_head_backprop"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -282,3 +291,57 @@ class KernelTimer:
 
     def total_ms(self):
         return float(sum(self.times_ms()))
+
+
+# ------------------------------------------------------------ optimiser ----
+def _f32_params(*ts):
+    _need_cuda(*ts)
+    for t in ts:
+        if t.dtype != torch.float32:
+            raise ValueError("parameters, gradients and moments are fp32")
+    n = ts[0].numel()
+    if any(t.numel() != n for t in ts):
+        raise ValueError("parameter, gradient and moment sizes differ")
+    return n
+
+
+def sgd_step(W, G, momentum_buf, lr, momentum=0.9, weight_decay=0.0, W_bf16=None, stream=None):
+    """b <- momentum b + (G + weight_decay W); W <- W - lr b (in place)."""
+    n = _f32_params(W, G, momentum_buf)
+    if W_bf16 is not None:
+        _need_cuda(W_bf16)
+    _check("dust_sgd_step", lib().dust_sgd_step(_ptr(W), _ptr(G), _ptr(momentum_buf), n, lr,
+                                                momentum, weight_decay, _ptr(W_bf16),
+                                                _stream(stream)))
+
+
+def adam_step(W, G, m, v, step, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0,
+              W_bf16=None, stream=None):
+    """One Adam step (decoupled weight decay), step counted from 1 (in place)."""
+    n = _f32_params(W, G, m, v)
+    if W_bf16 is not None:
+        _need_cuda(W_bf16)
+    _check("dust_adam_step", lib().dust_adam_step(_ptr(W), _ptr(G), _ptr(m), _ptr(v), n, lr,
+                                                  beta1, beta2, eps, weight_decay, step,
+                                                  _ptr(W_bf16), _stream(stream)))
+
+
+def head_backprop(logits, targets, x, want_g=False, out=None, ws=None, stream=None):
+    """Exact head gradient: returns (g or None, G_W, ws) with
+    g_t = softmax(z_t) - e_{y_t} and G_W = sum_t g_t x_t^T."""
+    _need_cuda(logits, targets, x)
+    T, V = logits.shape
+    d = x.shape[1]
+    dev = logits.device
+    xdt = DUST_BF16 if x.dtype == torch.bfloat16 else DUST_F32
+    if out is None:
+        g = torch.empty((T, V), dtype=torch.float32, device=dev) if want_g else None
+        G = torch.empty((V, d), dtype=torch.float32, device=dev)
+    else:
+        g, G = out
+    if ws is None:
+        ws = _workspace(lib().dust_head_backprop_workspace(T, V, d), dev)
+    _check("dust_head_backprop",
+           lib().dust_head_backprop(_ptr(logits), _ptr(targets), _ptr(x), xdt, T, V, d, _ptr(g),
+                                    _ptr(G), _ptr(ws), ws.numel(), _stream(stream)))
+    return g, G, ws

@@ -461,3 +461,98 @@ extern "C" dust_status dust_head_estimate(const float* logits, const int32_t* ta
     return gemm_bf16_launch(A.gbf, true, P.ldg, xb, true, ldx, V, d, T, 0, 1, G_W, d,
                             static_cast<uint32_t*>(ws), s);
 }
+
+// ------------------------------------------------------------------------
+// The exact head gradient, the backprop reference that the pages compare the
+// estimate with (single-batch cosine with backprop as a tuning objective,
+// Dust translation §2.3; cosine against backprop, §4.2):
+//   g_t = softmax(z_t) - e_{y_t},   G = sum_t g_t x_t^T.
+// ------------------------------------------------------------------------
+namespace dust {
+namespace {
+
+// One CTA per token: the row's max and exp-sum by block reductions, then
+// p - onehot written as fp32 (optional) and as the bf16 GEMM operand.
+__global__ void __launch_bounds__(256)
+    head_grad_rows_kernel(const float* __restrict__ logits, const int32_t* __restrict__ targets,
+                          int V, float* __restrict__ g_out, __nv_bfloat16* __restrict__ gbf,
+                          int64_t ldg, uint32_t* status) {
+    __shared__ float scratch[8];
+    const int64_t t = blockIdx.x;
+    const float* zr = logits + t * V;
+    float m = -INFINITY;
+    for (int v = threadIdx.x; v < V; v += blockDim.x) m = fmaxf(m, zr[v]);
+    m = block_max<false>(m, scratch);
+    float s = 0.f;
+    for (int v = threadIdx.x; v < V; v += blockDim.x) s += expf(zr[v] - m);
+    s = block_sum<false>(s, scratch);
+    const float inv = 1.0f / s;
+    int y = targets[t];
+    if (y < 0 || y >= V) {
+        if (threadIdx.x == 0) record_status(status, DUST_ERR_DEVICE_RANGE);
+        y = -1;
+    }
+    for (int v = threadIdx.x; v < V; v += blockDim.x) {
+        const float g = expf(zr[v] - m) * inv - (v == y ? 1.0f : 0.0f);
+        if (g_out) g_out[t * V + v] = g;
+        gbf[t * ldg + v] = __float2bfloat16_rn(g);
+    }
+}
+
+struct GradPlan {
+    int64_t ldg, ldx;
+    size_t off_gbf, off_xbf, bytes;
+};
+
+GradPlan grad_plan(int64_t T, int64_t V, int64_t d) {
+    GradPlan P{};
+    P.ldg = round_up(V, 8);
+    P.ldx = round_up(d, 8);
+    WsLayout w;
+    w.take(kCtlBytes);
+    P.off_gbf = w.take(static_cast<size_t>(T * P.ldg) * 2);
+    P.off_xbf = w.take(static_cast<size_t>(T * P.ldx) * 2);
+    P.bytes = w.used;
+    return P;
+}
+
+}  // namespace
+}  // namespace dust
+
+extern "C" size_t dust_head_backprop_workspace(int64_t T, int64_t V, int64_t d) {
+    if (T < 1 || V < 1 || d < 1) return 0;
+    return grad_plan(T, V, d).bytes;
+}
+
+extern "C" dust_status dust_head_backprop(const float* logits, const int32_t* targets,
+                                          const void* x, dust_dtype x_dtype, int64_t T,
+                                          int64_t V, int64_t d, float* g_out, float* G_W,
+                                          void* ws, size_t ws_bytes, void* stream) {
+    if (!logits || !targets || !x || !G_W) return DUST_ERR_INVALID_ARG;
+    if (T < 1 || V < 1 || d < 1) return DUST_ERR_INVALID_ARG;
+    if (x_dtype != DUST_F32 && x_dtype != DUST_BF16) return DUST_ERR_INVALID_ARG;
+    if (T > (1LL << 30) || V > (1LL << 30) || d > (1LL << 30)) return DUST_ERR_UNSUPPORTED;
+    const GradPlan P = grad_plan(T, V, d);
+    if (!ws || ws_bytes < P.bytes || !aligned(ws, 256)) return DUST_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    DUST_CUDA_TRY(cudaMemsetAsync(ws, 0, kCtlBytes, s));
+    __nv_bfloat16* gbf = reinterpret_cast<__nv_bfloat16*>(w + P.off_gbf);
+    head_grad_rows_kernel<<<static_cast<unsigned>(T), 256, 0, s>>>(
+        logits, targets, static_cast<int>(V), g_out, gbf, P.ldg, static_cast<uint32_t*>(ws));
+    dust_status st = launch_status();
+    if (st != DUST_OK) return st;
+    const void* xb = x;
+    int64_t ldx = d;
+    if (x_dtype == DUST_F32 || (d % 8) != 0 || !aligned(x, 16)) {
+        void* xbf = w + P.off_xbf;
+        st = x_dtype == DUST_F32
+                 ? f32_to_bf16_launch(static_cast<const float*>(x), T, d, d, xbf, P.ldx, s)
+                 : bf16_pad_launch(x, T, d, d, xbf, P.ldx, s);
+        if (st != DUST_OK) return st;
+        xb = xbf;
+        ldx = P.ldx;
+    }
+    return gemm_bf16_launch(gbf, true, P.ldg, xb, true, ldx, V, d, T, 0, 1, G_W, d,
+                            static_cast<uint32_t*>(ws), s);
+}

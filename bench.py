@@ -13,7 +13,8 @@ frequencies; weights are random N(0, 1/fan_in).  The cached logits (256 MB)
 are larger than the 126 MB L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dust|reference]
-                  [--workload head_batch|head_tiny|head_scale|interior|interior_scale|embed_scale]
+                  [--workload head_batch|head_tiny|head_scale|interior|interior_scale|embed_scale|
+                              head_sweep|optim_adam]
 
 Under torchrun (N > 1) every rank estimates its own batch (global token
 offset rank * T, so the noise differs per rank) with no collective on the data
@@ -335,6 +336,71 @@ def config_of(wl, n_gpus):
     return c
 
 
+OPTIM_PARAMS = 38_000_000  # the pages' 8-layer, 512-wide GPT has about 38M parameters
+OPTIM_BYTES_PER_PARAM = 4 * 7 + 2  # W, m, v read and written, G read (fp32); bf16 W out
+
+
+def run_optim(args):
+    """The optimiser step that consumes the estimate (Adam with decoupled
+    weight decay, writing the bf16 copy of W), over all parameters of the
+    pages' 38M-parameter GPT at once, inputs resident: parameter updates/s
+    and the fraction of the HBM roofline at 30 bytes per parameter."""
+    import torch
+
+    import activation_perturbation_es_noise_b300 as dust
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    n = OPTIM_PARAMS
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    Wt = torch.randn(n, device=dev, generator=gen)
+    G = torch.randn(n, device=dev, generator=gen)
+    m = torch.zeros(n, device=dev)
+    v = torch.zeros(n, device=dev)
+    Wb = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    t = [0]
+
+    def step():
+        t[0] += 1
+        dust.adam_step(Wt, G, m, v, t[0], 1e-3, weight_decay=0.01, W_bf16=Wb)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clocks:
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        e1.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    peaks, which = _peaks()
+    ach = OPTIM_BYTES_PER_PARAM * n / (ms * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        k = 200_000
+        a = [np.random.default_rng(1).standard_normal(k) for _ in range(2)]
+        t0 = time.perf_counter()
+        oracle.adam_step(a[0], a[1], np.zeros(k), np.zeros(k), 1, 1e-3, 0.9, 0.999, 1e-8, 0.01)
+        cpu = {"value": k / (time.perf_counter() - t0), "unit": "params/s", "cores": 1,
+               "kind": "oracle", "sample": "%d of %d parameters, one step" % (k, n)}
+    print(json.dumps({
+        "metric": "optimiser parameter updates/sec (Adam step) on 1 B300; % of HBM roofline",
+        "value": n / (ms * 1e-3), "unit": "params/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "optim_adam", "params": n, "l2": "inputs larger than L2 (no flush)"},
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                     "kernel": "optim_kernel<Adam>", "kernel_ms": ms,
+                     "peak_source": "hbm_gbs (%s)" % which},
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps,
+        "clocks": clocks.summary()}), flush=True)
+    return 0
+
+
 def run_head_sweep(args):
     """The tiny head workload at K = 64 .. 16384: token-evals/s per K and the
     cosine of G_W with the analytic head gradient sum_t (softmax(z_t) -
@@ -616,7 +682,7 @@ def main():
     ap.add_argument("--impl", default="dust", choices=["dust", "reference"])
     ap.add_argument("--workload", default="head_batch",
                     choices=["head_batch", "head_tiny", "head_scale", "interior",
-                             "interior_scale", "embed_scale", "head_sweep"])
+                             "interior_scale", "embed_scale", "head_sweep", "optim_adam"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
@@ -626,6 +692,8 @@ def main():
         return run_reference(args)
     if args.workload == "head_sweep":
         return run_head_sweep(args)
+    if args.workload == "optim_adam":
+        return run_optim(args)
     return run_dust(args)
 
 

@@ -238,6 +238,59 @@ dust_status dust_gemm_bf16(const void* A, int a_mn, int64_t lda, const void* B, 
                            int64_t ldb, int64_t M, int64_t N, int64_t K, float* G, int64_t ldg,
                            void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* Using the estimate: optimiser step and the backprop reference             */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * One step of SGD with momentum on n fp32 parameters, with the estimated
+ * gradient G (the pages train with SGD and momentum: Dust translation,
+ * experiment set-up; the form is the textbook heavy-ball one):
+ *   b <- momentum b + (G + weight_decay W),   W <- W - lr b.
+ * W and momentum_buf (device, n fp32, caller-owned, updated in place; the
+ * buffer starts at zero) and G (device, n fp32, read) must not overlap.
+ * W_bf16 (device, n bf16, or NULL) receives the updated W rounded to bf16,
+ * the operand of the next forward's tensor-core GEMM.  n = 0 does nothing
+ * and returns DUST_OK (the arrays may then be NULL).
+ * INVALID_ARG: a NULL array, n < 0, misaligned elements, lr or weight_decay
+ * not finite, weight_decay < 0, momentum outside [0, 1].  Asynchronous on
+ * `stream`; allocates nothing.
+ */
+dust_status dust_sgd_step(float* W, const float* G, float* momentum_buf, int64_t n, float lr,
+                          float momentum, float weight_decay, void* W_bf16, void* stream);
+
+/*
+ * One step of Adam (Kingma & Ba, 2015) with decoupled weight decay (AdamW) on
+ * n fp32 parameters (the pages report that Adam works on the estimate
+ * unchanged: Dust translation §3.3):
+ *   m <- beta1 m + (1 - beta1) G,   v <- beta2 v + (1 - beta2) G^2,
+ *   W <- W - lr ( (m / (1 - beta1^step)) / (sqrt(v / (1 - beta2^step)) + eps)
+ *                 + weight_decay W ).
+ * step counts from 1; m and v (device, n fp32, caller-owned) start at zero.
+ * Arrays as for dust_sgd_step.  INVALID_ARG also for step < 1, beta outside
+ * [0, 1), eps <= 0.
+ */
+dust_status dust_adam_step(float* W, const float* G, float* m, float* v, int64_t n, float lr,
+                           float beta1, float beta2, float eps, float weight_decay,
+                           int64_t step, void* W_bf16, void* stream);
+
+/* Workspace bytes for dust_head_backprop with these sizes. */
+size_t dust_head_backprop_workspace(int64_t T, int64_t V, int64_t d);
+
+/*
+ * The exact head gradient that the estimate is compared with (the pages tune
+ * by the single-batch cosine with backprop: Dust translation §2.3, §4.2):
+ *   g_t = softmax(z_t) - e_{y_t},   G_W = sum_t g_t x_t^T.
+ * Arguments as for dust_head_estimate (no noise): g_out (T x V fp32) may be
+ * NULL; G_W (V x d fp32) is computed from g and x rounded to bf16 with fp32
+ * accumulation.  A target outside [0, V) sets DUST_ERR_DEVICE_RANGE in the
+ * workspace status word (its row then has no -1 term).
+ */
+dust_status dust_head_backprop(const float* logits, const int32_t* targets, const void* x,
+                               dust_dtype x_dtype, int64_t T, int64_t V, int64_t d,
+                               float* g_out, float* G_W, void* ws, size_t ws_bytes,
+                               void* stream);
+
 /*
  * Failure-path check of the bounded waits: a one-warp kernel waits on a
  * barrier that nothing arrives at, gives up after limit_ns (1 .. 1e9) and

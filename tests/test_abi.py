@@ -79,3 +79,29 @@ def test_bad_arguments_rejected_on_host():
     assert L.dust_philox_fill(1, 0, 0, 0, -1, 4, fake, None, None) == 1
     # gemm: misaligned leading dimension
     assert L.dust_gemm_bf16(fake, 0, 7, fake, 0, 8, 4, 4, 4, fake, 4, fake, 256, None) == 1
+
+
+def test_optimiser_and_backprop_reject_bad_arguments_on_host():
+    L = dust.lib()
+    f = ctypes.c_void_p(256)
+    assert L.dust_sgd_step(None, f, f, 8, 0.1, 0.9, 0.0, None, None) == 1
+    assert L.dust_sgd_step(f, f, f, -1, 0.1, 0.9, 0.0, None, None) == 1
+    assert L.dust_sgd_step(f, f, f, 8, 0.1, 1.5, 0.0, None, None) == 1
+    assert L.dust_sgd_step(f, f, f, 8, float("nan"), 0.9, 0.0, None, None) == 1
+    assert L.dust_sgd_step(f, f, f, 8, 0.1, 0.9, -1.0, None, None) == 1
+    assert L.dust_sgd_step(f, f, f, 0, 0.1, 0.9, 0.0, None, None) == 0  # n = 0: nothing to do
+    adam = lambda **k: L.dust_adam_step(f, f, f, f, k.get("n", 8), 1e-3, k.get("b1", 0.9),
+                                        k.get("b2", 0.999), k.get("eps", 1e-8), 0.0,
+                                        k.get("step", 1), None, None)
+    assert L.dust_sgd_step(None, None, None, 0, 0.1, 0.9, 0.0, None, None) == 0
+    assert adam(step=0) == 1
+    assert adam(b1=1.0) == 1
+    assert adam(b2=-0.1) == 1
+    assert adam(eps=0.0) == 1
+    assert adam(n=0) == 0
+    assert L.dust_head_backprop_workspace(0, 4, 4) == 0
+    need = L.dust_head_backprop_workspace(4, 4, 4)
+    assert need > 0
+    assert L.dust_head_backprop(None, f, f, 0, 4, 4, 4, None, f, f, need, None) == 1
+    assert L.dust_head_backprop(f, f, f, 0, 4, 4, 4, None, f, f, need - 1, None) == 3
+    assert L.dust_head_backprop(f, f, f, 7, 4, 4, 4, None, f, f, need, None) == 1
