@@ -28,7 +28,8 @@ EXPORTS = ("dust_status_string", "dust_abi_version", "dust_workspace_status",
            "dust_linear_estimate", "dust_embed_workspace", "dust_embed_scatter",
            "dust_embed_scatter_static", "dust_philox_fill", "dust_gemm_bf16", "dust_set_kernel_events",
            "dust_kernel_event_count", "dust_wait_selftest", "dust_sgd_step", "dust_adam_step",
-           "dust_head_backprop_workspace", "dust_head_backprop")
+           "dust_head_backprop_workspace", "dust_head_backprop", "dust_head_estimate_baseline")
+BASELINE_MEAN, BASELINE_LEAVE_ONE_OUT, BASELINE_ANTITHETIC = 0, 1, 2
 
 
 class DustError(RuntimeError):
@@ -86,6 +87,8 @@ def lib():
         _F = ctypes.c_float
         L.dust_sgd_step.argtypes = [_P, _P, _P, _I64, _F, _F, _F, _P, _P]
         L.dust_adam_step.argtypes = [_P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _I64, _P, _P]
+        L.dust_head_estimate_baseline.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64,
+                                                  DustNoise, ctypes.c_int, _P, _P, _P, _SZ, _P]
         L.dust_head_backprop_workspace.argtypes = [_I64, _I64, _I64]
         L.dust_head_backprop_workspace.restype = _SZ
         L.dust_head_backprop.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _P, _P, _P,
@@ -93,7 +96,8 @@ def lib():
         for name in ("dust_set_kernel_events", "dust_wait_selftest", "dust_workspace_status",
                      "dust_head_estimate", "dust_linear_estimate", "dust_embed_scatter",
                      "dust_embed_scatter_static", "dust_philox_fill", "dust_gemm_bf16",
-                     "dust_sgd_step", "dust_adam_step", "dust_head_backprop"):
+                     "dust_sgd_step", "dust_adam_step", "dust_head_backprop",
+                     "dust_head_estimate_baseline"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -149,8 +153,10 @@ def head_workspace_bytes(T, V, d, K):
 
 
 def head_estimate(logits, targets, x, sigma, K, seed, layer=0, draw0=0, token0=0,
-                  want_g=True, out=None, ws=None, stream=None):
-    """LM-head estimator on cached logits.  Returns (g_hat or None, G_W, ws)."""
+                  want_g=True, out=None, ws=None, stream=None, baseline=BASELINE_MEAN):
+    """LM-head estimator on cached logits.  Returns (g_hat or None, G_W, ws).
+    baseline: BASELINE_MEAN (the pages'), BASELINE_LEAVE_ONE_OUT or
+    BASELINE_ANTITHETIC (K noise draws, each evaluated as +a and -a)."""
     _need_cuda(logits, targets, x)
     T, V = logits.shape
     d = x.shape[1]
@@ -165,9 +171,14 @@ def head_estimate(logits, targets, x, sigma, K, seed, layer=0, draw0=0, token0=0
     xdt = DUST_BF16 if x.dtype == torch.bfloat16 else DUST_F32
     if x.dtype not in (torch.bfloat16, torch.float32):
         raise ValueError("x must be bf16 or fp32")
-    st = lib().dust_head_estimate(_ptr(logits), _ptr(targets), _ptr(x), xdt, T, V, d,
-                                  noise(seed, sigma, K, layer, draw0, token0), _ptr(g), _ptr(G),
-                                  _ptr(ws), ws.numel(), _stream(stream))
+    nz = noise(seed, sigma, K, layer, draw0, token0)
+    if baseline == BASELINE_MEAN:
+        st = lib().dust_head_estimate(_ptr(logits), _ptr(targets), _ptr(x), xdt, T, V, d, nz,
+                                      _ptr(g), _ptr(G), _ptr(ws), ws.numel(), _stream(stream))
+    else:
+        st = lib().dust_head_estimate_baseline(_ptr(logits), _ptr(targets), _ptr(x), xdt, T, V,
+                                               d, nz, int(baseline), _ptr(g), _ptr(G), _ptr(ws),
+                                               ws.numel(), _stream(stream))
     _check("dust_head_estimate", st)
     return g, G, ws
 

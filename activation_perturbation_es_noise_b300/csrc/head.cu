@@ -96,17 +96,25 @@ __device__ __forceinline__ float block_max(float v, float* scratch) {
 
 // NB channel blocks of 4 per thread; ONE_WARP: the CTA is a single warp and
 // all reductions are shuffles.  Otherwise blockDim.x <= 256.
-template <int NB, bool ONE_WARP>
+// ANTI: antithetic pairs.  Every draw's noise a is used twice, as +a and -a;
+// the pair's centred decrease is c = -(dl(+a) - dl(-a)) / 2, so
+//   g_t = (1/(2 K sigma)) sum_i (dl_i(+a) - dl_i(-a)) a_i
+// needs neither the mean over draws nor the sum of the noise (S0).
+template <int NB, bool ONE_WARP, bool ANTI>
 __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
     head_draws_kernel(const HeadArgs A, const PhiloxKeys keys) {
     __shared__ float red[2][8];
+    __shared__ float red_m[2][8];
     __shared__ float red_y[2];
     __shared__ float scratch[8];
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int NT = ONE_WARP ? 32 : static_cast<int>(blockDim.x);
-    if (!ONE_WARP && tid < 16) red[tid >> 3][tid & 7] = 0.f;  // slots of absent warps
+    if (!ONE_WARP && tid < 16) {  // slots of absent warps
+        red[tid >> 3][tid & 7] = 0.f;
+        red_m[tid >> 3][tid & 7] = 0.f;
+    }
     const int t = blockIdx.x / A.Q;
     const int q = blockIdx.x - t * A.Q;
     const int i_begin = q * A.chunk;
@@ -197,17 +205,26 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
             a[b][2] = n.z;
             a[b][3] = n.w;
         }
-        float pb[NB];
+        float pb[NB], pm[NB];
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             float q = p[b][0] * ex2_approx(a[b][0]);
             q = fmaf(p[b][1], ex2_approx(a[b][1]), q);
             q = fmaf(p[b][2], ex2_approx(a[b][2]), q);
             pb[b] = fmaf(p[b][3], ex2_approx(a[b][3]), q);
+            if (ANTI) {
+                float r = p[b][0] * ex2_approx(-a[b][0]);
+                r = fmaf(p[b][1], ex2_approx(-a[b][1]), r);
+                r = fmaf(p[b][2], ex2_approx(-a[b][2]), r);
+                pm[b] = fmaf(p[b][3], ex2_approx(-a[b][3]), r);
+            }
         }
-        float part = pb[0];
+        float part = pb[0], partm = ANTI ? pm[0] : 0.f;
 #pragma unroll
-        for (int b = 1; b < NB; ++b) part += pb[b];
+        for (int b = 1; b < NB; ++b) {
+            part += pb[b];
+            if (ANTI) partm += pm[b];
+        }
         float ay = 0.f;
         if (ywarp) {  // warp-uniform: only the warp that holds the target's block
 #pragma unroll
@@ -215,13 +232,18 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
                 if (b == yb) ay = yc == 0 ? a[b][0] : yc == 1 ? a[b][1] : yc == 2 ? a[b][2] : a[b][3];
         }
         part = warp_sum(part);
-        float S;
+        if (ANTI) partm = warp_sum(partm);
+        float S, Sm = 1.f;
         if (ONE_WARP) {
             S = part;
+            Sm = partm;
             ay = __shfl_sync(0xFFFFFFFFu, ay, ylane);
         } else {
             const int buf = i & 1;
-            if (lane == 0) red[buf][warp] = part;
+            if (lane == 0) {
+                red[buf][warp] = part;
+                if (ANTI) red_m[buf][warp] = partm;
+            }
             if (owner) red_y[buf] = ay;
             __syncthreads();
             // Eight warp partials (absent warps read zero), summed by a
@@ -230,18 +252,33 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
             S += __shfl_xor_sync(0xFFFFFFFFu, S, 1);
             S += __shfl_xor_sync(0xFFFFFFFFu, S, 2);
             S += __shfl_xor_sync(0xFFFFFFFFu, S, 4);
+            if (ANTI) {
+                Sm = red_m[buf][lane & 7];
+                Sm += __shfl_xor_sync(0xFFFFFFFFu, Sm, 1);
+                Sm += __shfl_xor_sync(0xFFFFFFFFu, Sm, 2);
+                Sm += __shfl_xor_sync(0xFFFFFFFFu, Sm, 4);
+            }
             ay = (y >= 0) ? red_y[buf] : 0.f;
         }
-        // sigma a_y = b_y ln 2.
-        const float dl = fmaf(ay, -0.69314718055994531f, log_pos(S));
-        sdl += dl;
+        if (ANTI) {
+            // dl(+a) - dl(-a) = ln S+ - ln S- - 2 sigma a_y, sigma a_y = b_y ln 2.
+            const float dd = fmaf(ay, -1.3862943611198906f, log_pos(S) - log_pos(Sm));
 #pragma unroll
-        for (int b = 0; b < NB; ++b)
+            for (int b = 0; b < NB; ++b)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                s1[b][k] = fmaf(dl, a[b][k], s1[b][k]);
-                s0[b][k] += a[b][k];
-            }
+                for (int k = 0; k < 4; ++k) s1[b][k] = fmaf(dd, a[b][k], s1[b][k]);
+        } else {
+            // sigma a_y = b_y ln 2.
+            const float dl = fmaf(ay, -0.69314718055994531f, log_pos(S));
+            sdl += dl;
+#pragma unroll
+            for (int b = 0; b < NB; ++b)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    s1[b][k] = fmaf(dl, a[b][k], s1[b][k]);
+                    s0[b][k] += a[b][k];
+                }
+        }
     }
 
     if (A.Q == 1) {
@@ -362,9 +399,12 @@ HeadPlan head_plan(int64_t T, int64_t V, int64_t d, uint32_t K) {
 
 template <int NB, bool OW>
 dust_status launch_draws(const HeadPlan& P, const HeadArgs& A, const PhiloxKeys& keys,
-                         int64_t T, cudaStream_t s) {
+                         int64_t T, bool anti, cudaStream_t s) {
     timer_begin(s);
-    head_draws_kernel<NB, OW><<<static_cast<unsigned>(T * P.Q), P.nt, 0, s>>>(A, keys);
+    if (anti)
+        head_draws_kernel<NB, OW, true><<<static_cast<unsigned>(T * P.Q), P.nt, 0, s>>>(A, keys);
+    else
+        head_draws_kernel<NB, OW, false><<<static_cast<unsigned>(T * P.Q), P.nt, 0, s>>>(A, keys);
     timer_end(s);
     return launch_status();
 }
@@ -379,11 +419,16 @@ extern "C" size_t dust_head_workspace(int64_t T, int64_t V, int64_t d, uint32_t 
     return head_plan(T, V, d, K).ws_bytes;
 }
 
-extern "C" dust_status dust_head_estimate(const float* logits, const int32_t* targets,
-                                          const void* x, dust_dtype x_dtype, int64_t T,
-                                          int64_t V, int64_t d, dust_noise nz, float* g_hat,
-                                          float* G_W, void* ws, size_t ws_bytes, void* stream) {
+namespace {
+
+dust_status head_estimate(const float* logits, const int32_t* targets, const void* x,
+                          dust_dtype x_dtype, int64_t T, int64_t V, int64_t d, dust_noise nz,
+                          dust_baseline baseline, float* g_hat, float* G_W, void* ws,
+                          size_t ws_bytes, void* stream) {
     if (!logits || !targets || !x || !G_W) return DUST_ERR_INVALID_ARG;
+    if (baseline != DUST_BASELINE_MEAN && baseline != DUST_BASELINE_LEAVE_ONE_OUT &&
+        baseline != DUST_BASELINE_ANTITHETIC)
+        return DUST_ERR_INVALID_ARG;
     if (T < 1 || V < 1 || d < 1 || nz.num_draws < 2) return DUST_ERR_INVALID_ARG;
     if (!(nz.sigma > 0.0f) || !(nz.sigma < INFINITY)) return DUST_ERR_INVALID_ARG;
     if (x_dtype != DUST_F32 && x_dtype != DUST_BF16) return DUST_ERR_INVALID_ARG;
@@ -414,8 +459,14 @@ extern "C" dust_status dust_head_estimate(const float* logits, const int32_t* ta
     A.layer = nz.layer;
     const double s_l2e = static_cast<double>(nz.sigma) * 1.4426950408889634;
     A.sig_l2e = static_cast<float>(s_l2e);
-    A.g_scale = static_cast<float>(
-        1.0 / (static_cast<double>(nz.num_draws) * nz.sigma * static_cast<double>(A.sig_l2e)));
+    // g = (S1 - m S0) / (K sigma s) for the mean over draws; leave-one-out
+    // means scale it by K / (K - 1); antithetic pairs give S1 / (2 K sigma s).
+    const double ks = static_cast<double>(nz.sigma) * static_cast<double>(A.sig_l2e);
+    const double K = static_cast<double>(nz.num_draws);
+    A.g_scale = static_cast<float>(baseline == DUST_BASELINE_LEAVE_ONE_OUT ? 1.0 / ((K - 1.0) * ks)
+                                   : baseline == DUST_BASELINE_ANTITHETIC  ? 1.0 / (2.0 * K * ks)
+                                                                           : 1.0 / (K * ks));
+    const bool anti = baseline == DUST_BASELINE_ANTITHETIC;
     A.g_hat = g_hat;
     A.gbf = reinterpret_cast<__nv_bfloat16*>(w + P.off_gbf);
     A.ldg = P.ldg;
@@ -430,14 +481,14 @@ extern "C" dust_status dust_head_estimate(const float* logits, const int32_t* ta
     dust_status st;
     if (P.one_warp) {
         switch (P.nb) {
-            case 1: st = launch_draws<1, true>(P, A, keys, T, s); break;
-            case 2: st = launch_draws<2, true>(P, A, keys, T, s); break;
-            case 4: st = launch_draws<4, true>(P, A, keys, T, s); break;
-            default: st = launch_draws<8, true>(P, A, keys, T, s); break;
+            case 1: st = launch_draws<1, true>(P, A, keys, T, anti, s); break;
+            case 2: st = launch_draws<2, true>(P, A, keys, T, anti, s); break;
+            case 4: st = launch_draws<4, true>(P, A, keys, T, anti, s); break;
+            default: st = launch_draws<8, true>(P, A, keys, T, anti, s); break;
         }
     } else {
-        st = P.nb == 4 ? launch_draws<4, false>(P, A, keys, T, s)
-                       : launch_draws<8, false>(P, A, keys, T, s);
+        st = P.nb == 4 ? launch_draws<4, false>(P, A, keys, T, anti, s)
+                       : launch_draws<8, false>(P, A, keys, T, anti, s);
     }
     if (st != DUST_OK) return st;
     if (P.Q > 1) {
@@ -460,6 +511,26 @@ extern "C" dust_status dust_head_estimate(const float* logits, const int32_t* ta
     }
     return gemm_bf16_launch(A.gbf, true, P.ldg, xb, true, ldx, V, d, T, 0, 1, G_W, d,
                             static_cast<uint32_t*>(ws), s);
+}
+
+}  // namespace
+
+extern "C" dust_status dust_head_estimate(const float* logits, const int32_t* targets,
+                                          const void* x, dust_dtype x_dtype, int64_t T,
+                                          int64_t V, int64_t d, dust_noise nz, float* g_hat,
+                                          float* G_W, void* ws, size_t ws_bytes, void* stream) {
+    return head_estimate(logits, targets, x, x_dtype, T, V, d, nz, DUST_BASELINE_MEAN, g_hat,
+                         G_W, ws, ws_bytes, stream);
+}
+
+extern "C" dust_status dust_head_estimate_baseline(const float* logits, const int32_t* targets,
+                                                   const void* x, dust_dtype x_dtype, int64_t T,
+                                                   int64_t V, int64_t d, dust_noise nz,
+                                                   dust_baseline baseline, float* g_hat,
+                                                   float* G_W, void* ws, size_t ws_bytes,
+                                                   void* stream) {
+    return head_estimate(logits, targets, x, x_dtype, T, V, d, nz, baseline, g_hat, G_W, ws,
+                         ws_bytes, stream);
 }
 
 // ------------------------------------------------------------------------

@@ -13,8 +13,8 @@ frequencies; weights are random N(0, 1/fan_in).  The cached logits (256 MB)
 are larger than the 126 MB L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dust|reference]
-                  [--workload head_batch|head_tiny|head_scale|interior|interior_scale|embed_scale|
-                              head_sweep|optim_adam]
+                  [--workload head_batch|head_batch_antithetic|head_tiny|head_scale|interior|
+                              interior_scale|embed_scale|head_sweep|optim_adam]
 
 Under torchrun (N > 1) every rank estimates its own batch (global token
 offset rank * T, so the noise differs per rank) with no collective on the data
@@ -46,6 +46,9 @@ SM_MAX_MHZ = 2032.0
 # notes: Philox 9 + uniform 2 + Box-Muller 3 + CE 2 + accumulators 2 + share
 # of the per-draw reduction 2.
 HEAD_OPS_PER_ELEMENT_DRAW = 20
+# antithetic pair: one noise value (Philox 9, uniform 2, Box-Muller 3), two loss
+# terms (4), one accumulator, reduction share 2
+HEAD_OPS_PER_ELEMENT_PAIR = 21
 
 
 def _peaks():
@@ -150,6 +153,7 @@ def make_workload(name, device, rank):
         return {
             "kind": "head", "name": name, "T": T, "V": p["V"], "d": p["d"], "K": p["K"],
             "sigma": p["sigma"], "seq_len": p["seq_len"], "token0": rank_token0(rank, T),
+            "baseline": p.get("baseline", 0),
             "host": {"logits": wl["z"], "targets": wl["targets"],
                      "x": W.bf16_round(wl["x"]) if p["x_bf16"] else wl["x"]},
             "x_bf16": p["x_bf16"],
@@ -191,9 +195,10 @@ def make_step(wl, dust):
 
         def step():
             dust.head_estimate(d["logits"], d["targets"], d["x"], wl["sigma"], K, 1234, 0, 0,
-                               wl["token0"], out=(g, G), ws=ws)
+                               wl["token0"], out=(g, G), ws=ws, baseline=wl["baseline"])
         launches = 2 + (0 if wl["x_bf16"] else 1)
-        return step, K * T, launches, ws
+        # antithetic pairs: two perturbed evaluations per noise draw
+        return step, K * T * (2 if wl["baseline"] == 2 else 1), launches, ws
     if wl["kind"] == "interior":
         T, K = wl["T"], wl["K"]
         g = torch.empty((T, wl["C"]), dtype=torch.float32, device=d["x"].device)
@@ -235,7 +240,8 @@ def make_step(wl, dust):
 def roofline(wl, kernel_ms, traffic):
     peaks, which = _peaks()
     if wl["kind"] == "head":
-        ops = HEAD_OPS_PER_ELEMENT_DRAW * wl["T"] * wl["V"] * wl["K"]
+        per = HEAD_OPS_PER_ELEMENT_PAIR if wl.get("baseline") == 2 else HEAD_OPS_PER_ELEMENT_DRAW
+        ops = per * wl["T"] * wl["V"] * wl["K"]
         peak = N_SM * 128 * peaks.get("sm_max_mhz", SM_MAX_MHZ) * 1e6 / 1e12
         ach = ops / (kernel_ms * 1e-3) / 1e12
         return {"bound": "alu", "achieved": ach, "peak": peak, "unit": "Tops/s",
@@ -293,18 +299,19 @@ def oracle_sample(wl, budget_s=12.0):
     h = wl["host"]
     if wl["kind"] == "head":
         K = wl["K"]
+        anti = wl.get("baseline") == 2
+        fn = oracle.head_estimate_antithetic if anti else oracle.head_estimate
 
         def run(n):
             t0 = time.perf_counter()
-            oracle.head_estimate(h["logits"][:n], h["targets"][:n], h["x"][:n], wl["sigma"], K,
-                                 1234, 0, 0, 0)
+            fn(h["logits"][:n], h["targets"][:n], h["x"][:n], wl["sigma"], K, 1234, 0, 0, 0)
             return time.perf_counter() - t0
         n = 8
         dt = run(n)
         n = int(min(wl["T"], max(8, n * budget_s / max(dt, 1e-3))))
         dt = run(n)
-        return K * n / dt, "%d of %d tokens, all %d draws, full vocabulary %d" % (
-            n, wl["T"], K, wl["V"])
+        return K * n * (2 if anti else 1) / dt, "%d of %d tokens, all %d draws%s, full " \
+            "vocabulary %d" % (n, wl["T"], K, " (antithetic pairs)" if anti else "", wl["V"])
     if wl["kind"] == "interior":
         L = wl["seq_len"]
 
@@ -333,6 +340,8 @@ def config_of(wl, n_gpus):
     for k in ("V", "d", "C", "d_in", "d_model", "seq_len", "sigma", "gamma"):
         if k in wl:
             c[k] = wl[k]
+    if wl.get("baseline") == 2:
+        c["baseline"] = "antithetic pairs: draws counts noise draws, 2 evaluations each"
     return c
 
 
@@ -591,7 +600,7 @@ def run_dust(args):
 
             def call(d):
                 dust.head_estimate(d["logits"], d["targets"], d["x"], wl["sigma"], K, 1234, 0, 0,
-                                   wl["token0"], out=(g, G), ws=wse)
+                                   wl["token0"], out=(g, G), ws=wse, baseline=wl["baseline"])
         elif wl["kind"] == "interior":
             T, K = wl["T"], wl["K"]
             g = torch.empty((T, wl["C"]), dtype=torch.float32, device=device)
@@ -681,7 +690,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="dust", choices=["dust", "reference"])
     ap.add_argument("--workload", default="head_batch",
-                    choices=["head_batch", "head_tiny", "head_scale", "interior",
+                    choices=["head_batch", "head_batch_antithetic", "head_tiny", "head_scale",
+                             "interior",
                              "interior_scale", "embed_scale", "head_sweep", "optim_adam"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -127,6 +127,36 @@ dust_status dust_head_estimate(const float* logits, const int32_t* targets, cons
                                dust_noise nz, float* g_hat, float* G_W, void* ws,
                                size_t ws_bytes, void* stream);
 
+/*
+ * How the loss changes of the K draws become centred decreases c.  The pages
+ * centre by the mean over draws (Dust translation §2.2); the two others are
+ * the common variance-reduction baselines, which the pages do not describe:
+ *   DUST_BASELINE_MEAN           c_i = -(dl_i - mean_j dl_j)     (the pages)
+ *   DUST_BASELINE_LEAVE_ONE_OUT  c_i = -(dl_i - mean_{j != i} dl_j)
+ *                                (= K/(K-1) times the mean-centred estimate)
+ *   DUST_BASELINE_ANTITHETIC     each draw's noise is evaluated as +a and -a,
+ *                                c_i = -(dl_i(+a) - dl_i(-a)) / 2: 2K
+ *                                perturbed evaluations from K noise draws.
+ */
+typedef enum {
+    DUST_BASELINE_MEAN = 0,
+    DUST_BASELINE_LEAVE_ONE_OUT = 1,
+    DUST_BASELINE_ANTITHETIC = 2
+} dust_baseline;
+
+/*
+ * dust_head_estimate with a choice of baseline; everything else (arguments,
+ * limits, workspace from dust_head_workspace with the same K, errors) is as
+ * there.  With DUST_BASELINE_ANTITHETIC, nz.num_draws counts noise draws
+ * (pairs); draw i uses the noise of counter draw0 + i for both signs.  An
+ * unknown baseline value is INVALID_ARG.
+ */
+dust_status dust_head_estimate_baseline(const float* logits, const int32_t* targets,
+                                        const void* x, dust_dtype x_dtype, int64_t T, int64_t V,
+                                        int64_t d, dust_noise nz, dust_baseline baseline,
+                                        float* g_hat, float* G_W, void* ws, size_t ws_bytes,
+                                        void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Interior linear layer with causal credit                                  */
 /* ------------------------------------------------------------------------ */

@@ -87,6 +87,8 @@ HEAD_PARAMS = {
     "head_tiny": dict(HEAD_TINY, sigma=0.05, K=64),
     "head_batch": dict(HEAD_BATCH, sigma=0.05, K=64),
     "head_scale": dict(HEAD_SCALE, sigma=0.05, K=4096),
+    # the batch shape with antithetic pairs: 32 noise draws, 64 evaluations
+    "head_batch_antithetic": dict(HEAD_BATCH, sigma=0.05, K=32, baseline=2),
 }
 HEAD_SWEEP_K = (64, 256, 1024, 4096, 16384)
 
