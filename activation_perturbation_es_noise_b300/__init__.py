@@ -28,7 +28,8 @@ EXPORTS = ("dust_status_string", "dust_abi_version", "dust_workspace_status",
            "dust_linear_estimate", "dust_embed_workspace", "dust_embed_scatter",
            "dust_embed_scatter_static", "dust_philox_fill", "dust_gemm_bf16", "dust_set_kernel_events",
            "dust_kernel_event_count", "dust_wait_selftest", "dust_sgd_step", "dust_adam_step",
-           "dust_head_backprop_workspace", "dust_head_backprop", "dust_head_estimate_baseline")
+           "dust_head_backprop_workspace", "dust_head_backprop", "dust_head_estimate_baseline",
+           "dust_attn_value_workspace", "dust_attn_value_estimate")
 BASELINE_MEAN, BASELINE_LEAVE_ONE_OUT, BASELINE_ANTITHETIC = 0, 1, 2
 
 
@@ -89,6 +90,10 @@ def lib():
         L.dust_adam_step.argtypes = [_P, _P, _P, _P, _I64, _F, _F, _F, _F, _F, _I64, _P, _P]
         L.dust_head_estimate_baseline.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64,
                                                   DustNoise, ctypes.c_int, _P, _P, _P, _SZ, _P]
+        L.dust_attn_value_workspace.argtypes = [_I64, _I64, _I64, _I64, _I64, _U32]
+        L.dust_attn_value_workspace.restype = _SZ
+        L.dust_attn_value_estimate.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _I64,
+                                               _I64, DustNoise, _P, _P, _P, _SZ, _P]
         L.dust_head_backprop_workspace.argtypes = [_I64, _I64, _I64]
         L.dust_head_backprop_workspace.restype = _SZ
         L.dust_head_backprop.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _P, _P, _P,
@@ -97,7 +102,7 @@ def lib():
                      "dust_head_estimate", "dust_linear_estimate", "dust_embed_scatter",
                      "dust_embed_scatter_static", "dust_philox_fill", "dust_gemm_bf16",
                      "dust_sgd_step", "dust_adam_step", "dust_head_backprop",
-                     "dust_head_estimate_baseline"):
+                     "dust_head_estimate_baseline", "dust_attn_value_estimate"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -355,4 +360,33 @@ def head_backprop(logits, targets, x, want_g=False, out=None, ws=None, stream=No
     _check("dust_head_backprop",
            lib().dust_head_backprop(_ptr(logits), _ptr(targets), _ptr(x), xdt, T, V, d, _ptr(g),
                                     _ptr(G), _ptr(ws), ws.numel(), _stream(stream)))
+    return g, G, ws
+
+
+# ------------------------------------------------------------ attention ----
+def attn_value_estimate(P, E, x, seq_len, sigma, gamma, K, seed, layer=2, draw0=0, token0=0,
+                        want_g=True, out=None, ws=None, stream=None):
+    """Value projection of an attention layer, scored by the attention-output
+    error E (T x H*64).  P: (T/seq_len, H, seq_len, seq_len) fp32 cached
+    probabilities.  Returns (g_hat or None, G_W, ws)."""
+    _need_cuda(P, E, x)
+    nseq, H, L, L2 = P.shape
+    T, C = E.shape
+    if L != seq_len or L2 != seq_len or nseq * L != T or C != H * 64:
+        raise ValueError("P must be (T/seq_len, H, seq_len, seq_len) and E T x H*64")
+    d_in = x.shape[1]
+    dev = P.device
+    if out is None:
+        g = torch.empty((T, C), dtype=torch.float32, device=dev) if want_g else None
+        G = torch.empty((C, d_in), dtype=torch.float32, device=dev)
+    else:
+        g, G = out
+    if ws is None:
+        ws = _workspace(lib().dust_attn_value_workspace(T, seq_len, H, 64, d_in, K), dev)
+    xdt = DUST_BF16 if x.dtype == torch.bfloat16 else DUST_F32
+    _check("dust_attn_value_estimate",
+           lib().dust_attn_value_estimate(_ptr(P), _ptr(E), _ptr(x), xdt, T, seq_len, H, 64,
+                                          d_in, noise(seed, sigma, K, layer, draw0, token0, gamma),
+                                          _ptr(g), _ptr(G), _ptr(ws), ws.numel(),
+                                          _stream(stream)))
     return g, G, ws

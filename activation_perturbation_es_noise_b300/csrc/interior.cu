@@ -374,6 +374,22 @@ unsigned grid_cap(int64_t n, int threads) {
 }
 
 }  // namespace
+
+dust_status credit_and_ghat_launch(const float* dl, float* mean, float* r, int T, int seq_len,
+                                   int C, const dust_noise& nz, const PhiloxKeys& keys,
+                                   float* g_hat, __nv_bfloat16* gbf, cudaStream_t s) {
+    const int K = static_cast<int>(nz.num_draws);
+    const int nseq = T / seq_len;
+    draw_mean_kernel<<<static_cast<unsigned>(ceil_div(T, 256)), 256, 0, s>>>(dl, K, T, mean);
+    reward_scan_kernel<<<static_cast<unsigned>(ceil_div(static_cast<int64_t>(K) * nseq, 128)), 128,
+                         0, s>>>(dl, mean, K, T, seq_len, nz.gamma, r);
+    dust_status st = launch_status();
+    if (st != DUST_OK) return st;
+    GhatArgs ga{r, T, C, K, nz.draw0, nz.token0, nz.layer,
+                static_cast<float>(-1.0 / (static_cast<double>(K) * nz.sigma)), g_hat, gbf};
+    interior_ghat_kernel<<<grid_cap(static_cast<int64_t>(T) * (C / 8), 256), 256, 0, s>>>(ga, keys);
+    return launch_status();
+}
 }  // namespace dust
 
 using namespace dust;
@@ -480,14 +496,9 @@ extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, cons
         if (st != DUST_OK) return st;
     }
 
-    draw_mean_kernel<<<static_cast<unsigned>(ceil_div(T, 256)), 256, 0, s>>>(dl, K, Ti, mean);
-    reward_scan_kernel<<<static_cast<unsigned>(ceil_div(static_cast<int64_t>(K) * nseq, 128)), 128,
-                         0, s>>>(dl, mean, K, Ti, static_cast<int>(seq_len), nz.gamma, r);
-    if ((st = launch_status()) != DUST_OK) return st;
-    GhatArgs ga{r, Ti, Ci, K, nz.draw0, nz.token0, nz.layer,
-                static_cast<float>(-1.0 / (static_cast<double>(K) * nz.sigma)), g_hat, gbf};
-    interior_ghat_kernel<<<grid_cap(T * (C / 8), 256), 256, 0, s>>>(ga, keys);
-    if ((st = launch_status()) != DUST_OK) return st;
+    st = credit_and_ghat_launch(dl, mean, r, Ti, static_cast<int>(seq_len), Ci, nz, keys, g_hat,
+                                gbf, s);
+    if (st != DUST_OK) return st;
 
     const void* xb = x;
     int64_t ldx = d_in;

@@ -95,6 +95,14 @@ bool encode_bf16_2d(CUtensorMap* map, const void* ptr, int64_t inner, int64_t ou
 
 struct PhiloxKeys;
 
+// From per-draw loss changes dl (K x T): the centring by the mean over draws,
+// the gamma-discounted suffix scan per sequence (r, K x T), and
+// g = -(1/(K sigma)) sum_i r a with the noise regenerated over C channels
+// (C % 8 == 0), written as fp32 (g_hat, optional) and bf16 (gbf, T x C).
+dust_status credit_and_ghat_launch(const float* dl, float* mean, float* r, int T, int seq_len,
+                                   int C, const dust_noise& nz, const PhiloxKeys& keys,
+                                   float* g_hat, __nv_bfloat16* gbf, cudaStream_t s);
+
 // Interior GEMM 1 with its A operand (the GELU difference of the perturbed
 // output, split bf16) generated on chip: du = dh W2^T for nd draws.  With A2
 // non-null (seq_len a multiple of 128, T = Tp) the epilogue also runs the

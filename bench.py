@@ -14,7 +14,7 @@ are larger than the 126 MB L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dust|reference]
                   [--workload head_batch|head_batch_antithetic|head_tiny|head_scale|interior|
-                              interior_scale|embed_scale|head_sweep|optim_adam]
+                              interior_scale|embed_scale|head_sweep|optim_adam|attn_value]
 
 Under torchrun (N > 1) every rank estimates its own batch (global token
 offset rank * T, so the noise differs per rank) with no collective on the data
@@ -410,6 +410,77 @@ def run_optim(args):
     return 0
 
 
+ATTN = dict(nseq=8, H=8, L=2048, d_in=512, K=64, sigma=0.02, gamma=0.99)
+
+
+def run_attn_value(args):
+    """The value projection inside attention (8 x 2048 tokens, 8 heads of 64,
+    d_in 512, K = 64, gamma 0.99), inputs resident: token-evals/s, and the
+    re-forward kernel against the sustained bf16 tensor peak, counting the
+    three split-bf16 passes over the causal keys the kernel covers."""
+    import torch
+
+    import activation_perturbation_es_noise_b300 as dust
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    c = ATTN
+    nseq, H, L, K = c["nseq"], c["H"], c["L"], c["K"]
+    T = nseq * L
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(21)
+    s = torch.randn((nseq, H, L, L), generator=gen, device=dev) * 2.0
+    s = s.masked_fill(torch.triu(torch.ones(L, L, dtype=torch.bool, device=dev), 1), -1e30)
+    P = torch.softmax(s, dim=-1).contiguous()
+    del s
+    E = torch.randn((T, H * 64), generator=gen, device=dev) * 0.1
+    x = torch.randn((T, c["d_in"]), generator=gen, device=dev).to(torch.bfloat16)
+    g = torch.empty((T, H * 64), dtype=torch.float32, device=dev)
+    G = torch.empty((H * 64, c["d_in"]), dtype=torch.float32, device=dev)
+    ws = dust._workspace(dust.lib().dust_attn_value_workspace(T, L, H, 64, c["d_in"], K), dev)
+
+    def step():
+        dust.attn_value_estimate(P, E, x, L, c["sigma"], c["gamma"], K, 1234, out=(g, G), ws=ws)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clocks:
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        e1.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    timer = dust.KernelTimer(capacity=args.steps * (K // 4 + 1))
+    with timer:
+        torch.cuda._sleep(1_000_000 * args.steps)
+        for _ in range(args.steps):
+            step()
+    torch.cuda.synchronize()
+    kernel_ms = timer.total_ms() / args.steps
+    # covered key slices per (sequence, head): sum over query tiles of 128 x 128 (qb + 1)
+    nt = L // 128
+    pairs = 128 * 128 * nt * (nt + 1) // 2
+    flops = 3 * 2.0 * pairs * 64 * 4 * (K // 4) * nseq * H
+    peaks, which = _peaks()
+    ach = flops / (kernel_ms * 1e-3) / 1e12
+    print(json.dumps({
+        "metric": METRIC, "value": K * T / (ms * 1e-3), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32+bf16x3", "data": "synthetic",
+        "config": {"workload": "attn_value", "tokens": T, "draws": K, "heads": H, "dv": 64,
+                   "d_in": c["d_in"], "seq_len": L, "sigma": c["sigma"], "gamma": c["gamma"],
+                   "l2": "inputs larger than L2 (no flush)"},
+        "roofline": {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"],
+                     "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops_sustained"],
+                     "traffic": None, "kernel": "attn_v_kernel", "kernel_ms": kernel_ms,
+                     "peak_source": "bf16_tflops_sustained (%s)" % which},
+        "cpu_baseline": None, "e2e": None, "gpu_launches": args.steps * (2 * (K // 4) + 6),
+        "clocks": clocks.summary()}), flush=True)
+    return 0
+
+
 def run_head_sweep(args):
     """The tiny head workload at K = 64 .. 16384: token-evals/s per K and the
     cosine of G_W with the analytic head gradient sum_t (softmax(z_t) -
@@ -692,7 +763,8 @@ def main():
     ap.add_argument("--workload", default="head_batch",
                     choices=["head_batch", "head_batch_antithetic", "head_tiny", "head_scale",
                              "interior",
-                             "interior_scale", "embed_scale", "head_sweep", "optim_adam"])
+                             "interior_scale", "embed_scale", "head_sweep", "optim_adam",
+                             "attn_value"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
@@ -704,6 +776,8 @@ def main():
         return run_head_sweep(args)
     if args.workload == "optim_adam":
         return run_optim(args)
+    if args.workload == "attn_value":
+        return run_attn_value(args)
     return run_dust(args)
 
 

@@ -269,6 +269,46 @@ dust_status dust_gemm_bf16(const void* A, int a_mn, int64_t lda, const void* B, 
                            void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Inside attention: the values, scored by the attention-output error        */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes for dust_attn_value_estimate with these sizes (0 if they
+ * are invalid). */
+size_t dust_attn_value_workspace(int64_t T, int64_t seq_len, int64_t H, int64_t dv,
+                                 int64_t d_in, uint32_t K);
+
+/*
+ * Estimator for the value projection v = W_v x of a causal attention layer,
+ * perturbed per token inside the attention and scored by the attention-output
+ * error (Dust translation §2.3: perturbations inside attention are scored by
+ * the error of the attention output, with a decay gamma close to 1 for later
+ * tokens).  With the cached clean probabilities P, perturbing every value by
+ * sigma a_t changes head h's output of token s by
+ *   dO_s = sigma sum_{t <= s} P_{s,t} a_t[h]   (exactly, values enter linearly);
+ * the loss change of token s is read to first order as dl_s = <E_s, dO_s> over
+ * all heads, and then c = -(dl - mean over draws),
+ * r_t = sum_{s >= t, same sequence} gamma^(s-t) c_s,
+ * g_t = -(1/(K sigma)) sum_i r a, G_W = sum_t g_t x_t^T.
+ *
+ *   P    device fp32, (T/seq_len) x H x seq_len x seq_len: row s = query,
+ *        column t = key; entries with t > s are ignored (treated as 0).
+ *   E    device fp32, T x (H dv): the error estimate of the attention output
+ *        (head h in columns h dv .. h dv + dv - 1).
+ *   x    device, T x d_in, dtype x_dtype: the input of W_v.
+ *   g_hat device fp32 T x (H dv) output or NULL; G_W device fp32 (H dv) x d_in
+ *        output (g and x rounded to bf16, fp32 accumulation).
+ *   nz   noise of channel c = h dv + j of token t, draw i: the Philox counter
+ *        (c/4, token0 + t, draw0 + i, layer) as for the other estimators.
+ * Limits: dv = 64, seq_len a multiple of 128 (<= 8192), T a multiple of
+ * seq_len, 1 <= H <= 64, K >= 2.  Workspace from dust_attn_value_workspace
+ * (it holds P as split bf16, 2 x 2 bytes per entry of P).
+ */
+dust_status dust_attn_value_estimate(const float* P, const float* E, const void* x,
+                                     dust_dtype x_dtype, int64_t T, int64_t seq_len, int64_t H,
+                                     int64_t dv, int64_t d_in, dust_noise nz, float* g_hat,
+                                     float* G_W, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Using the estimate: optimiser step and the backprop reference             */
 /* ------------------------------------------------------------------------ */
 

@@ -16,7 +16,8 @@ The two dense contractions of the interior re-forward (Delta h W2^T and
 Delta e W_head^T) use numpy's float64 matmul as a library step; everything else
 is the C loops.  What consumes the estimate (the optimiser step, the exact head
 gradient it is compared with) is in optim.py; the head estimator with the
-leave-one-out and antithetic baselines in baselines.py.
+leave-one-out and antithetic baselines in baselines.py; the value projection
+inside attention, scored by the attention-output error, in attention.py.
 """
 import ctypes
 import os
@@ -24,6 +25,7 @@ import os
 import numpy as np
 
 from . import build as _build
+from .attention import attn_value_delta_loss, attn_value_estimate  # noqa: F401
 from .baselines import head_estimate_antithetic, head_estimate_leave_one_out  # noqa: F401
 from .optim import adam_step, head_backprop, head_grad_rows, sgd_step  # noqa: F401
 
