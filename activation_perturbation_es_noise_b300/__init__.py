@@ -29,7 +29,8 @@ EXPORTS = ("dust_status_string", "dust_abi_version", "dust_workspace_status",
            "dust_embed_scatter_static", "dust_philox_fill", "dust_gemm_bf16", "dust_set_kernel_events",
            "dust_kernel_event_count", "dust_wait_selftest", "dust_sgd_step", "dust_adam_step",
            "dust_head_backprop_workspace", "dust_head_backprop", "dust_head_estimate_baseline",
-           "dust_attn_value_workspace", "dust_attn_value_estimate")
+           "dust_attn_value_workspace", "dust_attn_value_estimate", "dust_attn_gate_workspace",
+           "dust_attn_gate_estimate")
 BASELINE_MEAN, BASELINE_LEAVE_ONE_OUT, BASELINE_ANTITHETIC = 0, 1, 2
 
 
@@ -94,6 +95,10 @@ def lib():
         L.dust_attn_value_workspace.restype = _SZ
         L.dust_attn_value_estimate.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _I64,
                                                _I64, DustNoise, _P, _P, _P, _SZ, _P]
+        L.dust_attn_gate_workspace.argtypes = [_I64, _I64, _I64, _I64, _U32]
+        L.dust_attn_gate_workspace.restype = _SZ
+        L.dust_attn_gate_estimate.argtypes = [_P, _P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _I64,
+                                              DustNoise, _P, _P, _P, _SZ, _P]
         L.dust_head_backprop_workspace.argtypes = [_I64, _I64, _I64]
         L.dust_head_backprop_workspace.restype = _SZ
         L.dust_head_backprop.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _P, _P, _P,
@@ -102,7 +107,8 @@ def lib():
                      "dust_head_estimate", "dust_linear_estimate", "dust_embed_scatter",
                      "dust_embed_scatter_static", "dust_philox_fill", "dust_gemm_bf16",
                      "dust_sgd_step", "dust_adam_step", "dust_head_backprop",
-                     "dust_head_estimate_baseline", "dust_attn_value_estimate"):
+                     "dust_head_estimate_baseline", "dust_attn_value_estimate",
+                     "dust_attn_gate_estimate"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -389,4 +395,27 @@ def attn_value_estimate(P, E, x, seq_len, sigma, gamma, K, seed, layer=2, draw0=
                                           d_in, noise(seed, sigma, K, layer, draw0, token0, gamma),
                                           _ptr(g), _ptr(G), _ptr(ws), ws.numel(),
                                           _stream(stream)))
+    return g, G, ws
+
+
+def attn_gate_estimate(z, o, E, x, seq_len, sigma, gamma, K, seed, layer=3, draw0=0, token0=0,
+                       want_g=True, out=None, ws=None, stream=None):
+    """Gate projection of a gated attention output sig(z) * o, scored by the
+    error E of the gated output (all T x C fp32).  Returns (g_hat or None, G_W, ws)."""
+    _need_cuda(z, o, E, x)
+    T, C = z.shape
+    d_in = x.shape[1]
+    dev = z.device
+    if out is None:
+        g = torch.empty((T, C), dtype=torch.float32, device=dev) if want_g else None
+        G = torch.empty((C, d_in), dtype=torch.float32, device=dev)
+    else:
+        g, G = out
+    if ws is None:
+        ws = _workspace(lib().dust_attn_gate_workspace(T, seq_len, C, d_in, K), dev)
+    xdt = DUST_BF16 if x.dtype == torch.bfloat16 else DUST_F32
+    _check("dust_attn_gate_estimate",
+           lib().dust_attn_gate_estimate(_ptr(z), _ptr(o), _ptr(E), _ptr(x), xdt, T, seq_len, C,
+                                         d_in, noise(seed, sigma, K, layer, draw0, token0, gamma),
+                                         _ptr(g), _ptr(G), _ptr(ws), ws.numel(), _stream(stream)))
     return g, G, ws

@@ -394,3 +394,142 @@ extern "C" dust_status dust_attn_value_estimate(const float* P, const float* E, 
     }
     return gemm_bf16_launch(gbf, true, C, xb, true, ldx, C, d_in, T, 0, 1, G_W, d_in, status, s);
 }
+
+// ------------------------------------------------------------------------
+// Gates of the attention output, the other elementwise member of the
+// attention internals the pages list (Dust translation §2.3): the gated
+// output is sig(z_s) * o_s per channel with z_s = W_g x_s.  Perturbing every
+// token's gate pre-activation changes only its own gated output,
+//   d(o~)_s = (sig(z_s + sigma a_s) - sig(z_s)) * o_s,
+// and it is scored, like the values, by the error E of the gated output:
+// dl_s = <E_s, d(o~)_s>.  sig(z + d) - sig(z) = sig(z + d) (1 - sig(z))
+// (1 - e^-d) has no cancellation for small d.
+// ------------------------------------------------------------------------
+namespace dust {
+namespace {
+
+struct GateArgs {
+    const float* z;  // T x C gate pre-activations
+    const float* o;  // T x C attention output before the gate
+    const float* E;  // T x C error of the gated output
+    float* dl;       // K x T
+    int T, C, K;
+    uint32_t draw0, token0, layer;
+    float sigma;
+};
+
+// One warp per token; each lane owns channel blocks lane, lane + 32, ... and
+// the warp sums its lanes by shuffles, draw after draw.
+__global__ void __launch_bounds__(256) attn_gate_dl_kernel(const GateArgs a, const PhiloxKeys keys) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= a.T) return;
+    const int nblk = a.C / 4;
+    const int64_t row = static_cast<int64_t>(t) * a.C;
+    const uint32_t token = a.token0 + static_cast<uint32_t>(t);
+    for (int i = 0; i < a.K; ++i) {
+        const DrawHalf dh = philox_draw_half(a.draw0 + static_cast<uint32_t>(i), token, keys);
+        float part = 0.f;
+        for (int j = lane; j < nblk; j += 32) {
+            const float4 n = words_to_normals(philox_rest(dh, philox_block_half(j, a.layer, keys), keys));
+            const float4 z = __ldg(reinterpret_cast<const float4*>(a.z + row) + j);
+            const float4 o = __ldg(reinterpret_cast<const float4*>(a.o + row) + j);
+            const float4 e = __ldg(reinterpret_cast<const float4*>(a.E + row) + j);
+            const float zz[4] = {z.x, z.y, z.z, z.w}, oo[4] = {o.x, o.y, o.z, o.w};
+            const float ee[4] = {e.x, e.y, e.z, e.w}, nn[4] = {n.x, n.y, n.z, n.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float d = a.sigma * nn[k];
+                const float s1 = 1.0f / (1.0f + expf(-(zz[k] + d)));
+                const float s0c = 1.0f / (1.0f + expf(zz[k]));  // 1 - sig(z)
+                part = fmaf(ee[k] * oo[k], s1 * s0c * -expm1f(-d), part);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, off);
+        if (lane == 0) a.dl[static_cast<int64_t>(i) * a.T + t] = part;
+    }
+}
+
+struct GatePlan {
+    int64_t ldx;
+    size_t off_dl, off_m, off_r, off_gbf, off_xbf, bytes;
+};
+
+GatePlan gate_plan(int64_t T, int64_t C, int64_t d_in, uint32_t K) {
+    GatePlan P{};
+    P.ldx = round_up(d_in, 8);
+    WsLayout w;
+    w.take(kCtlBytes);
+    P.off_dl = w.take(static_cast<size_t>(K) * T * 4);
+    P.off_m = w.take(static_cast<size_t>(T) * 4);
+    P.off_r = w.take(static_cast<size_t>(K) * T * 4);
+    P.off_gbf = w.take(static_cast<size_t>(T * C) * 2);
+    P.off_xbf = w.take(static_cast<size_t>(T * P.ldx) * 2);
+    P.bytes = w.used;
+    return P;
+}
+
+}  // namespace
+}  // namespace dust
+
+extern "C" size_t dust_attn_gate_workspace(int64_t T, int64_t seq_len, int64_t C, int64_t d_in,
+                                           uint32_t K) {
+    if (T < 1 || seq_len < 1 || T % seq_len != 0 || C < 8 || C % 8 != 0 || d_in < 1 || K < 2)
+        return 0;
+    return gate_plan(T, C, d_in, K).bytes;
+}
+
+extern "C" dust_status dust_attn_gate_estimate(const float* z, const float* o, const float* E,
+                                               const void* x, dust_dtype x_dtype, int64_t T,
+                                               int64_t seq_len, int64_t C, int64_t d_in,
+                                               dust_noise nz, float* g_hat, float* G_W, void* ws,
+                                               size_t ws_bytes, void* stream) {
+    if (!z || !o || !E || !x || !G_W) return DUST_ERR_INVALID_ARG;
+    if (T < 1 || seq_len < 1 || T % seq_len != 0 || C < 1 || d_in < 1) return DUST_ERR_INVALID_ARG;
+    if (x_dtype != DUST_F32 && x_dtype != DUST_BF16) return DUST_ERR_INVALID_ARG;
+    if (nz.num_draws < 2 || !(nz.sigma > 0.0f) || !(nz.sigma < INFINITY)) return DUST_ERR_INVALID_ARG;
+    if (!(nz.gamma >= 0.0f && nz.gamma <= 1.0f)) return DUST_ERR_INVALID_ARG;
+    if (C % 8 != 0 || T > (1LL << 28) || C > (1LL << 16) || d_in > (1LL << 20) ||
+        nz.num_draws > (1u << 24))
+        return DUST_ERR_UNSUPPORTED;
+    if (static_cast<uint64_t>(nz.token0) + static_cast<uint64_t>(T) > (1ULL << 32) ||
+        static_cast<uint64_t>(nz.draw0) + nz.num_draws > (1ULL << 32))
+        return DUST_ERR_INVALID_ARG;
+    if (!aligned(z, 16) || !aligned(o, 16) || !aligned(E, 16) || (g_hat && !aligned(g_hat, 16)))
+        return DUST_ERR_INVALID_ARG;
+    const GatePlan Pl = gate_plan(T, C, d_in, nz.num_draws);
+    if (!ws || ws_bytes < Pl.bytes || !aligned(ws, 256)) return DUST_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    uint32_t* status = static_cast<uint32_t*>(ws);
+    DUST_CUDA_TRY(cudaMemsetAsync(ws, 0, kCtlBytes, s));
+    float* dl = reinterpret_cast<float*>(w + Pl.off_dl);
+    float* mean = reinterpret_cast<float*>(w + Pl.off_m);
+    float* r = reinterpret_cast<float*>(w + Pl.off_r);
+    __nv_bfloat16* gbf = reinterpret_cast<__nv_bfloat16*>(w + Pl.off_gbf);
+    const PhiloxKeys keys = philox_round_keys(nz.seed);
+
+    GateArgs ga{z, o, E, dl, static_cast<int>(T), static_cast<int>(C),
+                static_cast<int>(nz.num_draws), nz.draw0, nz.token0, nz.layer, nz.sigma};
+    timer_begin(s);
+    attn_gate_dl_kernel<<<static_cast<unsigned>(ceil_div(T, 8)), 256, 0, s>>>(ga, keys);
+    timer_end(s);
+    dust_status st = launch_status();
+    if (st != DUST_OK) return st;
+    st = credit_and_ghat_launch(dl, mean, r, static_cast<int>(T), static_cast<int>(seq_len),
+                                static_cast<int>(C), nz, keys, g_hat, gbf, s);
+    if (st != DUST_OK) return st;
+    const void* xb = x;
+    int64_t ldx = d_in;
+    if (x_dtype == DUST_F32 || (d_in % 8) != 0 || !aligned(x, 16)) {
+        void* xbf = w + Pl.off_xbf;
+        st = x_dtype == DUST_F32
+                 ? f32_to_bf16_launch(static_cast<const float*>(x), T, d_in, d_in, xbf, Pl.ldx, s)
+                 : bf16_pad_launch(x, T, d_in, d_in, xbf, Pl.ldx, s);
+        if (st != DUST_OK) return st;
+        xb = xbf;
+        ldx = Pl.ldx;
+    }
+    return gemm_bf16_launch(gbf, true, C, xb, true, ldx, C, d_in, T, 0, 1, G_W, d_in, status, s);
+}

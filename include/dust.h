@@ -308,6 +308,27 @@ dust_status dust_attn_value_estimate(const float* P, const float* E, const void*
                                      int64_t dv, int64_t d_in, dust_noise nz, float* g_hat,
                                      float* G_W, void* ws, size_t ws_bytes, void* stream);
 
+/* Workspace bytes for dust_attn_gate_estimate with these sizes (0 if invalid). */
+size_t dust_attn_gate_workspace(int64_t T, int64_t seq_len, int64_t C, int64_t d_in, uint32_t K);
+
+/*
+ * Estimator for the gate projection z = W_g x of a gated attention output
+ * o~ = sig(z) * o (per channel, sig the logistic function), perturbed per
+ * token and scored like the values by the error E of the gated output
+ * (Dust translation §2.3):
+ *   d(o~)_s = (sig(z_s + sigma a_s) - sig(z_s)) * o_s,   dl_s = <E_s, d(o~)_s>,
+ * then the same centring, gamma-scan, g and G_W = g^T x as the values.
+ *   z, o, E  device fp32, T x C (16-byte aligned): gate pre-activations, the
+ *            attention output before the gate, the error of the gated output.
+ *   x        device, T x d_in (x_dtype): the input of W_g.
+ *   g_hat    T x C fp32 or NULL; G_W C x d_in fp32.
+ * Limits: C a multiple of 8, T a multiple of seq_len, K >= 2.
+ */
+dust_status dust_attn_gate_estimate(const float* z, const float* o, const float* E,
+                                    const void* x, dust_dtype x_dtype, int64_t T, int64_t seq_len,
+                                    int64_t C, int64_t d_in, dust_noise nz, float* g_hat,
+                                    float* G_W, void* ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Using the estimate: optimiser step and the backprop reference             */
 /* ------------------------------------------------------------------------ */

@@ -1,4 +1,5 @@
-"""fp64 oracle of the value-projection estimator inside attention.
+"""fp64 oracle of the estimators inside attention: the value projection and
+the gate of the attention output.
 
 TEST INFRASTRUCTURE ONLY, like the rest of oracle/.
 
@@ -50,3 +51,31 @@ def attn_value_estimate(P, E, x, seq_len, sigma, gamma, K, seed, layer, draw0=0,
     C = np.asarray(E).shape[1]
     g = ghat(r, C, sigma, seed, layer, draw0, token0)
     return {"dl": dl, "c": c, "r": r, "g": g, "G": outer(g, np.asarray(x, np.float64))}
+
+
+def attn_gate_delta_loss(z, o, E, sigma, K, seed, layer, draw0=0, token0=0):
+    """K x T: dl_{i,s} = sum_c E (sig(z + sigma a) - sig(z)) o, the gated
+    output's first-order loss change (sig the logistic function)."""
+    from . import noise
+    z = np.asarray(z, np.float64)
+    o = np.asarray(o, np.float64)
+    E = np.asarray(E, np.float64)
+    T, C = z.shape
+    sig = lambda u: 1.0 / (1.0 + np.exp(-u))
+    dl = np.empty((K, T), np.float64)
+    for i in range(K):
+        a = noise(seed, layer, draw0 + i, token0, T, C)
+        dl[i] = (E * (sig(z + sigma * a) - sig(z)) * o).sum(axis=1)
+    return dl
+
+
+def attn_gate_estimate(z, o, E, x, seq_len, sigma, gamma, K, seed, layer, draw0=0, token0=0):
+    """dict(dl, c, r, g, G) of the gate estimator (the gated output sig(z) * o,
+    scored by the error of the gated output)."""
+    from . import center, ghat, outer, reward
+    dl = attn_gate_delta_loss(z, o, E, sigma, K, seed, layer, draw0, token0)
+    c = center(dl)
+    r = reward(c, gamma, seq_len)
+    g = ghat(r, np.asarray(z).shape[1], sigma, seed, layer, draw0, token0)
+    return {"dl": dl, "c": c, "r": r, "g": g, "G": outer(g, np.asarray(x, np.float64))}
+

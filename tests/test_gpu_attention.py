@@ -76,3 +76,39 @@ def test_attn_value_rejects_unsupported_shapes(dust):
     with pytest.raises(dust.DustError):  # seq_len not a multiple of 128
         dust.attn_value_estimate(P, torch.zeros((128, 64), device="cuda"),
                                  torch.zeros((128, 8), device="cuda"), 64, 0.02, 0.9, 4, 1)
+
+
+@pytest.mark.parametrize("T,L,C,d_in,K,gamma", [(256, 128, 64, 16, 8, 0.95),
+                                                (300, 100, 520, 24, 5, 0.0),
+                                                (2048, 1024, 512, 64, 12, 0.99)])
+def test_attn_gate_matches_oracle(dust, orc, T, L, C, d_in, K, gamma):
+    gen = torch.Generator().manual_seed(T + C)
+    z, o, E = (torch.randn((T, C), generator=gen) for _ in range(3))
+    x = torch.randn((T, d_in), generator=gen)
+    g, G, ws = dust.attn_gate_estimate(z.cuda(), o.cuda(), E.cuda(), x.cuda(), L, 0.05, gamma, K,
+                                       1234, layer=3, draw0=2, token0=9)
+    torch.cuda.synchronize()
+    assert dust.workspace_status(ws) == 0
+    ref = orc.attn_gate_estimate(z.numpy(), o.numpy(), E.numpy(), x.numpy(), L, 0.05, gamma, K,
+                                 1234, 3, 2, 9)
+    eg, eG = rel_l2(g.cpu().numpy(), ref["g"]), rel_l2(G.cpu().numpy(), ref["G"])
+    assert eg <= G_TOL and eG <= GW_TOL, (eg, eG)
+    parity(g=eg, G_W=eG)
+
+
+def test_value_embedding_gradient_is_the_value_estimate_scattered(dust, orc):
+    """Value embeddings add to the values (v_t = W_v x_t + ve[id_t]), so their
+    estimated gradient is the value estimate g scattered into the table by
+    token id: the library's two entry points chained, against the oracle's."""
+    P, E, x = _case(2, 2, 128, 16, seed=77)
+    ids = torch.randint(0, 50, (256,), generator=torch.Generator().manual_seed(1),
+                        dtype=torch.int32)
+    g, _, _ = dust.attn_value_estimate(P.cuda(), E.cuda(), x.cuda(), 128, 0.02, 0.99, 6, 1234)
+    GE, _, ws = dust.embed_scatter(g, ids.cuda(), 50)
+    torch.cuda.synchronize()
+    assert dust.workspace_status(ws) == 0
+    ref = orc.attn_value_estimate(P.numpy(), E.numpy(), x.numpy(), 128, 0.02, 0.99, 6, 1234, 2)
+    _, ref_GE = orc.embed_scatter(ref["g"], ids.numpy(), 50)
+    e = rel_l2(GE.cpu().numpy(), ref_GE)
+    assert e <= G_TOL, e
+    parity(G_ve=e)

@@ -65,3 +65,45 @@ def test_large_population_approaches_backprop_through_the_values():
     g = oracle.attn_value_estimate(P, E, x, L, 0.1, 1.0, 20000, 11, 2)["g"]
     cos = (g * want).sum() / np.linalg.norm(g) / np.linalg.norm(want)
     assert cos > 0.99, cos
+
+
+def _gate_case(T=8, C=12, d_in=3, seed=0):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((T, C)), rng.standard_normal((T, C)),
+            rng.standard_normal((T, C)), rng.standard_normal((T, d_in)))
+
+
+def test_gate_small_sigma_limit_is_the_projection_onto_the_noise():
+    # sig(z + d) - sig(z) = sig(z)(1 - sig(z)) d + O(d^2): with gamma = 0, g_s
+    # -> (1/K) sum_i (<w_s, a_i> - mean) a_i, w = E sig(z)(1 - sig(z)) o.
+    z, o, E, x = _gate_case()
+    T, C = z.shape
+    K, sigma = 9, 1e-5
+    sg = 1.0 / (1.0 + np.exp(-z))
+    wgt = E * sg * (1.0 - sg) * o
+    a = np.stack([oracle.noise(8, 3, i, 0, T, C) for i in range(K)])
+    proj = (a * wgt[None]).sum(-1)
+    proj -= proj.mean(0, keepdims=True)
+    want = (proj[..., None] * a).sum(0) / K
+    got = oracle.attn_gate_estimate(z, o, E, x, T, sigma, 0.0, K, 8, 3)["g"]
+    assert np.linalg.norm(got - want) / np.linalg.norm(want) < 1e-4
+
+
+def test_gate_with_zero_output_estimates_nothing():
+    z, o, E, x = _gate_case(seed=1)
+    got = oracle.attn_gate_estimate(z, np.zeros_like(o), E, x, 8, 0.1, 0.9, 5, 8, 3)
+    assert np.all(got["dl"] == 0.0) and np.all(got["g"] == 0.0)
+
+
+def test_gate_change_is_the_difference_of_gated_outputs():
+    # dl equals <E, sig(z + sigma a) o - sig(z) o> computed as two full gated
+    # outputs (no shared intermediate).
+    z, o, E, x = _gate_case(T=4, C=8, seed=2)
+    sigma = 0.7
+    dl = oracle.attn_gate_delta_loss(z, o, E, sigma, 2, 31, 3)
+    for i in range(2):
+        a = oracle.noise(31, 3, i, 0, 4, 8)
+        out1 = o / (1.0 + np.exp(-(z + sigma * a)))
+        out0 = o / (1.0 + np.exp(-z))
+        np.testing.assert_allclose(dl[i], (E * out1).sum(1) - (E * out0).sum(1), rtol=1e-10,
+                                   atol=1e-13)
