@@ -85,21 +85,19 @@ struct NoiseArgs {
     __nv_bfloat16* N2;  // rows ((sq H + h) 4 + d) 64 + ch, 2L columns [hi | lo]
 };
 
-// The group's value noise: thread per (sequence, head, draw, channel block of
-// four, key), keys fastest so that each row's stores are contiguous across a
-// warp.  Draws past the group's count get zeros.
-__global__ void attn_noise_kernel(const NoiseArgs a, const PhiloxKeys keys) {
-    const int64_t total = static_cast<int64_t>(a.nseq) * a.H * kGroup * (kDv / 4) * a.L;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int t = static_cast<int>(i % a.L);
-        int64_t rest = i / a.L;
-        const int jb = static_cast<int>(rest % (kDv / 4));
-        rest /= kDv / 4;
-        const int d = static_cast<int>(rest % kGroup);
-        rest /= kGroup;
-        const int h = static_cast<int>(rest % a.H);
-        const int sq = static_cast<int>(rest / a.H);
+// The group's value noise: grid.y = (sequence, head, draw), threads over
+// (channel block of four, key) with keys fastest, so that each row's stores
+// are contiguous across a warp.  Draws past the group's count get zeros.
+__global__ void __launch_bounds__(256) attn_noise_kernel(const NoiseArgs a, const PhiloxKeys keys) {
+    const int y = blockIdx.y;  // (sq H + h) kGroup + d
+    const int d = y % kGroup;
+    const int sh = y / kGroup;
+    const int h = sh % a.H;
+    const int sq = sh / a.H;
+    const int per = (kDv / 4) * a.L;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < per; i += gridDim.x * blockDim.x) {
+        const int jb = i / a.L;
+        const int t = i - jb * a.L;
         float4 n = make_float4(0.f, 0.f, 0.f, 0.f);
         if (d < a.nd) {
             const uint32_t j = static_cast<uint32_t>(h * (kDv / 4) + jb);
@@ -107,7 +105,7 @@ __global__ void attn_noise_kernel(const NoiseArgs a, const PhiloxKeys keys) {
             n = words_to_normals(philox4x32_10(j, token, a.draw_first + d, a.layer, keys));
         }
         const float v[4] = {n.x, n.y, n.z, n.w};
-        const int64_t row0 = ((static_cast<int64_t>(sq) * a.H + h) * kGroup + d) * kDv + jb * 4;
+        const int64_t row0 = static_cast<int64_t>(y) * kDv + jb * 4;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             __nv_bfloat16* out = a.N2 + (row0 + k) * (2 * static_cast<int64_t>(a.L));
@@ -318,7 +316,8 @@ extern "C" dust_status dust_attn_value_estimate(const float* P, const float* E, 
     if (x_dtype != DUST_F32 && x_dtype != DUST_BF16) return DUST_ERR_INVALID_ARG;
     if (nz.num_draws < 2 || !(nz.sigma > 0.0f) || !(nz.sigma < INFINITY)) return DUST_ERR_INVALID_ARG;
     if (!(nz.gamma >= 0.0f && nz.gamma <= 1.0f)) return DUST_ERR_INVALID_ARG;
-    if (dv != kDv || seq_len % kQM != 0 || seq_len > 8192 || H > 64 || T > (1LL << 26) ||
+    if (dv != kDv || seq_len % kQM != 0 || seq_len > 8192 || H > 64 || T / seq_len * H > 16383 ||
+        T > (1LL << 26) ||
         d_in > (1LL << 20) || nz.num_draws > (1u << 20))
         return DUST_ERR_UNSUPPORTED;
     if (static_cast<uint64_t>(nz.token0) + static_cast<uint64_t>(T) > (1ULL << 32) ||
@@ -366,8 +365,9 @@ extern "C" dust_status dust_attn_value_estimate(const float* P, const float* E, 
         const int nd = K - i0 < kGroup ? K - i0 : kGroup;
         NoiseArgs na{static_cast<int>(nseq), Hi, L, nd, nz.draw0 + static_cast<uint32_t>(i0),
                      nz.token0, nz.layer, N2};
-        attn_noise_kernel<<<blocks_for(nseq * H * kGroup * (kDv / 4) * seq_len, 256), 256, 0, s>>>(
-            na, keys);
+        const dim3 ng(static_cast<unsigned>(ceil_div((kDv / 4) * seq_len, 256)),
+                      static_cast<unsigned>(nseq * H * kGroup));
+        attn_noise_kernel<<<ng, 256, 0, s>>>(na, keys);
         if ((st = launch_status()) != DUST_OK) return st;
         AttnArgs aa{E, dlh, Ti, L, Hi, nd, i0, nz.sigma, status};
         timer_begin(s);

@@ -253,17 +253,43 @@ __global__ void draw_mean_kernel(const float* __restrict__ dl, int K, int T, flo
 }
 
 // r_{i,t} = c_{i,t} + gamma r_{i,t+1} inside each sequence, c = -(dl - m).
+// r_t = sum_{s >= t, same sequence} gamma^(s-t) c_s with c = -(dl - m), one
+// warp per (draw, sequence): lane l owns a contiguous chunk of the sequence,
+// runs it once from zero (its chunk's value at the chunk start, A_l, and
+// gamma^len, P_l), the warp combines the chunks from the end by a shuffle
+// scan of (A, P) pairs, and each lane reruns its chunk from its true carry.
 __global__ void reward_scan_kernel(const float* __restrict__ dl, const float* __restrict__ m,
                                    int K, int T, int seq_len, float gamma, float* __restrict__ r) {
     const int nseq = T / seq_len;
-    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= K * nseq) return;
-    const int i = idx / nseq, s = idx - i * nseq;
+    const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (wid >= K * nseq) return;
+    const int i = wid / nseq, s = wid - i * nseq;
     const int64_t rowoff = static_cast<int64_t>(i) * T;
-    float acc = 0.f;
-    for (int t = (s + 1) * seq_len - 1; t >= s * seq_len; --t) {
-        const float c = -(dl[rowoff + t] - m[t]);
-        acc = fmaf(gamma, acc, c);
+    const int chunk = (seq_len + 31) / 32;
+    const int t0 = s * seq_len + min(seq_len, lane * chunk);
+    const int t1 = s * seq_len + min(seq_len, (lane + 1) * chunk);
+    float A = 0.f, P = 1.f;
+    for (int t = t1 - 1; t >= t0; --t) {
+        A = fmaf(gamma, A, -(dl[rowoff + t] - m[t]));
+        P *= gamma;
+    }
+    // Suffix combine over lanes: (A, P)_l <- (A_l + P_l A_{l+1}, P_l P_{l+1}),
+    // doubling the reach each step; afterwards A_l is r at the chunk's start.
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float An = __shfl_down_sync(0xFFFFFFFFu, A, o);
+        const float Pn = __shfl_down_sync(0xFFFFFFFFu, P, o);
+        if (lane + o < 32) {
+            A = fmaf(P, An, A);
+            P *= Pn;
+        }
+    }
+    // carry into this chunk's last token: r at the next chunk's start
+    float acc = __shfl_down_sync(0xFFFFFFFFu, A, 1);
+    if (lane == 31) acc = 0.f;
+    for (int t = t1 - 1; t >= t0; --t) {
+        acc = fmaf(gamma, acc, -(dl[rowoff + t] - m[t]));
         r[rowoff + t] = acc;
     }
 }
@@ -381,7 +407,7 @@ dust_status credit_and_ghat_launch(const float* dl, float* mean, float* r, int T
     const int K = static_cast<int>(nz.num_draws);
     const int nseq = T / seq_len;
     draw_mean_kernel<<<static_cast<unsigned>(ceil_div(T, 256)), 256, 0, s>>>(dl, K, T, mean);
-    reward_scan_kernel<<<static_cast<unsigned>(ceil_div(static_cast<int64_t>(K) * nseq, 128)), 128,
+    reward_scan_kernel<<<static_cast<unsigned>(ceil_div(static_cast<int64_t>(K) * nseq, 4)), 128,
                          0, s>>>(dl, mean, K, T, seq_len, nz.gamma, r);
     dust_status st = launch_status();
     if (st != DUST_OK) return st;

@@ -402,7 +402,7 @@ def run_optim(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "optim_adam", "params": n, "l2": "inputs larger than L2 (no flush)"},
         "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                     "frac": ach / peaks["hbm_gbs"], "traffic": load_traffic({"name": "optim_adam"}),
                      "kernel": "optim_kernel<Adam>", "kernel_ms": ms,
                      "peak_source": "hbm_gbs (%s)" % which},
         "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps,
@@ -474,7 +474,8 @@ def run_attn_value(args):
                    "l2": "inputs larger than L2 (no flush)"},
         "roofline": {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"],
                      "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops_sustained"],
-                     "traffic": None, "kernel": "attn_v_kernel", "kernel_ms": kernel_ms,
+                     "traffic": load_traffic({"name": "attn_value"}), "kernel": "attn_v_kernel",
+                     "kernel_ms": kernel_ms,
                      "peak_source": "bf16_tflops_sustained (%s)" % which},
         "cpu_baseline": None, "e2e": None, "gpu_launches": args.steps * (2 * (K // 4) + 6),
         "clocks": clocks.summary()}), flush=True)
