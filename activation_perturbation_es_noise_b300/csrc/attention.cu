@@ -18,8 +18,10 @@
 // Per group of four draws the noise of every (sequence, head) is written
 // once as split bf16 [hi | lo] (keys along the row), and one tcgen05 kernel
 // computes, for 128 queries x (4 draws x 64 channels), P A over the causal key
-// range with P = [P_hi | P_lo] and A = [A_hi | A_lo] from TMA in three passes
-// (hi.hi, hi.lo, lo.hi: the dropped lo.lo term is below 2^-16 relative), and
+// range with P = [P_hi | P_lo] and A = [A_hi | A_lo] from TMA, every key
+// slice bringing all four halves so that the three products hi.hi, hi.lo and
+// lo.hi are issued back to back (the dropped lo.lo term is below 2^-16
+// relative) and each byte is read once per tile, and
 // reduces the accumulator rows against E in its epilogue, so dO never leaves
 // the chip.  The credit and the error estimate reuse the interior layer's
 // kernels.
@@ -41,10 +43,11 @@ constexpr int kGroup = 4;         // draws per kernel launch (N = 4 x 64)
 constexpr int kQM = 128;          // queries per tile
 constexpr int kKB = 64;           // keys per stage
 constexpr int kNB = kGroup * kDv; // 256
-constexpr int kStages = 4;
+constexpr int kStages = 2;
 constexpr uint32_t kABytes = kQM * kKB * 2;   // 16 KB
 constexpr uint32_t kBBytes = kNB * kKB * 2;   // 32 KB
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
+// one stage = a 64-key slice of P_hi, P_lo, A_hi and A_lo
+constexpr uint32_t kStageBytes = 2 * kABytes + 2 * kBBytes;
 constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 + 256;
 
 __device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 a, __nv_bfloat16 b) {
@@ -125,8 +128,8 @@ struct AttnArgs {
 };
 
 // One CTA: query tile qb of sequence sq, head h (grid.x = tiles, heaviest
-// first; grid.y = sq H + h).  Warp 0 streams [P_hi | P_lo] and [A_hi | A_lo]
-// slices by TMA, warp 1 issues the MMAs of the three passes into one
+// first; grid.y = sq H + h).  Warp 0 streams the four halves of each 64-key
+// slice by TMA, warp 1 issues the three split products of each slice into one
 // 256-column accumulator, warps 2..5 reduce each query row against E.
 __global__ void __launch_bounds__(192, 1)
     attn_v_kernel(const __grid_constant__ CUtensorMap tp, const __grid_constant__ CUtensorMap tn,
@@ -150,8 +153,7 @@ __global__ void __launch_bounds__(192, 1)
     const int sh = blockIdx.y;  // sq H + h
     const int h = sh % a.H;
     const int sq = sh / a.H;
-    const int nslices = 2 * (qb + 1);  // 64-key slices up to the tile's last query
-    const int nit = 3 * nslices;
+    const int nit = 2 * (qb + 1);  // 64-key slices up to the tile's last query
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -177,12 +179,14 @@ __global__ void __launch_bounds__(192, 1)
                 const int s = it % kStages;
                 const uint32_t ph = (it / kStages) & 1u;
                 if (it >= kStages && !mbar_wait(empty_bar(s), ph ^ 1u, a.status)) break;
-                const int pass = it / nslices;  // 0: hi.hi, 1: hi.lo, 2: lo.hi
-                const int key0 = (it - pass * nslices) * kKB;
+                const int key0 = it * kKB;
                 mbar_arrive_expect_tx(full_bar(s), kStageBytes);
-                const uint32_t a_dst = base + s * kStageBytes;
-                tma_load_2d(a_dst, &tp, (pass == 2 ? a.L : 0) + key0, prow, full_bar(s));
-                tma_load_2d(a_dst + kABytes, &tn, (pass == 1 ? a.L : 0) + key0, nrow, full_bar(s));
+                const uint32_t dst = base + s * kStageBytes;
+                tma_load_2d(dst, &tp, key0, prow, full_bar(s));                    // P_hi
+                tma_load_2d(dst + kABytes, &tp, a.L + key0, prow, full_bar(s));    // P_lo
+                tma_load_2d(dst + 2 * kABytes, &tn, key0, nrow, full_bar(s));      // A_hi
+                tma_load_2d(dst + 2 * kABytes + kBBytes, &tn, a.L + key0, nrow,    // A_lo
+                            full_bar(s));
             }
         }
     } else if (warp == 1) {
@@ -197,13 +201,18 @@ __global__ void __launch_bounds__(192, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sa = base + s * kStageBytes;
-                const uint32_t sb = sa + kABytes;
+                const uint32_t pa = base + s * kStageBytes;  // P_hi, then P_lo
+                const uint32_t na = pa + 2 * kABytes;        // A_hi, then A_lo
 #pragma unroll
-                for (int kk = 0; kk < kKB / 16; ++kk)
-                    umma_bf16(tmem, sdesc_sw128(sa + kk * 32u, 16u, 1024u),
-                              sdesc_sw128(sb + kk * 32u, 16u, 1024u), idesc,
-                              (it | kk) != 0 ? 1u : 0u);
+                for (int kk = 0; kk < kKB / 16; ++kk) {
+                    const uint64_t ph_d = sdesc_sw128(pa + kk * 32u, 16u, 1024u);
+                    const uint64_t pl_d = sdesc_sw128(pa + kABytes + kk * 32u, 16u, 1024u);
+                    const uint64_t nh_d = sdesc_sw128(na + kk * 32u, 16u, 1024u);
+                    const uint64_t nl_d = sdesc_sw128(na + kBBytes + kk * 32u, 16u, 1024u);
+                    umma_bf16(tmem, ph_d, nh_d, idesc, (it | kk) != 0 ? 1u : 0u);
+                    umma_bf16(tmem, ph_d, nl_d, idesc, 1u);
+                    umma_bf16(tmem, pl_d, nh_d, idesc, 1u);
+                }
                 umma_commit(empty_bar(s));
             }
             (void)ok;
