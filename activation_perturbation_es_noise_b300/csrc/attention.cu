@@ -89,32 +89,39 @@ struct NoiseArgs {
 };
 
 // The group's value noise: grid.y = (sequence, head, draw), threads over
-// (channel block of four, key) with keys fastest, so that each row's stores
-// are contiguous across a warp.  Draws past the group's count get zeros.
+// (channel block of four, pair of keys) with keys fastest, so that each row's
+// stores are contiguous across a warp and two keys' values go out as one
+// 4-byte bf16 pair.  Draws past the group's count get zeros.
 __global__ void __launch_bounds__(256) attn_noise_kernel(const NoiseArgs a, const PhiloxKeys keys) {
     const int y = blockIdx.y;  // (sq H + h) kGroup + d
     const int d = y % kGroup;
     const int sh = y / kGroup;
     const int h = sh % a.H;
     const int sq = sh / a.H;
-    const int per = (kDv / 4) * a.L;
+    const int half_l = a.L / 2;
+    const int per = (kDv / 4) * half_l;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < per; i += gridDim.x * blockDim.x) {
-        const int jb = i / a.L;
-        const int t = i - jb * a.L;
-        float4 n = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int jb = i / half_l;
+        const int t = 2 * (i - jb * half_l);
+        float4 n0 = make_float4(0.f, 0.f, 0.f, 0.f), n1 = n0;
         if (d < a.nd) {
             const uint32_t j = static_cast<uint32_t>(h * (kDv / 4) + jb);
             const uint32_t token = a.token0 + static_cast<uint32_t>(sq * a.L + t);
-            n = words_to_normals(philox4x32_10(j, token, a.draw_first + d, a.layer, keys));
+            const BlockHalf bh = philox_block_half(j, a.layer, keys);
+            const uint32_t draw = a.draw_first + d;
+            n0 = words_to_normals(philox_rest(philox_draw_half(draw, token, keys), bh, keys));
+            n1 = words_to_normals(philox_rest(philox_draw_half(draw, token + 1, keys), bh, keys));
         }
-        const float v[4] = {n.x, n.y, n.z, n.w};
+        const float v0[4] = {n0.x, n0.y, n0.z, n0.w}, v1[4] = {n1.x, n1.y, n1.z, n1.w};
         const int64_t row0 = static_cast<int64_t>(y) * kDv + jb * 4;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             __nv_bfloat16* out = a.N2 + (row0 + k) * (2 * static_cast<int64_t>(a.L));
-            const __nv_bfloat16 hi = __float2bfloat16_rn(v[k]);
-            out[t] = hi;
-            out[a.L + t] = __float2bfloat16_rn(v[k] - __bfloat162float(hi));
+            const __nv_bfloat16 h0 = __float2bfloat16_rn(v0[k]), h1 = __float2bfloat16_rn(v1[k]);
+            *reinterpret_cast<uint32_t*>(out + t) = pack_bf16x2(h0, h1);
+            *reinterpret_cast<uint32_t*>(out + a.L + t) =
+                pack_bf16x2(__float2bfloat16_rn(v0[k] - __bfloat162float(h0)),
+                            __float2bfloat16_rn(v1[k] - __bfloat162float(h1)));
         }
     }
 }
@@ -374,7 +381,7 @@ extern "C" dust_status dust_attn_value_estimate(const float* P, const float* E, 
         const int nd = K - i0 < kGroup ? K - i0 : kGroup;
         NoiseArgs na{static_cast<int>(nseq), Hi, L, nd, nz.draw0 + static_cast<uint32_t>(i0),
                      nz.token0, nz.layer, N2};
-        const dim3 ng(static_cast<unsigned>(ceil_div((kDv / 4) * seq_len, 256)),
+        const dim3 ng(static_cast<unsigned>(ceil_div((kDv / 4) * seq_len / 2, 256)),
                       static_cast<unsigned>(nseq * H * kGroup));
         attn_noise_kernel<<<ng, 256, 0, s>>>(na, keys);
         if ((st = launch_status()) != DUST_OK) return st;
