@@ -30,7 +30,7 @@ EXPORTS = ("dust_status_string", "dust_abi_version", "dust_workspace_status",
            "dust_kernel_event_count", "dust_wait_selftest", "dust_sgd_step", "dust_adam_step",
            "dust_head_backprop_workspace", "dust_head_backprop", "dust_head_estimate_baseline",
            "dust_attn_value_workspace", "dust_attn_value_estimate", "dust_attn_gate_workspace",
-           "dust_attn_gate_estimate")
+           "dust_attn_gate_estimate", "dust_issue_probe")
 BASELINE_MEAN, BASELINE_LEAVE_ONE_OUT, BASELINE_ANTITHETIC = 0, 1, 2
 
 
@@ -99,6 +99,7 @@ def lib():
         L.dust_attn_gate_workspace.restype = _SZ
         L.dust_attn_gate_estimate.argtypes = [_P, _P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _I64,
                                               DustNoise, _P, _P, _P, _SZ, _P]
+        L.dust_issue_probe.argtypes = [ctypes.c_int, _I64, ctypes.POINTER(_I64), _P, _P]
         L.dust_head_backprop_workspace.argtypes = [_I64, _I64, _I64]
         L.dust_head_backprop_workspace.restype = _SZ
         L.dust_head_backprop.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _P, _P, _P,
@@ -108,7 +109,7 @@ def lib():
                      "dust_embed_scatter_static", "dust_philox_fill", "dust_gemm_bf16",
                      "dust_sgd_step", "dust_adam_step", "dust_head_backprop",
                      "dust_head_estimate_baseline", "dust_attn_value_estimate",
-                     "dust_attn_gate_estimate"):
+                     "dust_attn_gate_estimate", "dust_issue_probe"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -419,3 +420,25 @@ def attn_gate_estimate(z, o, E, x, seq_len, sigma, gamma, K, seed, layer=3, draw
                                          d_in, noise(seed, sigma, K, layer, draw0, token0, gamma),
                                          _ptr(g), _ptr(G), _ptr(ws), ws.numel(), _stream(stream)))
     return g, G, ws
+
+
+# ---------------------------------------------------------------- probes ----
+PROBE_OPS_PER_ROUND = {0: 16, 1: 8, 2: 8, 3: 16, 4: 16}  # per thread and round
+
+
+def issue_probe(kind, iters, stream=None):
+    """Operations per second of one probe kind (0: Philox multiply/xor,
+    1: ex2, 2: fp32 fma), timed with events on the stream: (ops/s, ms)."""
+    sink = torch.zeros(256, dtype=torch.int32, device="cuda")
+    n = _I64(0)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    _check("dust_issue_probe", lib().dust_issue_probe(kind, iters, ctypes.byref(n), _ptr(sink),
+                                                      ctypes.c_void_p(s.cuda_stream)))
+    e1.record(s)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1)
+    return n.value * iters * PROBE_OPS_PER_ROUND[kind] / (ms * 1e-3), ms
+

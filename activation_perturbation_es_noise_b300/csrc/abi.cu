@@ -48,6 +48,80 @@ __global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
     __syncthreads();
 }
 
+// Issue-rate probe: every thread runs `iters` rounds over eight independent
+// chains of one operation kind, so that throughput, not latency, bounds it.
+//   kind 0: the Philox step, a 32 x 32 -> 64-bit multiply and an xor of its
+//           halves (2 operations per chain and round);
+//   kind 1: ex2.approx (1 XU operation per chain and round);
+//   kind 2: fp32 fma (1 operation per chain and round).
+// The chains' results go to `sink` so that nothing is optimised away.
+__global__ void __launch_bounds__(256) issue_probe_kernel(int kind, int64_t iters,
+                                                          uint32_t* sink) {
+    const uint32_t tid = blockIdx.x * blockDim.x + threadIdx.x;
+    uint32_t acc = 0;
+    if (kind == 0) {
+        uint32_t x[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) x[c] = tid * 2654435761u + c;
+        for (int64_t i = 0; i < iters; ++i) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint64_t pr = static_cast<uint64_t>(x[c]) * 0xD2511F53u;
+                x[c] = static_cast<uint32_t>(pr >> 32) ^ static_cast<uint32_t>(pr);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc ^= x[c];
+    } else if (kind == 3 || kind == 4) {
+        // the same step with the product's halves as two 32-bit multiplies,
+        // written as PTX (3) or as C (4)
+        uint32_t x[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) x[c] = tid * 2654435761u + c;
+        for (int64_t i = 0; i < iters; ++i) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint32_t lo, hi;
+                if (kind == 3) {
+                    asm("mul.lo.u32 %0, %1, %2;" : "=r"(lo) : "r"(x[c]), "r"(0xD2511F53u));
+                    asm("mul.hi.u32 %0, %1, %2;" : "=r"(hi) : "r"(x[c]), "r"(0xD2511F53u));
+                } else {
+                    lo = x[c] * 0xD2511F53u;
+                    hi = __umulhi(x[c], 0xD2511F53u);
+                }
+                x[c] = hi ^ lo;
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc ^= x[c];
+    } else if (kind == 1) {
+        float f[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) f[c] = 0.001f * static_cast<float>((tid + c) & 255);
+        for (int64_t i = 0; i < iters; ++i) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float y;
+                asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(-f[c]));
+                f[c] = y;  // stays in (0, 1]
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc ^= __float_as_uint(f[c]);
+    } else {
+        float f[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) f[c] = 0.001f * static_cast<float>((tid + c) & 255);
+        for (int64_t i = 0; i < iters; ++i) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) f[c] = fmaf(f[c], 0.999f, 0.0001f);
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc ^= __float_as_uint(f[c]);
+    }
+    if (acc == 0x12345678u) sink[tid & 255] = acc;  // practically never taken
+}
+
 }  // namespace
 
 KernelTimer& kernel_timer() {
@@ -125,3 +199,16 @@ extern "C" dust_status dust_philox_fill(uint64_t seed, uint32_t layer, uint32_t 
         normals);
     return launch_status();
 }
+
+extern "C" dust_status dust_issue_probe(int kind, int64_t iters, int64_t* threads_out,
+                                        void* sink, void* stream) {
+    if (kind < 0 || kind > 4 || iters < 1 || iters > (1LL << 32) || !threads_out || !sink ||
+        !aligned(sink, 4))
+        return DUST_ERR_INVALID_ARG;
+    constexpr int kBlocks = 148 * 8, kThreads = 256;
+    *threads_out = static_cast<int64_t>(kBlocks) * kThreads;
+    issue_probe_kernel<<<kBlocks, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        kind, iters, static_cast<uint32_t*>(sink));
+    return launch_status();
+}
+

@@ -237,7 +237,19 @@ def make_step(wl, dust):
     raise SystemExit("bad workload")
 
 
-def roofline(wl, kernel_ms, traffic):
+def issue_probes(dust):
+    """Measured issue rates (T operations/s) of the library's probe kernel:
+    Philox's multiply/xor step, ex2 on the XU pipe, and fp32 fma."""
+    out = {}
+    for kind, name, iters in ((0, "philox_mul_xor", 10000), (1, "ex2", 4000), (2, "ffma", 40000)):
+        dust.issue_probe(kind, 16)  # warm-up
+        rate, _ = dust.issue_probe(kind, iters)
+        out[name] = rate / 1e12
+    out["unit"] = "Tops/s"
+    return out
+
+
+def roofline(wl, kernel_ms, traffic, probes=None):
     peaks, which = _peaks()
     if wl["kind"] == "head":
         per = HEAD_OPS_PER_ELEMENT_PAIR if wl.get("baseline") == 2 else HEAD_OPS_PER_ELEMENT_DRAW
@@ -247,7 +259,8 @@ def roofline(wl, kernel_ms, traffic):
         return {"bound": "alu", "achieved": ach, "peak": peak, "unit": "Tops/s",
                 "frac": ach / peak, "traffic": traffic, "kernel": "head_draws_kernel",
                 "kernel_ms": kernel_ms, "peak_source": "148 SMs x 128 lanes x %.0f MHz (%s clocks)"
-                % (peaks.get("sm_max_mhz", SM_MAX_MHZ), which)}
+                % (peaks.get("sm_max_mhz", SM_MAX_MHZ), which),
+                "issue_probe": probes}
     if wl["kind"] == "interior":
         # GEMM 2 of the re-forward: D draws x T rows x d_model x V, split-bf16 (2x)
         flops = 2.0 * wl["K"] * wl["T"] * wl["d_model"] * wl["V"] * 2
@@ -620,6 +633,7 @@ def run_dust(args):
     if dust.workspace_status(ws) != 0:
         raise SystemExit("kernel status word set during the timed steps")
     ms_max = max_over_ranks(ms, dist if world > 1 else None)
+    probes = issue_probes(dust) if wl["kind"] == "head" and rank == 0 else None
 
     # Optional: the same step captured once in a CUDA graph and replayed, which
     # removes the host's launch gaps between the call's kernels.
@@ -745,7 +759,7 @@ def run_dust(args):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f32" if wl["kind"] != "interior" else "f32+bf16x2",
                 "data": "synthetic", "config": config_of(wl, world),
-                "roofline": roofline(wl, kernel_ms, load_traffic(wl)),
+                "roofline": roofline(wl, kernel_ms, load_traffic(wl), probes),
                 "cpu_baseline": cpu, "e2e": e2e, "graph": graph,
                 "gpu_launches": launches * args.steps,
                 "clocks": clocks.summary()}

@@ -392,6 +392,21 @@ dust_status dust_head_backprop(const float* logits, const int32_t* targets, cons
 dust_status dust_wait_selftest(void* ws, uint64_t limit_ns, void* stream);
 
 /*
+ * Issue-rate probe for the benchmark's rooflines: launches 148 x 8 CTAs of 256
+ * threads (*threads_out receives the count) on `stream`, each thread running
+ * `iters` rounds over eight independent chains of one operation:
+ *   kind 0: a 32 x 32 -> 64-bit multiply and an xor of its halves (Philox's
+ *           step; 16 operations per thread and round),
+ *   kind 1: ex2.approx (8 XU operations per thread and round),
+ *   kind 2: fp32 fma (8 operations per thread and round).
+ * The caller times it with events on `stream`.  `sink` (device, >= 1 KB) only
+ * keeps the results alive.  INVALID_ARG for another kind, iters outside
+ * [1, 2^32], or a NULL pointer.
+ */
+dust_status dust_issue_probe(int kind, int64_t iters, int64_t* threads_out, void* sink,
+                             void* stream);
+
+/*
  * Benchmark hook.  While set, every launch of an entry point's dominant
  * kernel (the head's draw kernel, the interior layer's re-forward GEMM with
  * the cross-entropy epilogue, the embedding's piece sums) is bracketed on its
