@@ -398,7 +398,9 @@ dust_status dust_wait_selftest(void* ws, uint64_t limit_ns, void* stream);
  *   kind 0: a 32 x 32 -> 64-bit multiply and an xor of its halves (Philox's
  *           step; 16 operations per thread and round),
  *   kind 1: ex2.approx (8 XU operations per thread and round),
- *   kind 2: fp32 fma (8 operations per thread and round).
+ *   kind 2: fp32 fma (8 operations per thread and round),
+ *   kind 3, 4: kind 0's step with the product's halves as two 32-bit
+ *           multiplies, written as PTX (3) or as C (4) (16 per round).
  * The caller times it with events on `stream`.  `sink` (device, >= 1 KB) only
  * keeps the results alive.  INVALID_ARG for another kind, iters outside
  * [1, 2^32], or a NULL pointer.
