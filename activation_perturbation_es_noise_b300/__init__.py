@@ -30,7 +30,8 @@ EXPORTS = ("dust_status_string", "dust_abi_version", "dust_workspace_status",
            "dust_kernel_event_count", "dust_wait_selftest", "dust_sgd_step", "dust_adam_step",
            "dust_head_backprop_workspace", "dust_head_backprop", "dust_head_estimate_baseline",
            "dust_attn_value_workspace", "dust_attn_value_estimate", "dust_attn_gate_workspace",
-           "dust_attn_gate_estimate", "dust_issue_probe")
+           "dust_attn_gate_estimate", "dust_issue_probe", "dust_head_chunked_workspace",
+           "dust_head_estimate_chunked")
 BASELINE_MEAN, BASELINE_LEAVE_ONE_OUT, BASELINE_ANTITHETIC = 0, 1, 2
 
 
@@ -100,6 +101,10 @@ def lib():
         L.dust_attn_gate_estimate.argtypes = [_P, _P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _I64,
                                               DustNoise, _P, _P, _P, _SZ, _P]
         L.dust_issue_probe.argtypes = [ctypes.c_int, _I64, ctypes.POINTER(_I64), _P, _P]
+        L.dust_head_chunked_workspace.argtypes = [_I64, _I64, _I64, _U32, _I64]
+        L.dust_head_chunked_workspace.restype = _SZ
+        L.dust_head_estimate_chunked.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64,
+                                                 DustNoise, _I64, _P, _P, _P, _SZ, _P]
         L.dust_head_backprop_workspace.argtypes = [_I64, _I64, _I64]
         L.dust_head_backprop_workspace.restype = _SZ
         L.dust_head_backprop.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _P, _P, _P,
@@ -109,7 +114,8 @@ def lib():
                      "dust_embed_scatter_static", "dust_philox_fill", "dust_gemm_bf16",
                      "dust_sgd_step", "dust_adam_step", "dust_head_backprop",
                      "dust_head_estimate_baseline", "dust_attn_value_estimate",
-                     "dust_attn_gate_estimate", "dust_issue_probe"):
+                     "dust_attn_gate_estimate", "dust_issue_probe",
+                     "dust_head_estimate_chunked"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -441,4 +447,28 @@ def issue_probe(kind, iters, stream=None):
     e1.synchronize()
     ms = e0.elapsed_time(e1)
     return n.value * iters * PROBE_OPS_PER_ROUND[kind] / (ms * 1e-3), ms
+
+
+def head_estimate_chunked(logits, targets, x, sigma, K, seed, chunk, layer=0, draw0=0, token0=0,
+                          want_g=True, out=None, ws=None, stream=None):
+    """The head with one vocabulary chunk of width `chunk` perturbed per draw
+    (draw j perturbs chunk j mod V/chunk).  Returns (g_hat or None, G_W, ws)."""
+    _need_cuda(logits, targets, x)
+    T, V = logits.shape
+    d = x.shape[1]
+    dev = logits.device
+    if out is None:
+        g = torch.empty((T, V), dtype=torch.float32, device=dev) if want_g else None
+        G = torch.empty((V, d), dtype=torch.float32, device=dev)
+    else:
+        g, G = out
+    if ws is None:
+        ws = _workspace(lib().dust_head_chunked_workspace(T, V, d, K, chunk), dev)
+    xdt = DUST_BF16 if x.dtype == torch.bfloat16 else DUST_F32
+    _check("dust_head_estimate_chunked",
+           lib().dust_head_estimate_chunked(_ptr(logits), _ptr(targets), _ptr(x), xdt, T, V, d,
+                                            noise(seed, sigma, K, layer, draw0, token0), chunk,
+                                            _ptr(g), _ptr(G), _ptr(ws), ws.numel(),
+                                            _stream(stream)))
+    return g, G, ws
 

@@ -42,6 +42,14 @@ struct HeadArgs {
     float* part_s0;
     float* part_dl;  // Q x T
     uint32_t* status;
+    // Vocabulary-chunk mode (the kernel's CH flag): this launch covers columns
+    // col0 .. col0 + V - 1 of rows ldz apart, p is normalised by the full
+    // row's log-sum-exp lse[t], the rest of the row's probability mass stays
+    // unperturbed, and draw i uses the counter draw0 + i * draw_stride.
+    int64_t ldz;       // row stride of the logits, g_hat and the partials
+    int col0, Vfull;
+    uint32_t draw_stride;
+    const float* lse;
 };
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -100,7 +108,8 @@ __device__ __forceinline__ float block_max(float v, float* scratch) {
 // the pair's centred decrease is c = -(dl(+a) - dl(-a)) / 2, so
 //   g_t = (1/(2 K sigma)) sum_i (dl_i(+a) - dl_i(-a)) a_i
 // needs neither the mean over draws nor the sum of the noise (S0).
-template <int NB, bool ONE_WARP, bool ANTI>
+// CH: one vocabulary chunk per launch (see HeadArgs).
+template <int NB, bool ONE_WARP, bool ANTI, bool CH = false>
 __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
     head_draws_kernel(const HeadArgs A, const PhiloxKeys keys) {
     __shared__ float red[2][8];
@@ -121,7 +130,7 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
     const int i_end = min(A.K, i_begin + A.chunk);
     const int V = A.V;
     const bool vec = (V & 3) == 0;
-    const float* zrow = A.logits + static_cast<int64_t>(t) * V;
+    const float* zrow = A.logits + static_cast<int64_t>(t) * (CH ? A.ldz : V) + (CH ? A.col0 : 0);
 
     // Cached logits of this token -> registers; softmax.
     float p[NB][4];
@@ -142,27 +151,45 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
 #pragma unroll
         for (int k = 0; k < 4; ++k) zmax = fmaxf(zmax, p[b][k]);
     }
-    zmax = block_max<ONE_WARP>(zmax, scratch);
-    float zsum = 0.f;
+    float unpert = 0.f;  // CH: the probability mass outside the chunk
+    if (CH) {
+        const float lse = __ldg(A.lse + t);
+        float pc = 0.f;
 #pragma unroll
-    for (int b = 0; b < NB; ++b)
+        for (int b = 0; b < NB; ++b)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            p[b][k] = (p[b][k] == -INFINITY) ? 0.f : expf(p[b][k] - zmax);
-            zsum += p[b][k];
-        }
-    zsum = block_sum<ONE_WARP>(zsum, scratch);
-    const float zinv = 1.0f / zsum;
+            for (int k = 0; k < 4; ++k) {
+                p[b][k] = (p[b][k] == -INFINITY) ? 0.f : expf(p[b][k] - lse);
+                pc += p[b][k];
+            }
+        unpert = 1.0f - block_sum<ONE_WARP>(pc, scratch);
+    } else {
+        zmax = block_max<ONE_WARP>(zmax, scratch);
+        float zsum = 0.f;
 #pragma unroll
-    for (int b = 0; b < NB; ++b)
+        for (int b = 0; b < NB; ++b)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) p[b][k] *= zinv;
+            for (int k = 0; k < 4; ++k) {
+                p[b][k] = (p[b][k] == -INFINITY) ? 0.f : expf(p[b][k] - zmax);
+                zsum += p[b][k];
+            }
+        zsum = block_sum<ONE_WARP>(zsum, scratch);
+        const float zinv = 1.0f / zsum;
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) p[b][k] *= zinv;
+    }
 
-    // Target channel: the thread that owns it supplies sigma a_y every draw.
+    // Target channel: the thread that owns it supplies sigma a_y every draw
+    // (in chunk mode only when the target lies in the chunk).
     int y = __ldg(A.targets + t);
-    if (y < 0 || y >= V) {
+    if (y < 0 || y >= (CH ? A.Vfull : V)) {
         if (tid == 0 && q == 0) record_status(A.status, DUST_ERR_DEVICE_RANGE);
         y = -1;
+    } else if (CH) {
+        y -= A.col0;
+        if (y < 0 || y >= V) y = -1;
     }
     const int yblk = y >> 2;
     const bool owner = (y >= 0) && (yblk % NT == tid);
@@ -173,7 +200,8 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
 
     BlockHalf bh[NB];
 #pragma unroll
-    for (int b = 0; b < NB; ++b) bh[b] = philox_block_half(b * NT + tid, A.layer, keys);
+    for (int b = 0; b < NB; ++b)  // global channel blocks (the chunk's offset in chunk mode)
+        bh[b] = philox_block_half((CH ? A.col0 / 4 : 0) + b * NT + tid, A.layer, keys);
 
     float s1[NB][4], s0[NB][4];
 #pragma unroll
@@ -185,7 +213,8 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
 
 #pragma unroll 1
     for (int i = i_begin; i < i_end; ++i) {
-        const DrawHalf dh = philox_draw_half(A.draw0 + static_cast<uint32_t>(i), token, keys);
+        const DrawHalf dh = philox_draw_half(
+            A.draw0 + static_cast<uint32_t>(i) * (CH ? A.draw_stride : 1u), token, keys);
         // All NB blocks advance in lockstep (words, then normals, then the
         // loss terms) so that their independent chains interleave.
         uint4 w[NB];
@@ -235,7 +264,7 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
         if (ANTI) partm = warp_sum(partm);
         float S, Sm = 1.f;
         if (ONE_WARP) {
-            S = part;
+            S = CH ? part + unpert : part;
             Sm = partm;
             ay = __shfl_sync(0xFFFFFFFFu, ay, ylane);
         } else {
@@ -252,6 +281,7 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
             S += __shfl_xor_sync(0xFFFFFFFFu, S, 1);
             S += __shfl_xor_sync(0xFFFFFFFFu, S, 2);
             S += __shfl_xor_sync(0xFFFFFFFFu, S, 4);
+            if (CH) S += unpert;
             if (ANTI) {
                 Sm = red_m[buf][lane & 7];
                 Sm += __shfl_xor_sync(0xFFFFFFFFu, Sm, 1);
@@ -283,8 +313,10 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
 
     if (A.Q == 1) {
         const float mean = sdl / static_cast<float>(A.K);
-        float* grow = A.g_hat ? A.g_hat + static_cast<int64_t>(t) * V : nullptr;
-        __nv_bfloat16* brow = A.gbf + static_cast<int64_t>(t) * A.ldg;
+        float* grow = A.g_hat ? A.g_hat + static_cast<int64_t>(t) * (CH ? A.ldz : V) +
+                                    (CH ? A.col0 : 0)
+                              : nullptr;
+        __nv_bfloat16* brow = A.gbf + static_cast<int64_t>(t) * A.ldg + (CH ? A.col0 : 0);
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             const int j = b * NT + tid;
@@ -312,7 +344,7 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
             }
         }
     } else {
-        const int64_t off = (static_cast<int64_t>(q) * A.T + t) * V;
+        const int64_t off = (static_cast<int64_t>(q) * A.T + t) * (CH ? A.ldz : V) + (CH ? A.col0 : 0);
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             const int j = b * NT + tid;
@@ -331,21 +363,22 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
 }
 
 // Sums the draw-chunk partials in chunk order and forms g (fp32 + bf16 copy).
+// (Columns col0 .. col0 + V - 1 of rows ldz apart, as the draws kernel.)
 __global__ void head_finalize_kernel(const HeadArgs A) {
     const int t = blockIdx.y;
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= A.V) return;
     float sdl = 0.f, s1 = 0.f, s0 = 0.f;
     for (int q = 0; q < A.Q; ++q) {
-        const int64_t off = (static_cast<int64_t>(q) * A.T + t) * A.V + c;
+        const int64_t off = (static_cast<int64_t>(q) * A.T + t) * A.ldz + A.col0 + c;
         sdl += A.part_dl[static_cast<int64_t>(q) * A.T + t];
         s1 += A.part_s1[off];
         s0 += A.part_s0[off];
     }
     const float mean = sdl / static_cast<float>(A.K);
     const float g = (s1 - mean * s0) * A.g_scale;
-    if (A.g_hat) A.g_hat[static_cast<int64_t>(t) * A.V + c] = g;
-    A.gbf[static_cast<int64_t>(t) * A.ldg + c] = __float2bfloat16_rn(g);
+    if (A.g_hat) A.g_hat[static_cast<int64_t>(t) * A.ldz + A.col0 + c] = g;
+    A.gbf[static_cast<int64_t>(t) * A.ldg + A.col0 + c] = __float2bfloat16_rn(g);
 }
 
 struct HeadPlan {
@@ -399,12 +432,15 @@ HeadPlan head_plan(int64_t T, int64_t V, int64_t d, uint32_t K) {
 
 template <int NB, bool OW>
 dust_status launch_draws(const HeadPlan& P, const HeadArgs& A, const PhiloxKeys& keys,
-                         int64_t T, bool anti, cudaStream_t s) {
+                         int64_t T, bool anti, cudaStream_t s, bool chunk = false) {
     timer_begin(s);
-    if (anti)
-        head_draws_kernel<NB, OW, true><<<static_cast<unsigned>(T * P.Q), P.nt, 0, s>>>(A, keys);
+    const unsigned grid = static_cast<unsigned>(T * P.Q);
+    if (chunk)
+        head_draws_kernel<NB, OW, false, true><<<grid, P.nt, 0, s>>>(A, keys);
+    else if (anti)
+        head_draws_kernel<NB, OW, true><<<grid, P.nt, 0, s>>>(A, keys);
     else
-        head_draws_kernel<NB, OW, false><<<static_cast<unsigned>(T * P.Q), P.nt, 0, s>>>(A, keys);
+        head_draws_kernel<NB, OW, false><<<grid, P.nt, 0, s>>>(A, keys);
     timer_end(s);
     return launch_status();
 }
@@ -471,6 +507,10 @@ dust_status head_estimate(const float* logits, const int32_t* targets, const voi
     A.gbf = reinterpret_cast<__nv_bfloat16*>(w + P.off_gbf);
     A.ldg = P.ldg;
     A.status = static_cast<uint32_t*>(ws);
+    A.ldz = V;
+    A.col0 = 0;
+    A.Vfull = static_cast<int>(V);
+    A.draw_stride = 1;
     if (P.Q > 1) {
         A.part_s1 = reinterpret_cast<float*>(w + P.off_s1);
         A.part_s0 = reinterpret_cast<float*>(w + P.off_s0);
@@ -625,5 +665,165 @@ extern "C" dust_status dust_head_backprop(const float* logits, const int32_t* ta
         ldx = P.ldx;
     }
     return gemm_bf16_launch(gbf, true, P.ldg, xb, true, ldx, V, d, T, 0, 1, G_W, d,
+                            static_cast<uint32_t*>(ws), s);
+}
+
+// ------------------------------------------------------------------------
+// The head with a vocabulary chunk perturbed per draw.  The pages' head
+// perturbs the cached logits and each round recomputes the cross-entropy of
+// only a small chunk of the vocabulary (laoyaoba.com, section 机制拆解).  Read
+// plainly: with chunks of width w tiling the vocabulary, draw j perturbs chunk
+// j mod (V/w) only, so
+//   dl = log(1 + sum_{v in chunk} p_v (e^{sigma a_v} - 1)) - sigma a_y [y in chunk],
+// each chunk's draws are centred by their own mean, and each chunk's columns
+// of g average over that chunk's K w / V draws.  One launch per chunk.
+// ------------------------------------------------------------------------
+namespace dust {
+namespace {
+
+// Full-row log-sum-exp of the cached logits, one CTA per token.
+__global__ void __launch_bounds__(256) row_lse_kernel(const float* __restrict__ z, int V,
+                                                      float* __restrict__ lse) {
+    __shared__ float scratch[8];
+    const float* zr = z + static_cast<int64_t>(blockIdx.x) * V;
+    float m = -INFINITY;
+    for (int v = threadIdx.x; v < V; v += blockDim.x) m = fmaxf(m, zr[v]);
+    m = block_max<false>(m, scratch);
+    float s = 0.f;
+    for (int v = threadIdx.x; v < V; v += blockDim.x) s += expf(zr[v] - m);
+    s = block_sum<false>(s, scratch);
+    if (threadIdx.x == 0) lse[blockIdx.x] = m + logf(s);
+}
+
+struct ChunkPlan {
+    HeadPlan k;  // kernel configuration for one chunk (width w, K w / V draws)
+    int64_t ldg, ldx;
+    size_t off_gbf, off_xbf, off_lse, off_s1, off_s0, off_dl, bytes;
+};
+
+ChunkPlan chunk_plan(int64_t T, int64_t V, int64_t d, uint32_t K, int64_t w) {
+    ChunkPlan P{};
+    P.k = head_plan(T, w, d, static_cast<uint32_t>(K / (V / w)));
+    P.ldg = round_up(V, 8);
+    P.ldx = round_up(d, 8);
+    WsLayout ws;
+    ws.take(kCtlBytes);
+    P.off_gbf = ws.take(static_cast<size_t>(T * P.ldg) * 2);
+    P.off_xbf = ws.take(static_cast<size_t>(T * P.ldx) * 2);
+    P.off_lse = ws.take(static_cast<size_t>(T) * 4);
+    if (P.k.Q > 1) {
+        P.off_s1 = ws.take(static_cast<size_t>(P.k.Q) * T * V * 4);
+        P.off_s0 = ws.take(static_cast<size_t>(P.k.Q) * T * V * 4);
+        P.off_dl = ws.take(static_cast<size_t>(P.k.Q) * T * 4);
+    }
+    P.bytes = ws.used;
+    return P;
+}
+
+bool chunk_shape_ok(int64_t V, uint32_t K, int64_t w) {
+    return w >= 4 && w % 4 == 0 && w <= kMaxV && V % w == 0 && K % (V / w) == 0 &&
+           K / (V / w) >= 2;
+}
+
+}  // namespace
+}  // namespace dust
+
+extern "C" size_t dust_head_chunked_workspace(int64_t T, int64_t V, int64_t d, uint32_t K,
+                                              int64_t chunk) {
+    if (T < 1 || V < 1 || d < 1 || V > (1LL << 20) || !chunk_shape_ok(V, K, chunk)) return 0;
+    return chunk_plan(T, V, d, K, chunk).bytes;
+}
+
+extern "C" dust_status dust_head_estimate_chunked(const float* logits, const int32_t* targets,
+                                                  const void* x, dust_dtype x_dtype, int64_t T,
+                                                  int64_t V, int64_t d, dust_noise nz,
+                                                  int64_t chunk, float* g_hat, float* G_W,
+                                                  void* ws, size_t ws_bytes, void* stream) {
+    if (!logits || !targets || !x || !G_W) return DUST_ERR_INVALID_ARG;
+    if (T < 1 || V < 1 || d < 1 || nz.num_draws < 2) return DUST_ERR_INVALID_ARG;
+    if (!(nz.sigma > 0.0f) || !(nz.sigma < INFINITY)) return DUST_ERR_INVALID_ARG;
+    if (x_dtype != DUST_F32 && x_dtype != DUST_BF16) return DUST_ERR_INVALID_ARG;
+    if (!chunk_shape_ok(V, nz.num_draws, chunk)) return DUST_ERR_INVALID_ARG;
+    if (V > (1LL << 20) || T > (1LL << 30) || d > (1LL << 30) || nz.num_draws > (1u << 30))
+        return DUST_ERR_UNSUPPORTED;
+    if (static_cast<uint64_t>(nz.token0) + static_cast<uint64_t>(T) > (1ULL << 32))
+        return DUST_ERR_INVALID_ARG;
+    if (static_cast<uint64_t>(nz.draw0) + nz.num_draws > (1ULL << 32)) return DUST_ERR_INVALID_ARG;
+    if (!aligned(logits, 16) || (g_hat && !aligned(g_hat, 16))) return DUST_ERR_INVALID_ARG;
+    const ChunkPlan P = chunk_plan(T, V, d, nz.num_draws, chunk);
+    if (!ws || ws_bytes < P.bytes || !aligned(ws, 256)) return DUST_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    DUST_CUDA_TRY(cudaMemsetAsync(ws, 0, kCtlBytes, s));
+    float* lse = reinterpret_cast<float*>(w + P.off_lse);
+    row_lse_kernel<<<static_cast<unsigned>(T), 256, 0, s>>>(logits, static_cast<int>(V), lse);
+    dust_status st = launch_status();
+    if (st != DUST_OK) return st;
+
+    const int nchunks = static_cast<int>(V / chunk);
+    const uint32_t Kc = nz.num_draws / static_cast<uint32_t>(nchunks);
+    HeadArgs A{};
+    A.logits = logits;
+    A.targets = targets;
+    A.T = static_cast<int>(T);
+    A.V = static_cast<int>(chunk);
+    A.nblk = P.k.nblk;
+    A.K = static_cast<int>(Kc);
+    A.Q = P.k.Q;
+    A.chunk = P.k.chunk;
+    A.token0 = nz.token0;
+    A.layer = nz.layer;
+    const double s_l2e = static_cast<double>(nz.sigma) * 1.4426950408889634;
+    A.sig_l2e = static_cast<float>(s_l2e);
+    A.g_scale = static_cast<float>(
+        1.0 / (static_cast<double>(Kc) * nz.sigma * static_cast<double>(A.sig_l2e)));
+    A.g_hat = g_hat;
+    A.gbf = reinterpret_cast<__nv_bfloat16*>(w + P.off_gbf);
+    A.ldg = P.ldg;
+    A.status = static_cast<uint32_t*>(ws);
+    A.ldz = V;
+    A.Vfull = static_cast<int>(V);
+    A.draw_stride = static_cast<uint32_t>(nchunks);
+    A.lse = lse;
+    if (P.k.Q > 1) {
+        A.part_s1 = reinterpret_cast<float*>(w + P.off_s1);
+        A.part_s0 = reinterpret_cast<float*>(w + P.off_s0);
+        A.part_dl = reinterpret_cast<float*>(w + P.off_dl);
+    }
+    const PhiloxKeys keys = philox_round_keys(nz.seed);
+    for (int c = 0; c < nchunks; ++c) {
+        A.col0 = static_cast<int>(c * chunk);
+        A.draw0 = nz.draw0 + static_cast<uint32_t>(c);
+        if (P.k.one_warp) {
+            switch (P.k.nb) {
+                case 1: st = launch_draws<1, true>(P.k, A, keys, T, false, s, true); break;
+                case 2: st = launch_draws<2, true>(P.k, A, keys, T, false, s, true); break;
+                case 4: st = launch_draws<4, true>(P.k, A, keys, T, false, s, true); break;
+                default: st = launch_draws<8, true>(P.k, A, keys, T, false, s, true); break;
+            }
+        } else {
+            st = P.k.nb == 4 ? launch_draws<4, false>(P.k, A, keys, T, false, s, true)
+                             : launch_draws<8, false>(P.k, A, keys, T, false, s, true);
+        }
+        if (st != DUST_OK) return st;
+        if (P.k.Q > 1) {
+            dim3 grid(static_cast<unsigned>(ceil_div(chunk, 128)), static_cast<unsigned>(T));
+            head_finalize_kernel<<<grid, 128, 0, s>>>(A);
+            if ((st = launch_status()) != DUST_OK) return st;
+        }
+    }
+
+    const void* xb = x;
+    int64_t ldx = d;
+    if (x_dtype == DUST_F32 || (d % 8) != 0 || !aligned(x, 16)) {
+        void* xbf = w + P.off_xbf;
+        st = x_dtype == DUST_F32
+                 ? f32_to_bf16_launch(static_cast<const float*>(x), T, d, d, xbf, P.ldx, s)
+                 : bf16_pad_launch(x, T, d, d, xbf, P.ldx, s);
+        if (st != DUST_OK) return st;
+        xb = xbf;
+        ldx = P.ldx;
+    }
+    return gemm_bf16_launch(A.gbf, true, P.ldg, xb, true, ldx, V, d, T, 0, 1, G_W, d,
                             static_cast<uint32_t*>(ws), s);
 }

@@ -13,7 +13,8 @@ frequencies; weights are random N(0, 1/fan_in).  The cached logits (256 MB)
 are larger than the 126 MB L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dust|reference]
-                  [--workload head_batch|head_batch_antithetic|head_tiny|head_scale|interior|
+                  [--workload head_batch|head_batch_antithetic|head_batch_chunked|head_tiny|
+                              head_scale|interior|
                               interior_scale|embed_scale|head_sweep|optim_adam|attn_value]
 
 Under torchrun (N > 1) every rank estimates its own batch (global token
@@ -153,7 +154,7 @@ def make_workload(name, device, rank):
         return {
             "kind": "head", "name": name, "T": T, "V": p["V"], "d": p["d"], "K": p["K"],
             "sigma": p["sigma"], "seq_len": p["seq_len"], "token0": rank_token0(rank, T),
-            "baseline": p.get("baseline", 0),
+            "baseline": p.get("baseline", 0), "vchunk": p.get("chunk", 0),
             "host": {"logits": wl["z"], "targets": wl["targets"],
                      "x": W.bf16_round(wl["x"]) if p["x_bf16"] else wl["x"]},
             "x_bf16": p["x_bf16"],
@@ -192,6 +193,16 @@ def make_step(wl, dust):
         g = torch.empty((T, V), dtype=torch.float32, device=d["logits"].device)
         G = torch.empty((V, dd), dtype=torch.float32, device=g.device)
         ws = dust._workspace(dust.head_workspace_bytes(T, V, dd, K), g.device)
+
+        if wl["vchunk"]:
+            ws = dust._workspace(dust.lib().dust_head_chunked_workspace(T, V, dd, K, wl["vchunk"]),
+                                 g.device)
+
+            def step():
+                dust.head_estimate_chunked(d["logits"], d["targets"], d["x"], wl["sigma"], K, 1234,
+                                           wl["vchunk"], token0=wl["token0"], out=(g, G), ws=ws)
+            # lse, one draw kernel per chunk, the outer product
+            return step, K * T, 2 + V // wl["vchunk"], ws
 
         def step():
             dust.head_estimate(d["logits"], d["targets"], d["x"], wl["sigma"], K, 1234, 0, 0,
@@ -253,7 +264,8 @@ def roofline(wl, kernel_ms, traffic, probes=None):
     peaks, which = _peaks()
     if wl["kind"] == "head":
         per = HEAD_OPS_PER_ELEMENT_PAIR if wl.get("baseline") == 2 else HEAD_OPS_PER_ELEMENT_DRAW
-        ops = per * wl["T"] * wl["V"] * wl["K"]
+        width = wl.get("vchunk") or wl["V"]  # elements perturbed per draw
+        ops = per * wl["T"] * width * wl["K"]
         peak = N_SM * 128 * peaks.get("sm_max_mhz", SM_MAX_MHZ) * 1e6 / 1e12
         ach = ops / (kernel_ms * 1e-3) / 1e12
         return {"bound": "alu", "achieved": ach, "peak": peak, "unit": "Tops/s",
@@ -317,7 +329,11 @@ def oracle_sample(wl, budget_s=12.0):
 
         def run(n):
             t0 = time.perf_counter()
-            fn(h["logits"][:n], h["targets"][:n], h["x"][:n], wl["sigma"], K, 1234, 0, 0, 0)
+            if wl.get("vchunk"):
+                oracle.head_estimate_chunked(h["logits"][:n], h["targets"][:n], h["x"][:n],
+                                             wl["sigma"], K, 1234, 0, wl["vchunk"])
+            else:
+                fn(h["logits"][:n], h["targets"][:n], h["x"][:n], wl["sigma"], K, 1234, 0, 0, 0)
             return time.perf_counter() - t0
         n = 8
         dt = run(n)
@@ -355,6 +371,8 @@ def config_of(wl, n_gpus):
             c[k] = wl[k]
     if wl.get("baseline") == 2:
         c["baseline"] = "antithetic pairs: draws counts noise draws, 2 evaluations each"
+    if wl.get("vchunk"):
+        c["vocab_chunk"] = wl["vchunk"]
     return c
 
 
@@ -684,7 +702,16 @@ def run_dust(args):
             G = torch.empty((V, dd), dtype=torch.float32, device=device)
             wse = dust._workspace(dust.head_workspace_bytes(T, V, dd, K), device)
 
+            if wl["vchunk"]:
+                wse = dust._workspace(dust.lib().dust_head_chunked_workspace(
+                    T, V, dd, K, wl["vchunk"]), device)
+
             def call(d):
+                if wl["vchunk"]:
+                    dust.head_estimate_chunked(d["logits"], d["targets"], d["x"], wl["sigma"], K,
+                                               1234, wl["vchunk"], token0=wl["token0"],
+                                               out=(g, G), ws=wse)
+                    return
                 dust.head_estimate(d["logits"], d["targets"], d["x"], wl["sigma"], K, 1234, 0, 0,
                                    wl["token0"], out=(g, G), ws=wse, baseline=wl["baseline"])
         elif wl["kind"] == "interior":
@@ -776,7 +803,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="dust", choices=["dust", "reference"])
     ap.add_argument("--workload", default="head_batch",
-                    choices=["head_batch", "head_batch_antithetic", "head_tiny", "head_scale",
+                    choices=["head_batch", "head_batch_antithetic", "head_batch_chunked",
+                             "head_tiny", "head_scale",
                              "interior",
                              "interior_scale", "embed_scale", "head_sweep", "optim_adam",
                              "attn_value"])

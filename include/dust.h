@@ -157,6 +157,27 @@ dust_status dust_head_estimate_baseline(const float* logits, const int32_t* targ
                                         float* g_hat, float* G_W, void* ws, size_t ws_bytes,
                                         void* stream);
 
+/* Workspace bytes for dust_head_estimate_chunked (0 if the shape is invalid). */
+size_t dust_head_chunked_workspace(int64_t T, int64_t V, int64_t d, uint32_t K, int64_t chunk);
+
+/*
+ * The head with one vocabulary chunk perturbed per draw (the pages' head
+ * recomputes the cross-entropy of only a small chunk of the vocabulary per
+ * round: laoyaoba.com, section 机制拆解).  Chunks of width `chunk` tile the
+ * vocabulary; draw j (counter draw0 + j) perturbs chunk j mod (V/chunk) only:
+ *   dl = log(1 + sum_{v in chunk} p_v (e^{sigma a_v} - 1)) - sigma a_y [y in chunk],
+ * p the softmax of the full row.  Each chunk's draws are centred by their own
+ * mean, and each column of g averages over its chunk's K chunk / V draws:
+ *   g_t[v] = -(1/(K_c sigma)) sum_{draws i of v's chunk} c_{i,t} a_{i,t}[v].
+ * With chunk = V it is dust_head_estimate.  Arguments and outputs as there;
+ * chunk must be a multiple of 4 dividing V (<= 8192), and V/chunk must divide
+ * K with at least 2 draws per chunk (INVALID_ARG otherwise).
+ */
+dust_status dust_head_estimate_chunked(const float* logits, const int32_t* targets,
+                                       const void* x, dust_dtype x_dtype, int64_t T, int64_t V,
+                                       int64_t d, dust_noise nz, int64_t chunk, float* g_hat,
+                                       float* G_W, void* ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Interior linear layer with causal credit                                  */
 /* ------------------------------------------------------------------------ */

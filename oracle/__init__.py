@@ -27,7 +27,8 @@ import numpy as np
 from . import build as _build
 from .attention import (attn_gate_delta_loss, attn_gate_estimate,  # noqa: F401
                         attn_value_delta_loss, attn_value_estimate)
-from .baselines import head_estimate_antithetic, head_estimate_leave_one_out  # noqa: F401
+from .baselines import (head_estimate_antithetic, head_estimate_chunked,  # noqa: F401
+                        head_estimate_leave_one_out)
 from .optim import adam_step, head_backprop, head_grad_rows, sgd_step  # noqa: F401
 
 _lib = None

@@ -56,3 +56,38 @@ def head_estimate_antithetic(z, targets, x, sigma, K, seed, layer, draw0=0, toke
         acc += c[i][:, None] * a
     g = -acc / (K * sigma)
     return {"c": c, "g": g, "G": outer(g, np.asarray(x, np.float64))}
+
+
+def head_estimate_chunked(z, targets, x, sigma, K, seed, layer, chunk, draw0=0, token0=0):
+    """The head with one vocabulary chunk perturbed per draw (laoyaoba.com,
+    section 机制拆解: each round recomputes the cross-entropy of a small chunk of
+    the vocabulary), read as: chunks of width `chunk` tile the vocabulary, draw
+    j perturbs chunk j mod (V/chunk), the loss change is the full-row cross
+    entropy with only that chunk's logits moved, each chunk's draws are centred
+    by their own mean, and each chunk's columns of g average over its draws."""
+    from . import noise, outer
+    z = np.asarray(z, np.float64)
+    T, V = z.shape
+    nch = V // chunk
+    Kc = K // nch
+    y = np.asarray(targets, np.int64)
+    rows = np.arange(T)
+    lse0 = _lse(z)
+    g = np.zeros((T, V), np.float64)
+    for c in range(nch):
+        cols = slice(c * chunk, (c + 1) * chunk)
+        dls, noises = [], []
+        for k in range(Kc):
+            j = c + k * nch  # the draw's index within the call
+            a = noise(seed, layer, draw0 + j, token0, T, V)
+            zp = z.copy()
+            zp[:, cols] += sigma * a[:, cols]
+            dls.append((_lse(zp) - zp[rows, y]) - (lse0 - z[rows, y]))
+            noises.append(a[:, cols])
+        dl = np.stack(dls)                  # Kc x T
+        cc = -(dl - dl.mean(axis=0))
+        for k in range(Kc):
+            g[:, cols] += cc[k][:, None] * noises[k]
+        g[:, cols] *= -1.0 / (Kc * sigma)
+    return {"g": g, "G": outer(g, np.asarray(x, np.float64))}
+

@@ -65,3 +65,37 @@ def test_unknown_baseline_rejected(dust):
     with pytest.raises(dust.DustError):
         dust.head_estimate(z, torch.zeros(4, dtype=torch.int32, device="cuda"),
                            torch.zeros(4, 4, device="cuda"), 0.05, 4, 1, baseline=7)
+
+
+# one-warp CTAs at several block counts, 160-thread CTAs (a single chunk of
+# 4100 columns, absent warp slots), and the draw-split path with its finalize
+@pytest.mark.parametrize("T,d,V,K,chunk", [(256, 64, 512, 64, 128), (64, 512, 4096, 16, 1024),
+                                           (19, 16, 4100, 40, 820), (7, 16, 4100, 4, 4100),
+                                           (5, 8, 64, 128, 16)])
+def test_head_chunked_matches_oracle(dust, orc, T, d, V, K, chunk):
+    x, z, y = _inputs(T, d, V, seed=T + V + chunk)
+    g, G, ws = dust.head_estimate_chunked(to_dev(z), to_dev(y), to_dev(x), 0.05, K, 1234, chunk,
+                                          draw0=3, token0=11)
+    torch.cuda.synchronize()
+    assert dust.workspace_status(ws) == 0
+    ref = orc.head_estimate_chunked(z, y, x, 0.05, K, 1234, 0, chunk, 3, 11)
+    eg, eG = rel_l2(g.cpu().numpy(), ref["g"]), rel_l2(G.cpu().numpy(), ref["G"])
+    assert eg <= G_TOL and eG <= GW_TOL, (eg, eG)
+    parity(g=eg, G_W=eG)
+
+
+def test_head_chunked_with_one_chunk_equals_the_head(dust):
+    x, z, y = _inputs(64, 32, 512, seed=9)
+    g1, G1, _ = dust.head_estimate_chunked(to_dev(z), to_dev(y), to_dev(x), 0.05, 8, 7, 512)
+    g2, G2, _ = dust.head_estimate(to_dev(z), to_dev(y), to_dev(x), 0.05, 8, 7)
+    torch.cuda.synchronize()
+    # the same arithmetic up to the softmax's normaliser (full-row lse here)
+    assert rel_l2(g1.cpu().numpy(), g2.cpu().numpy()) <= 1e-5
+
+
+def test_head_chunked_rejects_bad_shapes(dust):
+    L = dust.lib()
+    assert L.dust_head_chunked_workspace(16, 512, 8, 8, 100) == 0  # does not divide V
+    assert L.dust_head_chunked_workspace(16, 512, 8, 6, 128) == 0  # 4 chunks do not divide K
+    assert L.dust_head_chunked_workspace(16, 512, 8, 4, 128) == 0  # 1 draw per chunk
+    assert L.dust_head_chunked_workspace(16, 512, 8, 8, 128) > 0

@@ -64,3 +64,42 @@ def test_antithetic_pair_changes_are_cross_entropies_of_the_perturbed_logits():
         a = oracle.noise(99, 0, i, 0, T, V)
         np.testing.assert_allclose(c[i], -(ce(z + sigma * a) - ce(z - sigma * a)) / 2,
                                    rtol=1e-12, atol=1e-14)
+
+
+def test_chunked_with_one_chunk_is_the_mean_estimator():
+    z, y, x = _inputs(V=40)
+    got = oracle.head_estimate_chunked(z, y, x, 0.05, 6, 1234, 0, 40)
+    want = oracle.head_estimate(z, y, x, 0.05, 6, 1234, 0)
+    np.testing.assert_allclose(got["g"], want["g"], rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(got["G"], want["G"], rtol=1e-9, atol=1e-12)
+
+
+def test_chunked_small_sigma_limit_is_the_projection_per_chunk():
+    # Each chunk's columns tend to (1/K_c) sum_i (<grad_c, a_i> - mean) a_i over
+    # that chunk's draws, grad = p - e_y restricted to the chunk.
+    z, y, x = _inputs(T=4, V=24)
+    T, V = z.shape
+    chunk, K, sigma = 8, 12, 1e-5
+    nch = V // chunk
+    grad = np.exp(z - z.max(1, keepdims=True))
+    grad /= grad.sum(1, keepdims=True)
+    grad[np.arange(T), y] -= 1.0
+    want = np.zeros((T, V))
+    for c in range(nch):
+        cols = slice(c * chunk, (c + 1) * chunk)
+        a = np.stack([oracle.noise(1234, 0, c + k * nch, 0, T, V)[:, cols] for k in range(K // nch)])
+        proj = (a * grad[None, :, cols]).sum(-1)
+        proj -= proj.mean(0, keepdims=True)
+        want[:, cols] = (proj[..., None] * a).sum(0) / (K // nch)
+    got = oracle.head_estimate_chunked(z, y, x, sigma, K, 1234, 0, chunk)["g"]
+    assert np.linalg.norm(got - want) / np.linalg.norm(want) < 1e-4
+
+
+def test_chunked_loss_change_uses_only_the_chunk():
+    # A chunk that does not hold the target and whose logits are far below the
+    # rest barely moves the loss: its columns of g stay tiny.
+    z, y, x = _inputs(T=3, V=16)
+    z[:, 8:] -= 30.0
+    y = np.array([0, 1, 2], np.int32)
+    g = oracle.head_estimate_chunked(z, y, x, 0.1, 8, 5, 0, 8)["g"]
+    assert np.abs(g[:, 8:]).max() < 1e-9 < np.abs(g[:, :8]).max()

@@ -89,6 +89,9 @@ HEAD_PARAMS = {
     "head_scale": dict(HEAD_SCALE, sigma=0.05, K=4096),
     # the batch shape with antithetic pairs: 32 noise draws, 64 evaluations
     "head_batch_antithetic": dict(HEAD_BATCH, sigma=0.05, K=32, baseline=2),
+    # one vocabulary chunk of 512 perturbed per draw: 512 draws cost the
+    # element work of 64 full-vocabulary draws
+    "head_batch_chunked": dict(HEAD_BATCH, sigma=0.05, K=512, chunk=512),
 }
 HEAD_SWEEP_K = (64, 256, 1024, 4096, 16384)
 
