@@ -369,13 +369,8 @@ extern "C" dust_status dust_attn_value_estimate(const float* P, const float* E, 
     if (!encode_bf16_2d(&tp, P2, 2 * seq_len, prows, 2 * seq_len, kKB, kQM) ||
         !encode_bf16_2d(&tn, N2, 2 * seq_len, nseq * H * kNB, 2 * seq_len, kKB, kNB))
         return DUST_ERR_CUDA;
-    static bool attr_set = false;
-    if (!attr_set) {
-        DUST_CUDA_TRY(cudaFuncSetAttribute(attn_v_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(kSmemBytes)));
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    DUST_CUDA_TRY(set_smem_once(attn_v_kernel, static_cast<int>(kSmemBytes), smem_set));
     const dim3 grid(static_cast<unsigned>(seq_len / kQM), static_cast<unsigned>(nseq * H));
     for (int i0 = 0; i0 < K; i0 += kGroup) {
         const int nd = K - i0 < kGroup ? K - i0 : kGroup;

@@ -353,12 +353,8 @@ dust_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtenso
                      cudaStream_t s) {
     auto kern = gemm_bf16_kernel<A_MN, B_MN, EPI>;
     constexpr uint32_t smem = smem_bytes<EPI>();
-    static bool attr_set = false;
-    if (!attr_set) {
-        DUST_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem)));
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};  // one per template instance
+    DUST_CUDA_TRY(set_smem_once(kern, static_cast<int>(smem), smem_set));
     const int ntiles = (sh.N + kBN - 1) / kBN;
     const unsigned gm = static_cast<unsigned>(ceil_div(sh.M, kBM));
     const unsigned gn = static_cast<unsigned>(ceil_div(ntiles, sh.n_per_cta));

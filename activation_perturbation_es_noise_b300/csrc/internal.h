@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
+
+#include <atomic>
 #include <stdint.h>
 
 #include "../../include/dust.h"
@@ -40,6 +42,22 @@ inline bool aligned(const void* p, size_t a) {
             return DUST_ERR_CUDA;                              \
         }                                                      \
     } while (0)
+
+// Raises a kernel's dynamic shared-memory limit once per device: the
+// attribute belongs to the device that is current when it is set, so a
+// process that drives several GPUs needs it on each (bit d of `done` records
+// device d; a race only repeats a harmless call).
+template <typename K>
+inline cudaError_t set_smem_once(K kern, int bytes, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 // Launch-error check after a kernel launch.
 inline dust_status launch_status() {

@@ -476,13 +476,8 @@ dust_status reforward1_launch(const float* y1, const float* h0, const void* coef
                               cudaStream_t s) {
     CUtensorMap tw2;
     if (!encode_bf16_2d(&tw2, W2, C, dm, C, kBK, 256)) return DUST_ERR_CUDA;
-    static bool attr_set = false;
-    if (!attr_set) {
-        DUST_CUDA_TRY(cudaFuncSetAttribute(reforward1_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(kSmemBytes)));
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    DUST_CUDA_TRY(set_smem_once(reforward1_kernel, static_cast<int>(kSmemBytes), smem_set));
     const bool ema = A2 != nullptr;
     if (ema && (seq_len % kBM != 0 || Tp != T)) return DUST_ERR_UNSUPPORTED;
     RefArgs a{};

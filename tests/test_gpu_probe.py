@@ -20,4 +20,4 @@ def test_probe_rates_are_physical(dust):
 
 def test_probe_rejects_bad_kind(dust):
     with pytest.raises(dust.DustError):
-        dust.issue_probe(3, 10)
+        dust.issue_probe(5, 10)
