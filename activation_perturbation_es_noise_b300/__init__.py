@@ -31,7 +31,7 @@ EXPORTS = ("dust_status_string", "dust_abi_version", "dust_workspace_status",
            "dust_head_backprop_workspace", "dust_head_backprop", "dust_head_estimate_baseline",
            "dust_attn_value_workspace", "dust_attn_value_estimate", "dust_attn_gate_workspace",
            "dust_attn_gate_estimate", "dust_issue_probe", "dust_head_chunked_workspace",
-           "dust_head_estimate_chunked")
+           "dust_head_estimate_chunked", "dust_es_perturb", "dust_es_estimate")
 BASELINE_MEAN, BASELINE_LEAVE_ONE_OUT, BASELINE_ANTITHETIC = 0, 1, 2
 
 
@@ -101,6 +101,8 @@ def lib():
         L.dust_attn_gate_estimate.argtypes = [_P, _P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _I64,
                                               DustNoise, _P, _P, _P, _SZ, _P]
         L.dust_issue_probe.argtypes = [ctypes.c_int, _I64, ctypes.POINTER(_I64), _P, _P]
+        L.dust_es_perturb.argtypes = [_P, _I64, DustNoise, _P, _P]
+        L.dust_es_estimate.argtypes = [_P, _I64, DustNoise, _P, _P]
         L.dust_head_chunked_workspace.argtypes = [_I64, _I64, _I64, _U32, _I64]
         L.dust_head_chunked_workspace.restype = _SZ
         L.dust_head_estimate_chunked.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64,
@@ -115,7 +117,7 @@ def lib():
                      "dust_sgd_step", "dust_adam_step", "dust_head_backprop",
                      "dust_head_estimate_baseline", "dust_attn_value_estimate",
                      "dust_attn_gate_estimate", "dust_issue_probe",
-                     "dust_head_estimate_chunked"):
+                     "dust_head_estimate_chunked", "dust_es_perturb", "dust_es_estimate"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -471,4 +473,26 @@ def head_estimate_chunked(logits, targets, x, sigma, K, seed, chunk, layer=0, dr
                                             _ptr(g), _ptr(G), _ptr(ws), ws.numel(),
                                             _stream(stream)))
     return g, G, ws
+
+
+# ------------------------------------------------------- weight-space ES ----
+def es_perturb(theta, sigma, K, seed, layer=9, draw0=0, token0=0, stream=None):
+    """K perturbed copies theta + sigma eps_i (K x n) of a small fp32 vector."""
+    _need_cuda(theta)
+    out = torch.empty((K, theta.numel()), dtype=torch.float32, device=theta.device)
+    _check("dust_es_perturb", lib().dust_es_perturb(_ptr(theta), theta.numel(),
+                                                    noise(seed, sigma, K, layer, draw0, token0),
+                                                    _ptr(out), _stream(stream)))
+    return out
+
+
+def es_estimate(losses, n, sigma, seed, layer=9, draw0=0, token0=0, stream=None):
+    """(1/(K sigma)) sum_i (L_i - mean L) eps_i from the K losses of the copies."""
+    _need_cuda(losses)
+    g = torch.empty(n, dtype=torch.float32, device=losses.device)
+    _check("dust_es_estimate", lib().dust_es_estimate(_ptr(losses), n,
+                                                      noise(seed, sigma, losses.numel(), layer,
+                                                            draw0, token0),
+                                                      _ptr(g), _stream(stream)))
+    return g
 

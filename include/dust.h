@@ -351,6 +351,27 @@ dust_status dust_attn_gate_estimate(const float* z, const float* o, const float*
                                     float* G_W, void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Weight-space ES for the residual-mixing scalars                           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The pages estimate every weight by perturbing activations except the 2L
+ * residual-mixing scalars (Dust translation §2.1); read plainly, those stay
+ * with weight-space ES.  The library supplies the population side, with the
+ * noise of the same counter scheme (parameter j as channel j of "token"
+ * nz.token0, draw nz.draw0 + i):
+ *   dust_es_perturb:  theta_out[i][j] = theta[j] + sigma eps_i[j]   (K x n)
+ *   dust_es_estimate: g[j] = (1/(K sigma)) sum_i (L_i - mean L) eps_i[j],
+ * an estimate of +dL/dtheta from the caller's K losses L (device, K fp32).
+ * theta, theta_out, losses and g are device fp32 arrays; 1 <= n <= 2^26,
+ * 2 <= K <= 2^20, sigma > 0; INVALID_ARG otherwise.  Asynchronous on stream.
+ */
+dust_status dust_es_perturb(const float* theta, int64_t n, dust_noise nz, float* theta_out,
+                            void* stream);
+dust_status dust_es_estimate(const float* losses, int64_t n, dust_noise nz, float* g,
+                             void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Using the estimate: optimiser step and the backprop reference             */
 /* ------------------------------------------------------------------------ */
 

@@ -29,7 +29,8 @@ from .attention import (attn_gate_delta_loss, attn_gate_estimate,  # noqa: F401
                         attn_value_delta_loss, attn_value_estimate)
 from .baselines import (head_estimate_antithetic, head_estimate_chunked,  # noqa: F401
                         head_estimate_leave_one_out)
-from .optim import adam_step, head_backprop, head_grad_rows, sgd_step  # noqa: F401
+from .optim import (adam_step, es_estimate, es_noise, head_backprop,  # noqa: F401
+                    head_grad_rows, sgd_step)
 
 _lib = None
 

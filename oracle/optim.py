@@ -72,3 +72,24 @@ def head_backprop(z, targets, x):
     g = head_grad_rows(z, targets)
     G = g.T @ np.asarray(x, np.float64)
     return {"g": g, "G": G}
+
+
+def es_noise(n, K, seed, layer, draw0=0, token0=0):
+    """eps_i[j], K x n: the oracle's normals with parameter j as channel j of
+    one token (the same counter scheme as the activation noise)."""
+    from . import noise
+    return np.stack([noise(seed, layer, draw0 + i, token0, 1, n)[0] for i in range(K)])
+
+
+def es_estimate(losses, n, sigma, seed, layer, draw0=0, token0=0):
+    """Weight-space ES for the residual-mixing scalars (hn.213312.xyz Dust
+    translation §2.1 leaves them out of the activation method):
+    g = (1/(K sigma)) sum_i (L_i - mean L) eps_i."""
+    L = np.asarray(losses, np.float64)
+    K = L.size
+    eps = es_noise(n, K, seed, layer, draw0, token0)
+    g = np.zeros(n)
+    for i in range(K):
+        g += (L[i] - L.mean()) * eps[i]
+    return g / (K * sigma)
+

@@ -146,3 +146,21 @@ def test_tuning_cosine_rises_with_population_and_sweep_picks_best(dust):
     # far too large a sigma leaves the linear regime: the cosine drops
     assert dict(rows)[3.0] < dict(rows)[0.05], rows
     parity(cos_K64=cos[0], cos_K1024=cos[1], cos_K16384=cos[2])
+
+
+def test_es_perturb_and_estimate_match_oracle(dust, orc):
+    n, K, sigma = 37, 24, 0.05
+    theta = torch.randn(n, generator=torch.Generator().manual_seed(2))
+    th = dust.es_perturb(theta.cuda(), sigma, K, 1234, layer=9, draw0=4)
+    torch.cuda.synchronize()
+    eps = orc.es_noise(n, K, 1234, 9, 4)
+    want = theta.double().numpy()[None] + float(np.float32(sigma)) * eps
+    assert np.abs(th.cpu().numpy() - want).max() <= 1e-6
+    w = torch.randn(n, generator=torch.Generator().manual_seed(3))
+    losses = (th.cpu().double() @ w.double()).float() + torch.linspace(0, 1e-3, K)
+    g = dust.es_estimate(losses.cuda(), n, sigma, 1234, layer=9, draw0=4)
+    torch.cuda.synchronize()
+    ref = orc.es_estimate(losses.numpy(), n, float(np.float32(sigma)), 1234, 9, 4)
+    e = rel_l2(g.cpu().numpy(), ref)
+    assert e <= 1e-4, e  # fp32 normals (within 5e-6) and sums, as for g elsewhere
+    parity(g_es=e)

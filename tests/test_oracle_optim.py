@@ -98,3 +98,30 @@ def test_head_backprop_matches_finite_differences():
             E[i, j] = h
             num[i, j] = (loss(Wh + E) - loss(Wh - E)) / (2 * h)
     np.testing.assert_allclose(G, num, rtol=1e-6, atol=1e-8)
+
+
+def test_es_estimate_on_a_linear_loss_is_the_sample_covariance_times_w():
+    # L(theta + sigma eps) - mean = sigma w.(eps_i - mean eps), so
+    # g = (1/K) sum_i (w.(eps_i - eps_bar)) eps_i = C w with the sample
+    # moment matrix C = (1/K) sum_i (eps_i - eps_bar) eps_i^T.
+    rng = np.random.default_rng(3)
+    n, K, sigma = 6, 40, 0.01
+    w = rng.standard_normal(n)
+    theta = rng.standard_normal(n)
+    eps = oracle.es_noise(n, K, 5, 9)
+    losses = (theta[None] + sigma * eps) @ w
+    C = ((eps - eps.mean(0)).T @ eps) / K
+    np.testing.assert_allclose(oracle.es_estimate(losses, n, sigma, 5, 9), C @ w, rtol=1e-10)
+
+
+def test_es_estimate_on_a_quadratic_tends_to_its_gradient():
+    # For L = theta^T A theta / 2, Gaussian smoothing leaves the gradient A theta.
+    rng = np.random.default_rng(4)
+    n, K, sigma = 3, 20000, 0.1
+    A = np.diag([1.0, 2.0, 3.0])
+    theta = rng.standard_normal(n)
+    th = theta[None] + sigma * oracle.es_noise(n, K, 6, 9)
+    losses = 0.5 * np.einsum("ki,ij,kj->k", th, A, th)
+    g = oracle.es_estimate(losses, n, sigma, 6, 9)
+    cos = g @ (A @ theta) / np.linalg.norm(g) / np.linalg.norm(A @ theta)
+    assert cos > 0.99, cos
