@@ -530,8 +530,7 @@ dust_status head_estimate(const float* logits, const int32_t* targets, const voi
             default: st = launch_draws<8, true>(P, A, keys, T, anti, s); break;
         }
     } else {
-        st = P.nb == 4 ? launch_draws<4, false>(P, A, keys, T, anti, s)
-                       : launch_draws<8, false>(P, A, keys, T, anti, s);
+        st = launch_draws<8, false>(P, A, keys, T, anti, s);  // head_plan: 8 blocks per thread
     }
     if (st != DUST_OK) return st;
     if (P.Q > 1) {
@@ -805,8 +804,7 @@ extern "C" dust_status dust_head_estimate_chunked(const float* logits, const int
                 default: st = launch_draws<8, true>(P.k, A, keys, T, false, s, true); break;
             }
         } else {
-            st = P.k.nb == 4 ? launch_draws<4, false>(P.k, A, keys, T, false, s, true)
-                             : launch_draws<8, false>(P.k, A, keys, T, false, s, true);
+            st = launch_draws<8, false>(P.k, A, keys, T, false, s, true);
         }
         if (st != DUST_OK) return st;
         if (P.k.Q > 1) {
