@@ -17,7 +17,8 @@ Delta e W_head^T) use numpy's float64 matmul as a library step; everything else
 is the C loops.  What consumes the estimate (the optimiser step, the exact head
 gradient it is compared with) is in optim.py; the head estimator with the
 leave-one-out and antithetic baselines in baselines.py; the value projection
-inside attention, scored by the attention-output error, in attention.py.
+inside attention, the gate, the queries and the keys, scored by the
+attention-output error, in attention.py.
 """
 import ctypes
 import os
@@ -25,8 +26,9 @@ import os
 import numpy as np
 
 from . import build as _build
-from .attention import (attn_gate_delta_loss, attn_gate_estimate,  # noqa: F401
-                        attn_value_delta_loss, attn_value_estimate)
+from .attention import (attn_forward, attn_gate_delta_loss, attn_gate_estimate,  # noqa: F401
+                        attn_qk_delta_loss, attn_qk_estimate, attn_value_delta_loss,
+                        attn_value_estimate)
 from .baselines import (head_estimate_antithetic, head_estimate_chunked,  # noqa: F401
                         head_estimate_leave_one_out)
 from .optim import (adam_step, es_estimate, es_noise, head_backprop,  # noqa: F401
