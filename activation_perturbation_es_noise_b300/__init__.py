@@ -30,7 +30,8 @@ EXPORTS = ("dust_status_string", "dust_abi_version", "dust_workspace_status",
            "dust_kernel_event_count", "dust_wait_selftest", "dust_sgd_step", "dust_adam_step",
            "dust_head_backprop_workspace", "dust_head_backprop", "dust_head_estimate_baseline",
            "dust_attn_value_workspace", "dust_attn_value_estimate", "dust_attn_gate_workspace",
-           "dust_attn_gate_estimate", "dust_issue_probe", "dust_head_chunked_workspace",
+           "dust_attn_gate_estimate", "dust_attn_qk_workspace", "dust_attn_qk_estimate",
+           "dust_issue_probe", "dust_head_chunked_workspace",
            "dust_head_estimate_chunked", "dust_es_perturb", "dust_es_estimate")
 BASELINE_MEAN, BASELINE_LEAVE_ONE_OUT, BASELINE_ANTITHETIC = 0, 1, 2
 
@@ -96,6 +97,11 @@ def lib():
         L.dust_attn_value_workspace.restype = _SZ
         L.dust_attn_value_estimate.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _I64,
                                                _I64, DustNoise, _P, _P, _P, _SZ, _P]
+        L.dust_attn_qk_workspace.argtypes = [_I64, _I64, _I64, _I64, _I64, _U32]
+        L.dust_attn_qk_workspace.restype = _SZ
+        L.dust_attn_qk_estimate.argtypes = [ctypes.c_int, _P, _P, _P, _P, _P, _P, _P,
+                                            ctypes.c_int, _I64, _I64, _I64, _I64, _I64,
+                                            DustNoise, _P, _P, _P, _SZ, _P]
         L.dust_attn_gate_workspace.argtypes = [_I64, _I64, _I64, _I64, _U32]
         L.dust_attn_gate_workspace.restype = _SZ
         L.dust_attn_gate_estimate.argtypes = [_P, _P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _I64,
@@ -116,7 +122,7 @@ def lib():
                      "dust_embed_scatter_static", "dust_philox_fill", "dust_gemm_bf16",
                      "dust_sgd_step", "dust_adam_step", "dust_head_backprop",
                      "dust_head_estimate_baseline", "dust_attn_value_estimate",
-                     "dust_attn_gate_estimate", "dust_issue_probe",
+                     "dust_attn_gate_estimate", "dust_attn_qk_estimate", "dust_issue_probe",
                      "dust_head_estimate_chunked", "dust_es_perturb", "dust_es_estimate"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -427,6 +433,43 @@ def attn_gate_estimate(z, o, E, x, seq_len, sigma, gamma, K, seed, layer=3, draw
            lib().dust_attn_gate_estimate(_ptr(z), _ptr(o), _ptr(E), _ptr(x), xdt, T, seq_len, C,
                                          d_in, noise(seed, sigma, K, layer, draw0, token0, gamma),
                                          _ptr(g), _ptr(G), _ptr(ws), ws.numel(), _stream(stream)))
+    return g, G, ws
+
+
+def attn_qk_estimate(which, Q, Kk, V, O, P, E, x, seq_len, sigma, gamma, K, seed, layer=None,
+                     draw0=0, token0=0, want_g=True, out=None, ws=None, stream=None):
+    """Query (which 0) or key (which 1) projection of a causal softmax
+    attention layer, scored by the attention-output error E.  Q, Kk, V, O, E:
+    T x H*64 fp32 (the clean forward and the error); P: (T/seq_len, H,
+    seq_len, seq_len) fp32, the clean probabilities.  The noise layer defaults
+    to 4 (queries) or 5 (keys).  Returns (g_hat or None, G_W, ws)."""
+    _need_cuda(Q, Kk, V, O, P, E, x)
+    if which not in (0, 1):
+        raise ValueError("which is 0 (queries) or 1 (keys)")
+    if layer is None:
+        layer = 4 + which
+    nseq, H, L, L2 = P.shape
+    T, C = Q.shape
+    if L != seq_len or L2 != seq_len or nseq * L != T or C != H * 64:
+        raise ValueError("P must be (T/seq_len, H, seq_len, seq_len) and Q T x H*64")
+    for t in (Kk, V, O, E):
+        if tuple(t.shape) != (T, C):
+            raise ValueError("Kk, V, O and E must have Q's shape")
+    d_in = x.shape[1]
+    dev = Q.device
+    if out is None:
+        g = torch.empty((T, C), dtype=torch.float32, device=dev) if want_g else None
+        G = torch.empty((C, d_in), dtype=torch.float32, device=dev)
+    else:
+        g, G = out
+    if ws is None:
+        ws = _workspace(lib().dust_attn_qk_workspace(T, seq_len, H, 64, d_in, K), dev)
+    xdt = DUST_BF16 if x.dtype == torch.bfloat16 else DUST_F32
+    _check("dust_attn_qk_estimate",
+           lib().dust_attn_qk_estimate(which, _ptr(Q), _ptr(Kk), _ptr(V), _ptr(O), _ptr(P),
+                                       _ptr(E), _ptr(x), xdt, T, seq_len, H, 64, d_in,
+                                       noise(seed, sigma, K, layer, draw0, token0, gamma),
+                                       _ptr(g), _ptr(G), _ptr(ws), ws.numel(), _stream(stream)))
     return g, G, ws
 
 

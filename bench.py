@@ -15,7 +15,8 @@ are larger than the 126 MB L2, so no flush is needed between steps.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dust|reference]
                   [--workload head_batch|head_batch_antithetic|head_batch_chunked|head_tiny|
                               head_scale|interior|
-                              interior_scale|embed_scale|head_sweep|optim_adam|attn_value]
+                              interior_scale|embed_scale|head_sweep|optim_adam|attn_value|
+                              attn_qk]
 
 Under torchrun (N > 1) every rank estimates its own batch (global token
 offset rank * T, so the noise differs per rank) with no collective on the data
@@ -513,6 +514,81 @@ def run_attn_value(args):
     return 0
 
 
+def run_attn_qk(args):
+    """The query projection inside attention (which 0; 8 x 2048 tokens, 8
+    heads of 64, d_in 512, K = 64, gamma 0.99), inputs resident: token-evals/s,
+    and the perturbed-score kernel against the fp32 FMA rate of the CUDA cores
+    (148 SMs x 128 lanes x 2 flops x the maximum SM clock), counting 2 x 64
+    fused multiply-adds per causal (query, key) pair and draw: the score shift
+    <a_s, k_t> and the weighted value sum."""
+    import torch
+
+    import activation_perturbation_es_noise_b300 as dust
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    c = ATTN
+    nseq, H, L, K = c["nseq"], c["H"], c["L"], c["K"]
+    T, C = nseq * L, H * 64
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(22)
+    Q, Kk, V = (torch.randn((T, C), generator=gen, device=dev) for _ in range(3))
+    q4, k4, v4 = (t.view(nseq, L, H, 64).transpose(1, 2) for t in (Q, Kk, V))
+    s = (q4 @ k4.transpose(-1, -2)) / 8.0
+    s = s.masked_fill(torch.triu(torch.ones(L, L, dtype=torch.bool, device=dev), 1), -1e30)
+    P = torch.softmax(s, dim=-1).contiguous()
+    del s
+    O = (P @ v4).transpose(1, 2).reshape(T, C).contiguous()
+    E = torch.randn((T, C), generator=gen, device=dev) * 0.1
+    x = torch.randn((T, c["d_in"]), generator=gen, device=dev).to(torch.bfloat16)
+    g = torch.empty((T, C), dtype=torch.float32, device=dev)
+    G = torch.empty((C, c["d_in"]), dtype=torch.float32, device=dev)
+    ws = dust._workspace(dust.lib().dust_attn_qk_workspace(T, L, H, 64, c["d_in"], K), dev)
+
+    def step():
+        dust.attn_qk_estimate(0, Q, Kk, V, O, P, E, x, L, c["sigma"], c["gamma"], K, 1234,
+                              out=(g, G), ws=ws)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clocks:
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        e1.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    timer = dust.KernelTimer(capacity=args.steps + 1)
+    with timer:
+        torch.cuda._sleep(1_000_000 * args.steps)
+        for _ in range(args.steps):
+            step()
+    torch.cuda.synchronize()
+    kernel_ms = timer.total_ms() / args.steps
+    pairs = nseq * H * L * (L + 1) // 2
+    flops = 2.0 * 2 * 64 * pairs * K
+    peaks, which = _peaks()
+    mhz = peaks.get("sm_max_mhz", SM_MAX_MHZ)
+    peak = N_SM * 128 * 2 * mhz * 1e6 / 1e12
+    ach = flops / (kernel_ms * 1e-3) / 1e12
+    print(json.dumps({
+        "metric": METRIC, "value": K * T / (ms * 1e-3), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "attn_qk", "which": "queries", "tokens": T, "draws": K,
+                   "heads": H, "dv": 64, "d_in": c["d_in"], "seq_len": L, "sigma": c["sigma"],
+                   "gamma": c["gamma"], "l2": "inputs larger than L2 (no flush)"},
+        "roofline": {"bound": "alu", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                     "frac": ach / peak, "traffic": load_traffic({"name": "attn_qk"}),
+                     "kernel": "attn_qk_kernel", "kernel_ms": kernel_ms,
+                     "peak_source": "fp32 FMA: 148 SMs x 128 lanes x 2 x %.0f MHz (%s clocks)"
+                     % (mhz, which)},
+        "cpu_baseline": None, "e2e": None, "gpu_launches": args.steps * 5,
+        "clocks": clocks.summary()}), flush=True)
+    return 0
+
+
 def run_head_sweep(args):
     """The tiny head workload at K = 64 .. 16384: token-evals/s per K and the
     cosine of G_W with the analytic head gradient sum_t (softmax(z_t) -
@@ -807,7 +883,7 @@ def main():
                              "head_tiny", "head_scale",
                              "interior",
                              "interior_scale", "embed_scale", "head_sweep", "optim_adam",
-                             "attn_value"])
+                             "attn_value", "attn_qk"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
@@ -821,6 +897,8 @@ def main():
         return run_optim(args)
     if args.workload == "attn_value":
         return run_attn_value(args)
+    if args.workload == "attn_qk":
+        return run_attn_qk(args)
     return run_dust(args)
 
 

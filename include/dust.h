@@ -350,6 +350,50 @@ dust_status dust_attn_gate_estimate(const float* z, const float* o, const float*
                                     int64_t C, int64_t d_in, dust_noise nz, float* g_hat,
                                     float* G_W, void* ws, size_t ws_bytes, void* stream);
 
+/* Workspace bytes for dust_attn_qk_estimate with these sizes (0 if invalid). */
+size_t dust_attn_qk_workspace(int64_t T, int64_t seq_len, int64_t H, int64_t dv, int64_t d_in,
+                              uint32_t K);
+
+/*
+ * Estimator for the query projection (which = 0) or the key projection
+ * (which = 1) of a causal softmax attention layer, perturbed per token inside
+ * the attention and scored like the values by the attention-output error
+ * (Dust translation §2.3).  Perturbing every query by sigma a_s (or every key
+ * by sigma a_t) moves the scores by ds_{s,t} = sigma <a_s, k_t> / sqrt(dv)
+ * (or sigma <q_s, a_t> / sqrt(dv)); with the cached clean probabilities P and
+ * output O the perturbed output of token s is, exactly,
+ *   dO_s = (sum_{t<=s} w_{s,t} v_t - W_s o_s) / (1 + W_s),
+ *   w_{s,t} = P_{s,t} (exp(ds_{s,t}) - 1),   W_s = sum_{t<=s} w_{s,t},
+ * since the perturbed softmax row is P e^{ds} / sum P e^{ds}.  Then
+ * dl_s = <E_s, dO_s> over all heads, and the same centring, gamma-scan, g and
+ * G_W = g^T x as the values.
+ *
+ *   which  0 queries, 1 keys.
+ *   Q, Kk, V, O, E  device fp32, T x (H dv) (Q, Kk, V, O 16-byte aligned): the clean
+ *          queries, keys and values, the clean attention output (head h in
+ *          columns h dv .. h dv + dv - 1) and its error estimate.
+ *   P      device fp32, (T/seq_len) x H x seq_len x seq_len, the clean
+ *          probabilities of the same forward (row s = query, column t = key;
+ *          entries with t > s are not read).  P and O must come from Q, Kk and
+ *          V (rows of P summing to 1, O = P V): the formula above uses both.
+ *   x      device, T x d_in (x_dtype): the input of W_q (or W_k).
+ *   g_hat  T x (H dv) fp32 or NULL: the estimate for the queries (keys).
+ *   G_W    (H dv) x d_in fp32 (g and x rounded to bf16, fp32 accumulation).
+ *   nz     noise of channel c of token t, draw i: the Philox counter
+ *          (c/4, token0 + t, draw0 + i, layer), as for the other estimators.
+ * Limits: dv = 64, seq_len a multiple of 128 (<= 8192), T a multiple of
+ * seq_len, 1 <= H <= 64, T/seq_len <= 65535, 2 <= K <= 65535.  The
+ * perturbed scores are computed on the CUDA cores in fp32 (one thread per
+ * query row, keys and values staged in shared memory, heads summed in order);
+ * the workspace (from dust_attn_qk_workspace) holds the loss changes, the
+ * credits and the bf16 copies for the outer product.
+ */
+dust_status dust_attn_qk_estimate(int which, const float* Q, const float* Kk, const float* V,
+                                  const float* O, const float* P, const float* E, const void* x,
+                                  dust_dtype x_dtype, int64_t T, int64_t seq_len, int64_t H,
+                                  int64_t dv, int64_t d_in, dust_noise nz, float* g_hat,
+                                  float* G_W, void* ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Weight-space ES for the residual-mixing scalars                           */
 /* ------------------------------------------------------------------------ */
