@@ -20,10 +20,14 @@
 // its 64 scaled noise values (queries) or its scaled query (keys) and its 64
 // accumulators in registers; 32-key tiles of the clean keys (or the keys'
 // noise) and of the values are staged in shared memory and read as
-// broadcasts.  A CTA covers one tile of 128 queries of one sequence for one
+// broadcasts; the matching 128 x 32 tile of P is staged too (coalesced rows,
+// padded against bank conflicts) so that no thread reads its own P row from
+// global memory.  A CTA covers one tile of 128 queries of one sequence for one
 // draw and walks the heads in order, so the per-token sum over heads needs no
-// second pass.  The per-pair work, 2 x 64 fused multiply-adds and one e^x - 1,
-// is the kernel's roofline.
+// second pass.  The draws are the fastest grid index: the CTAs resident at one
+// time share their sequence, query tile and head, and P, K and V come from L2
+// after the first of them.  The per-pair work, 2 x 64 fused multiply-adds and
+// one e^x - 1, is the kernel's roofline.
 #include "dust_common.cuh"
 #include "internal.h"
 #include "noise.cuh"
@@ -62,17 +66,19 @@ __device__ __forceinline__ float expm1_shift(float x) {
     return expm1f(x);
 }
 
-// grid: (query tiles of 128, sequences, draws); block: 128 threads.
+// grid: (draws, query tiles x sequences, heaviest tiles first); block: 128 threads.
 // KEYS: the staged tiles carry the keys' noise and the thread holds its query;
 // otherwise the thread holds its query's noise and the tiles the clean keys.
 template <bool KEYS>
 __global__ void __launch_bounds__(kQKRows) attn_qk_kernel(const QKArgs a, const PhiloxKeys keys) {
     __shared__ __align__(16) float kt[kQKKeys][kHd];
     __shared__ __align__(16) float vt[kQKKeys][kHd];
+    __shared__ float pt[kQKRows][kQKKeys + 1];
     const int r = threadIdx.x;
-    const int qb = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);  // heavy first
-    const int sq = blockIdx.y;
-    const int i = blockIdx.z;
+    const int nseq = a.T / a.L;
+    const int qb = a.L / kQKRows - 1 - static_cast<int>(blockIdx.y) / nseq;  // heavy first
+    const int sq = static_cast<int>(blockIdx.y) % nseq;
+    const int i = blockIdx.x;
     const uint32_t draw = a.draw0 + static_cast<uint32_t>(i);
     const int s = qb * kQKRows + r;                          // query position in its sequence
     const int64_t tg = static_cast<int64_t>(sq) * a.L + s;   // token
@@ -108,7 +114,8 @@ __global__ void __launch_bounds__(kQKRows) attn_qk_kernel(const QKArgs a, const 
 #pragma unroll
         for (int c = 0; c < kHd; ++c) acc[c] = 0.f;
         float wsum = 0.f;
-        const float* prow = a.P + ((static_cast<int64_t>(sq) * a.H + h) * a.L + s) * a.L;
+        // row qb 128 of this (sequence, head)'s probabilities
+        const float* ptile = a.P + ((static_cast<int64_t>(sq) * a.H + h) * a.L + qb * kQKRows) * a.L;
 
         for (int k0 = 0; k0 < kend; k0 += kQKKeys) {
             __syncthreads();  // the previous tile (or head) is no longer read
@@ -126,6 +133,15 @@ __global__ void __launch_bounds__(kQKRows) attn_qk_kernel(const QKArgs a, const 
                 *reinterpret_cast<float4*>(&vt[kk][4 * jb]) = v4;
                 *reinterpret_cast<float4*>(&kt[kk][4 * jb]) = k4;
             }
+            for (int e = r; e < kQKRows * (kQKKeys / 4); e += kQKRows) {
+                const int row = e / (kQKKeys / 4), q4 = e % (kQKKeys / 4);
+                const float4 p4 = __ldg(reinterpret_cast<const float4*>(
+                    ptile + static_cast<int64_t>(row) * a.L + k0 + 4 * q4));
+                pt[row][4 * q4] = p4.x;
+                pt[row][4 * q4 + 1] = p4.y;
+                pt[row][4 * q4 + 2] = p4.z;
+                pt[row][4 * q4 + 3] = p4.w;
+            }
             __syncthreads();
             const int tmax = min(kQKKeys, s - k0 + 1);  // causal: keys t <= s
             for (int kk = 0; kk < tmax; ++kk) {
@@ -133,7 +149,7 @@ __global__ void __launch_bounds__(kQKRows) attn_qk_kernel(const QKArgs a, const 
 #pragma unroll
                 for (int c = 0; c < kHd; ++c) d4[c & 3] = fmaf(qa[c], kt[kk][c], d4[c & 3]);
                 const float ds = (d4[0] + d4[1]) + (d4[2] + d4[3]);
-                const float w = __ldg(prow + k0 + kk) * expm1_shift(ds);
+                const float w = pt[r][kk] * expm1_shift(ds);
                 wsum += w;
 #pragma unroll
                 for (int c = 0; c < kHd; ++c) acc[c] = fmaf(w, vt[kk][c], acc[c]);
@@ -193,14 +209,14 @@ extern "C" dust_status dust_attn_qk_estimate(int which, const float* Q, const fl
     if (x_dtype != DUST_F32 && x_dtype != DUST_BF16) return DUST_ERR_INVALID_ARG;
     if (nz.num_draws < 2 || !(nz.sigma > 0.0f) || !(nz.sigma < INFINITY)) return DUST_ERR_INVALID_ARG;
     if (!(nz.gamma >= 0.0f && nz.gamma <= 1.0f)) return DUST_ERR_INVALID_ARG;
-    if (dv != kHd || seq_len % kQKRows != 0 || seq_len > 8192 || H > 64 || T / seq_len > 65535 ||
-        nz.num_draws > 65535 || T > (1LL << 26) || d_in > (1LL << 20))
+    if (dv != kHd || seq_len % kQKRows != 0 || seq_len > 8192 || H > 64 || T / kQKRows > 65535 ||
+        nz.num_draws > 65535 || d_in > (1LL << 20))
         return DUST_ERR_UNSUPPORTED;
     if (static_cast<uint64_t>(nz.token0) + static_cast<uint64_t>(T) > (1ULL << 32) ||
         static_cast<uint64_t>(nz.draw0) + nz.num_draws > (1ULL << 32))
         return DUST_ERR_INVALID_ARG;
     if (!aligned(Q, 16) || !aligned(Kk, 16) || !aligned(V, 16) || !aligned(O, 16) ||
-        !aligned(P, 4) || !aligned(E, 4) || (g_hat && !aligned(g_hat, 16)))
+        !aligned(P, 16) || !aligned(E, 4) || (g_hat && !aligned(g_hat, 16)))
         return DUST_ERR_INVALID_ARG;
     const QKPlan Pl = qk_plan(T, H, d_in, nz.num_draws);
     if (!ws || ws_bytes < Pl.bytes || !aligned(ws, 256)) return DUST_ERR_WORKSPACE;
@@ -217,8 +233,7 @@ extern "C" dust_status dust_attn_qk_estimate(int which, const float* Q, const fl
 
     const QKArgs qa{Q, Kk, V, O, P, E, dl, static_cast<int>(T), static_cast<int>(seq_len),
                     static_cast<int>(H), nz.draw0, nz.token0, nz.layer, nz.sigma * 0.125f};
-    const dim3 grid(static_cast<unsigned>(seq_len / kQKRows), static_cast<unsigned>(T / seq_len),
-                    nz.num_draws);
+    const dim3 grid(nz.num_draws, static_cast<unsigned>(T / kQKRows));
     timer_begin(s);
     if (which == 1)
         attn_qk_kernel<true><<<grid, kQKRows, 0, s>>>(qa, keys);
