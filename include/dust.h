@@ -369,7 +369,7 @@ size_t dust_attn_qk_workspace(int64_t T, int64_t seq_len, int64_t H, int64_t dv,
  * G_W = g^T x as the values.
  *
  *   which  0 queries, 1 keys.
- *   Q, Kk, V, O, E  device fp32, T x (H dv) (Q, Kk, V, O 16-byte aligned): the clean
+ *   Q, Kk, V, O, E  device fp32, T x (H dv), 16-byte aligned: the clean
  *          queries, keys and values, the clean attention output (head h in
  *          columns h dv .. h dv + dv - 1) and its error estimate.
  *   P      device fp32, (T/seq_len) x H x seq_len x seq_len, the clean
@@ -382,9 +382,9 @@ size_t dust_attn_qk_workspace(int64_t T, int64_t seq_len, int64_t H, int64_t dv,
  *   nz     noise of channel c of token t, draw i: the Philox counter
  *          (c/4, token0 + t, draw0 + i, layer), as for the other estimators.
  * Limits: dv = 64, seq_len a multiple of 128 (<= 8192), T a multiple of
- * seq_len, 1 <= H <= 64, T/seq_len <= 65535, 2 <= K <= 65535.  The
- * perturbed scores are computed on the CUDA cores in fp32 (one thread per
- * query row, keys and values staged in shared memory, heads summed in order);
+ * seq_len, 1 <= H <= 64, T/128 <= 65535, 2 <= K <= 65535.  The perturbed
+ * scores are computed on the CUDA cores in fp32 (per 128-query tile and
+ * 32-key tile, register-blocked score and value products, heads summed in order);
  * the workspace (from dust_attn_qk_workspace) holds the loss changes, the
  * credits and the bf16 copies for the outer product.
  */
