@@ -27,11 +27,18 @@
 // time share their sequence, query tile and head, and P, K and V come from L2
 // after the first of them.  The per-pair work, 2 x 64 fused multiply-adds and
 // one e^x - 1, is the kernel's roofline.
+#include <algorithm>
+#include <cudaTypedefs.h>
+
 #include "dust_common.cuh"
 #include "internal.h"
 #include "noise.cuh"
 
 namespace dust {
+
+bool encode_bf16_2d(CUtensorMap* map, const void* ptr, int64_t inner, int64_t outer,
+                    int64_t stride_elems, uint32_t box_inner, uint32_t box_outer);
+
 namespace {
 
 constexpr int kHd = 64;       // channels per head
@@ -265,9 +272,405 @@ __global__ void __launch_bounds__(kQKThreads, 3) attn_qk_kernel(const QKArgs a, 
 
 std::atomic<uint64_t> qk_smem_set[2];
 
+// ------------------------------------------------------------------------
+// The queries on the tensor cores.  The same two products per key slice, now
+// 64 keys wide, as split-bf16 tcgen05 MMAs (hi.hi + hi.lo + lo.hi, fp32
+// accumulation in tensor memory):
+//   ds[128 x 64] = A[128 x 64 ch] K_slice^T,   A = (sigma / 8) x the queries' noise
+//   acc[128 x 64 ch] += W[128 x 64] V_slice,   W = P (e^ds - 1), causal,
+// with the exponential, P and the causal mask on the CUDA cores in between.
+// Warp 0 brings each slice's K ([hi | lo], keys x channels) and V^T ([hi |
+// lo], channels x keys) by TMA, warp 1 issues the MMAs, warps 2..17 (four per
+// tensor-memory lane quarter, 16 keys or channels each) generate A per head,
+// turn each ds slice into W in shared memory, and reduce acc against E at the
+// end of a head.  ds has two tensor-memory buffers and W two shared-memory
+// buffers, so the next slice's score product runs while this one's W is
+// formed.  Every wait is bounded; on a timeout the roles stop and the status
+// word records it.
+// ------------------------------------------------------------------------
+constexpr int kTcKeys = 64;                  // keys per slice
+constexpr int kTcGroups = 4;                 // epilogue warps per lane quarter
+constexpr int kTcCols = 64 / kTcGroups;      // keys (channels) per epilogue thread
+constexpr int kTcEpi = 128 * kTcGroups;
+constexpr int kTcThreads = 64 + kTcEpi;      // TMA, MMA, epilogue
+constexpr uint32_t kT8 = 64u * 128u;         // 64 rows x 128 bytes
+constexpr uint32_t kT16 = 128u * 128u;       // 128 rows x 128 bytes
+constexpr uint32_t kTcStage = 4u * kT8;      // K_hi, K_lo, Vt_hi, Vt_lo
+constexpr uint32_t kTcOffA = 2u * kTcStage;  // A_hi, A_lo
+constexpr uint32_t kTcOffW = kTcOffA + 2u * kT16;  // W[2] = {hi, lo} each
+constexpr uint32_t kTcOffBar = kTcOffW + 4u * kT16;
+constexpr uint32_t kTcSmem = kTcOffBar + 256u + 1024u;
+
+struct QKTcArgs {
+    const float* P;
+    const float* O;
+    const float* E;
+    float* dl;
+    int T, L, H;
+    uint32_t draw0, token0, layer;
+    float scale;
+    uint32_t* status;
+};
+
+__device__ __forceinline__ void tc_fence_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void epi_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kTcEpi) : "memory");
+}
+// True on every epilogue thread iff `ok` holds on all of them.
+__device__ __forceinline__ bool epi_all(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n"
+        " bar.red.and.pred p, 2, %2, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(r)
+        : "r"(ok ? 1u : 0u), "n"(kTcEpi)
+        : "memory");
+    return r != 0;
+}
+// 32 lanes x 16 consecutive 32-bit columns of tensor memory.
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ uint32_t bf16_pair(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+// hi and lo bf16 pairs of (a, b): hi = bf16(x), lo = bf16(x - hi).
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = bf16_pair(a - __low2float(h), b - __high2float(h));
+}
+// Byte offset of the 16-byte chunk c of row r in a 128-byte-swizzled K-major tile.
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+    return static_cast<uint32_t>(r) * 128u + ((static_cast<uint32_t>(c ^ (r & 7)) & 7u) << 4);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    attn_q_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                     const QKTcArgs a, const PhiloxKeys keys) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ float s_w[2][kTcGroups][kQKRows];  // row sums of w per head parity and key group
+    __shared__ float s_dl[kTcGroups][kQKRows];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* base_gen = smem_raw + (base - raw);
+    const uint32_t bars = base + kTcOffBar;
+    auto kv_full = [&](int s) { return bars + 8u * s; };
+    auto kv_empty = [&](int s) { return bars + 16u + 8u * s; };
+    auto ds_full = [&](int b) { return bars + 32u + 8u * b; };
+    auto ds_empty = [&](int b) { return bars + 48u + 8u * b; };
+    auto w_full = [&](int b) { return bars + 64u + 8u * b; };
+    auto w_empty = [&](int b) { return bars + 80u + 8u * b; };
+    const uint32_t a_full = bars + 96u, acc_full = bars + 104u, acc_empty = bars + 112u;
+    const uint32_t tmem_slot = bars + 120u;
+    volatile uint32_t* tmem_slot_gen =
+        reinterpret_cast<volatile uint32_t*>(base_gen + (tmem_slot - base));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nseq = a.T / a.L;
+    const int qb = a.L / kQKRows - 1 - static_cast<int>(blockIdx.y) / nseq;  // heavy first
+    const int sq = static_cast<int>(blockIdx.y) % nseq;
+    const int i = blockIdx.x;
+    const uint32_t draw = a.draw0 + static_cast<uint32_t>(i);
+    const int ns = (qb + 1) * (kQKRows / kTcKeys);  // key slices per head
+    const int64_t tok0 = static_cast<int64_t>(sq) * a.L + qb * kQKRows;
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(kv_full(b), 1);
+            mbar_init(kv_empty(b), 1);
+            mbar_init(ds_full(b), 1);
+            mbar_init(ds_empty(b), kTcEpi);
+            mbar_init(w_full(b), kTcEpi);
+            mbar_init(w_empty(b), 1);
+        }
+        mbar_init(a_full, kTcEpi);
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, kTcEpi);
+        mbar_fence_init();
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot_gen;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            bool ok = true;
+            for (int h = 0, g = 0; h < a.H && ok; ++h) {
+                for (int j = 0; j < ns; ++j, ++g) {
+                    const int st = g & 1;
+                    if (g >= 2 && !mbar_wait(kv_empty(st), ((g >> 1) & 1) ^ 1u, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = base + st * kTcStage;
+                    const int key0 = j * kTcKeys;
+                    mbar_arrive_expect_tx(kv_full(st), kTcStage);
+                    const int C = a.H * kHd;
+                    tma_load_2d(dst, &tk, h * kHd, sq * a.L + key0, kv_full(st));               // K_hi
+                    tma_load_2d(dst + kT8, &tk, C + h * kHd, sq * a.L + key0, kv_full(st));     // K_lo
+                    tma_load_2d(dst + 2 * kT8, &tv, key0, (sq * a.H + h) * kHd, kv_full(st));   // Vt_hi
+                    tma_load_2d(dst + 3 * kT8, &tv, a.L + key0, (sq * a.H + h) * kHd,          // Vt_lo
+                                kv_full(st));
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kQKRows, kTcKeys, false, false);
+            const uint32_t a_hi = base + kTcOffA, a_lo = a_hi + kT16;
+            bool ok = true;
+            // score product of slice g into ds buffer g & 1
+            auto g1 = [&](int g) -> bool {
+                const int st = g & 1;
+                if (!mbar_wait(kv_full(st), (g >> 1) & 1, a.status)) return false;
+                if (g >= 2 && !mbar_wait(ds_empty(st), ((g >> 1) & 1) ^ 1u, a.status)) return false;
+                tc_fence_after();
+                const uint32_t kh = base + st * kTcStage, kl = kh + kT8;
+                const uint32_t d = tmem + kTcKeys * st;
+#pragma unroll
+                for (int kk = 0; kk < kHd / 16; ++kk) {
+                    const uint64_t ah = sdesc_sw128(a_hi + kk * 32u, 16u, 1024u);
+                    const uint64_t al = sdesc_sw128(a_lo + kk * 32u, 16u, 1024u);
+                    const uint64_t bh = sdesc_sw128(kh + kk * 32u, 16u, 1024u);
+                    const uint64_t bl = sdesc_sw128(kl + kk * 32u, 16u, 1024u);
+                    umma_bf16(d, ah, bh, idesc, kk != 0 ? 1u : 0u);
+                    umma_bf16(d, ah, bl, idesc, 1u);
+                    umma_bf16(d, al, bh, idesc, 1u);
+                }
+                umma_commit(ds_full(st));
+                return true;
+            };
+            // value product of slice g (j-th of its head) into acc
+            auto g2 = [&](int g, int j) -> bool {
+                const int st = g & 1;
+                if (!mbar_wait(w_full(st), (g >> 1) & 1, a.status)) return false;
+                tc_fence_after();
+                const uint32_t wh = base + kTcOffW + st * 2u * kT16, wl = wh + kT16;
+                const uint32_t vh = base + st * kTcStage + 2 * kT8, vl = vh + kT8;
+#pragma unroll
+                for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+                    const uint64_t ah = sdesc_sw128(wh + kk * 32u, 16u, 1024u);
+                    const uint64_t al = sdesc_sw128(wl + kk * 32u, 16u, 1024u);
+                    const uint64_t bh = sdesc_sw128(vh + kk * 32u, 16u, 1024u);
+                    const uint64_t bl = sdesc_sw128(vl + kk * 32u, 16u, 1024u);
+                    umma_bf16(tmem + 128, ah, bh, idesc, (j | kk) != 0 ? 1u : 0u);
+                    umma_bf16(tmem + 128, ah, bl, idesc, 1u);
+                    umma_bf16(tmem + 128, al, bh, idesc, 1u);
+                }
+                umma_commit(w_empty(st));
+                umma_commit(kv_empty(st));
+                return true;
+            };
+            for (int h = 0, g0 = 0; h < a.H && ok; ++h, g0 += ns) {
+                if (!mbar_wait(a_full, h & 1, a.status)) break;
+                tc_fence_after();
+                ok = g1(g0);
+                for (int j = 0; j < ns && ok; ++j) {
+                    if (j + 1 < ns) ok = g1(g0 + j + 1);
+                    if (ok && j == 0 && h > 0) {
+                        ok = mbar_wait(acc_empty, (h - 1) & 1, a.status);
+                        tc_fence_after();
+                    }
+                    if (ok) ok = g2(g0 + j, j);
+                }
+                if (ok) umma_commit(acc_full);
+            }
+        }
+    } else {
+        const int e = threadIdx.x - 64;
+        const int quarter = warp & 3;           // tensor-memory lane quarter
+        const int grp = e >> 7;                 // keys (channels) kTcCols grp .. + kTcCols - 1
+        const int row = quarter * 32 + lane;    // query row in the tile
+        const int s = qb * kQKRows + row;       // its position in the sequence
+        const int C = a.H * kHd;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t a_hi = base + kTcOffA, a_lo = a_hi + kT16;
+        const DrawHalf dh = philox_draw_half(draw, a.token0 + static_cast<uint32_t>(tok0 + row), keys);
+        bool ok = true;
+        float dl = 0.f;
+        for (int h = 0, g = 0; h < a.H; ++h) {
+            // A for this head: the row's channels kTcCols grp .. + kTcCols - 1, scaled and split
+            if (ok) {
+#pragma unroll
+                for (int m = 0; m < kTcCols / 8; ++m) {  // 16-byte chunk: 8 channels
+                    const int c8 = (kTcCols / 8) * grp + m;
+                    const int jb = h * (kHd / 4) + 2 * c8;
+                    const float4 n0 = words_to_normals(
+                        philox_rest(dh, philox_block_half(static_cast<uint32_t>(jb), a.layer, keys), keys));
+                    const float4 n1 = words_to_normals(philox_rest(
+                        dh, philox_block_half(static_cast<uint32_t>(jb + 1), a.layer, keys), keys));
+                    uint32_t hi[4], lo[4];
+                    split_pair(a.scale * n0.x, a.scale * n0.y, hi[0], lo[0]);
+                    split_pair(a.scale * n0.z, a.scale * n0.w, hi[1], lo[1]);
+                    split_pair(a.scale * n1.x, a.scale * n1.y, hi[2], lo[2]);
+                    split_pair(a.scale * n1.z, a.scale * n1.w, hi[3], lo[3]);
+                    const uint32_t off = sw128(row, c8);
+                    st_shared_v4(a_hi + off, hi[0], hi[1], hi[2], hi[3]);
+                    st_shared_v4(a_lo + off, lo[0], lo[1], lo[2], lo[3]);
+                }
+                tc_fence_async_shared();
+            }
+            mbar_arrive(a_full);
+            float wsum = 0.f;
+            const float* prow =
+                a.P + ((static_cast<int64_t>(sq) * a.H + h) * a.L + s) * a.L + kTcCols * grp;
+            for (int j = 0; j < ns; ++j, ++g) {
+                const int st = g & 1;
+                const int k0 = j * kTcKeys + kTcCols * grp;  // this thread's first key
+                if (!ok) continue;
+                float4 pv[kTcCols / 4];
+#pragma unroll
+                for (int q = 0; q < kTcCols / 4; ++q)
+                    pv[q] = __ldg(reinterpret_cast<const float4*>(prow + j * kTcKeys) + q);
+                ok = mbar_wait(ds_full(st), (g >> 1) & 1, a.status);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) continue;
+                tc_fence_after();
+                uint32_t r[kTcCols];
+                tmem_ld_32x32b_x16(tmem + lane_off + kTcKeys * st + kTcCols * grp, r);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(ds_empty(st));
+                float w[kTcCols];
+#pragma unroll
+                for (int q = 0; q < kTcCols / 4; ++q) {
+                    const float pr[4] = {pv[q].x, pv[q].y, pv[q].z, pv[q].w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int t = k0 + 4 * q + u;
+                        const float x = t <= s ? pr[u] * expm1_shift(__uint_as_float(r[4 * q + u])) : 0.f;
+                        w[4 * q + u] = x;
+                        wsum += x;
+                    }
+                }
+                if (g >= 2) {
+                    ok = mbar_wait(w_empty(st), ((g >> 1) & 1) ^ 1u, a.status);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) continue;
+                }
+                const uint32_t wh = base + kTcOffW + st * 2u * kT16, wl = wh + kT16;
+#pragma unroll
+                for (int m = 0; m < kTcCols / 8; ++m) {
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) split_pair(w[8 * m + 2 * u], w[8 * m + 2 * u + 1], hi[u], lo[u]);
+                    const uint32_t off = sw128(row, (kTcCols / 8) * grp + m);
+                    st_shared_v4(wh + off, hi[0], hi[1], hi[2], hi[3]);
+                    st_shared_v4(wl + off, lo[0], lo[1], lo[2], lo[3]);
+                }
+                tc_fence_async_shared();
+                mbar_arrive(w_full(st));
+            }
+            // end of the head: W_s, then <E, dO> over this thread's channels
+            s_w[h & 1][grp][row] = wsum;
+            ok = epi_all(ok);
+            if (ok) {
+                ok = mbar_wait(acc_full, h & 1, a.status);
+                ok = __all_sync(0xffffffffu, ok);
+            }
+            if (ok) {
+                tc_fence_after();
+                uint32_t r[kTcCols];
+                tmem_ld_32x32b_x16(tmem + lane_off + 128 + kTcCols * grp, r);
+                tmem_wait_ld();
+                tc_fence_before();
+                float W = 0.f;
+#pragma unroll
+                for (int q = 0; q < kTcGroups; ++q) W += s_w[h & 1][q][row];
+                const int64_t off = (tok0 + row) * C + h * kHd + kTcCols * grp;
+                float eo = 0.f;
+#pragma unroll
+                for (int q = 0; q < kTcCols / 4; ++q) {
+                    const float4 o4 = ld4(a.O + off + 4 * q), e4 = ld4(a.E + off + 4 * q);
+                    eo = fmaf(e4.x, fmaf(-W, o4.x, __uint_as_float(r[4 * q])), eo);
+                    eo = fmaf(e4.y, fmaf(-W, o4.y, __uint_as_float(r[4 * q + 1])), eo);
+                    eo = fmaf(e4.z, fmaf(-W, o4.z, __uint_as_float(r[4 * q + 2])), eo);
+                    eo = fmaf(e4.w, fmaf(-W, o4.w, __uint_as_float(r[4 * q + 3])), eo);
+                }
+                dl += eo / (1.0f + W);
+            }
+            mbar_arrive(acc_empty);
+        }
+        s_dl[grp][row] = dl;
+        epi_sync();
+        if (ok && grp == 0) {
+            float sum = 0.f;
+#pragma unroll
+            for (int q = 0; q < kTcGroups; ++q) sum += s_dl[q][row];
+            a.dl[static_cast<int64_t>(i) * a.T + tok0 + row] = sum;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
+// K (T x C fp32) -> [K_hi | K_lo] rows of 2C bf16.
+__global__ void qk_split_rows_kernel(const float* __restrict__ X, int64_t T, int C,
+                                     __nv_bfloat16* __restrict__ X2) {
+    const int64_t n2 = T * (C / 2);
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n2;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = i / (C / 2);
+        const int c = static_cast<int>(i - t * (C / 2)) * 2;
+        const float2 v = *reinterpret_cast<const float2*>(X + t * C + c);
+        uint32_t hi, lo;
+        split_pair(v.x, v.y, hi, lo);
+        *reinterpret_cast<uint32_t*>(X2 + t * 2 * C + c) = hi;
+        *reinterpret_cast<uint32_t*>(X2 + t * 2 * C + C + c) = lo;
+    }
+}
+
+// V (T x C fp32) -> V^T per (sequence, head): row (sq H + h) 64 + c, columns
+// [hi of keys 0 .. L-1 | lo of keys 0 .. L-1].  One 64-key x 64-channel tile
+// per block through shared memory.
+__global__ void __launch_bounds__(256) qk_split_vt_kernel(const float* __restrict__ V, int L, int H,
+                                                          __nv_bfloat16* __restrict__ Vt2) {
+    __shared__ float tile[64][65];
+    const int kt = blockIdx.x;            // key tile
+    const int sh = blockIdx.y;            // sq H + h
+    const int h = sh % H, sq = sh / H;
+    const int C = H * kHd;
+    for (int e = threadIdx.x; e < 64 * 64; e += 256) {
+        const int t = e / 64, c = e % 64;
+        tile[t][c] = V[(static_cast<int64_t>(sq) * L + kt * 64 + t) * C + h * kHd + c];
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < 64 * 32; e += 256) {
+        const int c = e / 32, t = 2 * (e % 32);
+        uint32_t hi, lo;
+        split_pair(tile[t][c], tile[t + 1][c], hi, lo);
+        __nv_bfloat16* row = Vt2 + (static_cast<int64_t>(sh) * kHd + c) * (2 * static_cast<int64_t>(L));
+        *reinterpret_cast<uint32_t*>(row + kt * 64 + t) = hi;
+        *reinterpret_cast<uint32_t*>(row + L + kt * 64 + t) = lo;
+    }
+}
+
+std::atomic<uint64_t> qk_tc_smem_set{0};
+
 struct QKPlan {
     int64_t ldx;
-    size_t off_dl, off_m, off_r, off_gbf, off_xbf, bytes;
+    size_t off_dl, off_m, off_r, off_gbf, off_xbf, off_k2, off_v2, bytes;
 };
 
 QKPlan qk_plan(int64_t T, int64_t H, int64_t d_in, uint32_t K) {
@@ -281,6 +684,8 @@ QKPlan qk_plan(int64_t T, int64_t H, int64_t d_in, uint32_t K) {
     P.off_r = w.take(static_cast<size_t>(K) * T * 4);
     P.off_gbf = w.take(static_cast<size_t>(T * C) * 2);
     P.off_xbf = w.take(static_cast<size_t>(T * P.ldx) * 2);
+    P.off_k2 = w.take(static_cast<size_t>(T * C) * 4);  // [K_hi | K_lo] bf16
+    P.off_v2 = w.take(static_cast<size_t>(T * C) * 4);  // V^T [hi | lo] bf16
     P.bytes = w.used;
     return P;
 }
@@ -310,7 +715,7 @@ extern "C" dust_status dust_attn_qk_estimate(int which, const float* Q, const fl
     if (nz.num_draws < 2 || !(nz.sigma > 0.0f) || !(nz.sigma < INFINITY)) return DUST_ERR_INVALID_ARG;
     if (!(nz.gamma >= 0.0f && nz.gamma <= 1.0f)) return DUST_ERR_INVALID_ARG;
     if (dv != kHd || seq_len % kQKRows != 0 || seq_len > 8192 || H > 64 || T / kQKRows > 65535 ||
-        nz.num_draws > 65535 || d_in > (1LL << 20))
+        T / seq_len * H > 65535 || nz.num_draws > 65535 || d_in > (1LL << 20))
         return DUST_ERR_UNSUPPORTED;
     if (static_cast<uint64_t>(nz.token0) + static_cast<uint64_t>(T) > (1ULL << 32) ||
         static_cast<uint64_t>(nz.draw0) + nz.num_draws > (1ULL << 32))
@@ -334,16 +739,37 @@ extern "C" dust_status dust_attn_qk_estimate(int which, const float* Q, const fl
     const QKArgs qa{Q, Kk, V, O, P, E, dl, static_cast<int>(T), static_cast<int>(seq_len),
                     static_cast<int>(H), nz.draw0, nz.token0, nz.layer, nz.sigma * 0.125f};
     const dim3 grid(nz.num_draws, static_cast<unsigned>(T / kQKRows));
-    DUST_CUDA_TRY(which == 1 ? set_smem_once(attn_qk_kernel<true>, kQKSmemBytes, qk_smem_set[1])
-                             : set_smem_once(attn_qk_kernel<false>, kQKSmemBytes, qk_smem_set[0]));
-    timer_begin(s);
-    if (which == 1)
+    dust_status st = DUST_OK;
+    if (which == 0) {
+        // queries: split K and V^T once, then the tensor-core kernel
+        __nv_bfloat16* K2 = reinterpret_cast<__nv_bfloat16*>(w + Pl.off_k2);
+        __nv_bfloat16* V2 = reinterpret_cast<__nv_bfloat16*>(w + Pl.off_v2);
+        qk_split_rows_kernel<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(T * C / 2, 256), 148 * 16)),
+                               256, 0, s>>>(Kk, T, static_cast<int>(C), K2);
+        if ((st = launch_status()) != DUST_OK) return st;
+        qk_split_vt_kernel<<<dim3(static_cast<unsigned>(seq_len / 64),
+                                  static_cast<unsigned>(T / seq_len * H)),
+                             256, 0, s>>>(V, static_cast<int>(seq_len), static_cast<int>(H), V2);
+        if ((st = launch_status()) != DUST_OK) return st;
+        CUtensorMap tk, tv;
+        if (!encode_bf16_2d(&tk, K2, 2 * C, T, 2 * C, kTcKeys, kTcKeys) ||
+            !encode_bf16_2d(&tv, V2, 2 * seq_len, T / seq_len * H * kHd, 2 * seq_len, kTcKeys,
+                            kHd))
+            return DUST_ERR_CUDA;
+        DUST_CUDA_TRY(set_smem_once(attn_q_tc_kernel, static_cast<int>(kTcSmem), qk_tc_smem_set));
+        const QKTcArgs ta{P, O, E, dl, static_cast<int>(T), static_cast<int>(seq_len),
+                          static_cast<int>(H), nz.draw0, nz.token0, nz.layer, nz.sigma * 0.125f,
+                          status};
+        timer_begin(s);
+        attn_q_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(tk, tv, ta, keys);
+        timer_end(s);
+    } else {
+        DUST_CUDA_TRY(set_smem_once(attn_qk_kernel<true>, kQKSmemBytes, qk_smem_set[1]));
+        timer_begin(s);
         attn_qk_kernel<true><<<grid, kQKThreads, kQKSmemBytes, s>>>(qa, keys);
-    else
-        attn_qk_kernel<false><<<grid, kQKThreads, kQKSmemBytes, s>>>(qa, keys);
-    timer_end(s);
-    dust_status st = launch_status();
-    if (st != DUST_OK) return st;
+        timer_end(s);
+    }
+    if ((st = launch_status()) != DUST_OK) return st;
     st = credit_and_ghat_launch(dl, mean, r, static_cast<int>(T), static_cast<int>(seq_len),
                                 static_cast<int>(C), nz, keys, g_hat, gbf, s);
     if (st != DUST_OK) return st;

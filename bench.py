@@ -517,10 +517,9 @@ def run_attn_value(args):
 def run_attn_qk(args):
     """The query projection inside attention (which 0; 8 x 2048 tokens, 8
     heads of 64, d_in 512, K = 64, gamma 0.99), inputs resident: token-evals/s,
-    and the perturbed-score kernel against the fp32 FMA rate of the CUDA cores
-    (148 SMs x 128 lanes x 2 flops x the maximum SM clock), counting 2 x 64
-    fused multiply-adds per causal (query, key) pair and draw: the score shift
-    <a_s, k_t> and the weighted value sum."""
+    and the tensor-core kernel against the sustained bf16 peak, counting the
+    flops it executes: per 64-key slice of the causal range, two 128 x 64 x 64
+    products (score shifts, weighted values), each as three split-bf16 passes."""
     import torch
 
     import activation_perturbation_es_noise_b300 as dust
@@ -566,25 +565,24 @@ def run_attn_qk(args):
             step()
     torch.cuda.synchronize()
     kernel_ms = timer.total_ms() / args.steps
-    pairs = nseq * H * L * (L + 1) // 2
-    flops = 2.0 * 2 * 64 * pairs * K
+    nt = L // 128
+    slices = 2 * nt * (nt + 1) // 2  # 64-key slices per (sequence, head, draw)
+    flops = 3 * 2 * (2.0 * 128 * 64 * 64) * slices * nseq * H * K
     peaks, which = _peaks()
-    mhz = peaks.get("sm_max_mhz", SM_MAX_MHZ)
-    peak = N_SM * 128 * 2 * mhz * 1e6 / 1e12
+    peak = peaks["bf16_tflops_sustained"]
     ach = flops / (kernel_ms * 1e-3) / 1e12
     print(json.dumps({
         "metric": METRIC, "value": K * T / (ms * 1e-3), "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32+bf16x3", "data": "synthetic",
         "config": {"workload": "attn_qk", "which": "queries", "tokens": T, "draws": K,
                    "heads": H, "dv": 64, "d_in": c["d_in"], "seq_len": L, "sigma": c["sigma"],
                    "gamma": c["gamma"], "l2": "inputs larger than L2 (no flush)"},
-        "roofline": {"bound": "alu", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+        "roofline": {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                      "frac": ach / peak, "traffic": load_traffic({"name": "attn_qk"}),
-                     "kernel": "attn_qk_kernel", "kernel_ms": kernel_ms,
-                     "peak_source": "fp32 FMA: 148 SMs x 128 lanes x 2 x %.0f MHz (%s clocks)"
-                     % (mhz, which)},
-        "cpu_baseline": None, "e2e": None, "gpu_launches": args.steps * 5,
+                     "kernel": "attn_q_tc_kernel", "kernel_ms": kernel_ms,
+                     "peak_source": "bf16_tflops_sustained (%s)" % which},
+        "cpu_baseline": None, "e2e": None, "gpu_launches": args.steps * 7,
         "clocks": clocks.summary()}), flush=True)
     return 0
 
