@@ -16,17 +16,12 @@
 // dl_s = sum_h <E_s[h], dO_s[h]>, then the usual centring, gamma-scan, g and
 // G_W = g^T x (the interior layer's kernels and the outer-product GEMM).
 //
-// This version runs on the CUDA cores in fp32, as two register-blocked
-// products per 32-key tile (the flash-attention shape): the score shifts of a
-// 128-query tile against the key tile, the weights w = P (e^ds - 1) formed in
-// registers (P read straight from L2, the causal mask applied), and w times
-// the value tile added to a 128 x 64 accumulator spread over the CTA's
-// registers.  A CTA covers one tile of 128 queries of one sequence for one
-// draw and walks the heads in order, so the per-token sum over heads needs no
-// second pass.  The draws are the fastest grid index: the CTAs resident at one
-// time share their sequence, query tile and head, and P, K and V come from L2
-// after the first of them.  The per-pair work, 2 x 64 fused multiply-adds and
-// one e^x - 1, is the kernel's roofline.
+// Both contractions run on the tensor cores (attn_qk_tc_kernel below); the
+// exponential, P and the causal mask sit between them on the CUDA cores.  A
+// CTA covers one tile of 128 queries of one sequence for one draw and walks
+// the heads in order, so the per-token sum over heads needs no second pass;
+// the draws are the fastest grid index, so the CTAs resident at one time share
+// P and V (and, for the queries, K) through L2.
 #include <algorithm>
 #include <cudaTypedefs.h>
 
@@ -43,20 +38,6 @@ namespace {
 
 constexpr int kHd = 64;       // channels per head
 constexpr int kQKRows = 128;  // query rows per CTA
-constexpr int kQKKeys = 32;   // keys per staged tile
-
-struct QKArgs {
-    const float* Q;   // T x C clean queries (C = H 64)
-    const float* Kk;  // T x C clean keys
-    const float* V;   // T x C clean values
-    const float* O;   // T x C clean attention output
-    const float* P;   // nseq x H x L x L clean probabilities (causal rows)
-    const float* E;   // T x C error of the attention output
-    float* dl;        // K x T loss changes
-    int T, L, H;
-    uint32_t draw0, token0, layer;
-    float scale;      // sigma / sqrt(64)
-};
 
 // e^x - 1 for the score shifts: the Taylor polynomial to x^6 for |x| < 1/4
 // (truncation below 5e-8 relative there, and no cancellation), else expm1f.
@@ -72,215 +53,17 @@ __device__ __forceinline__ float expm1_shift(float x) {
     return expm1f(x);
 }
 
-// Shared memory of one CTA (floats): the thread side of the scores, transposed
-// (channel-major, 64 x 128), a key tile transposed (64 x 32), a value tile
-// (32 x 64), the weights w transposed (32 x 128), and per-row partial sums.
-constexpr int kQKThreads = 128;
-constexpr int kOffA = 0;
-constexpr int kOffK = kOffA + kHd * kQKRows;
-constexpr int kOffV = kOffK + kHd * kQKKeys;
-constexpr int kOffW = kOffV + kQKKeys * kHd;
-constexpr int kOffWs = kOffW + kQKKeys * kQKRows;  // 2 x 128 row sums of w
-constexpr int kOffDl = kOffWs + 2 * kQKRows;       // 2 x 128 partial dl
-constexpr int kQKSmemBytes = (kOffDl + 2 * kQKRows) * 4;
-
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
-// Row of a thread's x-th query (x < 8) relative to its first row.
-__device__ __forceinline__ constexpr int qk_row(int x) { return (x & 3) + 32 * (x >> 2); }
-
-// grid: (draws, query tiles x sequences, heaviest tiles first); block: 256.
-// Per 32-key tile two register-blocked products on the CUDA cores:
-//   ds[128 x 32] = A[128 x 64] Kt^T   (A: scaled noise of the queries, or the
-//                                     scaled queries when the keys carry it)
-//   w = P (e^ds - 1), masked causally;  acc[128 x 64] += w[128 x 32] V[32 x 64].
-// Warp w covers rows 64 (w mod 2) .. + 63 in both; lane (r8 = lane mod 8,
-// q = lane / 8) owns rows 4 r8 .. + 3 and 32 + 4 r8 .. + 3 of them (eight lanes'
-// 16-byte loads cover 128 contiguous bytes: no bank conflicts), keys 16 (w / 2) + 4 q .. + 3 of
-// the first product and channels 32 (w / 2) + 8 q .. + 7 of the second, so
-// that each 16-byte shared load feeds 32 / 3 (first) or 16 (second) fused
-// multiply-adds.
-template <bool KEYS>
-__global__ void __launch_bounds__(kQKThreads, 3) attn_qk_kernel(const QKArgs a, const PhiloxKeys keys) {
-    extern __shared__ __align__(16) float sm[];
-    float* At = sm + kOffA;  // [c][row]
-    float* Kt = sm + kOffK;  // [c][key]
-    float* Vt = sm + kOffV;  // [key][c]
-    float* Wt = sm + kOffW;  // [key][row]
-    float* wsp = sm + kOffWs;
-    float* dlp = sm + kOffDl;
-    const int tid = threadIdx.x;
-    const int lane = tid & 31, wi = tid >> 5;
-    const int r8 = lane & 7, q = lane >> 3;
-    const int rb = wi & 1, hb = wi >> 1;   // row block (64 rows), half (keys / channels)
-    const int row0 = 64 * rb + 4 * r8;     // rows row0 + (x & 3) + 32 (x >> 2), x < 8
-    const int key0 = 16 * hb + 4 * q;      // its 4 keys of a key tile (first product)
-    const int ch0 = 32 * hb + 8 * q;       // its 8 channels (second product)
-    const int nseq = a.T / a.L;
-    const int qb = a.L / kQKRows - 1 - static_cast<int>(blockIdx.y) / nseq;  // heavy first
-    const int sq = static_cast<int>(blockIdx.y) % nseq;
-    const int i = blockIdx.x;
-    const uint32_t draw = a.draw0 + static_cast<uint32_t>(i);
-    const int C = a.H * kHd;
-    const int64_t tok0 = static_cast<int64_t>(sq) * a.L + qb * kQKRows;  // the tile's first token
-    const int s0 = qb * kQKRows + row0;                                   // position of row0
-    const int kend = (qb + 1) * kQKRows;
-
-    float dlr[8];
-#pragma unroll
-    for (int x = 0; x < 8; ++x) dlr[x] = 0.f;
-    for (int h = 0; h < a.H; ++h) {
-        // the thread side of the scores, channel-major (lanes over rows: no conflicts)
-        for (int e = tid; e < kQKRows * (kHd / 4); e += kQKThreads) {
-            const int row = e % kQKRows, jb = e / kQKRows;
-            float4 v;
-            if (KEYS) {
-                v = ld4(a.Q + (tok0 + row) * C + h * kHd + 4 * jb);
-            } else {
-                v = words_to_normals(philox4x32_10(static_cast<uint32_t>(h * (kHd / 4) + jb),
-                                                   a.token0 + static_cast<uint32_t>(tok0 + row),
-                                                   draw, a.layer, keys));
-            }
-            At[(4 * jb) * kQKRows + row] = a.scale * v.x;
-            At[(4 * jb + 1) * kQKRows + row] = a.scale * v.y;
-            At[(4 * jb + 2) * kQKRows + row] = a.scale * v.z;
-            At[(4 * jb + 3) * kQKRows + row] = a.scale * v.w;
-        }
-        float acc[8][8];
-        float wsacc[8];
-#pragma unroll
-        for (int x = 0; x < 8; ++x) {
-            wsacc[x] = 0.f;
-#pragma unroll
-            for (int y = 0; y < 8; ++y) acc[x][y] = 0.f;
-        }
-        const float* prow = a.P + ((static_cast<int64_t>(sq) * a.H + h) * a.L + s0) * a.L;
-
-        for (int k0 = 0; k0 < kend; k0 += kQKKeys) {
-            __syncthreads();  // the previous tile's Kt, Vt, Wt (and At's writes) settled
-            for (int e = tid; e < kQKKeys * (kHd / 4); e += kQKThreads) {
-                const int key = e % kQKKeys, jb = e / kQKKeys;
-                const int64_t tk = static_cast<int64_t>(sq) * a.L + k0 + key;
-                float4 v;
-                if (KEYS)
-                    v = words_to_normals(philox4x32_10(static_cast<uint32_t>(h * (kHd / 4) + jb),
-                                                       a.token0 + static_cast<uint32_t>(tk), draw,
-                                                       a.layer, keys));
-                else
-                    v = ld4(a.Kk + tk * C + h * kHd + 4 * jb);
-                Kt[(4 * jb) * kQKKeys + key] = v.x;
-                Kt[(4 * jb + 1) * kQKKeys + key] = v.y;
-                Kt[(4 * jb + 2) * kQKKeys + key] = v.z;
-                Kt[(4 * jb + 3) * kQKKeys + key] = v.w;
-            }
-            for (int e = tid; e < kQKKeys * (kHd / 4); e += kQKThreads) {
-                const int key = e / (kHd / 4), jb = e % (kHd / 4);
-                const int64_t tk = static_cast<int64_t>(sq) * a.L + k0 + key;
-                *reinterpret_cast<float4*>(Vt + key * kHd + 4 * jb) =
-                    ld4(a.V + tk * C + h * kHd + 4 * jb);
-            }
-            __syncthreads();
-            // ds = A Kt^T for 8 rows x 4 keys
-            float w[8][4];
-#pragma unroll
-            for (int x = 0; x < 8; ++x)
-#pragma unroll
-                for (int y = 0; y < 4; ++y) w[x][y] = 0.f;
-#pragma unroll 8
-            for (int c = 0; c < kHd; ++c) {
-                const float4 a0 = ld4(At + c * kQKRows + row0);
-                const float4 a1 = ld4(At + c * kQKRows + row0 + 32);
-                const float4 kv = ld4(Kt + c * kQKKeys + key0);
-                const float ar[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                const float kr[4] = {kv.x, kv.y, kv.z, kv.w};
-#pragma unroll
-                for (int x = 0; x < 8; ++x)
-#pragma unroll
-                    for (int y = 0; y < 4; ++y) w[x][y] = fmaf(ar[x], kr[y], w[x][y]);
-            }
-            // w = P (e^ds - 1) on keys t <= s, in place
-#pragma unroll
-            for (int x = 0; x < 8; ++x) {
-                const float4 pv = __ldg(reinterpret_cast<const float4*>(
-                    prow + static_cast<int64_t>(qk_row(x)) * a.L + k0 + key0));
-                const float pr[4] = {pv.x, pv.y, pv.z, pv.w};
-                float part = 0.f;
-#pragma unroll
-                for (int y = 0; y < 4; ++y) {
-                    const bool live = k0 + key0 + y <= s0 + qk_row(x);
-                    w[x][y] = live ? pr[y] * expm1_shift(w[x][y]) : 0.f;
-                    part += w[x][y];
-                }
-                part += __shfl_xor_sync(0xffffffffu, part, 8);
-                part += __shfl_xor_sync(0xffffffffu, part, 16);
-                wsacc[x] += part;  // this half's 16 keys
-            }
-#pragma unroll
-            for (int y = 0; y < 4; ++y) {
-                *reinterpret_cast<float4*>(Wt + (key0 + y) * kQKRows + row0) =
-                    make_float4(w[0][y], w[1][y], w[2][y], w[3][y]);
-                *reinterpret_cast<float4*>(Wt + (key0 + y) * kQKRows + row0 + 32) =
-                    make_float4(w[4][y], w[5][y], w[6][y], w[7][y]);
-            }
-            __syncthreads();
-            // acc += w V for 8 rows x 8 channels
-#pragma unroll 4
-            for (int t = 0; t < kQKKeys; ++t) {
-                const float4 w0 = ld4(Wt + t * kQKRows + row0);
-                const float4 w1 = ld4(Wt + t * kQKRows + row0 + 32);
-                const float4 v0 = ld4(Vt + t * kHd + ch0);
-                const float4 v1 = ld4(Vt + t * kHd + ch0 + 4);
-                const float wr[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                const float vr[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-                for (int x = 0; x < 8; ++x)
-#pragma unroll
-                    for (int y = 0; y < 8; ++y) acc[x][y] = fmaf(wr[x], vr[y], acc[x][y]);
-            }
-        }
-        // W_s from both halves' partial sums, then <E, dO> over this thread's channels
-        if (q == 0) {
-#pragma unroll
-            for (int x = 0; x < 8; ++x) wsp[hb * kQKRows + row0 + qk_row(x)] = wsacc[x];
-        }
-        __syncthreads();
-#pragma unroll
-        for (int x = 0; x < 8; ++x) {
-            const float W = wsp[row0 + qk_row(x)] + wsp[kQKRows + row0 + qk_row(x)];
-            const int64_t off = (tok0 + row0 + qk_row(x)) * C + h * kHd + ch0;
-            const float4 o0 = ld4(a.O + off), o1 = ld4(a.O + off + 4);
-            const float4 e0 = ld4(a.E + off), e1 = ld4(a.E + off + 4);
-            const float ov[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
-            const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-            float eo = 0.f;
-#pragma unroll
-            for (int y = 0; y < 8; ++y) eo = fmaf(ev[y], fmaf(-W, ov[y], acc[x][y]), eo);
-            eo += __shfl_xor_sync(0xffffffffu, eo, 8);
-            eo += __shfl_xor_sync(0xffffffffu, eo, 16);
-            dlr[x] += eo / (1.0f + W);  // this half's 32 channels
-        }
-        __syncthreads();  // wsp and At are rewritten by the next head
-    }
-    if (q == 0) {
-#pragma unroll
-        for (int x = 0; x < 8; ++x) dlp[hb * kQKRows + row0 + qk_row(x)] = dlr[x];
-    }
-    __syncthreads();
-    if (tid < kQKRows)
-        a.dl[static_cast<int64_t>(i) * a.T + tok0 + tid] = dlp[tid] + dlp[kQKRows + tid];
-}
-
-std::atomic<uint64_t> qk_smem_set[2];
-
 // ------------------------------------------------------------------------
-// The queries on the tensor cores.  The same two products per key slice, now
-// 64 keys wide, as split-bf16 tcgen05 MMAs (hi.hi + hi.lo + lo.hi, fp32
-// accumulation in tensor memory):
-//   ds[128 x 64] = A[128 x 64 ch] K_slice^T,   A = (sigma / 8) x the queries' noise
-//   acc[128 x 64 ch] += W[128 x 64] V_slice,   W = P (e^ds - 1), causal,
-// with the exponential, P and the causal mask on the CUDA cores in between.
-// Warp 0 brings each slice's K ([hi | lo], keys x channels) and V^T ([hi |
-// lo], channels x keys) by TMA, warp 1 issues the MMAs, warps 2..17 (four per
+// Per 64-key slice, two split-bf16 tcgen05 products (hi.hi + hi.lo + lo.hi,
+// fp32 accumulation in tensor memory):
+//   ds[128 x 64] = A[128 x 64 ch] B_slice^T,   acc[128 x 64 ch] += W[128 x 64] V_slice,
+//   W = P (e^ds - 1), causal.
+// Queries: A = (sigma / 8) x the queries' noise, B = the clean keys.  Keys:
+// A = (sigma / 8) x the clean queries, B = the keys' noise (written for a
+// group of draws by qk_key_noise_kernel).  Warp 0 brings each slice's B ([hi
+// | lo], keys x channels) and V^T ([hi | lo], channels x keys) by TMA, warp 1 issues the MMAs, warps 2..17 (four per
 // tensor-memory lane quarter, 16 keys or channels each) generate A per head,
 // turn each ds slice into W in shared memory, and reduce acc against E at the
 // end of a head.  ds has two tensor-memory buffers and W two shared-memory
@@ -302,11 +85,13 @@ constexpr uint32_t kTcOffBar = kTcOffW + 4u * kT16;
 constexpr uint32_t kTcSmem = kTcOffBar + 256u + 1024u;
 
 struct QKTcArgs {
+    const float* Q;  // clean queries (keys mode: the thread side of the scores)
     const float* P;
     const float* O;
     const float* E;
     float* dl;
     int T, L, H;
+    int i0;  // first draw of this launch within the call (dl row)
     uint32_t draw0, token0, layer;
     float scale;
     uint32_t* status;
@@ -360,9 +145,13 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
     return static_cast<uint32_t>(r) * 128u + ((static_cast<uint32_t>(c ^ (r & 7)) & 7u) << 4);
 }
 
+// KEYS: A is the scaled clean queries and the score product's B operand is
+// the keys' noise (tk then maps the group's noise, draw d at rows d T ..);
+// otherwise A is the queries' noise and B the clean keys.
+template <bool KEYS>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    attn_q_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                     const QKTcArgs a, const PhiloxKeys keys) {
+    attn_qk_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                      const QKTcArgs a, const PhiloxKeys keys) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ float s_w[2][kTcGroups][kQKRows];  // row sums of w per head parity and key group
     __shared__ float s_dl[kTcGroups][kQKRows];
@@ -385,9 +174,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int nseq = a.T / a.L;
     const int qb = a.L / kQKRows - 1 - static_cast<int>(blockIdx.y) / nseq;  // heavy first
     const int sq = static_cast<int>(blockIdx.y) % nseq;
-    const int i = blockIdx.x;
+    const int i = a.i0 + static_cast<int>(blockIdx.x);
     const uint32_t draw = a.draw0 + static_cast<uint32_t>(i);
     const int ns = (qb + 1) * (kQKRows / kTcKeys);  // key slices per head
+    const int krow0 = (KEYS ? static_cast<int>(blockIdx.x) * a.T : 0) + sq * a.L;  // B rows
     const int64_t tok0 = static_cast<int64_t>(sq) * a.L + qb * kQKRows;
 
     if (threadIdx.x == 0) {
@@ -426,8 +216,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int key0 = j * kTcKeys;
                     mbar_arrive_expect_tx(kv_full(st), kTcStage);
                     const int C = a.H * kHd;
-                    tma_load_2d(dst, &tk, h * kHd, sq * a.L + key0, kv_full(st));               // K_hi
-                    tma_load_2d(dst + kT8, &tk, C + h * kHd, sq * a.L + key0, kv_full(st));     // K_lo
+                    tma_load_2d(dst, &tk, h * kHd, krow0 + key0, kv_full(st));               // K_hi
+                    tma_load_2d(dst + kT8, &tk, C + h * kHd, krow0 + key0, kv_full(st));     // K_lo
                     tma_load_2d(dst + 2 * kT8, &tv, key0, (sq * a.H + h) * kHd, kv_full(st));   // Vt_hi
                     tma_load_2d(dst + 3 * kT8, &tv, a.L + key0, (sq * a.H + h) * kHd,          // Vt_lo
                                 kv_full(st));
@@ -515,10 +305,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int m = 0; m < kTcCols / 8; ++m) {  // 16-byte chunk: 8 channels
                     const int c8 = (kTcCols / 8) * grp + m;
                     const int jb = h * (kHd / 4) + 2 * c8;
-                    const float4 n0 = words_to_normals(
-                        philox_rest(dh, philox_block_half(static_cast<uint32_t>(jb), a.layer, keys), keys));
-                    const float4 n1 = words_to_normals(philox_rest(
-                        dh, philox_block_half(static_cast<uint32_t>(jb + 1), a.layer, keys), keys));
+                    float4 n0, n1;
+                    if (KEYS) {
+                        n0 = ld4(a.Q + (tok0 + row) * C + 4 * jb);
+                        n1 = ld4(a.Q + (tok0 + row) * C + 4 * jb + 4);
+                    } else {
+                        n0 = words_to_normals(philox_rest(
+                            dh, philox_block_half(static_cast<uint32_t>(jb), a.layer, keys), keys));
+                        n1 = words_to_normals(philox_rest(
+                            dh, philox_block_half(static_cast<uint32_t>(jb + 1), a.layer, keys), keys));
+                    }
                     uint32_t hi[4], lo[4];
                     split_pair(a.scale * n0.x, a.scale * n0.y, hi[0], lo[0]);
                     split_pair(a.scale * n0.z, a.scale * n0.w, hi[1], lo[1]);
@@ -625,6 +421,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
+// The keys' noise of draws draw_first .. + nd - 1 as bf16 [hi | lo] rows of
+// 2C, draw d at rows d T .. d T + T - 1 (the counter scheme of every layer).
+__global__ void qk_key_noise_kernel(int nd, int64_t T, int C, uint32_t draw_first, uint32_t token0,
+                                    uint32_t layer, PhiloxKeys keys, __nv_bfloat16* __restrict__ N2) {
+    const int nb = C / 4;
+    const int64_t n = static_cast<int64_t>(nd) * T * nb;
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int jb = static_cast<int>(idx % nb);
+        const int64_t dt = idx / nb;  // d T + t
+        const int d = static_cast<int>(dt / T);
+        const int64_t t = dt - static_cast<int64_t>(d) * T;
+        const float4 v = words_to_normals(philox4x32_10(static_cast<uint32_t>(jb),
+                                                        token0 + static_cast<uint32_t>(t),
+                                                        draw_first + static_cast<uint32_t>(d), layer,
+                                                        keys));
+        uint32_t hi0, lo0, hi1, lo1;
+        split_pair(v.x, v.y, hi0, lo0);
+        split_pair(v.z, v.w, hi1, lo1);
+        __nv_bfloat16* row = N2 + dt * 2 * C;
+        *reinterpret_cast<uint2*>(row + 4 * jb) = make_uint2(hi0, hi1);
+        *reinterpret_cast<uint2*>(row + C + 4 * jb) = make_uint2(lo0, lo1);
+    }
+}
+
 // K (T x C fp32) -> [K_hi | K_lo] rows of 2C bf16.
 __global__ void qk_split_rows_kernel(const float* __restrict__ X, int64_t T, int C,
                                      __nv_bfloat16* __restrict__ X2) {
@@ -666,11 +487,12 @@ __global__ void __launch_bounds__(256) qk_split_vt_kernel(const float* __restric
     }
 }
 
-std::atomic<uint64_t> qk_tc_smem_set{0};
+std::atomic<uint64_t> qk_tc_smem_set[2];
+constexpr int kKeyGroup = 16;  // draws whose key noise is held at once (keys mode)
 
 struct QKPlan {
     int64_t ldx;
-    size_t off_dl, off_m, off_r, off_gbf, off_xbf, off_k2, off_v2, bytes;
+    size_t off_dl, off_m, off_r, off_gbf, off_xbf, off_k2, off_v2, off_n2, bytes;
 };
 
 QKPlan qk_plan(int64_t T, int64_t H, int64_t d_in, uint32_t K) {
@@ -686,6 +508,8 @@ QKPlan qk_plan(int64_t T, int64_t H, int64_t d_in, uint32_t K) {
     P.off_xbf = w.take(static_cast<size_t>(T * P.ldx) * 2);
     P.off_k2 = w.take(static_cast<size_t>(T * C) * 4);  // [K_hi | K_lo] bf16
     P.off_v2 = w.take(static_cast<size_t>(T * C) * 4);  // V^T [hi | lo] bf16
+    P.off_n2 = w.take(static_cast<size_t>(T * C) * 4 *  // keys' noise of a draw group
+                      static_cast<size_t>(K < static_cast<uint32_t>(kKeyGroup) ? K : kKeyGroup));
     P.bytes = w.used;
     return P;
 }
@@ -736,38 +560,55 @@ extern "C" dust_status dust_attn_qk_estimate(int which, const float* Q, const fl
     __nv_bfloat16* gbf = reinterpret_cast<__nv_bfloat16*>(w + Pl.off_gbf);
     const PhiloxKeys keys = philox_round_keys(nz.seed);
 
-    const QKArgs qa{Q, Kk, V, O, P, E, dl, static_cast<int>(T), static_cast<int>(seq_len),
-                    static_cast<int>(H), nz.draw0, nz.token0, nz.layer, nz.sigma * 0.125f};
-    const dim3 grid(nz.num_draws, static_cast<unsigned>(T / kQKRows));
     dust_status st = DUST_OK;
-    if (which == 0) {
-        // queries: split K and V^T once, then the tensor-core kernel
+    {
+        // K (queries) and V^T split once; the keys' noise per group of draws
         __nv_bfloat16* K2 = reinterpret_cast<__nv_bfloat16*>(w + Pl.off_k2);
         __nv_bfloat16* V2 = reinterpret_cast<__nv_bfloat16*>(w + Pl.off_v2);
-        qk_split_rows_kernel<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(T * C / 2, 256), 148 * 16)),
-                               256, 0, s>>>(Kk, T, static_cast<int>(C), K2);
-        if ((st = launch_status()) != DUST_OK) return st;
+        __nv_bfloat16* N2 = reinterpret_cast<__nv_bfloat16*>(w + Pl.off_n2);
+        if (which == 0) {
+            qk_split_rows_kernel<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(T * C / 2, 256), 148 * 16)),
+                                   256, 0, s>>>(Kk, T, static_cast<int>(C), K2);
+            if ((st = launch_status()) != DUST_OK) return st;
+        }
         qk_split_vt_kernel<<<dim3(static_cast<unsigned>(seq_len / 64),
                                   static_cast<unsigned>(T / seq_len * H)),
                              256, 0, s>>>(V, static_cast<int>(seq_len), static_cast<int>(H), V2);
         if ((st = launch_status()) != DUST_OK) return st;
+        const int group = which == 0 ? static_cast<int>(nz.num_draws)
+                                     : std::min(static_cast<int>(nz.num_draws), kKeyGroup);
         CUtensorMap tk, tv;
-        if (!encode_bf16_2d(&tk, K2, 2 * C, T, 2 * C, kTcKeys, kTcKeys) ||
+        if (!encode_bf16_2d(&tk, which == 0 ? K2 : N2, 2 * C, which == 0 ? T : group * T, 2 * C,
+                            kTcKeys, kTcKeys) ||
             !encode_bf16_2d(&tv, V2, 2 * seq_len, T / seq_len * H * kHd, 2 * seq_len, kTcKeys,
                             kHd))
             return DUST_ERR_CUDA;
-        DUST_CUDA_TRY(set_smem_once(attn_q_tc_kernel, static_cast<int>(kTcSmem), qk_tc_smem_set));
-        const QKTcArgs ta{P, O, E, dl, static_cast<int>(T), static_cast<int>(seq_len),
-                          static_cast<int>(H), nz.draw0, nz.token0, nz.layer, nz.sigma * 0.125f,
-                          status};
-        timer_begin(s);
-        attn_q_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(tk, tv, ta, keys);
-        timer_end(s);
-    } else {
-        DUST_CUDA_TRY(set_smem_once(attn_qk_kernel<true>, kQKSmemBytes, qk_smem_set[1]));
-        timer_begin(s);
-        attn_qk_kernel<true><<<grid, kQKThreads, kQKSmemBytes, s>>>(qa, keys);
-        timer_end(s);
+        if (which == 0)
+            DUST_CUDA_TRY(set_smem_once(attn_qk_tc_kernel<false>, static_cast<int>(kTcSmem), qk_tc_smem_set[0]));
+        else
+            DUST_CUDA_TRY(set_smem_once(attn_qk_tc_kernel<true>, static_cast<int>(kTcSmem), qk_tc_smem_set[1]));
+        for (int i0 = 0; i0 < static_cast<int>(nz.num_draws); i0 += group) {
+            const int nd = std::min(group, static_cast<int>(nz.num_draws) - i0);
+            if (which == 1) {
+                const int64_t n = static_cast<int64_t>(nd) * T * (C / 4);
+                qk_key_noise_kernel<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(n, 256), 148 * 16)),
+                                      256, 0, s>>>(nd, T, static_cast<int>(C),
+                                                   nz.draw0 + static_cast<uint32_t>(i0), nz.token0,
+                                                   nz.layer, keys, N2);
+                if ((st = launch_status()) != DUST_OK) return st;
+            }
+            const QKTcArgs ta{Q, P, O, E, dl, static_cast<int>(T), static_cast<int>(seq_len),
+                              static_cast<int>(H), i0, nz.draw0, nz.token0, nz.layer,
+                              nz.sigma * 0.125f, status};
+            const dim3 grid(static_cast<unsigned>(nd), static_cast<unsigned>(T / kQKRows));
+            timer_begin(s);
+            if (which == 0)
+                attn_qk_tc_kernel<false><<<grid, kTcThreads, kTcSmem, s>>>(tk, tv, ta, keys);
+            else
+                attn_qk_tc_kernel<true><<<grid, kTcThreads, kTcSmem, s>>>(tk, tv, ta, keys);
+            timer_end(s);
+            if ((st = launch_status()) != DUST_OK) return st;
+        }
     }
     if ((st = launch_status()) != DUST_OK) return st;
     st = credit_and_ghat_launch(dl, mean, r, static_cast<int>(T), static_cast<int>(seq_len),

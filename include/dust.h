@@ -382,11 +382,13 @@ size_t dust_attn_qk_workspace(int64_t T, int64_t seq_len, int64_t H, int64_t dv,
  *   nz     noise of channel c of token t, draw i: the Philox counter
  *          (c/4, token0 + t, draw0 + i, layer), as for the other estimators.
  * Limits: dv = 64, seq_len a multiple of 128 (<= 8192), T a multiple of
- * seq_len, 1 <= H <= 64, T/128 <= 65535, 2 <= K <= 65535.  The perturbed
- * scores are computed on the CUDA cores in fp32 (per 128-query tile and
- * 32-key tile, register-blocked score and value products, heads summed in order);
- * the workspace (from dust_attn_qk_workspace) holds the loss changes, the
- * credits and the bf16 copies for the outer product.
+ * seq_len, 1 <= H <= 64, T/128 <= 65535, (T/seq_len) H <= 65535,
+ * 2 <= K <= 65535.  Both products (the score shifts and the reweighted
+ * values) run on the tensor cores as split-bf16 (hi/lo) operands with fp32
+ * accumulation, per 128-query tile and 64-key slice, heads summed in order.
+ * The workspace (from dust_attn_qk_workspace) holds the loss changes, the
+ * credits, the bf16 copies for the outer product, K and V^T split into bf16
+ * hi/lo, and for the keys the split noise of up to 16 draws at a time.
  */
 dust_status dust_attn_qk_estimate(int which, const float* Q, const float* Kk, const float* V,
                                   const float* O, const float* P, const float* E, const void* x,
