@@ -580,7 +580,7 @@ def run_attn_qk(args):
                    "gamma": c["gamma"], "l2": "inputs larger than L2 (no flush)"},
         "roofline": {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                      "frac": ach / peak, "traffic": load_traffic({"name": "attn_qk"}),
-                     "kernel": "attn_q_tc_kernel", "kernel_ms": kernel_ms,
+                     "kernel": "attn_qk_tc_kernel<queries>", "kernel_ms": kernel_ms,
                      "peak_source": "bf16_tflops_sustained (%s)" % which},
         "cpu_baseline": None, "e2e": None, "gpu_launches": args.steps * 7,
         "clocks": clocks.summary()}), flush=True)
