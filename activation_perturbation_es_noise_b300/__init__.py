@@ -31,6 +31,7 @@ EXPORTS = ("dust_status_string", "dust_abi_version", "dust_workspace_status",
            "dust_head_backprop_workspace", "dust_head_backprop", "dust_head_estimate_baseline",
            "dust_attn_value_workspace", "dust_attn_value_estimate", "dust_attn_gate_workspace",
            "dust_attn_gate_estimate", "dust_attn_qk_workspace", "dust_attn_qk_estimate",
+           "dust_block_workspace", "dust_block_job_offset", "dust_block_estimate",
            "dust_issue_probe", "dust_head_chunked_workspace",
            "dust_head_estimate_chunked", "dust_es_perturb", "dust_es_estimate")
 BASELINE_MEAN, BASELINE_LEAVE_ONE_OUT, BASELINE_ANTITHETIC = 0, 1, 2
@@ -48,6 +49,17 @@ class DustNoise(ctypes.Structure):
                 ("draw0", ctypes.c_uint32), ("num_draws", ctypes.c_uint32),
                 ("token0", ctypes.c_uint32), ("sigma", ctypes.c_float),
                 ("gamma", ctypes.c_float)]
+
+
+JOB_HEAD, JOB_LINEAR, JOB_ATTN_VALUE, JOB_ATTN_GATE, JOB_ATTN_QUERY, JOB_ATTN_KEY = range(6)
+
+
+class DustLayerJob(ctypes.Structure):
+    _fields_ = [("type", ctypes.c_int), ("in_", ctypes.c_void_p * 6), ("x", ctypes.c_void_p),
+                ("x_dtype", ctypes.c_int), ("T", ctypes.c_int64), ("seq_len", ctypes.c_int64),
+                ("d_in", ctypes.c_int64), ("n1", ctypes.c_int64), ("n2", ctypes.c_int64),
+                ("n3", ctypes.c_int64), ("ema_decay", ctypes.c_float), ("nz", DustNoise),
+                ("g_hat", ctypes.c_void_p), ("G_W", ctypes.c_void_p)]
 
 
 _lib = None
@@ -97,6 +109,13 @@ def lib():
         L.dust_attn_value_workspace.restype = _SZ
         L.dust_attn_value_estimate.argtypes = [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _I64,
                                                _I64, DustNoise, _P, _P, _P, _SZ, _P]
+        JP = ctypes.POINTER(DustLayerJob)
+        L.dust_block_workspace.argtypes = [JP, ctypes.c_int]
+        L.dust_block_workspace.restype = _SZ
+        L.dust_block_job_offset.argtypes = [JP, ctypes.c_int, ctypes.c_int]
+        L.dust_block_job_offset.restype = _SZ
+        L.dust_block_estimate.argtypes = [JP, ctypes.c_int, _P, _SZ, ctypes.POINTER(_P),
+                                          ctypes.c_int]
         L.dust_attn_qk_workspace.argtypes = [_I64, _I64, _I64, _I64, _I64, _U32]
         L.dust_attn_qk_workspace.restype = _SZ
         L.dust_attn_qk_estimate.argtypes = [ctypes.c_int, _P, _P, _P, _P, _P, _P, _P,
@@ -122,7 +141,8 @@ def lib():
                      "dust_embed_scatter_static", "dust_philox_fill", "dust_gemm_bf16",
                      "dust_sgd_step", "dust_adam_step", "dust_head_backprop",
                      "dust_head_estimate_baseline", "dust_attn_value_estimate",
-                     "dust_attn_gate_estimate", "dust_attn_qk_estimate", "dust_issue_probe",
+                     "dust_attn_gate_estimate", "dust_attn_qk_estimate", "dust_block_estimate",
+                     "dust_issue_probe",
                      "dust_head_estimate_chunked", "dust_es_perturb", "dust_es_estimate"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -471,6 +491,104 @@ def attn_qk_estimate(which, Q, Kk, V, O, P, E, x, seq_len, sigma, gamma, K, seed
                                        noise(seed, sigma, K, layer, draw0, token0, gamma),
                                        _ptr(g), _ptr(G), _ptr(ws), ws.numel(), _stream(stream)))
     return g, G, ws
+
+
+# ---------------------------------------------------------------- block ----
+class LayerJob:
+    """One layer type's perturbed pass for dust_block_estimate: the C job
+    plus the tensors it points at (kept alive) and its outputs (g, G)."""
+
+    def __init__(self, jtype, ins, x, T, seq_len, n, nz, want_g, C_out, ema_decay=0.0):
+        _need_cuda(*ins, x)
+        if x.dtype not in (torch.bfloat16, torch.float32):
+            raise ValueError("x must be bf16 or fp32")
+        dev = x.device
+        d_in = x.shape[1]
+        self.tensors = list(ins) + [x]
+        self.g = torch.empty((T, C_out), dtype=torch.float32, device=dev) if want_g else None
+        self.G = torch.empty((C_out, d_in), dtype=torch.float32, device=dev)
+        n = list(n) + [0] * (3 - len(n))
+        self.c = DustLayerJob()
+        self.c.type = jtype
+        for k, t in enumerate(ins):
+            self.c.in_[k] = t.data_ptr()
+        self.c.x = x.data_ptr()
+        self.c.x_dtype = DUST_BF16 if x.dtype == torch.bfloat16 else DUST_F32
+        self.c.T, self.c.seq_len, self.c.d_in = T, seq_len, d_in
+        self.c.n1, self.c.n2, self.c.n3 = n
+        self.c.ema_decay = float(ema_decay)
+        self.c.nz = nz
+        self.c.g_hat = self.g.data_ptr() if self.g is not None else None
+        self.c.G_W = self.G.data_ptr()
+
+
+def job_head(logits, targets, x, sigma, K, seed, layer=0, draw0=0, token0=0, want_g=True):
+    T, V = logits.shape
+    return LayerJob(JOB_HEAD, [logits, targets], x, T, T, [V],
+                    noise(seed, sigma, K, layer, draw0, token0), want_g, V)
+
+
+def job_linear(x, y1, W2, ema_decay, W_head, z_clean, targets, seq_len, sigma, gamma, K, seed,
+               layer=1, draw0=0, token0=0, want_g=True):
+    T, C = y1.shape
+    return LayerJob(JOB_LINEAR, [y1, W2, W_head, z_clean, targets], x, T, seq_len,
+                    [C, W2.shape[0], W_head.shape[0]],
+                    noise(seed, sigma, K, layer, draw0, token0, gamma), want_g, C, ema_decay)
+
+
+def job_attn_value(P, E, x, seq_len, sigma, gamma, K, seed, layer=2, draw0=0, token0=0,
+                   want_g=True):
+    T, C = E.shape
+    return LayerJob(JOB_ATTN_VALUE, [P, E], x, T, seq_len, [P.shape[1]],
+                    noise(seed, sigma, K, layer, draw0, token0, gamma), want_g, C)
+
+
+def job_attn_gate(z, o, E, x, seq_len, sigma, gamma, K, seed, layer=3, draw0=0, token0=0,
+                  want_g=True):
+    T, C = z.shape
+    return LayerJob(JOB_ATTN_GATE, [z, o, E], x, T, seq_len, [C],
+                    noise(seed, sigma, K, layer, draw0, token0, gamma), want_g, C)
+
+
+def job_attn_qk(which, Q, Kk, V, O, P, E, x, seq_len, sigma, gamma, K, seed, layer=None,
+                draw0=0, token0=0, want_g=True):
+    if which not in (0, 1):
+        raise ValueError("which is 0 (queries) or 1 (keys)")
+    T, C = Q.shape
+    return LayerJob(JOB_ATTN_KEY if which else JOB_ATTN_QUERY, [Q, Kk, V, O, P, E], x, T,
+                    seq_len, [P.shape[1]],
+                    noise(seed, sigma, K, 4 + which if layer is None else layer, draw0, token0,
+                          gamma), want_g, C)
+
+
+def _job_array(jobs):
+    arr = (DustLayerJob * len(jobs))()
+    for k, j in enumerate(jobs):
+        arr[k] = j.c
+    return arr
+
+
+def block_workspace_bytes(jobs):
+    return lib().dust_block_workspace(_job_array(jobs), len(jobs))
+
+
+def block_job_offset(jobs, j):
+    return lib().dust_block_job_offset(_job_array(jobs), len(jobs), j)
+
+
+def block_estimate(jobs, streams=None, ws=None):
+    """Runs the layer jobs (one perturbed pass each, distinct noise layers)
+    through dust_block_estimate, job j on streams[j % len(streams)] (default:
+    the current stream).  Returns ([(g or None, G) per job], ws)."""
+    arr = _job_array(jobs)
+    if ws is None:
+        ws = _workspace(lib().dust_block_workspace(arr, len(jobs)), jobs[0].G.device)
+    if streams is None:
+        streams = [torch.cuda.current_stream()]
+    sarr = (_P * len(streams))(*[s.cuda_stream for s in streams])
+    _check("dust_block_estimate",
+           lib().dust_block_estimate(arr, len(jobs), _ptr(ws), ws.numel(), sarr, len(streams)))
+    return [(j.g, j.G) for j in jobs], ws
 
 
 # ---------------------------------------------------------------- probes ----

@@ -496,6 +496,83 @@ dust_status dust_wait_selftest(void* ws, uint64_t limit_ns, void* stream);
 dust_status dust_issue_probe(int kind, int64_t iters, int64_t* threads_out, void* sink,
                              void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* A whole block: one perturbed pass per layer type                           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The pages perturb the different layer types of a block in separate
+ * forwards, so that one type's noise never moves another type's loss
+ * (Dust translation §2.3; laoyaoba.com section 机制拆解).  A dust_layer_job
+ * describes one such pass, for one weight, from the block's cached clean
+ * activations; dust_block_estimate validates a list of them, gives each its
+ * own slice of one workspace, requires their noise layer ids to differ, and
+ * runs them as separate estimator calls, spread round-robin over the
+ * caller's streams.
+ */
+typedef enum {
+    DUST_JOB_HEAD = 0,        /* dust_head_estimate                            */
+    DUST_JOB_LINEAR = 1,      /* dust_linear_estimate (interior, MLP input)    */
+    DUST_JOB_ATTN_VALUE = 2,  /* dust_attn_value_estimate                      */
+    DUST_JOB_ATTN_GATE = 3,   /* dust_attn_gate_estimate                       */
+    DUST_JOB_ATTN_QUERY = 4,  /* dust_attn_qk_estimate, which = 0              */
+    DUST_JOB_ATTN_KEY = 5     /* dust_attn_qk_estimate, which = 1              */
+} dust_job_type;
+
+/*
+ * One layer type's pass.  `in` holds the entry point's device inputs in its
+ * own argument order; `x`/`x_dtype`/`d_in` are the weight's input; the sizes
+ * n1..n3 are the entry point's remaining dimensions:
+ *
+ *   HEAD        in = {logits, targets}                  n1 = V
+ *   LINEAR      in = {y1, W2, W_head, z_clean, targets}  n1 = C, n2 = d_model,
+ *                                                        n3 = V, ema_decay
+ *   ATTN_VALUE  in = {P, E}                              n1 = H
+ *   ATTN_GATE   in = {z, o, E}                           n1 = C
+ *   ATTN_QUERY,
+ *   ATTN_KEY    in = {Q, Kk, V, O, P, E}                 n1 = H
+ *
+ * (head: d = d_in; attention: dv = 64).  Unused `in` entries and sizes are
+ * ignored.  nz is the pass's noise (its `layer` must differ from every other
+ * job's); g_hat (or NULL) and G_W are the outputs, as for the entry point.
+ */
+typedef struct {
+    int type;             /* dust_job_type */
+    const void* in[6];
+    const void* x;
+    dust_dtype x_dtype;
+    int64_t T, seq_len, d_in;
+    int64_t n1, n2, n3;
+    float ema_decay;
+    dust_noise nz;
+    float* g_hat;
+    float* G_W;
+} dust_layer_job;
+
+/* Workspace bytes for the jobs: each job's own workspace, 256-byte aligned,
+ * in list order.  0 if n < 1, a type is unknown or a job's sizes are
+ * invalid for its entry point. */
+size_t dust_block_workspace(const dust_layer_job* jobs, int n);
+
+/* Byte offset of job j's slice in that workspace (its status word is the
+ * slice's first word: dust_workspace_status(ws + offset, ...)); (size_t)-1
+ * if j is out of range or the jobs are invalid. */
+size_t dust_block_job_offset(const dust_layer_job* jobs, int n, int j);
+
+/*
+ * Runs the jobs: job j on streams[j % nstreams] (or on the default stream
+ * when streams is NULL or nstreams < 1).  With several streams, every stream
+ * first waits for the work already queued on streams[0], and streams[0]
+ * finally waits for all of them, so the call is ordered on streams[0] like a
+ * single estimator call.  Checked before anything is queued: n >= 1, known
+ * types, distinct nz.layer across jobs, non-NULL G_W, a workspace of
+ * dust_block_workspace bytes (256-byte aligned).  A job's own argument
+ * errors are returned as its entry point returns them; jobs before it have
+ * been queued by then.  Device-side status: per job, at its offset.
+ */
+dust_status dust_block_estimate(const dust_layer_job* jobs, int n, void* ws, size_t ws_bytes,
+                                void* const* streams, int nstreams);
+
 /*
  * Benchmark hook.  While set, every launch of an entry point's dominant
  * kernel (the head's draw kernel, the interior layer's re-forward GEMM with

@@ -105,3 +105,50 @@ def test_optimiser_and_backprop_reject_bad_arguments_on_host():
     assert L.dust_head_backprop(None, f, f, 0, 4, 4, 4, None, f, f, need, None) == 1
     assert L.dust_head_backprop(f, f, f, 0, 4, 4, 4, None, f, f, need - 1, None) == 3
     assert L.dust_head_backprop(f, f, f, 7, 4, 4, 4, None, f, f, need, None) == 1
+
+
+def _host_job(jtype, layer, **kw):
+    j = dust.DustLayerJob()
+    j.type = jtype
+    j.nz = dust.noise(1, 0.05, kw.pop("K", 8), layer)
+    for k, v in kw.items():
+        setattr(j, k, v)
+    j.G_W = 256  # never dereferenced: the calls below fail before any launch
+    return j
+
+
+def test_block_workspace_is_the_jobs_slices_in_order():
+    L = dust.lib()
+    jobs = [_host_job(dust.JOB_HEAD, 0, T=256, seq_len=256, d_in=64, n1=512),
+            _host_job(dust.JOB_ATTN_VALUE, 2, T=256, seq_len=128, d_in=32, n1=2),
+            _host_job(dust.JOB_ATTN_QUERY, 4, T=256, seq_len=128, d_in=32, n1=2, K=5)]
+    arr = (dust.DustLayerJob * 3)(*jobs)
+    sizes = [L.dust_head_workspace(256, 512, 64, 8),
+             L.dust_attn_value_workspace(256, 128, 2, 64, 32, 8),
+             L.dust_attn_qk_workspace(256, 128, 2, 64, 32, 5)]
+    assert all(b > 0 for b in sizes)
+    up = [(b + 255) // 256 * 256 for b in sizes]
+    assert L.dust_block_workspace(arr, 3) == sum(up)
+    assert [L.dust_block_job_offset(arr, 3, j) for j in range(3)] == [0, up[0], up[0] + up[1]]
+    assert L.dust_block_job_offset(arr, 3, 3) == ctypes.c_size_t(-1).value
+
+
+def test_block_rejects_bad_jobs_before_any_launch():
+    L = dust.lib()
+    good = _host_job(dust.JOB_ATTN_GATE, 3, T=256, seq_len=128, d_in=16, n1=64)
+    bad_type = _host_job(17, 5, T=256, seq_len=128, d_in=16, n1=64)
+    one_draw = _host_job(dust.JOB_ATTN_GATE, 6, T=256, seq_len=128, d_in=16, n1=64, K=1)
+    assert L.dust_block_workspace((dust.DustLayerJob * 2)(good, bad_type), 2) == 0
+    assert L.dust_block_workspace((dust.DustLayerJob * 1)(one_draw), 1) == 0
+    assert L.dust_block_workspace((dust.DustLayerJob * 1)(good), 0) == 0
+    ws = ctypes.c_void_p(4096)  # never touched: every case fails on the host
+    same_layer = _host_job(dust.JOB_ATTN_VALUE, 3, T=256, seq_len=128, d_in=16, n1=1)
+    arr = (dust.DustLayerJob * 2)(good, same_layer)
+    assert L.dust_block_estimate(arr, 2, ws, 1 << 30, None, 0) == 1  # INVALID_ARG
+    no_out = _host_job(dust.JOB_ATTN_GATE, 3, T=256, seq_len=128, d_in=16, n1=64)
+    no_out.G_W = None
+    assert L.dust_block_estimate((dust.DustLayerJob * 1)(no_out), 1, ws, 1 << 30, None, 0) == 1
+    assert L.dust_block_estimate((dust.DustLayerJob * 1)(good), 1, None, 0, None, 0) == 3  # WORKSPACE
+    assert L.dust_block_estimate((dust.DustLayerJob * 1)(good), 1, ctypes.c_void_p(4100),
+                                 1 << 30, None, 0) == 3  # unaligned workspace
+
