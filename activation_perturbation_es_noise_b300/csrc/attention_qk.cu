@@ -62,11 +62,11 @@ __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast
 //   W = P (e^ds - 1), causal.
 // Queries: A = (sigma / 8) x the queries' noise, B = the clean keys.  Keys:
 // A = (sigma / 8) x the clean queries, B = the keys' noise (written for a
-// group of draws by qk_key_noise_kernel).  Warp 0 brings each slice's B ([hi
-// | lo], keys x channels) and V^T ([hi | lo], channels x keys) by TMA, warp 1 issues the MMAs, warps 2..17 (four per
-// tensor-memory lane quarter, 16 keys or channels each) generate A per head,
-// turn each ds slice into W in shared memory, and reduce acc against E at the
-// end of a head.  ds has two tensor-memory buffers and W two shared-memory
+// group of draws by qk_key_noise_kernel).  Warp 0 brings each slice's B
+// ([hi | lo], keys x channels) and V^T ([hi | lo], channels x keys) by TMA,
+// warp 1 issues the MMAs, and warps 2..17 (four per tensor-memory lane
+// quarter, 16 keys or channels each) generate A per head, turn each ds slice
+// into W in shared memory, and reduce acc against E at the end of a head.  ds has two tensor-memory buffers and W two shared-memory
 // buffers, so the next slice's score product runs while this one's W is
 // formed.  Every wait is bounded; on a timeout the roles stop and the status
 // word records it.
