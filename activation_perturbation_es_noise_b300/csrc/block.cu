@@ -106,6 +106,8 @@ extern "C" dust_status dust_block_estimate(const dust_layer_job* jobs, int n, vo
     if (!plan(jobs, n, off, total)) return DUST_ERR_INVALID_ARG;
     for (int j = 0; j < n; ++j) {
         if (!jobs[j].G_W) return DUST_ERR_INVALID_ARG;
+        // the interior entry point reads x as bf16 only
+        if (jobs[j].type == DUST_JOB_LINEAR && jobs[j].x_dtype != DUST_BF16) return DUST_ERR_INVALID_ARG;
         for (int k = 0; k < j; ++k)  // separate noise per pass
             if (jobs[k].nz.layer == jobs[j].nz.layer) return DUST_ERR_INVALID_ARG;
     }

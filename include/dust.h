@@ -532,7 +532,8 @@ typedef enum {
  *   ATTN_QUERY,
  *   ATTN_KEY    in = {Q, Kk, V, O, P, E}                 n1 = H
  *
- * (head: d = d_in; attention: dv = 64).  Unused `in` entries and sizes are
+ * (head: d = d_in; attention: dv = 64; LINEAR: x must be DUST_BF16, as
+ * dust_linear_estimate reads it).  Unused `in` entries and sizes are
  * ignored.  nz is the pass's noise (its `layer` must differ from every other
  * job's); g_hat (or NULL) and G_W are the outputs, as for the entry point.
  */
@@ -565,10 +566,11 @@ size_t dust_block_job_offset(const dust_layer_job* jobs, int n, int j);
  * first waits for the work already queued on streams[0], and streams[0]
  * finally waits for all of them, so the call is ordered on streams[0] like a
  * single estimator call.  Checked before anything is queued: n >= 1, known
- * types, distinct nz.layer across jobs, non-NULL G_W, a workspace of
- * dust_block_workspace bytes (256-byte aligned).  A job's own argument
- * errors are returned as its entry point returns them; jobs before it have
- * been queued by then.  Device-side status: per job, at its offset.
+ * types, distinct nz.layer across jobs, non-NULL G_W, bf16 x for LINEAR,
+ * a workspace of dust_block_workspace bytes (256-byte aligned).  A job's
+ * own argument errors are returned as its entry point returns them; jobs
+ * before it have been queued by then.  Device-side status: per job, at its
+ * offset.
  */
 dust_status dust_block_estimate(const dust_layer_job* jobs, int n, void* ws, size_t ws_bytes,
                                 void* const* streams, int nstreams);

@@ -148,6 +148,10 @@ def test_block_rejects_bad_jobs_before_any_launch():
     no_out = _host_job(dust.JOB_ATTN_GATE, 3, T=256, seq_len=128, d_in=16, n1=64)
     no_out.G_W = None
     assert L.dust_block_estimate((dust.DustLayerJob * 1)(no_out), 1, ws, 1 << 30, None, 0) == 1
+    lin = _host_job(dust.JOB_LINEAR, 8, T=256, seq_len=128, d_in=64, n1=128, n2=64, n3=256)
+    assert L.dust_block_workspace((dust.DustLayerJob * 1)(lin), 1) > 0
+    lin.x_dtype = dust.DUST_F32  # the interior layer reads x as bf16 only
+    assert L.dust_block_estimate((dust.DustLayerJob * 1)(lin), 1, ws, 1 << 30, None, 0) == 1
     assert L.dust_block_estimate((dust.DustLayerJob * 1)(good), 1, None, 0, None, 0) == 3  # WORKSPACE
     assert L.dust_block_estimate((dust.DustLayerJob * 1)(good), 1, ctypes.c_void_p(4100),
                                  1 << 30, None, 0) == 3  # unaligned workspace
