@@ -33,7 +33,8 @@ EXPORTS = ("dust_status_string", "dust_abi_version", "dust_workspace_status",
            "dust_attn_gate_estimate", "dust_attn_qk_workspace", "dust_attn_qk_estimate",
            "dust_block_workspace", "dust_block_job_offset", "dust_block_estimate",
            "dust_issue_probe", "dust_head_chunked_workspace",
-           "dust_head_estimate_chunked", "dust_es_perturb", "dust_es_estimate")
+           "dust_head_estimate_chunked", "dust_es_perturb", "dust_es_estimate",
+           "dust_box_muller_fast")
 BASELINE_MEAN, BASELINE_LEAVE_ONE_OUT, BASELINE_ANTITHETIC = 0, 1, 2
 
 
@@ -95,6 +96,7 @@ def lib():
         L.dust_embed_scatter.argtypes = [_P, _P, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]
         L.dust_embed_scatter_static.argtypes = [_P, _P, _I64, _I64, _I64, _P, _P, _P]
         L.dust_philox_fill.argtypes = [ctypes.c_uint64, _U32, _U32, _I64, _I64, _I64, _P, _P, _P]
+        L.dust_box_muller_fast.argtypes = [_P, _I64, _P, _P]
         L.dust_gemm_bf16.argtypes = [_P, ctypes.c_int, _I64, _P, ctypes.c_int, _I64, _I64, _I64,
                                      _I64, _P, _I64, _P, _SZ, _P]
         L.dust_set_kernel_events.argtypes = [_P, _P, ctypes.c_int]
@@ -143,7 +145,8 @@ def lib():
                      "dust_head_estimate_baseline", "dust_attn_value_estimate",
                      "dust_attn_gate_estimate", "dust_attn_qk_estimate", "dust_block_estimate",
                      "dust_issue_probe",
-                     "dust_head_estimate_chunked", "dust_es_perturb", "dust_es_estimate"):
+                     "dust_head_estimate_chunked", "dust_es_perturb", "dust_es_estimate",
+           "dust_box_muller_fast"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -291,6 +294,19 @@ def philox_fill(seed, layer, draw, token0, ntok, nchan, device="cuda", stream=No
                                 _ptr(normals), _stream(stream))
     _check("dust_philox_fill", st)
     return words, normals
+
+
+def box_muller_fast(words, stream=None):
+    """Normals (fp32, same shape) of device words taken in pairs (int32 tensor
+    holding the uint32 bits, an even number of elements) by the kernels' fast
+    Box-Muller."""
+    _need_cuda(words)
+    if words.dtype != torch.int32 or not words.is_contiguous() or words.numel() % 2:
+        raise ValueError("words: contiguous int32 tensor with an even number of elements")
+    out = torch.empty(words.shape, dtype=torch.float32, device=words.device)
+    _check("dust_box_muller_fast",
+           lib().dust_box_muller_fast(_ptr(words), words.numel() // 2, _ptr(out), _stream(stream)))
+    return out
 
 
 def wait_selftest(limit_ns, stream=None):

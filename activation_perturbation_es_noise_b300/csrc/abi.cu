@@ -1,5 +1,5 @@
 // abi.cu -- status strings, the workspace status read-back and the noise
-// regenerator test hook.
+// regenerator test hooks.
 #include "dust_common.cuh"
 #include "internal.h"
 #include "noise.cuh"
@@ -30,6 +30,18 @@ __global__ void philox_fill_kernel(PhiloxKeys keys, uint32_t layer, uint32_t dra
                 if (normals) normals[t * nchan + c] = av[k];
             }
         }
+    }
+}
+
+// One thread per pair of words: the kernels' fast Box-Muller at scale 1.
+__global__ void box_muller_fast_kernel(const uint2* __restrict__ words, int64_t npairs,
+                                       float2* __restrict__ normals) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < npairs;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint2 w = words[i];
+        float2 a;
+        box_muller_fast(w.x, w.y, a.x, a.y, -2.0f * 0.69314718055994531f);
+        normals[i] = a;
     }
 }
 
@@ -197,6 +209,20 @@ extern "C" dust_status dust_philox_fill(uint64_t seed, uint32_t layer, uint32_t 
     philox_fill_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
         philox_round_keys(seed), layer, draw, static_cast<uint32_t>(token0), ntok, nchan, words,
         normals);
+    return launch_status();
+}
+
+extern "C" dust_status dust_box_muller_fast(const uint32_t* words, int64_t npairs,
+                                            float* normals, void* stream) {
+    if (npairs < 0 || npairs > (1LL << 40)) return DUST_ERR_INVALID_ARG;
+    if (npairs == 0) return DUST_OK;
+    if (!words || !normals || !aligned(words, 8) || !aligned(normals, 8))
+        return DUST_ERR_INVALID_ARG;
+    int64_t blocks = ceil_div(npairs, 256);
+    if (blocks > 148 * 64) blocks = 148 * 64;
+    box_muller_fast_kernel<<<static_cast<unsigned>(blocks), 256, 0,
+                             static_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<const uint2*>(words), npairs, reinterpret_cast<float2*>(normals));
     return launch_status();
 }
 

@@ -322,11 +322,11 @@ extern "C" size_t dust_attn_value_workspace(int64_t T, int64_t seq_len, int64_t 
     return attn_plan(T, seq_len, H, d_in, K).bytes;
 }
 
-extern "C" dust_status dust_attn_value_estimate(const float* P, const float* E, const void* x,
-                                                dust_dtype x_dtype, int64_t T, int64_t seq_len,
-                                                int64_t H, int64_t dv, int64_t d_in,
-                                                dust_noise nz, float* g_hat, float* G_W,
-                                                void* ws, size_t ws_bytes, void* stream) {
+dust_status dust::attn_value_check(const float* P, const float* E, const void* x,
+                                   dust_dtype x_dtype, int64_t T, int64_t seq_len, int64_t H,
+                                   int64_t dv, int64_t d_in, const dust_noise& nz,
+                                   const float* g_hat, const float* G_W, const void* ws,
+                                   size_t ws_bytes) {
     if (!P || !E || !x || !G_W) return DUST_ERR_INVALID_ARG;
     if (T < 1 || seq_len < 1 || T % seq_len != 0 || H < 1 || d_in < 1) return DUST_ERR_INVALID_ARG;
     if (x_dtype != DUST_F32 && x_dtype != DUST_BF16) return DUST_ERR_INVALID_ARG;
@@ -343,6 +343,18 @@ extern "C" dust_status dust_attn_value_estimate(const float* P, const float* E, 
         return DUST_ERR_INVALID_ARG;
     const AttnPlan Pl = attn_plan(T, seq_len, H, d_in, nz.num_draws);
     if (!ws || ws_bytes < Pl.bytes || !aligned(ws, 256)) return DUST_ERR_WORKSPACE;
+    return DUST_OK;
+}
+
+extern "C" dust_status dust_attn_value_estimate(const float* P, const float* E, const void* x,
+                                                dust_dtype x_dtype, int64_t T, int64_t seq_len,
+                                                int64_t H, int64_t dv, int64_t d_in,
+                                                dust_noise nz, float* g_hat, float* G_W,
+                                                void* ws, size_t ws_bytes, void* stream) {
+    const dust_status chk = attn_value_check(P, E, x, x_dtype, T, seq_len, H, dv, d_in, nz, g_hat,
+                                             G_W, ws, ws_bytes);
+    if (chk != DUST_OK) return chk;
+    const AttnPlan Pl = attn_plan(T, seq_len, H, d_in, nz.num_draws);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* w = static_cast<uint8_t*>(ws);
     uint32_t* status = static_cast<uint32_t*>(ws);
@@ -491,11 +503,10 @@ extern "C" size_t dust_attn_gate_workspace(int64_t T, int64_t seq_len, int64_t C
     return gate_plan(T, C, d_in, K).bytes;
 }
 
-extern "C" dust_status dust_attn_gate_estimate(const float* z, const float* o, const float* E,
-                                               const void* x, dust_dtype x_dtype, int64_t T,
-                                               int64_t seq_len, int64_t C, int64_t d_in,
-                                               dust_noise nz, float* g_hat, float* G_W, void* ws,
-                                               size_t ws_bytes, void* stream) {
+dust_status dust::attn_gate_check(const float* z, const float* o, const float* E, const void* x,
+                                  dust_dtype x_dtype, int64_t T, int64_t seq_len, int64_t C,
+                                  int64_t d_in, const dust_noise& nz, const float* g_hat,
+                                  const float* G_W, const void* ws, size_t ws_bytes) {
     if (!z || !o || !E || !x || !G_W) return DUST_ERR_INVALID_ARG;
     if (T < 1 || seq_len < 1 || T % seq_len != 0 || C < 1 || d_in < 1) return DUST_ERR_INVALID_ARG;
     if (x_dtype != DUST_F32 && x_dtype != DUST_BF16) return DUST_ERR_INVALID_ARG;
@@ -511,6 +522,18 @@ extern "C" dust_status dust_attn_gate_estimate(const float* z, const float* o, c
         return DUST_ERR_INVALID_ARG;
     const GatePlan Pl = gate_plan(T, C, d_in, nz.num_draws);
     if (!ws || ws_bytes < Pl.bytes || !aligned(ws, 256)) return DUST_ERR_WORKSPACE;
+    return DUST_OK;
+}
+
+extern "C" dust_status dust_attn_gate_estimate(const float* z, const float* o, const float* E,
+                                               const void* x, dust_dtype x_dtype, int64_t T,
+                                               int64_t seq_len, int64_t C, int64_t d_in,
+                                               dust_noise nz, float* g_hat, float* G_W, void* ws,
+                                               size_t ws_bytes, void* stream) {
+    const dust_status chk = attn_gate_check(z, o, E, x, x_dtype, T, seq_len, C, d_in, nz, g_hat,
+                                            G_W, ws, ws_bytes);
+    if (chk != DUST_OK) return chk;
+    const GatePlan Pl = gate_plan(T, C, d_in, nz.num_draws);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* w = static_cast<uint8_t*>(ws);
     uint32_t* status = static_cast<uint32_t*>(ws);

@@ -539,12 +539,12 @@ extern "C" size_t dust_attn_qk_workspace(int64_t T, int64_t seq_len, int64_t H, 
     return qk_plan(T, H, d_in, K).bytes;
 }
 
-extern "C" dust_status dust_attn_qk_estimate(int which, const float* Q, const float* Kk,
-                                             const float* V, const float* O, const float* P,
-                                             const float* E, const void* x, dust_dtype x_dtype,
-                                             int64_t T, int64_t seq_len, int64_t H, int64_t dv,
-                                             int64_t d_in, dust_noise nz, float* g_hat,
-                                             float* G_W, void* ws, size_t ws_bytes, void* stream) {
+dust_status dust::attn_qk_check(int which, const float* Q, const float* Kk, const float* V,
+                                const float* O, const float* P, const float* E, const void* x,
+                                dust_dtype x_dtype, int64_t T, int64_t seq_len, int64_t H,
+                                int64_t dv, int64_t d_in, const dust_noise& nz,
+                                const float* g_hat, const float* G_W, const void* ws,
+                                size_t ws_bytes) {
     if (which != 0 && which != 1) return DUST_ERR_INVALID_ARG;
     if (!Q || !Kk || !V || !O || !P || !E || !x || !G_W) return DUST_ERR_INVALID_ARG;
     if (T < 1 || seq_len < 1 || T % seq_len != 0 || H < 1 || d_in < 1) return DUST_ERR_INVALID_ARG;
@@ -562,6 +562,19 @@ extern "C" dust_status dust_attn_qk_estimate(int which, const float* Q, const fl
         return DUST_ERR_INVALID_ARG;
     const QKPlan Pl = qk_plan(T, H, d_in, nz.num_draws);
     if (!ws || ws_bytes < Pl.bytes || !aligned(ws, 256)) return DUST_ERR_WORKSPACE;
+    return DUST_OK;
+}
+
+extern "C" dust_status dust_attn_qk_estimate(int which, const float* Q, const float* Kk,
+                                             const float* V, const float* O, const float* P,
+                                             const float* E, const void* x, dust_dtype x_dtype,
+                                             int64_t T, int64_t seq_len, int64_t H, int64_t dv,
+                                             int64_t d_in, dust_noise nz, float* g_hat,
+                                             float* G_W, void* ws, size_t ws_bytes, void* stream) {
+    const dust_status chk = attn_qk_check(which, Q, Kk, V, O, P, E, x, x_dtype, T, seq_len, H, dv,
+                                          d_in, nz, g_hat, G_W, ws, ws_bytes);
+    if (chk != DUST_OK) return chk;
+    const QKPlan Pl = qk_plan(T, H, d_in, nz.num_draws);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* w = static_cast<uint8_t*>(ws);
     uint32_t* status = static_cast<uint32_t*>(ws);

@@ -10,6 +10,7 @@
 // round-robin on the given streams, joined back onto the first stream.
 // Nothing here launches a kernel of its own.
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "dust_common.cuh"
@@ -44,6 +45,142 @@ bool plan(const dust_layer_job* jobs, int n, std::vector<size_t>& off, size_t& t
     }
     total = at;
     return true;
+}
+
+// The job's own entry-point checks on its slice of the workspace, run for
+// every job before anything is queued.
+dust_status check_job(const dust_layer_job& j, const void* ws, size_t bytes) {
+    const void* const* in = j.in;
+    const float* f0 = static_cast<const float*>(in[0]);
+    switch (j.type) {
+        case DUST_JOB_HEAD:
+            return head_estimate_check(f0, static_cast<const int32_t*>(in[1]), j.x, j.x_dtype, j.T,
+                                       j.n1, j.d_in, j.nz, DUST_BASELINE_MEAN, j.g_hat, j.G_W,
+                                       ws, bytes);
+        case DUST_JOB_LINEAR:
+            // the interior entry point reads x as bf16 only
+            if (j.x_dtype != DUST_BF16) return DUST_ERR_INVALID_ARG;
+            return linear_estimate_check(j.x, f0, in[1], j.ema_decay, in[2],
+                                         static_cast<const float*>(in[3]),
+                                         static_cast<const int32_t*>(in[4]), j.T, j.seq_len,
+                                         j.d_in, j.n1, j.n2, j.n3, j.nz, j.g_hat, j.G_W, ws,
+                                         bytes);
+        case DUST_JOB_ATTN_VALUE:
+            return attn_value_check(f0, static_cast<const float*>(in[1]), j.x, j.x_dtype, j.T,
+                                    j.seq_len, j.n1, 64, j.d_in, j.nz, j.g_hat, j.G_W, ws, bytes);
+        case DUST_JOB_ATTN_GATE:
+            return attn_gate_check(f0, static_cast<const float*>(in[1]),
+                                   static_cast<const float*>(in[2]), j.x, j.x_dtype, j.T,
+                                   j.seq_len, j.n1, j.d_in, j.nz, j.g_hat, j.G_W, ws, bytes);
+        case DUST_JOB_ATTN_QUERY:
+        case DUST_JOB_ATTN_KEY:
+            return attn_qk_check(j.type == DUST_JOB_ATTN_KEY ? 1 : 0, f0,
+                                 static_cast<const float*>(in[1]),
+                                 static_cast<const float*>(in[2]),
+                                 static_cast<const float*>(in[3]),
+                                 static_cast<const float*>(in[4]),
+                                 static_cast<const float*>(in[5]), j.x, j.x_dtype, j.T,
+                                 j.seq_len, j.n1, 64, j.d_in, j.nz, j.g_hat, j.G_W, ws, bytes);
+        default: return DUST_ERR_INVALID_ARG;
+    }
+}
+
+// Byte ranges of one job's buffers: its outputs (g_hat, G_W) and every input
+// it reads, sized from the job's dimensions (all already validated).
+struct Range {
+    uintptr_t lo, hi;
+};
+
+int64_t out_width(const dust_layer_job& j) {  // channels of g_hat / rows of G_W
+    switch (j.type) {
+        case DUST_JOB_ATTN_VALUE:
+        case DUST_JOB_ATTN_QUERY:
+        case DUST_JOB_ATTN_KEY: return j.n1 * 64;
+        default: return j.n1;
+    }
+}
+
+void add_range(std::vector<Range>& v, const void* p, int64_t bytes) {
+    if (p && bytes > 0) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+        v.push_back({a, a + static_cast<uintptr_t>(bytes)});
+    }
+}
+
+void job_outputs(const dust_layer_job& j, std::vector<Range>& v) {
+    const int64_t C = out_width(j);
+    add_range(v, j.g_hat, j.T * C * 4);
+    add_range(v, j.G_W, C * j.d_in * 4);
+}
+
+void job_inputs(const dust_layer_job& j, std::vector<Range>& v) {
+    const int64_t T = j.T, L = j.seq_len;
+    add_range(v, j.x, T * j.d_in * (j.x_dtype == DUST_BF16 ? 2 : 4));
+    switch (j.type) {
+        case DUST_JOB_HEAD:
+            add_range(v, j.in[0], T * j.n1 * 4);
+            add_range(v, j.in[1], T * 4);
+            break;
+        case DUST_JOB_LINEAR:
+            add_range(v, j.in[0], T * j.n1 * 4);        // y1
+            add_range(v, j.in[1], j.n2 * j.n1 * 2);     // W2
+            add_range(v, j.in[2], j.n3 * j.n2 * 2);     // W_head
+            add_range(v, j.in[3], T * j.n3 * 4);        // z_clean
+            add_range(v, j.in[4], T * 4);               // targets
+            break;
+        case DUST_JOB_ATTN_VALUE:
+            add_range(v, j.in[0], (T / L) * j.n1 * L * L * 4);  // P
+            add_range(v, j.in[1], T * j.n1 * 64 * 4);           // E
+            break;
+        case DUST_JOB_ATTN_GATE:
+            for (int k = 0; k < 3; ++k) add_range(v, j.in[k], T * j.n1 * 4);
+            break;
+        case DUST_JOB_ATTN_QUERY:
+        case DUST_JOB_ATTN_KEY:
+            for (int k = 0; k < 4; ++k) add_range(v, j.in[k], T * j.n1 * 64 * 4);  // Q K V O
+            add_range(v, j.in[4], (T / L) * j.n1 * L * L * 4);                  // P
+            add_range(v, j.in[5], T * j.n1 * 64 * 4);                           // E
+            break;
+        default: break;
+    }
+}
+
+bool overlap(const std::vector<Range>& a, const std::vector<Range>& b) {
+    for (const Range& x : a)
+        for (const Range& y : b)
+            if (x.lo < y.hi && y.lo < x.hi) return true;
+    return false;
+}
+
+// Every check of the block call, before any event or launch: the jobs'
+// own argument checks on their workspace slices, distinct noise layers, and
+// no job writing memory that another job reads or writes (with several
+// streams that would race; on one stream a later job would clobber an
+// earlier one's result).
+dust_status check_block(const dust_layer_job* jobs, int n, const std::vector<size_t>& off,
+                        size_t total, void* ws, size_t ws_bytes) {
+    if (!ws || ws_bytes < total || !aligned(ws, 256)) return DUST_ERR_WORKSPACE;
+    const uint8_t* base = static_cast<const uint8_t*>(ws);
+    std::vector<std::vector<Range>> outs(static_cast<size_t>(n)), ins(static_cast<size_t>(n));
+    for (int j = 0; j < n; ++j) {
+        const size_t bytes = (j + 1 < n ? off[j + 1] : total) - off[j];
+        const dust_status st = check_job(jobs[j], base + off[j], bytes);
+        if (st != DUST_OK) return st;
+        for (int k = 0; k < j; ++k)  // separate noise per pass
+            if (jobs[k].nz.layer == jobs[j].nz.layer) return DUST_ERR_INVALID_ARG;
+        job_outputs(jobs[j], outs[j]);
+        job_inputs(jobs[j], ins[j]);
+        add_range(ins[j], base + off[j], static_cast<int64_t>(bytes));  // its workspace slice
+        if (outs[j].size() == 2 &&  // g_hat and G_W of one job
+            overlap({outs[j][0]}, {outs[j][1]}))
+            return DUST_ERR_INVALID_ARG;
+    }
+    for (int j = 0; j < n; ++j)
+        for (int k = 0; k < n; ++k) {
+            if (k == j) continue;
+            if (overlap(outs[j], outs[k]) || overlap(outs[j], ins[k])) return DUST_ERR_INVALID_ARG;
+        }
+    return DUST_OK;
 }
 
 dust_status run_job(const dust_layer_job& j, void* ws, size_t bytes, void* stream) {
@@ -99,43 +236,68 @@ extern "C" size_t dust_block_job_offset(const dust_layer_job* jobs, int n, int j
     return off[j];
 }
 
+namespace dust {
+namespace {
+
+// Fork/join events, created once per device and reused by every call made
+// with that device current; the mutex is held for the whole call so that two
+// host threads never record the same event at once.
+struct BlockEvents {
+    std::mutex mu;
+    std::vector<cudaEvent_t> ev[64];
+};
+BlockEvents& block_events() {
+    static BlockEvents* e = new BlockEvents();  // never destroyed: events live until exit
+    return *e;
+}
+
+dust_status events_for_device(std::vector<cudaEvent_t>& ev, int need) {
+    while (static_cast<int>(ev.size()) < need) {
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return DUST_ERR_CUDA;
+        }
+        ev.push_back(e);
+    }
+    return DUST_OK;
+}
+
+}  // namespace
+}  // namespace dust
+
 extern "C" dust_status dust_block_estimate(const dust_layer_job* jobs, int n, void* ws,
                                            size_t ws_bytes, void* const* streams, int nstreams) {
     std::vector<size_t> off;
     size_t total = 0;
     if (!plan(jobs, n, off, total)) return DUST_ERR_INVALID_ARG;
-    for (int j = 0; j < n; ++j) {
-        if (!jobs[j].G_W) return DUST_ERR_INVALID_ARG;
-        // the interior entry point reads x as bf16 only
-        if (jobs[j].type == DUST_JOB_LINEAR && jobs[j].x_dtype != DUST_BF16) return DUST_ERR_INVALID_ARG;
-        for (int k = 0; k < j; ++k)  // separate noise per pass
-            if (jobs[k].nz.layer == jobs[j].nz.layer) return DUST_ERR_INVALID_ARG;
-    }
-    if (!ws || ws_bytes < total || !aligned(ws, 256)) return DUST_ERR_WORKSPACE;
+    const dust_status chk = check_block(jobs, n, off, total, ws, ws_bytes);
+    if (chk != DUST_OK) return chk;
     const int ns = (streams && nstreams > 0) ? nstreams : 1;
     auto stream_of = [&](int k) -> void* { return (streams && nstreams > 0) ? streams[k] : nullptr; };
 
-    // Fork: every other stream waits for what is queued on the first.
-    std::vector<cudaEvent_t> ev;
-    auto release = [&]() {
-        for (cudaEvent_t e : ev) cudaEventDestroy(e);
-    };
+    std::unique_lock<std::mutex> lock;
+    std::vector<cudaEvent_t>* ev = nullptr;
     if (ns > 1) {
-        ev.resize(static_cast<size_t>(ns), nullptr);
-        for (int k = 0; k < ns; ++k) {
-            if (cudaEventCreateWithFlags(&ev[k], cudaEventDisableTiming) != cudaSuccess) {
-                ev.resize(static_cast<size_t>(k));
-                release();
-                return DUST_ERR_CUDA;
-            }
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return DUST_ERR_CUDA;
         }
-        if (cudaEventRecord(ev[0], static_cast<cudaStream_t>(stream_of(0))) != cudaSuccess) {
-            release();
+        if (dev < 0 || dev >= 64) return DUST_ERR_UNSUPPORTED;
+        BlockEvents& be = block_events();
+        lock = std::unique_lock<std::mutex>(be.mu);
+        ev = &be.ev[dev];
+        if (events_for_device(*ev, ns) != DUST_OK) return DUST_ERR_CUDA;
+        // Fork: every other stream waits for what is queued on the first.
+        if (cudaEventRecord((*ev)[0], static_cast<cudaStream_t>(stream_of(0))) != cudaSuccess) {
+            (void)cudaGetLastError();
             return DUST_ERR_CUDA;
         }
         for (int k = 1; k < ns; ++k)
-            if (cudaStreamWaitEvent(static_cast<cudaStream_t>(stream_of(k)), ev[0], 0) != cudaSuccess) {
-                release();
+            if (cudaStreamWaitEvent(static_cast<cudaStream_t>(stream_of(k)), (*ev)[0], 0) !=
+                cudaSuccess) {
+                (void)cudaGetLastError();
                 return DUST_ERR_CUDA;
             }
     }
@@ -149,11 +311,13 @@ extern "C" dust_status dust_block_estimate(const dust_layer_job* jobs, int n, vo
     // so that nothing queued is left unordered with the caller's stream).
     if (ns > 1) {
         for (int k = 1; k < ns; ++k) {
-            if (cudaEventRecord(ev[k], static_cast<cudaStream_t>(stream_of(k))) != cudaSuccess ||
-                cudaStreamWaitEvent(static_cast<cudaStream_t>(stream_of(0)), ev[k], 0) != cudaSuccess)
+            if (cudaEventRecord((*ev)[k], static_cast<cudaStream_t>(stream_of(k))) != cudaSuccess ||
+                cudaStreamWaitEvent(static_cast<cudaStream_t>(stream_of(0)), (*ev)[k], 0) !=
+                    cudaSuccess) {
+                (void)cudaGetLastError();
                 st = st == DUST_OK ? DUST_ERR_CUDA : st;
+            }
         }
-        release();
     }
     return st;
 }

@@ -21,6 +21,8 @@
 // the noise of those channels from its counter, reduces sum p e^{sigma a}
 // across the CTA, and folds dl a into the accumulators.  Nothing per draw ever
 // leaves the chip.
+#include <cmath>
+
 #include "dust_common.cuh"
 #include "internal.h"
 #include "noise.cuh"
@@ -34,7 +36,10 @@ struct HeadArgs {
     int T, V, nblk, K, Q, chunk;
     uint32_t draw0, token0, layer;
     float sig_l2e;  // s = sigma * log2(e): the kernel works with b = s a
+    float clog;     // -2 ln(2) s^2: the fast Box-Muller's log constant for b = s a
     float g_scale;  // 1 / (K sigma s): turns the b-scaled sums into g
+    float qscale;   // 2^E > 0: the pair kernel's fixed-point scale of sum p 2^b
+    float qinv;     // 2^-E (qscale = 0: float sums instead)
     float* g_hat;   // T x V fp32, may be null
     __nv_bfloat16* gbf;
     int64_t ldg;    // row stride of gbf (elements)
@@ -228,7 +233,7 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
         float a[NB][4];
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-            const float4 n = words_to_normals(w[b], A.sig_l2e);
+            const float4 n = words_to_normals_fast(w[b], A.clog);
             a[b][0] = n.x;
             a[b][1] = n.y;
             a[b][2] = n.z;
@@ -381,6 +386,268 @@ __global__ void head_finalize_kernel(const HeadArgs A) {
     A.gbf[static_cast<int64_t>(t) * A.ldg + A.col0 + c] = __float2bfloat16_rn(g);
 }
 
+// The mean-baseline draws, two per pass (leave-one-out is the same kernel
+// with another final scale).
+//
+// The token's probabilities live in shared memory, not registers, and every
+// pass over the thread's channel blocks generates two draws' noise block by
+// block: the two Philox chains of a block interleave, and the block's two
+// noise vectors (b = s a) go to shared memory, where the accumulation after
+// the reduction reads them back.  That leaves the S1/S0 accumulators and the
+// working set in 128 registers, so four 128-thread CTAs share an SM, and
+// halves the CTA reductions and barriers per draw.  The two sums
+// sum_v p_v 2^b_v are reduced across the CTA in fixed point, as exact 32-bit
+// integer sums (redux.sync per warp, one shared-memory add per warp), so
+// their value does not depend on the order of the adds: qscale = 2^E with
+// E chosen on the host so that the largest possible sum, 2^(5.8 s), stays
+// below 2^32.  When sigma is too large for 24 fractional bits the sums are
+// floats added in warp order instead.  The loss change is
+// ln S - b_y ln 2, with the hardware log2 for ln S (absolute error about
+// 1.7e-7, against loss changes of order sigma).
+//
+// Dynamic shared memory: NB x NT float4 of probabilities, then 2 x NB x NT
+// float4 of noise.
+// NTC: the CTA's thread count when it is fixed at compile time (32 for
+// one-warp CTAs, 128 for the 4096-entry vocabulary), else 0 (blockDim.x, up
+// to 256): constant strides keep the shared-memory addressing off the
+// integer multiplier that Philox saturates.
+template <int NB, bool ONE_WARP, int NTC>
+__global__ void __launch_bounds__(NTC == 0 ? 256 : NTC, NTC == 32 ? 16 : (NTC == 128 ? 4 : 2))
+    head_pair_kernel(const HeadArgs A, const PhiloxKeys keys) {
+    extern __shared__ float4 pair_smem[];
+    __shared__ uint32_t qsum[3][2];   // fixed-point sums, three rotating slots
+    __shared__ float fsum[2][2][8];   // float sums per warp, two slots
+    __shared__ float red_y[2][2];     // b of the target channel, per draw
+    __shared__ float scratch[8];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int NT = ONE_WARP ? 32 : (NTC > 0 ? NTC : static_cast<int>(blockDim.x));
+    const int NW = NT >> 5;
+    float4* psm = pair_smem;
+    float4* nsm = pair_smem + NB * NT;  // [draw of the pair][block][thread]
+    if (tid < 6) qsum[tid >> 1][tid & 1] = 0u;
+    const int t = blockIdx.x / A.Q;
+    const int q = blockIdx.x - t * A.Q;
+    const int i_begin = q * A.chunk;
+    const int i_end = min(A.K, i_begin + A.chunk);
+    const int V = A.V;
+    const bool vec = (V & 3) == 0;
+    const float* zrow = A.logits + static_cast<int64_t>(t) * V;
+
+    // Cached logits of this token -> softmax -> shared memory.
+    float p[NB][4];
+    float zmax = -INFINITY;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        const int j = b * NT + tid;
+        if (vec && j < A.nblk) {
+            const float4 z4 = __ldg(reinterpret_cast<const float4*>(zrow) + j);
+            p[b][0] = z4.x; p[b][1] = z4.y; p[b][2] = z4.z; p[b][3] = z4.w;
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int c = 4 * j + k;
+                p[b][k] = (j < A.nblk && c < V) ? __ldg(zrow + c) : -INFINITY;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) zmax = fmaxf(zmax, p[b][k]);
+    }
+    zmax = block_max<ONE_WARP>(zmax, scratch);
+    float zsum = 0.f;
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            p[b][k] = (p[b][k] == -INFINITY) ? 0.f : expf(p[b][k] - zmax);
+            zsum += p[b][k];
+        }
+    zsum = block_sum<ONE_WARP>(zsum, scratch);
+    const float zinv = 1.0f / zsum;
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+        psm[b * NT + tid] = make_float4(p[b][0] * zinv, p[b][1] * zinv, p[b][2] * zinv,
+                                        p[b][3] * zinv);
+
+    int y = __ldg(A.targets + t);
+    if (y < 0 || y >= V) {
+        if (tid == 0 && q == 0) record_status(A.status, DUST_ERR_DEVICE_RANGE);
+        y = -1;
+    }
+    const int yblk = y >> 2;
+    const bool owner = (y >= 0) && (yblk % NT == tid);
+    const int yb = (y >= 0) ? yblk / NT : -1;
+    const int yc = y & 3;
+    const int ylane = (y >= 0) ? (yblk % NT) & 31 : 0;
+    const bool ywarp = (y >= 0) && (((yblk % NT) >> 5) == warp);
+
+    float s1[NB][4], s0[NB][4];
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) s1[b][k] = s0[b][k] = 0.f;
+    float sdl = 0.f;
+    const uint32_t token = A.token0 + static_cast<uint32_t>(t);
+    const bool fixed = A.qscale > 0.f;
+    if (!ONE_WARP) __syncthreads();  // qsum zeroed before the first pass adds to it
+
+    int pass = 0;
+#pragma unroll 1
+    for (int i = i_begin; i < i_end; i += 2, ++pass) {
+        // The second draw of an odd count's last pass is generated but not
+        // counted (w1 = 0).
+        const float w1 = (i + 1 < i_end) ? 1.f : 0.f;
+        const DrawHalf dh0 = philox_draw_half(A.draw0 + static_cast<uint32_t>(i), token, keys);
+        const DrawHalf dh1 = philox_draw_half(A.draw0 + static_cast<uint32_t>(i + 1), token, keys);
+        float pt0 = 0.f, pt1 = 0.f, ay0 = 0.f, ay1 = 0.f;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            // Blocks past the vocabulary (only in the last block row) carry
+            // real noise of unused counters; their probabilities are zero and
+            // their accumulators are never written.
+            const BlockHalf hb = philox_block_half(b * NT + tid, A.layer, keys);
+            const uint4 wd0 = philox_rest(dh0, hb, keys);
+            const uint4 wd1 = philox_rest(dh1, hb, keys);
+            const float4 n0 = words_to_normals_fast(wd0, A.clog);
+            const float4 n1 = words_to_normals_fast(wd1, A.clog);
+            const float4 pb = psm[b * NT + tid];
+            float e = pb.x * ex2_approx(n0.x);
+            e = fmaf(pb.y, ex2_approx(n0.y), e);
+            e = fmaf(pb.z, ex2_approx(n0.z), e);
+            e = fmaf(pb.w, ex2_approx(n0.w), e);
+            float f = pb.x * ex2_approx(n1.x);
+            f = fmaf(pb.y, ex2_approx(n1.y), f);
+            f = fmaf(pb.z, ex2_approx(n1.z), f);
+            f = fmaf(pb.w, ex2_approx(n1.w), f);
+            pt0 = b == 0 ? e : pt0 + e;
+            pt1 = b == 0 ? f : pt1 + f;
+            nsm[b * NT + tid] = n0;
+            nsm[(NB + b) * NT + tid] = n1;
+            if (ywarp && b == yb) {  // warp-uniform
+                ay0 = yc == 0 ? n0.x : yc == 1 ? n0.y : yc == 2 ? n0.z : n0.w;
+                ay1 = yc == 0 ? n1.x : yc == 1 ? n1.y : yc == 2 ? n1.z : n1.w;
+            }
+        }
+        const int slot = pass % 3, buf = pass & 1;
+        float S0, S1;
+        if (fixed) {
+            const uint32_t q0 = __float2uint_rn(pt0 * A.qscale);
+            const uint32_t q1 = __float2uint_rn(pt1 * A.qscale);
+            uint32_t r0, r1;
+            asm volatile("redux.sync.add.u32 %0, %1, 0xffffffff;" : "=r"(r0) : "r"(q0));
+            asm volatile("redux.sync.add.u32 %0, %1, 0xffffffff;" : "=r"(r1) : "r"(q1));
+            if (ONE_WARP) {
+                S0 = static_cast<float>(r0) * A.qinv;
+                S1 = static_cast<float>(r1) * A.qinv;
+            } else if (lane == 0) {
+                atomicAdd(&qsum[slot][0], r0);
+                atomicAdd(&qsum[slot][1], r1);
+            }
+        } else {
+            const float f0 = warp_sum(pt0), f1 = warp_sum(pt1);
+            if (ONE_WARP) {
+                S0 = f0;
+                S1 = f1;
+            } else if (lane == 0) {
+                fsum[buf][0][warp] = f0;
+                fsum[buf][1][warp] = f1;
+            }
+        }
+        if (ONE_WARP) {
+            ay0 = __shfl_sync(0xFFFFFFFFu, ay0, ylane);
+            ay1 = __shfl_sync(0xFFFFFFFFu, ay1, ylane);
+        } else {
+            if (owner) {
+                red_y[buf][0] = ay0;
+                red_y[buf][1] = ay1;
+            }
+            __syncthreads();
+            if (fixed) {
+                S0 = static_cast<float>(qsum[slot][0]) * A.qinv;
+                S1 = static_cast<float>(qsum[slot][1]) * A.qinv;
+                // the slot read two passes ago is free again (every thread
+                // has passed this pass's barrier since reading it)
+                if (tid < 2) qsum[(pass + 2) % 3][tid] = 0u;
+            } else {
+                S0 = fsum[buf][0][0];
+                S1 = fsum[buf][1][0];
+                for (int w2 = 1; w2 < NW; ++w2) {
+                    S0 += fsum[buf][0][w2];
+                    S1 += fsum[buf][1][w2];
+                }
+            }
+            ay0 = y >= 0 ? red_y[buf][0] : 0.f;
+            ay1 = y >= 0 ? red_y[buf][1] : 0.f;
+        }
+        // dl = ln S - sigma a_y, with sigma a_y = b_y ln 2.
+        const float dl0 = (lg2_approx(S0) - ay0) * 0.69314718055994531f;
+        const float dl1 = (lg2_approx(S1) - ay1) * 0.69314718055994531f * w1;
+        sdl += dl0 + dl1;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const float4 n0 = nsm[b * NT + tid];
+            const float4 n1 = nsm[(NB + b) * NT + tid];
+            s1[b][0] = fmaf(dl1, n1.x, fmaf(dl0, n0.x, s1[b][0]));
+            s1[b][1] = fmaf(dl1, n1.y, fmaf(dl0, n0.y, s1[b][1]));
+            s1[b][2] = fmaf(dl1, n1.z, fmaf(dl0, n0.z, s1[b][2]));
+            s1[b][3] = fmaf(dl1, n1.w, fmaf(dl0, n0.w, s1[b][3]));
+            s0[b][0] = fmaf(n1.x, w1, s0[b][0] + n0.x);
+            s0[b][1] = fmaf(n1.y, w1, s0[b][1] + n0.y);
+            s0[b][2] = fmaf(n1.z, w1, s0[b][2] + n0.z);
+            s0[b][3] = fmaf(n1.w, w1, s0[b][3] + n0.w);
+        }
+    }
+
+    if (A.Q == 1) {
+        const float mean = sdl / static_cast<float>(A.K);
+        float* grow = A.g_hat ? A.g_hat + static_cast<int64_t>(t) * V : nullptr;
+        __nv_bfloat16* brow = A.gbf + static_cast<int64_t>(t) * A.ldg;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const int j = b * NT + tid;
+            if (j >= A.nblk) continue;
+            float g[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) g[k] = (s1[b][k] - mean * s0[b][k]) * A.g_scale;
+            if (vec) {
+                if (grow) *reinterpret_cast<float4*>(grow + 4 * j) = make_float4(g[0], g[1], g[2], g[3]);
+                __nv_bfloat162 lo = __floats2bfloat162_rn(g[0], g[1]);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(g[2], g[3]);
+                uint2 pk;
+                pk.x = *reinterpret_cast<uint32_t*>(&lo);
+                pk.y = *reinterpret_cast<uint32_t*>(&hi);
+                *reinterpret_cast<uint2*>(brow + 4 * j) = pk;
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int c = 4 * j + k;
+                    if (c < V) {
+                        if (grow) grow[c] = g[k];
+                        brow[c] = __float2bfloat16_rn(g[k]);
+                    }
+                }
+            }
+        }
+    } else {
+        const int64_t off = (static_cast<int64_t>(q) * A.T + t) * V;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const int j = b * NT + tid;
+            if (j >= A.nblk) continue;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int c = 4 * j + k;
+                if (c < V) {
+                    A.part_s1[off + c] = s1[b][k];
+                    A.part_s0[off + c] = s0[b][k];
+                }
+            }
+        }
+        if (tid == 0) A.part_dl[static_cast<int64_t>(q) * A.T + t] = sdl;
+    }
+}
+
 struct HeadPlan {
     int nblk, nb, nt, Q, chunk;
     bool one_warp;
@@ -433,6 +700,39 @@ HeadPlan head_plan(int64_t T, int64_t V, int64_t d, uint32_t K) {
     return P;
 }
 
+// The fast Box-Muller's log constant for b = s a, and the pair kernel's
+// fixed-point scale: |a| < 5.8 by construction (u >= 2^-24), so every sum
+// sum_v p_v 2^b_v (the p sum to 1) is below 2^(5.8 s); 2^E keeps it, and the
+// lanes' rounding, below 2^32.  Below 24 fractional bits the kernel adds
+// floats instead (qscale = 0).
+void set_noise_scales(HeadArgs& A, double s) {
+    A.clog = static_cast<float>(-2.0 * 0.69314718055994531 * s * s);
+    const int E = static_cast<int>(std::floor(31.9 - 5.8 * s));
+    if (E >= 24) {
+        A.qscale = std::ldexp(1.0f, E);
+        A.qinv = std::ldexp(1.0f, -E);
+    } else {
+        A.qscale = 0.f;
+        A.qinv = 0.f;
+    }
+}
+
+size_t pair_smem_bytes(int nb, int nt) { return static_cast<size_t>(3) * nb * nt * 16; }
+
+template <int NB, bool OW, int NTC>
+dust_status launch_pairs(const HeadPlan& P, const HeadArgs& A, const PhiloxKeys& keys, int64_t T,
+                         cudaStream_t s) {
+    static std::atomic<uint64_t> smem_set{0};
+    // the kernel's largest dynamic shared memory (up to 256 threads when NTC = 0)
+    const size_t smem_max = pair_smem_bytes(NB, NTC == 0 ? 256 : NTC);
+    const size_t smem = pair_smem_bytes(NB, P.nt);
+    DUST_CUDA_TRY(set_smem_once(head_pair_kernel<NB, OW, NTC>, static_cast<int>(smem_max), smem_set));
+    timer_begin(s);
+    head_pair_kernel<NB, OW, NTC><<<static_cast<unsigned>(T * P.Q), P.nt, smem, s>>>(A, keys);
+    timer_end(s);
+    return launch_status();
+}
+
 template <int NB, bool OW>
 dust_status launch_draws(const HeadPlan& P, const HeadArgs& A, const PhiloxKeys& keys,
                          int64_t T, bool anti, cudaStream_t s, bool chunk = false) {
@@ -458,12 +758,12 @@ extern "C" size_t dust_head_workspace(int64_t T, int64_t V, int64_t d, uint32_t 
     return head_plan(T, V, d, K).ws_bytes;
 }
 
-namespace {
+namespace dust {
 
-dust_status head_estimate(const float* logits, const int32_t* targets, const void* x,
-                          dust_dtype x_dtype, int64_t T, int64_t V, int64_t d, dust_noise nz,
-                          dust_baseline baseline, float* g_hat, float* G_W, void* ws,
-                          size_t ws_bytes, void* stream) {
+dust_status head_estimate_check(const float* logits, const int32_t* targets, const void* x,
+                                dust_dtype x_dtype, int64_t T, int64_t V, int64_t d,
+                                const dust_noise& nz, dust_baseline baseline, const float* g_hat,
+                                const float* G_W, const void* ws, size_t ws_bytes) {
     if (!logits || !targets || !x || !G_W) return DUST_ERR_INVALID_ARG;
     if (baseline != DUST_BASELINE_MEAN && baseline != DUST_BASELINE_LEAVE_ONE_OUT &&
         baseline != DUST_BASELINE_ANTITHETIC)
@@ -480,6 +780,21 @@ dust_status head_estimate(const float* logits, const int32_t* targets, const voi
         return DUST_ERR_INVALID_ARG;
     const HeadPlan P = head_plan(T, V, d, nz.num_draws);
     if (!ws || ws_bytes < P.ws_bytes || !aligned(ws, 256)) return DUST_ERR_WORKSPACE;
+    return DUST_OK;
+}
+
+}  // namespace dust
+
+namespace {
+
+dust_status head_estimate(const float* logits, const int32_t* targets, const void* x,
+                          dust_dtype x_dtype, int64_t T, int64_t V, int64_t d, dust_noise nz,
+                          dust_baseline baseline, float* g_hat, float* G_W, void* ws,
+                          size_t ws_bytes, void* stream) {
+    const dust_status chk = head_estimate_check(logits, targets, x, x_dtype, T, V, d, nz,
+                                                baseline, g_hat, G_W, ws, ws_bytes);
+    if (chk != DUST_OK) return chk;
+    const HeadPlan P = head_plan(T, V, d, nz.num_draws);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* w = static_cast<uint8_t*>(ws);
     DUST_CUDA_TRY(cudaMemsetAsync(ws, 0, kCtlBytes, s));
@@ -498,6 +813,7 @@ dust_status head_estimate(const float* logits, const int32_t* targets, const voi
     A.layer = nz.layer;
     const double s_l2e = static_cast<double>(nz.sigma) * 1.4426950408889634;
     A.sig_l2e = static_cast<float>(s_l2e);
+    set_noise_scales(A, s_l2e);
     // g = (S1 - m S0) / (K sigma s) for the mean over draws; leave-one-out
     // means scale it by K / (K - 1); antithetic pairs give S1 / (2 K sigma s).
     const double ks = static_cast<double>(nz.sigma) * static_cast<double>(A.sig_l2e);
@@ -522,15 +838,28 @@ dust_status head_estimate(const float* logits, const int32_t* targets, const voi
     const PhiloxKeys keys = philox_round_keys(nz.seed);
 
     dust_status st;
-    if (P.one_warp) {
-        switch (P.nb) {
-            case 1: st = launch_draws<1, true>(P, A, keys, T, anti, s); break;
-            case 2: st = launch_draws<2, true>(P, A, keys, T, anti, s); break;
-            case 4: st = launch_draws<4, true>(P, A, keys, T, anti, s); break;
-            default: st = launch_draws<8, true>(P, A, keys, T, anti, s); break;
+    if (anti) {
+        if (P.one_warp) {
+            switch (P.nb) {
+                case 1: st = launch_draws<1, true>(P, A, keys, T, true, s); break;
+                case 2: st = launch_draws<2, true>(P, A, keys, T, true, s); break;
+                case 4: st = launch_draws<4, true>(P, A, keys, T, true, s); break;
+                default: st = launch_draws<8, true>(P, A, keys, T, true, s); break;
+            }
+        } else {
+            st = launch_draws<8, false>(P, A, keys, T, true, s);  // head_plan: 8 blocks per thread
         }
+    } else if (P.one_warp) {
+        switch (P.nb) {
+            case 1: st = launch_pairs<1, true, 32>(P, A, keys, T, s); break;
+            case 2: st = launch_pairs<2, true, 32>(P, A, keys, T, s); break;
+            case 4: st = launch_pairs<4, true, 32>(P, A, keys, T, s); break;
+            default: st = launch_pairs<8, true, 32>(P, A, keys, T, s); break;
+        }
+    } else if (P.nt == 128) {
+        st = launch_pairs<8, false, 128>(P, A, keys, T, s);
     } else {
-        st = launch_draws<8, false>(P, A, keys, T, anti, s);  // head_plan: 8 blocks per thread
+        st = launch_pairs<8, false, 0>(P, A, keys, T, s);
     }
     if (st != DUST_OK) return st;
     if (P.Q > 1) {
@@ -777,6 +1106,7 @@ extern "C" dust_status dust_head_estimate_chunked(const float* logits, const int
     A.layer = nz.layer;
     const double s_l2e = static_cast<double>(nz.sigma) * 1.4426950408889634;
     A.sig_l2e = static_cast<float>(s_l2e);
+    set_noise_scales(A, s_l2e);
     A.g_scale = static_cast<float>(
         1.0 / (static_cast<double>(Kc) * nz.sigma * static_cast<double>(A.sig_l2e)));
     A.g_hat = g_hat;

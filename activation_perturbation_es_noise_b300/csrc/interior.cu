@@ -426,13 +426,13 @@ extern "C" size_t dust_linear_workspace(int64_t T, int64_t d_in, int64_t C, int6
     return interior_plan(T, d_in, C, d_model, V, K).bytes;
 }
 
-extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, const void* W2,
-                                            float ema_decay, const void* W_head,
-                                            const float* z_clean, const int32_t* targets,
-                                            int64_t T, int64_t seq_len, int64_t d_in, int64_t C,
-                                            int64_t d_model, int64_t V, dust_noise nz,
-                                            float* g_hat, float* G_W1, void* ws, size_t ws_bytes,
-                                            void* stream) {
+dust_status dust::linear_estimate_check(const void* x, const float* y1, const void* W2,
+                                        float ema_decay, const void* W_head,
+                                        const float* z_clean, const int32_t* targets, int64_t T,
+                                        int64_t seq_len, int64_t d_in, int64_t C,
+                                        int64_t d_model, int64_t V, const dust_noise& nz,
+                                        const float* g_hat, const float* G_W1, const void* ws,
+                                        size_t ws_bytes) {
     if (!x || !y1 || !W2 || !W_head || !z_clean || !targets || !G_W1) return DUST_ERR_INVALID_ARG;
     if (T < 1 || seq_len < 1 || T % seq_len != 0 || d_in < 1 || C < 1 || d_model < 1 || V < 1)
         return DUST_ERR_INVALID_ARG;
@@ -451,6 +451,21 @@ extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, cons
         return DUST_ERR_INVALID_ARG;
     const InteriorPlan P = interior_plan(T, d_in, C, d_model, V, nz.num_draws);
     if (!ws || ws_bytes < P.bytes || !aligned(ws, 256)) return DUST_ERR_WORKSPACE;
+    return DUST_OK;
+}
+
+extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, const void* W2,
+                                            float ema_decay, const void* W_head,
+                                            const float* z_clean, const int32_t* targets,
+                                            int64_t T, int64_t seq_len, int64_t d_in, int64_t C,
+                                            int64_t d_model, int64_t V, dust_noise nz,
+                                            float* g_hat, float* G_W1, void* ws, size_t ws_bytes,
+                                            void* stream) {
+    const dust_status chk = linear_estimate_check(x, y1, W2, ema_decay, W_head, z_clean, targets,
+                                                  T, seq_len, d_in, C, d_model, V, nz, g_hat,
+                                                  G_W1, ws, ws_bytes);
+    if (chk != DUST_OK) return chk;
+    const InteriorPlan P = interior_plan(T, d_in, C, d_model, V, nz.num_draws);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* w = static_cast<uint8_t*>(ws);
     uint32_t* status = static_cast<uint32_t*>(ws);

@@ -136,6 +136,33 @@ dust_status reforward1_launch(const float* y1, const float* h0, const void* coef
                               void* A2, int64_t seq_len, float lam, uint32_t* status,
                               cudaStream_t s);
 
+// Host-side argument checks of the estimator entry points, workspace size
+// included: exactly what each entry point verifies before it enqueues
+// anything (the block scheduler runs them on every job first).
+dust_status head_estimate_check(const float* logits, const int32_t* targets, const void* x,
+                                dust_dtype x_dtype, int64_t T, int64_t V, int64_t d,
+                                const dust_noise& nz, dust_baseline baseline, const float* g_hat,
+                                const float* G_W, const void* ws, size_t ws_bytes);
+dust_status linear_estimate_check(const void* x, const float* y1, const void* W2,
+                                  float ema_decay, const void* W_head, const float* z_clean,
+                                  const int32_t* targets, int64_t T, int64_t seq_len,
+                                  int64_t d_in, int64_t C, int64_t d_model, int64_t V,
+                                  const dust_noise& nz, const float* g_hat, const float* G_W1,
+                                  const void* ws, size_t ws_bytes);
+dust_status attn_value_check(const float* P, const float* E, const void* x, dust_dtype x_dtype,
+                             int64_t T, int64_t seq_len, int64_t H, int64_t dv, int64_t d_in,
+                             const dust_noise& nz, const float* g_hat, const float* G_W,
+                             const void* ws, size_t ws_bytes);
+dust_status attn_gate_check(const float* z, const float* o, const float* E, const void* x,
+                            dust_dtype x_dtype, int64_t T, int64_t seq_len, int64_t C,
+                            int64_t d_in, const dust_noise& nz, const float* g_hat,
+                            const float* G_W, const void* ws, size_t ws_bytes);
+dust_status attn_qk_check(int which, const float* Q, const float* Kk, const float* V,
+                          const float* O, const float* P, const float* E, const void* x,
+                          dust_dtype x_dtype, int64_t T, int64_t seq_len, int64_t H, int64_t dv,
+                          int64_t d_in, const dust_noise& nz, const float* g_hat,
+                          const float* G_W, const void* ws, size_t ws_bytes);
+
 // rows x cols fp32 (row stride ld_in) -> bf16 (row stride ld_out, padding
 // columns set to zero).
 dust_status f32_to_bf16_launch(const float* in, int64_t rows, int64_t cols, int64_t ld_in,

@@ -278,6 +278,20 @@ dust_status dust_philox_fill(uint64_t seed, uint32_t layer, uint32_t draw, int64
                              void* stream);
 
 /*
+ * The Box-Muller step that the throughput-bound kernels use (the head's draw
+ * kernels), on caller-chosen words: for pair k, words[2k] (even) and
+ * words[2k+1] (odd) become normals[2k] = rho cos theta and
+ * normals[2k+1] = rho sin theta with rho = sqrt(-2 ln u(w_even)),
+ * theta = 2 pi u(w_odd) and u(w) = ((w >> 9) + 0.5) 2^-23, computed with the
+ * hardware log2, square root and sin/cos (the map of dust_noise, to within
+ * the error those approximations leave).  words and normals are device
+ * arrays of 2 npairs elements, 8-byte aligned.  INVALID_ARG for a negative
+ * count or a NULL or misaligned array.
+ */
+dust_status dust_box_muller_fast(const uint32_t* words, int64_t npairs, float* normals,
+                                 void* stream);
+
+/*
  * The outer-product GEMM alone: G[m][n] = sum_k A(m, k) B(n, k) in fp32 from
  * bf16 operands on the tensor cores.  A is stored M-major (k rows of M
  * elements, row stride lda elements) when a_mn != 0, else K-major (M rows of

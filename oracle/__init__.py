@@ -98,6 +98,19 @@ def uniform(word):
     return lib().orc_uniform(int(word))
 
 
+def box_muller(words):
+    """Normals of Philox words taken in pairs (n x 2 uint32, even word first),
+    fp64: rho = sqrt(-2 ln u(w_even)), theta = 2 pi u(w_odd), the pair
+    (rho cos theta, rho sin theta); u(w) = ((w >> 9) + 0.5) 2^-23 (Box & Muller,
+    1958, with the uniform map of the noise).  The same map as the C oracle's
+    token normals, applied to any words (tests feed it chosen ones)."""
+    w = _c(words, np.uint32).reshape(-1, 2).astype(np.float64)
+    u = (np.floor(w / 512.0) + 0.5) * 2.0 ** -23
+    rho = np.sqrt(-2.0 * np.log(u[:, 0]))
+    theta = 2.0 * np.pi * u[:, 1]
+    return np.stack([rho * np.cos(theta), rho * np.sin(theta)], axis=1)
+
+
 def noise_words(seed, layer, draw, token0, ntok, nchan):
     """Raw Philox words, ntok x nchan: word c%4 of block (c/4, token, draw, layer)."""
     out = np.empty((ntok, nchan), np.uint32)

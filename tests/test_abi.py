@@ -156,3 +156,58 @@ def test_block_rejects_bad_jobs_before_any_launch():
     assert L.dust_block_estimate((dust.DustLayerJob * 1)(good), 1, ctypes.c_void_p(4100),
                                  1 << 30, None, 0) == 3  # unaligned workspace
 
+
+
+def _gate_job(layer, base, sigma=0.05, K=8):
+    """A gate job on fake, 16-byte-aligned addresses starting at `base` (never
+    dereferenced: every call below must fail on the host)."""
+    T, C, d = 256, 64, 16
+    j = dust.DustLayerJob()
+    j.type = dust.JOB_ATTN_GATE
+    j.nz = dust.noise(1, sigma, K, layer)
+    j.T, j.seq_len, j.d_in, j.n1 = T, 128, d, C
+    step = T * C * 4
+    for k in range(3):
+        j.in_[k] = base + k * step
+    j.x = base + 3 * step
+    j.x_dtype = dust.DUST_F32
+    j.g_hat = base + 4 * step
+    j.G_W = base + 5 * step
+    return j
+
+
+def test_block_checks_every_job_before_queueing_anything():
+    """A bad sigma, gamma or missing input in the LAST job is reported as that
+    entry point's INVALID_ARG.  Job 0 is valid; had it been queued first, the
+    call on this GPU-less host would have failed with DUST_ERR_CUDA instead."""
+    L = dust.lib()
+    ws = ctypes.c_void_p(1 << 40)
+    good = _gate_job(3, 1 << 32)
+    for mutate in (lambda j: setattr(j.nz, "sigma", -1.0),
+                   lambda j: setattr(j.nz, "gamma", 2.0),
+                   lambda j: j.in_.__setitem__(1, None)):
+        last = _gate_job(4, 1 << 33)
+        mutate(last)
+        arr = (dust.DustLayerJob * 2)(good, last)
+        assert L.dust_block_estimate(arr, 2, ws, 1 << 30, None, 0) == 1
+    # the same two valid jobs get past every check and only then need the GPU
+    arr = (dust.DustLayerJob * 2)(good, _gate_job(4, 1 << 33))
+    assert L.dust_block_estimate(arr, 2, ws, 1 << 30, None, 0) == 4
+
+
+def test_block_rejects_jobs_whose_buffers_overlap():
+    L = dust.lib()
+    ws = ctypes.c_void_p(1 << 40)
+    a = _gate_job(3, 1 << 32)
+    b = _gate_job(4, 1 << 33)
+    b.G_W = a.G_W  # two passes writing one weight gradient
+    assert L.dust_block_estimate((dust.DustLayerJob * 2)(a, b), 2, ws, 1 << 30, None, 0) == 1
+    b = _gate_job(4, 1 << 33)
+    b.g_hat = a.in_[2]  # one pass writing what another reads
+    assert L.dust_block_estimate((dust.DustLayerJob * 2)(a, b), 2, ws, 1 << 30, None, 0) == 1
+    b = _gate_job(4, 1 << 33)
+    b.G_W = (1 << 40) + 512  # an output inside the workspace
+    assert L.dust_block_estimate((dust.DustLayerJob * 2)(a, b), 2, ws, 1 << 30, None, 0) == 1
+    c = _gate_job(3, 1 << 32)
+    c.g_hat = c.G_W  # one pass's two outputs on top of each other
+    assert L.dust_block_estimate((dust.DustLayerJob * 1)(c), 1, ws, 1 << 30, None, 0) == 1

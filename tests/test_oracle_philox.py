@@ -7,7 +7,8 @@ block b of a stream with word offset o is Philox4x32-10 of the 128-bit counter
 whose low 64 bits are B // 65536 and whose third word is B % 65536, where
 B = o / 4 + b, under the key (seed low word, seed high word).  This exercises
 counter words 0-2, both key words, every round and all four output words; the
-fourth counter word is compared against cuRAND's device API in the GPU tests.
+fourth counter word is compared against cuRAND's device API, run as a black
+box on the GPU, in tests/test_gpu_curand_device.py.
 
 The uniform map and Box-Muller step are pinned by exactness and by their
 distribution: moments, a Kolmogorov-Smirnov test against N(0, 1), channel
@@ -151,3 +152,13 @@ def test_ragged_channel_count(orc):
     full = orc.noise(5, 0, 3, 7, 3, 12)
     part = orc.noise(5, 0, 3, 7, 3, 10)
     np.testing.assert_array_equal(full[:, :10], part)
+
+
+def test_box_muller_on_words_matches_counter_normals(orc):
+    """oracle.box_muller (the map on given words) equals the C oracle's normals
+    of the same counters: two implementations of one map, written apart."""
+    seed, layer, draw, t0, ntok, nchan = 0xABCDEF0123, 2, 9, 77, 40, 64
+    w = orc.noise_words(seed, layer, draw, t0, ntok, nchan)
+    a = orc.noise(seed, layer, draw, t0, ntok, nchan)
+    got = orc.box_muller(w.reshape(-1, 2)).reshape(ntok, nchan)
+    np.testing.assert_allclose(got, a, rtol=0, atol=1e-12)
