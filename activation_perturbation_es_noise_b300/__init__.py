@@ -607,6 +607,19 @@ def block_estimate(jobs, streams=None, ws=None):
     return [(j.g, j.G) for j in jobs], ws
 
 
+# ------------------------------------------------------------ data parallel ----
+def sum_over_ranks(G, group=None):
+    """The one exchange of a data-parallel estimator step: with the sequences of
+    a batch sharded across ranks (each rank estimating its own tokens, noise
+    keyed by the global token index), the weight gradient is the sum of the
+    ranks' G_W, reduced in place by an all-reduce (NCCL between GPUs, gloo on
+    CPU).  A no-op without an initialised process group of two or more ranks."""
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size(group) > 1:
+        dist.all_reduce(G, op=dist.ReduceOp.SUM, group=group)
+    return G
+
+
 # ---------------------------------------------------------------- probes ----
 PROBE_OPS_PER_ROUND = {0: 16, 1: 8, 2: 8, 3: 16, 4: 16}  # per thread and round
 

@@ -109,8 +109,8 @@ __global__ void __launch_bounds__(256) attn_noise_kernel(const NoiseArgs a, cons
             const uint32_t token = a.token0 + static_cast<uint32_t>(sq * a.L + t);
             const BlockHalf bh = philox_block_half(j, a.layer, keys);
             const uint32_t draw = a.draw_first + d;
-            n0 = words_to_normals(philox_rest(philox_draw_half(draw, token, keys), bh, keys));
-            n1 = words_to_normals(philox_rest(philox_draw_half(draw, token + 1, keys), bh, keys));
+            n0 = words_to_normals_fast(philox_rest(philox_draw_half(draw, token, keys), bh, keys));
+            n1 = words_to_normals_fast(philox_rest(philox_draw_half(draw, token + 1, keys), bh, keys));
         }
         const float v0[4] = {n0.x, n0.y, n0.z, n0.w}, v1[4] = {n1.x, n1.y, n1.z, n1.w};
         const int64_t row0 = static_cast<int64_t>(y) * kDv + jb * 4;
@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(256) attn_gate_dl_kernel(const GateArgs a, con
         const DrawHalf dh = philox_draw_half(a.draw0 + static_cast<uint32_t>(i), token, keys);
         float part = 0.f;
         for (int j = lane; j < nblk; j += 32) {
-            const float4 n = words_to_normals(philox_rest(dh, philox_block_half(j, a.layer, keys), keys));
+            const float4 n = words_to_normals_fast(philox_rest(dh, philox_block_half(j, a.layer, keys), keys));
             const float4 z = __ldg(reinterpret_cast<const float4*>(a.z + row) + j);
             const float4 o = __ldg(reinterpret_cast<const float4*>(a.o + row) + j);
             const float4 e = __ldg(reinterpret_cast<const float4*>(a.E + row) + j);

@@ -40,8 +40,9 @@ constexpr int kHd = 64;       // channels per head
 constexpr int kQKRows = 128;  // query rows per CTA
 
 // e^x - 1 for the score shifts: x (1 + x/2 + x^2/6 + x^3/24) for |x| < 1/8
-// (truncation below 2e-6 relative there, under the 2^-16 of the bf16 split
-// the result goes through next, and no cancellation), else expm1f.
+// (truncation about 2e-6 relative at x = 1/8 and 2.2e-6 at x = -1/8, under
+// the 2^-16 of the bf16 split the result goes through next, and no
+// cancellation), else expm1f.
 __device__ __forceinline__ float expm1_shift(float x) {
     if (fabsf(x) < 0.125f) {
         float q = fmaf(x, 1.0f / 24.0f, 1.0f / 6.0f);
@@ -309,9 +310,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         n0 = ld4(a.Q + (tok0 + row) * C + 4 * jb);
                         n1 = ld4(a.Q + (tok0 + row) * C + 4 * jb + 4);
                     } else {
-                        n0 = words_to_normals(philox_rest(
+                        n0 = words_to_normals_fast(philox_rest(
                             dh, philox_block_half(static_cast<uint32_t>(jb), a.layer, keys), keys));
-                        n1 = words_to_normals(philox_rest(
+                        n1 = words_to_normals_fast(philox_rest(
                             dh, philox_block_half(static_cast<uint32_t>(jb + 1), a.layer, keys), keys));
                     }
                     uint32_t hi[4], lo[4];
@@ -446,7 +447,7 @@ __global__ void qk_key_noise_kernel(int nd, int64_t T, int C, uint32_t draw_firs
         const int64_t dt = idx / nb;  // d T + t
         const int d = static_cast<int>(dt / T);
         const int64_t t = dt - static_cast<int64_t>(d) * T;
-        const float4 v = words_to_normals(philox4x32_10(static_cast<uint32_t>(jb),
+        const float4 v = words_to_normals_fast(philox4x32_10(static_cast<uint32_t>(jb),
                                                         token0 + static_cast<uint32_t>(t),
                                                         draw_first + static_cast<uint32_t>(d), layer,
                                                         keys));

@@ -11,12 +11,14 @@
 // The scratch is a file-scope __device__ array of kEmbedStaticScratchBytes
 // (32 MiB; enough for 16384 tokens x 1536 channels over 4096 rows).  Every GPU
 // that loads the library holds it until the process exits.  Its device address
-// is looked up once per device (cudaGetSymbolAddress, with that device
-// current) by the first call made on that device, so that first call should
-// come before any stream capture.  Every call shares the one array, and the
-// embedding pipeline clears the parts it needs zeroed on each call; two calls
-// that overlap on the GPU (different streams, no ordering between them) race
-// on it.
+// is looked up once per device and context (cudaGetSymbolAddress, with that
+// device current) by the first call made there, so that first call should
+// come before any stream capture; a call that finds a different context on
+// the device (the primary context was reset and recreated) looks the address
+// up again, since the module may then sit elsewhere.  Every call shares the
+// one array, and the embedding pipeline clears the parts it needs zeroed on
+// each call; two calls that overlap on the GPU (different streams, no
+// ordering between them) race on it.
 #include <mutex>
 
 #include "dust_common.cuh"
@@ -31,7 +33,28 @@ constexpr int kMaxDevices = 64;
 __device__ __align__(256) uint8_t g_embed_scratch[kEmbedStaticScratchBytes];
 
 void* g_scratch_addr[kMaxDevices];
+void* g_scratch_ctx[kMaxDevices];  // the context the address was looked up in
 std::mutex g_scratch_mutex;
+
+// The driver's cuCtxGetCurrent, reached through the runtime (the library links
+// no driver library of its own).
+using CtxGetCurrentFn = int (*)(void**);
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+        else
+            (void)cudaGetLastError();
+    }
+    return fn;
+}
 
 // Device address of the scratch on the current device.  In host code the name
 // g_embed_scratch is only a host-side handle, never a device address.
@@ -43,13 +66,21 @@ dust_status scratch_address(void** out) {
     }
     if (dev < 0 || dev >= kMaxDevices) return DUST_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
+    const CtxGetCurrentFn cur = ctx_get_current();
+    if (!cur) return DUST_ERR_CUDA;
+    void* ctx = nullptr;
+    if (cur(&ctx) != 0) return DUST_ERR_CUDA;
+    if (g_scratch_addr[dev] == nullptr || ctx == nullptr || g_scratch_ctx[dev] != ctx) {
+        // (the lookup makes the device's primary context current if this
+        // thread has none yet; the context is read again after it)
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_embed_scratch) != cudaSuccess || p == nullptr) {
             (void)cudaGetLastError();
             return DUST_ERR_CUDA;
         }
+        if (cur(&ctx) != 0 || ctx == nullptr) return DUST_ERR_CUDA;
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_addr[dev];
     return DUST_OK;

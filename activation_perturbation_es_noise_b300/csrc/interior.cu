@@ -129,7 +129,7 @@ __global__ void interior_dh_kernel(const DhArgs a, const PhiloxKeys keys) {
             __nv_bfloat16* row = a.A1 + chunk_row(t, i, a.nd) * (2 * static_cast<int64_t>(a.C));
             __nv_bfloat16 h[4], l[4];
             if (valid) {
-                const float4 nrm = words_to_normals(
+                const float4 nrm = words_to_normals_fast(
                     philox_rest(philox_draw_half(a.draw_first + i, a.token0 + t, keys), bh, keys));
                 float d[4];
                 if (a.taylor) {
@@ -331,7 +331,7 @@ __global__ void interior_ghat_kernel(const GhatArgs a, const PhiloxKeys keys) {
             for (int u = 0; u < 2; ++u) w[u] = philox_rest(dh, bh[u], keys);
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                const float4 nrm = words_to_normals(w[u]);
+                const float4 nrm = words_to_normals_fast(w[u]);
                 acc[u].x = fmaf(ri, nrm.x, acc[u].x);
                 acc[u].y = fmaf(ri, nrm.y, acc[u].y);
                 acc[u].z = fmaf(ri, nrm.z, acc[u].z);

@@ -217,8 +217,13 @@ __device__ __forceinline__ void box_muller_fast(uint32_t w_even, uint32_t w_odd,
     a_sin = -rho * s;
 }
 
-// clog = -2 ln(2) scale^2: the normals come out multiplied by scale.
-__device__ __forceinline__ float4 words_to_normals_fast(uint4 w, float clog) {
+// clog = -2 ln(2) scale^2: the normals come out multiplied by scale (the
+// default, kClogUnit, gives standard normals).  Every estimator kernel draws
+// its noise through this form, so the perturbation of a draw and the noise
+// its error estimate is weighted by are the same numbers.
+constexpr float kClogUnit = -1.3862943611198906f;
+
+__device__ __forceinline__ float4 words_to_normals_fast(uint4 w, float clog = kClogUnit) {
     float4 a;
     box_muller_fast(w.x, w.y, a.x, a.y, clog);
     box_muller_fast(w.z, w.w, a.z, a.w, clog);

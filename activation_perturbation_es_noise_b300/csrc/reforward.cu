@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float4 c1 = __ldg(cp), c2 = __ldg(cp + 1);
                             const float4 c3 = __ldg(cp + 2), c4 = __ldg(cp + 3);
                             const float4 nrm =
-                                words_to_normals(philox_rest(dhalf[m], bhalf, keys));
+                                words_to_normals_fast(philox_rest(dhalf[m], bhalf, keys));
                             const float e0 = a.sigma * nrm.x, e1 = a.sigma * nrm.y;
                             const float e2 = a.sigma * nrm.z, e3 = a.sigma * nrm.w;
                             const float d0 = e0 * fmaf(e0, fmaf(e0, fmaf(e0, c4.x, c3.x), c2.x), c1.x);
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t hi0 = 0, hi1 = 0, lo0 = 0, lo1 = 0;
                         if (t < a.T) {
                             const float4 nrm =
-                                words_to_normals(philox_rest(dhalf[m], bhalf, keys));
+                                words_to_normals_fast(philox_rest(dhalf[m], bhalf, keys));
                             const float4 y = yv[m], g = gv[m];
                             const float d0 = gelu_as(fmaf(a.sigma, nrm.x, y.x)) - g.x;
                             const float d1 = gelu_as(fmaf(a.sigma, nrm.y, y.y)) - g.y;

@@ -19,8 +19,10 @@ are larger than the 126 MB L2, so no flush is needed between steps.
                               attn_qk]
 
 Under torchrun (N > 1) every rank estimates its own batch (global token
-offset rank * T, so the noise differs per rank) with no collective on the data
-path; rank 0 prints the aggregate over the slowest rank's time.
+offset rank * T, so the noise differs per rank), and each step ends with the
+step's one exchange, the sum of the ranks' weight gradients (an NCCL
+all-reduce of G_W, inside the timed step); rank 0 prints the aggregate over
+the slowest rank's time.
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded
 sample of the same workload (the pages give no implementation to run).
@@ -185,8 +187,8 @@ def make_workload(name, device, rank):
 
 
 def make_step(wl, dust):
-    """Returns (step(), evals per step, launches per step) with outputs and
-    workspace allocated once."""
+    """Returns (step(), evals per step, launches per step, workspace, G_W) with
+    outputs and workspace allocated once."""
     import torch
     d = wl["dev"]
     if wl["kind"] == "head":
@@ -203,14 +205,14 @@ def make_step(wl, dust):
                 dust.head_estimate_chunked(d["logits"], d["targets"], d["x"], wl["sigma"], K, 1234,
                                            wl["vchunk"], token0=wl["token0"], out=(g, G), ws=ws)
             # lse, one draw kernel per chunk, the outer product
-            return step, K * T, 2 + V // wl["vchunk"], ws
+            return step, K * T, 2 + V // wl["vchunk"], ws, G
 
         def step():
             dust.head_estimate(d["logits"], d["targets"], d["x"], wl["sigma"], K, 1234, 0, 0,
                                wl["token0"], out=(g, G), ws=ws, baseline=wl["baseline"])
         launches = 2 + (0 if wl["x_bf16"] else 1)
         # antithetic pairs: two perturbed evaluations per noise draw
-        return step, K * T * (2 if wl["baseline"] == 2 else 1), launches, ws
+        return step, K * T * (2 if wl["baseline"] == 2 else 1), launches, ws, G
     if wl["kind"] == "interior":
         T, K = wl["T"], wl["K"]
         g = torch.empty((T, wl["C"]), dtype=torch.float32, device=d["x"].device)
@@ -236,7 +238,7 @@ def make_step(wl, dust):
         # GEMM 1 (+ EMA in its epilogue for whole token blocks per sequence), GEMM 2
         per_chunk = (2 if wl["seq_len"] % 128 == 0 else 3) if fused else 4
         # softmax (+ clean GELU when fused), per chunk, mean + scan + g, outer product
-        return step, K * T, (2 if fused else 1) + chunks * per_chunk + 3 + 1, ws
+        return step, K * T, (2 if fused else 1) + chunks * per_chunk + 3 + 1, ws, G
     if wl["kind"] == "embed":
         T, dd, V = wl["T"], wl["d"], wl["V"]
         G = torch.empty((V, dd), dtype=torch.float32, device=d["g"].device)
@@ -245,7 +247,7 @@ def make_step(wl, dust):
 
         def step():
             dust.embed_scatter(d["g"], d["ids"], V, out=(G, perm), ws=ws)
-        return step, T, 12, ws
+        return step, T, 12, ws, G
     raise SystemExit("bad workload")
 
 
@@ -367,6 +369,9 @@ def oracle_sample(wl, budget_s=12.0):
 def config_of(wl, n_gpus):
     c = {"workload": wl["name"], "tokens": wl["T"], "draws": wl["K"],
          "l2": "inputs larger than L2 (no flush)", "parallelism": "dp%d" % n_gpus}
+    if n_gpus > 1:
+        c["tokens_per_rank"] = wl["T"]
+        c["exchange"] = "G_W summed over ranks (all-reduce) every step"
     for k in ("V", "d", "C", "d_in", "d_model", "seq_len", "sigma", "gamma"):
         if k in wl:
             c[k] = wl[k]
@@ -690,7 +695,14 @@ def run_dust(args):
 
     dust.lib()
     wl = make_workload(args.workload, device, rank)
-    step, evals, launches, ws = make_step(wl, dust)
+    estimate, evals, launches, ws, G_out = make_step(wl, dust)
+
+    def step():
+        # one estimator call, then the step's one exchange (N > 1): the sum of
+        # the ranks' weight gradients
+        estimate()
+        if world > 1:
+            dust.sum_over_ranks(G_out)
     for _ in range(max(args.warmup, 3 if args.warmup >= 3 else args.warmup)):
         step()
     torch.cuda.synchronize()
@@ -808,6 +820,12 @@ def run_dust(args):
 
             def call(d):
                 dust.embed_scatter(d["g"], d["ids"], V, out=(G, perm), ws=wse)
+        estimate_call = call
+
+        def call(d):
+            estimate_call(d)
+            if world > 1:
+                dust.sum_over_ranks(G)
         Gh = torch.empty(G.shape, dtype=torch.float32).pin_memory()
         d2h = Gh.numel() * 4
         copy_s = torch.cuda.Stream(device=device)

@@ -252,8 +252,10 @@ dust_status dust_embed_scatter(const float* g_hat, const int32_t* ids, int64_t T
  * scratch is a fixed 32 MiB array inside the library (held on every GPU that
  * loads the library until the process exits).  Sizes whose workspace
  * (dust_embed_workspace) exceeds 32 MiB return DUST_ERR_UNSUPPORTED.  The
- * first call on a device looks up the array's device address, so make it
- * before any stream capture.  All calls share the array: calls that overlap on
+ * first call on a device looks up the array's device address (and so does the
+ * first call after the device's context was reset and recreated, where the
+ * array may have moved), so make it before any stream capture.  All calls
+ * share the array: calls that overlap on
  * the GPU race, so order them (one stream).  Device-side id errors go to the
  * shared array's status word and cannot be read back through this call.
  * Allocates nothing (no cudaMalloc, no allocating library routine).

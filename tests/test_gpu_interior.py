@@ -129,6 +129,30 @@ def test_interior_full_size_sequences(dust, orc, name, K, seqs):
     parity(g_sequences=worst, G_W_vs_g_x=eG)
 
 
+def test_interior_config_sequence_all_draws(dust, orc):
+    """The interior workload exactly as the bench times it (8 x 2048 tokens,
+    512 -> 2048, d_model 512, V 4096, K = 256: seven chunks of 37 draws, the
+    last one 34), sequence 0 against the oracle run on that sequence alone:
+    its 2048 rows of g, and its share of G_W1.  x enters only the outer
+    product (g depends on y1, not on x), so the call is made with x zeroed
+    outside sequence 0: G_W1 is then exactly sequence 0's share,
+    sum_{t in seq 0} g_t x_t^T, which the oracle's G of that sequence is."""
+    p, d = _full("interior", W.INTERIOR_PARAMS["interior"]["K"])
+    K, L = p["K"], p["seq_len"]
+    assert K == 256
+    d0 = dict(d)
+    x0 = np.zeros_like(d["x"])
+    x0[:L] = d["x"][:L]
+    d0["x"] = x0
+    g, G = _run(dust, d0, p["sigma"], p["gamma"], K, W.NOISE_SEED)
+    ref = _ref(orc, _seq(d, 0, L), p["sigma"], p["gamma"], K, W.NOISE_SEED, token0=0)
+    eg = rel_l2(g[:L], ref["g"])
+    assert eg <= G_TOL, eg
+    eG = rel_l2(G, ref["G"])
+    assert eG <= GW_TOL, eG
+    parity(g_seq0=eg, G_W_seq0=eG)
+
+
 @pytest.mark.parametrize("dm", [64, 576])
 def test_interior_exact_gelu_path(dust, orc, dm):
     """sigma = 0.05 (5.77 sigma > 0.15): the GELU difference is evaluated

@@ -4,8 +4,9 @@ Sequences are independent and the noise is keyed by the global token index,
 so ranks that each estimate their own slice of a batch (token offset
 rank * T_rank, as bench.py gives them) reproduce the single-rank result: the
 rows of g concatenate, and the per-rank weight gradients sum to the full one
-(the only exchange a data-parallel step would add).  The oracle stands in for
-the per-rank compute; the point here is the layout and the reductions.
+through the same helper bench.py's multi-rank step calls after every
+estimate (the step's one exchange).  The oracle stands in for the per-rank
+compute; the point here is the layout and the reductions.
 """
 import os
 import socket
@@ -39,6 +40,7 @@ def _worker(rank, world, port, out_path):
     sys.path.insert(0, ROOT)
     import bench
     import oracle
+    import activation_perturbation_es_noise_b300 as dust
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=world)
@@ -51,7 +53,7 @@ def _worker(rank, world, port, out_path):
     gathered = [torch.empty_like(g) for _ in range(world)]
     dist.all_gather(gathered, g)
     G = torch.from_numpy(res["G"])
-    dist.all_reduce(G, op=dist.ReduceOp.SUM)
+    dust.sum_over_ranks(G)
     slowest = bench.max_over_ranks(float(rank + 1), dist)
     if rank == 0:
         np.savez(out_path, g=torch.cat(gathered).numpy(), G=G.numpy(), slowest=slowest)
