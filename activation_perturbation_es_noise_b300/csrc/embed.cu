@@ -3,14 +3,30 @@
 // id_t (Dust translation, hn.213312.xyz, §2.2 信用分配, last sentences).
 //
 // Done without floating-point atomics so that the result is bitwise
-// reproducible:
-//   1. stable LSD radix sort of the ids (8-bit digits, 1024-token chunks):
-//      perm lists the tokens ordered by (id, t);
-//   2. every id's run of sorted tokens is cut into pieces of at most kPiece
-//      tokens; a CTA sums one piece's rows of g in ascending t;
-//   3. rows with one piece were written directly; rows with several pieces
-//      add their partial sums in piece order; rows no token hits are zero.
+// reproducible, in two launches:
+//   1. sort (one cooperative launch after a memset of its counters; a
+//      bounded grid-wide barrier between radix passes): per 1024-token chunk
+//      the sort keys (an id outside [0, V) becomes V, sorted last and left
+//      out), the first pass's digit counts and every id's token count
+//      (integer atomics, warp-aggregated: the same sums in any order); then
+//      one stable LSD radix scatter per 8-bit digit, each CTA deriving its
+//      chunk's scatter offsets from the digit counts of all chunks and
+//      counting the next pass's digits per output chunk; the last pass writes
+//      the permutation (tokens ordered by (id, t)).  Alongside, CTA 0 scans
+//      the id counts into segment starts, piece offsets (pieces of at most
+//      kPiece sorted tokens of one id) and the offsets of the ids no token
+//      hits, and every CTA then writes part of the piece table and the list
+//      of empty ids;
+//   2. rows: one warp per work unit, (piece, 512-column slice) or (empty id,
+//      slice).  A piece sums its rows of g in ascending t; a row with one
+//      piece is written directly.  A row with several writes partials and
+//      adds them as a two-level tree in a fixed order: the warp that finishes
+//      the last piece of a group of kGroup consecutive pieces (an integer
+//      counter per group and slice) adds the group's partials in piece order
+//      into the group's first partial, and the warp that finishes the row's
+//      last group adds the group sums in group order.  Empty rows are zero.
 #include <algorithm>
+#include <atomic>
 
 #include "dust_common.cuh"
 #include "internal.h"
@@ -18,10 +34,24 @@
 namespace dust {
 namespace {
 
-constexpr int kChunk = 1024;   // tokens per radix-sort CTA
+constexpr int kChunk = 1024;   // tokens per radix-sort chunk (one CTA's threads)
 constexpr int kPiece = 32;     // tokens per partial row sum
+constexpr int kGroup = 8;      // partials added together at the first level
+constexpr int kSliceF4 = 128;  // float4 columns (512 floats) per row work unit
+constexpr int kSliceF = 128;   // float columns per work unit without float4 rows
+constexpr int kRowThreads = 256;
 constexpr int64_t kMaxT = 1LL << 26;
 constexpr int64_t kMaxV = 1LL << 24;
+
+// Control words after the status word (word 0) of the workspace.
+enum { kBarCount = 8,   // grid barrier: CTAs arrived
+       kBarGen = 9,     // grid barrier: generation
+       kNPieces = 16,   // pieces in the table
+       kNEmpty = 17 };  // ids no token hits
+
+struct Piece {
+    int32_t v, start, len, multi;
+};
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
@@ -29,243 +59,542 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
-// Keys: valid ids as they are; an id outside [0, V) becomes V (sorted last,
-// left out of every row) and is recorded in the status word.
-__global__ void embed_keys_kernel(const int32_t* __restrict__ ids, int T, int V,
-                                  uint32_t* __restrict__ keys, int32_t* __restrict__ vals,
-                                  uint32_t* status) {
-    const int t = blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= T) return;
-    int id = ids[t];
-    if (id < 0 || id >= V) {
-        record_status(status, DUST_ERR_DEVICE_RANGE);
-        id = V;
-    }
-    keys[t] = static_cast<uint32_t>(id);
-    vals[t] = t;
-}
-
-// Per-chunk digit counts, stored digit-major: hist[digit * nchunks + chunk].
-__global__ void __launch_bounds__(kChunk)
-    radix_hist_kernel(const uint32_t* __restrict__ keys, int T, int shift, int nchunks,
-                      uint32_t* __restrict__ hist) {
-    __shared__ uint32_t cnt[256];
-    const int c = blockIdx.x;
-    if (threadIdx.x < 256) cnt[threadIdx.x] = 0;
-    __syncthreads();
-    const int i = c * kChunk + threadIdx.x;
-    if (i < T) atomicAdd(&cnt[(keys[i] >> shift) & 255u], 1u);
-    __syncthreads();
-    if (threadIdx.x < 256) hist[static_cast<int64_t>(threadIdx.x) * nchunks + c] = cnt[threadIdx.x];
-}
-
-// Exclusive prefix sum of n words in one CTA of 1024 threads; out[n] = total.
-// Block 1 of a two-block launch scans (in2, out2) instead, with each word w
-// taken as ceil(w / kPiece) when pieces2 is set (the pieces of each id).
-__global__ void __launch_bounds__(1024)
-    exclusive_scan_kernel(const uint32_t* __restrict__ in, uint32_t* __restrict__ out, int64_t n,
-                          const uint32_t* __restrict__ in2 = nullptr,
-                          uint32_t* __restrict__ out2 = nullptr, int pieces2 = 0) {
-    const bool second = blockIdx.x == 1;
-    if (second) {
-        in = in2;
-        out = out2;
-    }
-    __shared__ uint32_t wsum[32];
-    __shared__ uint32_t carry_s;
+// Exclusive prefix sums of NC word sequences at once, over n elements, by one
+// CTA of 1024 threads (4096 elements per round, with carries); f(i, v) fills
+// v[0..NC) for element i, out[c][i] receives the prefixes, tot[c] the totals.
+// Every thread of the CTA must call it.
+template <int NC, typename F>
+__device__ void cta_exclusive_scan(int64_t n, F f, uint32_t* const (&out)[NC],
+                                   uint32_t (&tot)[NC]) {
+    __shared__ uint32_t wsum[NC][32];
+    __shared__ uint32_t carry[NC];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) carry_s = 0;
+    if (tid < NC) carry[tid] = 0;
     __syncthreads();
     for (int64_t base = 0; base < n; base += 4 * 1024) {
-        uint32_t v[4];
-        uint32_t local = 0;
+        uint32_t v[4][NC], local[NC], incl[NC];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) local[c] = 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int64_t i = base + 4 * tid + k;
-            v[k] = i < n ? in[i] : 0u;
-            if (second && pieces2) v[k] = (v[k] + kPiece - 1) / kPiece;
-            local += v[k];
-        }
-        uint32_t incl = local;
+            if (i < n) {
+                f(i, v[k]);
+            } else {
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += y;
+                for (int c = 0; c < NC; ++c) v[k][c] = 0;
+            }
+#pragma unroll
+            for (int c = 0; c < NC; ++c) local[c] += v[k][c];
         }
-        if (lane == 31) wsum[warp] = incl;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            incl[c] = local[c];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl[c], o);
+                if (lane >= o) incl[c] += y;
+            }
+            if (lane == 31) wsum[c][warp] = incl[c];
+        }
         __syncthreads();
-        if (warp == 0) {
-            uint32_t w = wsum[lane];
+        if (warp < NC) {
+            const uint32_t w = wsum[warp][lane];
             uint32_t wi = w;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, wi, o);
                 if (lane >= o) wi += y;
             }
-            wsum[lane] = wi - w;  // exclusive prefix of warp totals
+            wsum[warp][lane] = wi - w;  // exclusive prefix of warp totals
         }
         __syncthreads();
-        const uint32_t carry = carry_s;
-        uint32_t run = carry + wsum[warp] + incl - local;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int64_t i = base + 4 * tid + k;
-            if (i < n) out[i] = run;
-            run += v[k];
+        for (int c = 0; c < NC; ++c) {
+            uint32_t run = carry[c] + wsum[c][warp] + incl[c] - local[c];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int64_t i = base + 4 * tid + k;
+                if (i < n) out[c][i] = run;
+                run += v[k][c];
+            }
+            if (tid == 1023) incl[c] = run;  // this round's end
         }
         __syncthreads();
-        if (tid == 1023) carry_s = run;
+        if (tid == 1023) {
+#pragma unroll
+            for (int c = 0; c < NC; ++c) carry[c] = incl[c];
+        }
         __syncthreads();
     }
-    if (tid == 0) out[n] = carry_s;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) tot[c] = carry[c];
+    __syncthreads();  // every thread has read the totals before carry[] is reused
 }
 
-// Stable scatter of one radix pass.  Within a chunk the rank of a token among
-// earlier tokens with the same digit is (tokens of that digit in earlier
-// warps) + (earlier lanes of this warp with that digit).
-__global__ void __launch_bounds__(kChunk)
-    radix_scatter_kernel(const uint32_t* __restrict__ keys_in, const int32_t* __restrict__ vals_in,
-                         int T, int shift, int nchunks, const uint32_t* __restrict__ offs,
-                         uint32_t* __restrict__ keys_out, int32_t* __restrict__ vals_out) {
-    __shared__ uint32_t wcnt[32][256];
-    const int c = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int k = tid; k < 32 * 256; k += kChunk) (&wcnt[0][0])[k] = 0;
+// Grid-wide barrier of the cooperative sort launch (all CTAs resident):
+// ctl[kBarCount] counts arrivals, the last arriver resets it and bumps
+// ctl[kBarGen].  The wait is bounded: past kWaitLimitNs the CTA records
+// DUST_ERR_TIMEOUT and the barrier returns false in all its threads.
+__device__ bool grid_barrier(uint32_t* ctl) {
+    __shared__ bool ok;
     __syncthreads();
-    const int i = c * kChunk + tid;
-    const bool valid = i < T;
-    const uint32_t key = valid ? keys_in[i] : 0u;
-    const uint32_t dig = valid ? (key >> shift) & 255u : 256u;  // 256: padding lane
-    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, dig);
-    const uint32_t lrank = __popc(peers & lanemask_lt());
-    if (valid && lrank == 0) wcnt[warp][dig] = __popc(peers);
-    __syncthreads();
-    if (tid < 256) {
-        uint32_t acc = 0;
-        for (int w = 0; w < 32; ++w) {
-            const uint32_t x = wcnt[w][tid];
-            wcnt[w][tid] = acc;
-            acc += x;
+    if (threadIdx.x == 0) {
+        volatile uint32_t* gen = ctl + kBarGen;
+        const uint32_t g0 = *gen;
+        __threadfence();
+        bool good = true;
+        if (atomicAdd(ctl + kBarCount, 1u) + 1 == gridDim.x) {
+            atomicExch(ctl + kBarCount, 0u);
+            __threadfence();
+            atomicAdd(ctl + kBarGen, 1u);
+        } else {
+            const uint64_t t0 = globaltimer_ns();
+            while (*gen == g0) {
+                if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                    record_status(ctl, DUST_ERR_TIMEOUT);
+                    good = false;
+                    break;
+                }
+            }
         }
+        __threadfence();
+        ok = good;
     }
     __syncthreads();
-    if (valid) {
-        const uint32_t pos = offs[static_cast<int64_t>(dig) * nchunks + c] + wcnt[warp][dig] + lrank;
-        keys_out[pos] = key;
-        vals_out[pos] = vals_in[i];
-    }
+    return ok;
 }
 
-// counts[v] = number of sorted tokens with key v (keys sorted; v < V).
-__global__ void key_counts_kernel(const uint32_t* __restrict__ keys, int T, int V,
-                                  uint32_t* __restrict__ counts) {
-    const int k = blockIdx.x * blockDim.x + threadIdx.x;
-    if (k >= T) return;
-    const uint32_t key = keys[k];
-    if (key >= static_cast<uint32_t>(V)) return;
-    const bool first = (k == 0) || keys[k - 1] != key;
-    if (!first) return;
-    int e = k + 1;  // run end by binary search over the sorted keys
-    int lo = k + 1, hi = T;
-    while (lo < hi) {
-        const int mid = lo + ((hi - lo) >> 1);
-        if (keys[mid] == key) lo = mid + 1; else hi = mid;
-    }
-    e = lo;
-    counts[key] = static_cast<uint32_t>(e - k);
-}
-
-struct Piece {
-    int32_t v, start, len, multi;
+struct SortArgs {
+    const int32_t* ids;
+    int T, V, nchunks, passes, nslices;
+    uint32_t* keys[2];  // ping-pong sort keys (id, or V for an invalid id)
+    int32_t* vals[2];   // ping-pong token indices
+    int32_t* perm_out;  // the last pass's values, or null
+    uint32_t* hist;     // passes x 256 x nchunks digit counts
+    uint32_t* offs;     // their exclusive prefix sums
+    uint32_t* cnt;      // V tokens per id
+    uint32_t* seg;      // V first sorted position of every id
+    uint32_t* poff;     // V + 1 first piece of every id
+    uint32_t* eoff;     // V empty ids before every id
+    Piece* table;
+    int32_t* empty;     // ids with no token, in order
+    uint32_t* row_done; // V x nslices counters of the rows kernel
+    uint32_t* group_done;  // np_max x nslices counters of the rows kernel
+    int64_t np_max;
+    uint32_t* ctl;      // workspace control words (status word 0)
 };
 
-__global__ void piece_table_kernel(const uint32_t* __restrict__ seg, const uint32_t* __restrict__ counts,
-                                   const uint32_t* __restrict__ poff, int V, Piece* __restrict__ table) {
-    const int v = blockIdx.x * blockDim.x + threadIdx.x;
-    if (v >= V) return;
-    const uint32_t n = counts[v], p0 = poff[v], np = poff[v + 1] - p0;
-    for (uint32_t k = 0; k < np; ++k) {
-        Piece pc;
-        pc.v = v;
-        pc.start = static_cast<int32_t>(seg[v] + k * kPiece);
-        pc.len = static_cast<int32_t>(min(static_cast<uint32_t>(kPiece), n - k * kPiece));
-        pc.multi = np > 1;
-        table[p0 + k] = pc;
+// offs[d] for chunk c: tokens of every chunk with a smaller digit, plus
+// tokens of digit d in earlier chunks (the exclusive prefix of the
+// digit-major counts hist[d][c]).  Threads 0..255 take one digit each.
+__device__ void chunk_offsets(const uint32_t* hist, int nchunks, int c, uint32_t* offs) {
+    __shared__ uint32_t tot[256];
+    const int tid = threadIdx.x;
+    uint32_t pre = 0;
+    if (tid < 256) {
+        uint32_t t = 0;
+        const uint32_t* row = hist + static_cast<int64_t>(tid) * nchunks;
+        for (int k = 0; k < nchunks; ++k) {
+            const uint32_t h = __ldcg(row + k);
+            pre += k < c ? h : 0u;
+            t += h;
+        }
+        tot[tid] = t;
+    }
+    __syncthreads();
+    if (tid < 32) {  // exclusive scan of the 256 digit totals, 8 per lane
+        uint32_t v[8], local = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            v[k] = tot[8 * tid + k];
+            local += v[k];
+        }
+        uint32_t incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (tid >= o) incl += y;
+        }
+        uint32_t run = incl - local;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            tot[8 * tid + k] = run;
+            run += v[k];
+        }
+    }
+    __syncthreads();
+    if (tid < 256) offs[tid] = tot[tid] + pre;
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kChunk) embed_sort_kernel(const SortArgs a) {
+    __shared__ uint32_t wcnt[32][256];
+    __shared__ uint32_t choffs[256];
+    const int tid = threadIdx.x;
+    const int64_t gthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid;
+    const int64_t hist_words = static_cast<int64_t>(256) * a.nchunks;
+
+    // The rows kernel's counters (nothing here uses them).
+    for (int64_t k = gtid; k < static_cast<int64_t>(a.V) * a.nslices; k += gthreads)
+        a.row_done[k] = 0;
+    for (int64_t k = gtid; k < a.np_max * a.nslices; k += gthreads) a.group_done[k] = 0;
+
+    // Keys, the first digit's counts per chunk, tokens per id (cnt and the
+    // later passes' digit counts were cleared by the caller's memset).
+    uint32_t* h = &wcnt[0][0];
+    for (int c = blockIdx.x; c < a.nchunks; c += gridDim.x) {
+        __syncthreads();
+        if (tid < 256) h[tid] = 0;
+        __syncthreads();
+        const int t = c * kChunk + tid;
+        const bool valid = t < a.T;
+        uint32_t key = 0xFFFFFFFFu;
+        if (valid) {
+            int id = __ldg(a.ids + t);
+            if (id < 0 || id >= a.V) {
+                record_status(a.ctl, DUST_ERR_DEVICE_RANGE);
+                id = a.V;
+            }
+            key = static_cast<uint32_t>(id);
+            a.keys[0][t] = key;
+            a.vals[0][t] = t;
+            atomicAdd(&h[key & 255u], 1u);
+        }
+        // one atomic per distinct id in the warp
+        const bool counted = valid && key < static_cast<uint32_t>(a.V);
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, counted ? key : 0xFFFFFFFFu);
+        if (counted && (peers & lanemask_lt()) == 0) atomicAdd(a.cnt + key, __popc(peers));
+        __syncthreads();
+        if (tid < 256) a.hist[static_cast<int64_t>(tid) * a.nchunks + c] = h[tid];
+    }
+
+    int cur = 0;
+    for (int pass = 0; pass < a.passes; ++pass) {
+        if (!grid_barrier(a.ctl)) return;
+        if (pass == 1) {
+            // the piece table and the empty-id list (offsets from CTA 0, before
+            // the barrier just passed)
+            for (int64_t v = gtid; v < a.V; v += gthreads) {
+                const uint32_t n = __ldcg(a.cnt + v);
+                if (n == 0) {
+                    a.empty[__ldcg(a.eoff + v)] = static_cast<int32_t>(v);
+                    continue;
+                }
+                const uint32_t p0 = __ldcg(a.poff + v), s0 = __ldcg(a.seg + v);
+                const uint32_t np = (n + kPiece - 1) / kPiece;
+                for (uint32_t k = 0; k < np; ++k) {
+                    Piece pc;
+                    pc.v = static_cast<int32_t>(v);
+                    pc.start = static_cast<int32_t>(s0 + k * kPiece);
+                    pc.len = static_cast<int32_t>(min(static_cast<uint32_t>(kPiece), n - k * kPiece));
+                    pc.multi = np > 1;
+                    a.table[p0 + k] = pc;
+                }
+            }
+        }
+        const bool last = pass == a.passes - 1;
+        const uint32_t* hist_cur = a.hist + pass * hist_words;
+        uint32_t* hist_next = last ? nullptr : a.hist + (pass + 1) * hist_words;
+        const uint32_t* keys_in = a.keys[cur];
+        const int32_t* vals_in = a.vals[cur];
+        uint32_t* keys_out = a.keys[cur ^ 1];
+        int32_t* vals_out = (last && a.perm_out) ? a.perm_out : a.vals[cur ^ 1];
+        const int shift = 8 * pass;
+        const int lane = tid & 31, warp = tid >> 5;
+        // Stable scatter of each chunk of this CTA: the rank of a token among
+        // earlier tokens of its chunk with the same digit is (tokens of that
+        // digit in earlier warps) + (earlier lanes of this warp with it).
+        for (int c = blockIdx.x; c < a.nchunks; c += gridDim.x) {
+            chunk_offsets(hist_cur, a.nchunks, c, choffs);
+            for (int k = tid; k < 32 * 256; k += kChunk) (&wcnt[0][0])[k] = 0;
+            __syncthreads();
+            const int i = c * kChunk + tid;
+            const bool valid = i < a.T;
+            const uint32_t key = valid ? __ldcg(keys_in + i) : 0u;
+            const uint32_t dig = valid ? (key >> shift) & 255u : 256u;  // 256: padding lane
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, dig);
+            const uint32_t lrank = __popc(peers & lanemask_lt());
+            if (valid && lrank == 0) wcnt[warp][dig] = __popc(peers);
+            __syncthreads();
+            if (tid < 256) {
+                uint32_t acc = 0;
+                for (int w = 0; w < 32; ++w) {
+                    const uint32_t x = wcnt[w][tid];
+                    wcnt[w][tid] = acc;
+                    acc += x;
+                }
+            }
+            __syncthreads();
+            if (valid) {
+                const uint32_t pos = choffs[dig] + wcnt[warp][dig] + lrank;
+                keys_out[pos] = key;
+                vals_out[pos] = __ldcg(vals_in + i);
+                if (hist_next) {
+                    const uint32_t d2 = (key >> (shift + 8)) & 255u;
+                    atomicAdd(hist_next + static_cast<int64_t>(d2) * a.nchunks + pos / kChunk, 1u);
+                }
+            }
+            __syncthreads();  // wcnt and choffs are reused by the next chunk
+        }
+        if (pass == 0 && blockIdx.x == 0) {
+            // segment starts, piece offsets and empty-id offsets of every id
+            uint32_t* const out[3] = {a.seg, a.poff, a.eoff};
+            uint32_t tot[3];
+            cta_exclusive_scan<3>(a.V,
+                                  [&](int64_t v, uint32_t* x) {
+                                      const uint32_t n = __ldcg(a.cnt + v);
+                                      x[0] = n;
+                                      x[1] = (n + kPiece - 1) / kPiece;
+                                      x[2] = n == 0 ? 1u : 0u;
+                                  },
+                                  out, tot);
+            if (tid == 0) {
+                a.poff[a.V] = tot[1];
+                a.ctl[kNPieces] = tot[1];
+                a.ctl[kNEmpty] = tot[2];
+            }
+        }
+        cur ^= 1;
+    }
+    if (a.passes == 1) {  // (V < 256: no second pass to build the table beside)
+        if (!grid_barrier(a.ctl)) return;
+        for (int64_t v = gtid; v < a.V; v += gthreads) {
+            const uint32_t n = __ldcg(a.cnt + v);
+            if (n == 0) {
+                a.empty[__ldcg(a.eoff + v)] = static_cast<int32_t>(v);
+                continue;
+            }
+            const uint32_t p0 = __ldcg(a.poff + v), s0 = __ldcg(a.seg + v);
+            const uint32_t np = (n + kPiece - 1) / kPiece;
+            for (uint32_t k = 0; k < np; ++k) {
+                Piece pc;
+                pc.v = static_cast<int32_t>(v);
+                pc.start = static_cast<int32_t>(s0 + k * kPiece);
+                pc.len = static_cast<int32_t>(min(static_cast<uint32_t>(kPiece), n - k * kPiece));
+                pc.multi = np > 1;
+                a.table[p0 + k] = pc;
+            }
+        }
     }
 }
 
-// One CTA per piece: rows g[perm[start .. start+len)] summed in that order.
-// The piece's token indices are staged in shared memory first, so the row
-// loads of a thread do not wait on index loads and can all be in flight.
+struct RowArgs {
+    const float* g;
+    const int32_t* perm;
+    const Piece* table;
+    const uint32_t* poff;
+    const int32_t* empty;
+    const uint32_t* ctl;
+    uint32_t* row_done;    // V x nslices counters of finished groups (cleared by the sort)
+    uint32_t* group_done;  // pieces x nslices counters of finished pieces, at a group's
+                           // first piece (cleared by the sort)
+    int d, nslices;
+    float* G_E;
+    float* partial;  // npieces x d
+};
+
+// out[c] = sum_{q < n} rows[q * d + c], in order q = 0, 1, ..., for the warp's
+// four columns of a slice; the loads of two rows are in flight together.
 template <bool VEC>
-__global__ void piece_sum_kernel(const float* __restrict__ g, const int32_t* __restrict__ perm,
-                                 const Piece* __restrict__ table, const uint32_t* __restrict__ poff,
-                                 int V, int d, float* __restrict__ G_E, float* __restrict__ partial) {
-    __shared__ int32_t rows[kPiece];
-    const int npieces = static_cast<int>(poff[V]);
-    for (int pi = blockIdx.x; pi < npieces; pi += gridDim.x) {
-        const Piece pc = table[pi];
-        __syncthreads();
-        if (threadIdx.x < pc.len) rows[threadIdx.x] = __ldg(perm + pc.start + threadIdx.x);
-        __syncthreads();
-        float* dst = pc.multi ? partial + static_cast<int64_t>(pi) * d
-                              : G_E + static_cast<int64_t>(pc.v) * d;
-        if (VEC) {
-            const int d4 = d >> 2;
-            for (int c = threadIdx.x; c < d4; c += blockDim.x) {
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-                for (int r = 0; r < pc.len; ++r) {
-                    const float4 x = __ldg(reinterpret_cast<const float4*>(
-                                               g + static_cast<int64_t>(rows[r]) * d) + c);
-                    acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+__device__ __forceinline__ void add_rows_in_order(const float* rows, uint32_t n, int64_t d,
+                                                  int c0, int w, float* out) {
+    if (VEC) {
+        float4 acc[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (uint32_t q = 0; q < n; q += 2) {
+            float4 x[2][4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int c = c0 + 32 * k;
+                    x[j][k] = (q + j < n && c < w)
+                                  ? __ldcg(reinterpret_cast<const float4*>(rows + (q + j) * d) + c)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                reinterpret_cast<float4*>(dst)[c] = acc;
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                if (q + j < n)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        acc[k].x += x[j][k].x; acc[k].y += x[j][k].y;
+                        acc[k].z += x[j][k].z; acc[k].w += x[j][k].w;
+                    }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int c = c0 + 32 * k;
+            if (c < w) reinterpret_cast<float4*>(out)[c] = acc[k];
+        }
+    } else {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (uint32_t q = 0; q < n; q += 2) {
+            float x[2][4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int c = c0 + 32 * k;
+                    x[j][k] = (q + j < n && c < w) ? __ldcg(rows + (q + j) * d + c) : 0.f;
+                }
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                if (q + j < n)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) acc[k] += x[j][k];
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int c = c0 + 32 * k;
+            if (c < w) out[c] = acc[k];
+        }
+    }
+}
+
+// One warp per work unit: (piece, column slice) for every piece, then (empty
+// id, slice).  Lane l takes columns l, l + 32, l + 64, l + 96 of the slice
+// (float4 columns when VEC: d % 4 == 0 and 16-byte aligned rows).  The rows'
+// token indices are read once per lane and passed round by shuffles.
+template <bool VEC>
+__global__ void __launch_bounds__(kRowThreads) embed_rows_kernel(const RowArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gwarp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const int npieces = static_cast<int>(__ldg(a.ctl + kNPieces));
+    const int nempty = static_cast<int>(__ldg(a.ctl + kNEmpty));
+    const int64_t nunits = static_cast<int64_t>(npieces + nempty) * a.nslices;
+    const int w = VEC ? a.d >> 2 : a.d;  // columns of the element type
+    const int per = VEC ? kSliceF4 : kSliceF;
+    // A unit's piece and this lane's row index (one unit ahead: the next
+    // unit's table entry and row indices are read while this one streams).
+    auto fetch = [&](int64_t u, Piece& pc, int& myrow) {
+        pc.v = -1;
+        pc.len = 0;
+        myrow = 0;
+        if (u >= nunits) return;
+        const int item = static_cast<int>(u / a.nslices);
+        if (item >= npieces) {
+            pc.v = __ldg(a.empty + (item - npieces));
+            return;
+        }
+        pc = a.table[item];
+        myrow = lane < pc.len ? __ldg(a.perm + pc.start + lane) : 0;
+    };
+    Piece pc;
+    int myrow;
+    fetch(gwarp, pc, myrow);
+    for (int64_t u = gwarp; u < nunits; u += nwarps) {
+        Piece pn;
+        int rown;
+        fetch(u + nwarps, pn, rown);
+        const int item = static_cast<int>(u / a.nslices);
+        const int s = static_cast<int>(u - static_cast<int64_t>(item) * a.nslices);
+        const int c0 = s * per + lane;
+        if (item >= npieces) {  // an id no token hits: zeros
+            const int64_t v = pc.v;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int c = c0 + 32 * k;
+                if (c < w) {
+                    if (VEC)
+                        reinterpret_cast<float4*>(a.G_E + v * a.d)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    else
+                        a.G_E[v * a.d + c] = 0.f;
+                }
+            }
+            pc = pn;
+            myrow = rown;
+            continue;
+        }
+        float* dst = pc.multi ? a.partial + static_cast<int64_t>(item) * a.d
+                              : a.G_E + static_cast<int64_t>(pc.v) * a.d;
+        if (VEC) {
+            float4 acc[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+            for (int r = 0; r < pc.len; ++r) {
+                const float4* src = reinterpret_cast<const float4*>(
+                    a.g + static_cast<int64_t>(__shfl_sync(0xFFFFFFFFu, myrow, r)) * a.d);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int c = c0 + 32 * k;
+                    if (c < w) {
+                        const float4 x = __ldg(src + c);
+                        acc[k].x += x.x; acc[k].y += x.y; acc[k].z += x.z; acc[k].w += x.w;
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int c = c0 + 32 * k;
+                if (c < w) reinterpret_cast<float4*>(dst)[c] = acc[k];
             }
         } else {
-            for (int c = threadIdx.x; c < d; c += blockDim.x) {
-                float acc = 0.f;
-#pragma unroll 8
-                for (int r = 0; r < pc.len; ++r) acc += __ldg(g + static_cast<int64_t>(rows[r]) * d + c);
-                dst[c] = acc;
-            }
-        }
-    }
-}
-
-// Rows with no token -> 0; rows with several pieces -> sum of partials in
-// piece order; rows with one piece are already final.  blockIdx.y = row.
-template <bool VEC>
-__global__ void rows_finish_kernel(const uint32_t* __restrict__ poff, int V, int d,
-                                   const float* __restrict__ partial, float* __restrict__ G_E) {
-    for (int v = blockIdx.y; v < V; v += gridDim.y) {
-        const uint32_t p0 = __ldg(poff + v), np = __ldg(poff + v + 1) - p0;
-        if (np == 1) continue;
-        const int w = VEC ? d >> 2 : d;
-        for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < w; c += gridDim.x * blockDim.x) {
-            if (VEC) {
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (uint32_t k = 0; k < np; ++k) {
-                    const float4 x = __ldg(reinterpret_cast<const float4*>(
-                                               partial + static_cast<int64_t>(p0 + k) * d) + c);
-                    acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int r = 0; r < pc.len; ++r) {
+                const float* src =
+                    a.g + static_cast<int64_t>(__shfl_sync(0xFFFFFFFFu, myrow, r)) * a.d;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int c = c0 + 32 * k;
+                    if (c < w) acc[k] += __ldg(src + c);
                 }
-                reinterpret_cast<float4*>(G_E + static_cast<int64_t>(v) * d)[c] = acc;
-            } else {
-                float acc = 0.f;
-                for (uint32_t k = 0; k < np; ++k)
-                    acc += __ldg(partial + static_cast<int64_t>(p0 + k) * d + c);
-                G_E[static_cast<int64_t>(v) * d + c] = acc;
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int c = c0 + 32 * k;
+                if (c < w) dst[c] = acc[k];
             }
         }
+        if (pc.multi) {
+            // Two-level tree: the warp that completes a group of kGroup pieces
+            // adds them into the group's first partial; the warp that
+            // completes the row's last group adds the group sums into the row.
+            __threadfence();
+            __syncwarp();
+            const uint32_t p0 = a.poff[pc.v], np = a.poff[pc.v + 1] - p0;
+            const uint32_t k = static_cast<uint32_t>(item) - p0;  // piece within the row
+            const uint32_t gfirst = p0 + (k / kGroup) * kGroup;    // the group's first piece
+            const uint32_t gsize = min(static_cast<uint32_t>(kGroup), p0 + np - gfirst);
+            uint32_t fin = 0;
+            if (lane == 0)
+                fin = atomicAdd(a.group_done + static_cast<int64_t>(gfirst) * a.nslices + s,
+                                1u) == gsize - 1;
+            if (__shfl_sync(0xFFFFFFFFu, fin, 0)) {
+                __threadfence();
+                float* gdst = a.partial + static_cast<int64_t>(gfirst) * a.d;
+                add_rows_in_order<VEC>(gdst, gsize, a.d, c0, w, gdst);
+                __threadfence();
+                __syncwarp();
+                const uint32_t ng = (np + kGroup - 1) / kGroup;
+                fin = 0;
+                if (lane == 0)
+                    fin = atomicAdd(a.row_done + static_cast<int64_t>(pc.v) * a.nslices + s, 1u) ==
+                          ng - 1;
+                if (__shfl_sync(0xFFFFFFFFu, fin, 0)) {
+                    __threadfence();
+                    add_rows_in_order<VEC>(a.partial + static_cast<int64_t>(p0) * a.d, ng,
+                                           static_cast<int64_t>(kGroup) * a.d, c0, w,
+                                           a.G_E + static_cast<int64_t>(pc.v) * a.d);
+                }
+            }
+        }
+        pc = pn;
+        myrow = rown;
     }
 }
 
 struct EmbedPlan {
-    int nchunks, passes;
+    int nchunks, passes, nslices;
     int64_t np_max;
-    size_t off_k0, off_v0, off_k1, off_v1, off_hist, off_offs, off_cnt, off_seg, off_poff,
-        off_table, off_part, bytes;
+    size_t zero_bytes;  // [ctl | digit counts | id counts]: cleared before the sort
+    size_t off_hist, off_cnt, off_eoff, off_done, off_gdone, off_k0, off_v0, off_k1, off_v1, off_offs,
+        off_seg, off_poff, off_table, off_empty, off_part, bytes;
 };
 
 EmbedPlan embed_plan(int64_t T, int64_t d, int64_t V) {
@@ -274,24 +603,57 @@ EmbedPlan embed_plan(int64_t T, int64_t d, int64_t V) {
     int bits = 1;
     while ((1LL << bits) <= V) ++bits;  // keys are in [0, V]
     P.passes = (bits + 7) / 8;
+    // column slices per row: ceil(d/4 / 128) float4 or ceil(d / 128) float
+    // slices; the counters are sized for the larger count
+    P.nslices = static_cast<int>(ceil_div(d, kSliceF));
     P.np_max = ceil_div(T, kPiece) + (T < V ? T : V) + 1;
     const size_t Tn = static_cast<size_t>(T > 0 ? T : 1);
-    const size_t Vn = static_cast<size_t>(V) + 1;
+    const size_t Vn = static_cast<size_t>(V);
+    const size_t hist_words = static_cast<size_t>(256) * P.nchunks;
     WsLayout w;
     w.take(kCtlBytes);
+    P.off_hist = w.take(static_cast<size_t>(P.passes) * hist_words * 4);
+    P.off_cnt = w.take(Vn * 4);
+    P.zero_bytes = w.used;
+    P.off_eoff = w.take(Vn * 4);
+    P.off_done = w.take(Vn * static_cast<size_t>(P.nslices) * 4);
+    P.off_gdone = w.take(static_cast<size_t>(P.np_max) * static_cast<size_t>(P.nslices) * 4);
     P.off_k0 = w.take(Tn * 4);
     P.off_v0 = w.take(Tn * 4);
     P.off_k1 = w.take(Tn * 4);
     P.off_v1 = w.take(Tn * 4);
-    P.off_hist = w.take(static_cast<size_t>(256) * P.nchunks * 4);
-    P.off_offs = w.take((static_cast<size_t>(256) * P.nchunks + 1) * 4);
-    P.off_cnt = w.take(Vn * 4);
+    P.off_offs = w.take(static_cast<size_t>(P.passes) * hist_words * 4);
     P.off_seg = w.take(Vn * 4);
-    P.off_poff = w.take(Vn * 4);
+    P.off_poff = w.take((Vn + 1) * 4);
     P.off_table = w.take(static_cast<size_t>(P.np_max) * sizeof(Piece));
+    P.off_empty = w.take(Vn * 4);
     P.off_part = w.take(static_cast<size_t>(P.np_max) * static_cast<size_t>(d) * 4);
     P.bytes = w.used;
     return P;
+}
+
+// CTAs of the sort kernel that fit on the current device at once (the grid
+// of its cooperative launch is at most this), looked up once per device.
+int sort_grid_limit() {
+    static std::atomic<int> limit[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (dev < 0 || dev >= 64) return 0;
+    int cached = limit[dev].load(std::memory_order_acquire);
+    if (cached > 0) return cached;
+    int per_sm = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, embed_sort_kernel, kChunk, 0) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    cached = per_sm * sms;
+    limit[dev].store(cached, std::memory_order_release);
+    return cached;
 }
 
 }  // namespace
@@ -314,74 +676,64 @@ extern "C" dust_status dust_embed_scatter(const float* g_hat, const int32_t* ids
     if (!ws || ws_bytes < P.bytes || !aligned(ws, 256)) return DUST_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* w = static_cast<uint8_t*>(ws);
-    uint32_t* status = static_cast<uint32_t*>(ws);
-    DUST_CUDA_TRY(cudaMemsetAsync(ws, 0, kCtlBytes, s));
+    uint32_t* ctl = static_cast<uint32_t*>(ws);
     if (T == 0) {
+        DUST_CUDA_TRY(cudaMemsetAsync(ws, 0, kCtlBytes, s));
         DUST_CUDA_TRY(cudaMemsetAsync(G_E, 0, static_cast<size_t>(V * d) * 4, s));
         return DUST_OK;
     }
-    const int Ti = static_cast<int>(T), Vi = static_cast<int>(V), di = static_cast<int>(d);
-    uint32_t* k0 = reinterpret_cast<uint32_t*>(w + P.off_k0);
-    int32_t* v0 = reinterpret_cast<int32_t*>(w + P.off_v0);
-    uint32_t* k1 = reinterpret_cast<uint32_t*>(w + P.off_k1);
-    int32_t* v1 = reinterpret_cast<int32_t*>(w + P.off_v1);
-    uint32_t* hist = reinterpret_cast<uint32_t*>(w + P.off_hist);
-    uint32_t* offs = reinterpret_cast<uint32_t*>(w + P.off_offs);
-    uint32_t* cnt = reinterpret_cast<uint32_t*>(w + P.off_cnt);
-    uint32_t* seg = reinterpret_cast<uint32_t*>(w + P.off_seg);
-    uint32_t* poff = reinterpret_cast<uint32_t*>(w + P.off_poff);
-    Piece* table = reinterpret_cast<Piece*>(w + P.off_table);
-    float* part = reinterpret_cast<float*>(w + P.off_part);
-    dust_status st;
-
-    const unsigned tb = static_cast<unsigned>(ceil_div(T, 256));
-    embed_keys_kernel<<<tb, 256, 0, s>>>(ids, Ti, Vi, k0, v0, status);
-    if ((st = launch_status()) != DUST_OK) return st;
-    for (int pass = 0; pass < P.passes; ++pass) {
-        const int shift = 8 * pass;
-        // the last pass writes the permutation straight into perm_out
-        int32_t* vout = (pass == P.passes - 1 && perm_out) ? perm_out : v1;
-        radix_hist_kernel<<<P.nchunks, kChunk, 0, s>>>(k0, Ti, shift, P.nchunks, hist);
-        exclusive_scan_kernel<<<1, 1024, 0, s>>>(hist, offs, static_cast<int64_t>(256) * P.nchunks);
-        radix_scatter_kernel<<<P.nchunks, kChunk, 0, s>>>(k0, v0, Ti, shift, P.nchunks, offs, k1,
-                                                          vout);
-        if (vout != v1) v1 = vout;
-        if ((st = launch_status()) != DUST_OK) return st;
-        uint32_t* tk = k0; k0 = k1; k1 = tk;
-        int32_t* tv = v0; v0 = v1; v1 = tv;
-    }
-    // k0/v0 now hold the sorted keys and the permutation.
-    DUST_CUDA_TRY(cudaMemsetAsync(cnt, 0, static_cast<size_t>(V + 1) * 4, s));
-    key_counts_kernel<<<tb, 256, 0, s>>>(k0, Ti, Vi, cnt);
-    // segment starts and piece offsets in one launch
-    exclusive_scan_kernel<<<2, 1024, 0, s>>>(cnt, seg, V, cnt, poff, 1);
-    const unsigned vb = static_cast<unsigned>(ceil_div(V, 256));
-    piece_table_kernel<<<vb, 256, 0, s>>>(seg, cnt, poff, Vi, table);
-    if ((st = launch_status()) != DUST_OK) return st;
-    // Pieces are at most np_max; launch enough CTAs to cover the usual count
-    // and let the grid-stride loop take the rest.
+    const int limit = sort_grid_limit();
+    if (limit < 1) return DUST_ERR_CUDA;
     const bool vec = (d % 4 == 0) && aligned(g_hat, 16) && aligned(G_E, 16);
-    // one CTA per piece
-    const int threads = static_cast<int>(std::min<int64_t>(256, round_up(vec ? d / 4 : d, 32)));
-    const unsigned pgrid = static_cast<unsigned>(std::min<int64_t>(P.np_max, 148 * 64));
-    timer_begin(s);
-    if (vec)
-        piece_sum_kernel<true><<<pgrid, threads, 0, s>>>(g_hat, v0, table, poff, Vi, di, G_E,
-                                                         part);
-    else
-        piece_sum_kernel<false><<<pgrid, threads, 0, s>>>(g_hat, v0, table, poff, Vi, di, G_E,
-                                                          part);
-    timer_end(s);
-    if ((st = launch_status()) != DUST_OK) return st;
+
+    SortArgs sa{};
+    sa.ids = ids;
+    sa.T = static_cast<int>(T);
+    sa.V = static_cast<int>(V);
+    sa.nchunks = P.nchunks;
+    sa.passes = P.passes;
+    sa.nslices = P.nslices;
+    sa.keys[0] = reinterpret_cast<uint32_t*>(w + P.off_k0);
+    sa.keys[1] = reinterpret_cast<uint32_t*>(w + P.off_k1);
+    sa.vals[0] = reinterpret_cast<int32_t*>(w + P.off_v0);
+    sa.vals[1] = reinterpret_cast<int32_t*>(w + P.off_v1);
+    sa.perm_out = perm_out;
+    sa.hist = reinterpret_cast<uint32_t*>(w + P.off_hist);
+    sa.offs = reinterpret_cast<uint32_t*>(w + P.off_offs);
+    sa.cnt = reinterpret_cast<uint32_t*>(w + P.off_cnt);
+    sa.seg = reinterpret_cast<uint32_t*>(w + P.off_seg);
+    sa.poff = reinterpret_cast<uint32_t*>(w + P.off_poff);
+    sa.eoff = reinterpret_cast<uint32_t*>(w + P.off_eoff);
+    sa.table = reinterpret_cast<Piece*>(w + P.off_table);
+    sa.empty = reinterpret_cast<int32_t*>(w + P.off_empty);
+    sa.row_done = reinterpret_cast<uint32_t*>(w + P.off_done);
+    sa.group_done = reinterpret_cast<uint32_t*>(w + P.off_gdone);
+    sa.np_max = P.np_max;
+    sa.ctl = ctl;
+    // the last pass's values: perm_out, or the ping-pong buffer it lands in
+    const int32_t* perm = perm_out ? perm_out : sa.vals[P.passes & 1];
+
+    timer_begin(s);  // the benchmark hook times the whole call
+    // status and barrier words, the later passes' digit counts, the id counts
+    DUST_CUDA_TRY(cudaMemsetAsync(ws, 0, P.zero_bytes, s));
     {
-        const int64_t w = vec ? d / 4 : d;
-        const dim3 fg(static_cast<unsigned>(ceil_div(w, 128)),
-                      static_cast<unsigned>(std::min<int64_t>(V, 65535)));
-        if (vec)
-            rows_finish_kernel<true><<<fg, 128, 0, s>>>(poff, Vi, di, part, G_E);
-        else
-            rows_finish_kernel<false><<<fg, 128, 0, s>>>(poff, Vi, di, part, G_E);
+        const unsigned grid = static_cast<unsigned>(std::min(P.nchunks, limit));
+        void* args[] = {&sa};
+        DUST_CUDA_TRY(cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(embed_sort_kernel),
+                                                  dim3(grid), dim3(kChunk), args, 0, s));
     }
-    if ((st = launch_status()) != DUST_OK) return st;
-    return DUST_OK;
+    RowArgs ra{g_hat, perm, reinterpret_cast<const Piece*>(w + P.off_table),
+               reinterpret_cast<const uint32_t*>(w + P.off_poff),
+               reinterpret_cast<const int32_t*>(w + P.off_empty), ctl,
+               reinterpret_cast<uint32_t*>(w + P.off_done),
+               reinterpret_cast<uint32_t*>(w + P.off_gdone), static_cast<int>(d),
+               static_cast<int>(vec ? ceil_div(d / 4, kSliceF4) : ceil_div(d, kSliceF)), G_E,
+               reinterpret_cast<float*>(w + P.off_part)};
+    const unsigned rgrid = 148 * 8;
+    if (vec)
+        embed_rows_kernel<true><<<rgrid, kRowThreads, 0, s>>>(ra);
+    else
+        embed_rows_kernel<false><<<rgrid, kRowThreads, 0, s>>>(ra);
+    timer_end(s);
+    return launch_status();
 }

@@ -411,7 +411,8 @@ __global__ void head_finalize_kernel(const HeadArgs A) {
 // one-warp CTAs, 128 for the 4096-entry vocabulary), else 0 (blockDim.x, up
 // to 256): constant strides keep the shared-memory addressing off the
 // integer multiplier that Philox saturates.
-template <int NB, bool ONE_WARP, int NTC>
+// FIXED: the sums are reduced in fixed point (qscale > 0), else as floats.
+template <int NB, bool ONE_WARP, int NTC, bool FIXED>
 __global__ void __launch_bounds__(NTC == 0 ? 256 : NTC, NTC == 32 ? 16 : (NTC == 128 ? 4 : 2))
     head_pair_kernel(const HeadArgs A, const PhiloxKeys keys) {
     extern __shared__ float4 pair_smem[];
@@ -489,7 +490,7 @@ __global__ void __launch_bounds__(NTC == 0 ? 256 : NTC, NTC == 32 ? 16 : (NTC ==
         for (int k = 0; k < 4; ++k) s1[b][k] = s0[b][k] = 0.f;
     float sdl = 0.f;
     const uint32_t token = A.token0 + static_cast<uint32_t>(t);
-    const bool fixed = A.qscale > 0.f;
+    constexpr bool fixed = FIXED;
     if (!ONE_WARP) __syncthreads();  // qsum zeroed before the first pass adds to it
 
     int pass = 0;
@@ -719,18 +720,27 @@ void set_noise_scales(HeadArgs& A, double s) {
 
 size_t pair_smem_bytes(int nb, int nt) { return static_cast<size_t>(3) * nb * nt * 16; }
 
-template <int NB, bool OW, int NTC>
-dust_status launch_pairs(const HeadPlan& P, const HeadArgs& A, const PhiloxKeys& keys, int64_t T,
-                         cudaStream_t s) {
+template <int NB, bool OW, int NTC, bool FIXED>
+dust_status launch_pairs_as(const HeadPlan& P, const HeadArgs& A, const PhiloxKeys& keys,
+                            int64_t T, cudaStream_t s) {
     static std::atomic<uint64_t> smem_set{0};
     // the kernel's largest dynamic shared memory (up to 256 threads when NTC = 0)
     const size_t smem_max = pair_smem_bytes(NB, NTC == 0 ? 256 : NTC);
     const size_t smem = pair_smem_bytes(NB, P.nt);
-    DUST_CUDA_TRY(set_smem_once(head_pair_kernel<NB, OW, NTC>, static_cast<int>(smem_max), smem_set));
+    DUST_CUDA_TRY(set_smem_once(head_pair_kernel<NB, OW, NTC, FIXED>, static_cast<int>(smem_max),
+                                smem_set));
     timer_begin(s);
-    head_pair_kernel<NB, OW, NTC><<<static_cast<unsigned>(T * P.Q), P.nt, smem, s>>>(A, keys);
+    head_pair_kernel<NB, OW, NTC, FIXED><<<static_cast<unsigned>(T * P.Q), P.nt, smem, s>>>(A,
+                                                                                           keys);
     timer_end(s);
     return launch_status();
+}
+
+template <int NB, bool OW, int NTC>
+dust_status launch_pairs(const HeadPlan& P, const HeadArgs& A, const PhiloxKeys& keys, int64_t T,
+                         cudaStream_t s) {
+    return A.qscale > 0.f ? launch_pairs_as<NB, OW, NTC, true>(P, A, keys, T, s)
+                          : launch_pairs_as<NB, OW, NTC, false>(P, A, keys, T, s);
 }
 
 template <int NB, bool OW>

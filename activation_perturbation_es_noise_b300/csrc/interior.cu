@@ -505,13 +505,17 @@ extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, cons
     for (int i0 = 0; i0 < K; i0 += P.nd) {
         const int nd = std::min(P.nd, K - i0);
         const int64_t rows = nd * P.Tp;
+        // (the benchmark hook times GEMM 1 here, GEMM 2 inside gemm_ce_launch,
+        // and the credit + g pass after the loop)
         if (P.fused) {
             // Whole token blocks per sequence: the EMA runs in GEMM 1's
             // epilogue, one CTA walking a sequence's blocks for one draw.
+            timer_begin(s);
             st = reforward1_launch(y1, h0, coef, taylor, W2, T, P.Tp, C, d_model, nd,
                                    nz.draw0 + static_cast<uint32_t>(i0), nz.token0, nz.layer,
                                    nz.sigma, keys, du, fuse_ema ? A2 : nullptr, seq_len,
                                    ema_decay, status, s);
+            timer_end(s);
             if (st != DUST_OK) return st;
         } else {
             DhArgs da{y1, h0, static_cast<const float4*>(coef), taylor ? 1 : 0, Ti,
@@ -519,8 +523,10 @@ extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, cons
                       nz.token0, nz.layer, nz.sigma, A1};
             interior_dh_kernel<<<grid_cap(P.Tp * (C / 4), 256), 256, 0, s>>>(da, keys);
             if ((st = launch_status()) != DUST_OK) return st;
+            timer_begin(s);
             st = gemm_bf16_launch(A1, false, 2 * C, W2, false, C, rows, d_model, 2 * C, C, 1, du,
                                   d_model, status, s);
+            timer_end(s);
             if (st != DUST_OK) return st;
         }
         if (!fuse_ema) {
@@ -537,8 +543,10 @@ extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, cons
         if (st != DUST_OK) return st;
     }
 
+    timer_begin(s);
     st = credit_and_ghat_launch(dl, mean, r, Ti, static_cast<int>(seq_len), Ci, nz, keys, g_hat,
                                 gbf, s);
+    timer_end(s);
     if (st != DUST_OK) return st;
 
     const void* xb = x;

@@ -592,10 +592,12 @@ dust_status dust_block_estimate(const dust_layer_job* jobs, int n, void* ws, siz
                                 void* const* streams, int nstreams);
 
 /*
- * Benchmark hook.  While set, every launch of an entry point's dominant
- * kernel (the head's draw kernel, the interior layer's re-forward GEMM with
- * the cross-entropy epilogue, the embedding's piece sums) is bracketed on its
- * stream by cudaEventRecord(start_events[n]) and cudaEventRecord(
+ * Benchmark hook.  While set, every launch of an entry point's main kernels
+ * (the head's draw kernel; the interior layer's two re-forward GEMMs, in the
+ * order GEMM 1, GEMM 2 with the cross-entropy epilogue per chunk of draws,
+ * then its credit and g pass; the embedding's piece sums; the attention
+ * kernels; the optimiser step) is bracketed on its stream by
+ * cudaEventRecord(start_events[n]) and cudaEventRecord(
  * stop_events[n]) for n = 0, 1, ... up to capacity - 1.  The events are the
  * caller's (created with timing enabled).  Passing NULL arrays turns the hook
  * off.  The hook is process-wide and not thread-safe: it is for timing runs.

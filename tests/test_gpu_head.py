@@ -169,3 +169,15 @@ def test_head_without_g_output(dust, orc):
     g2, G2, _ = dust.head_estimate(to_dev(z), to_dev(y), to_dev(x), 0.05, 8, 3)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(G1.cpu().numpy(), G2.cpu().numpy())
+
+
+@pytest.mark.parametrize("T,d,V,K", [(96, 32, 4096, 6), (64, 16, 1000, 5), (33, 8, 6000, 4)])
+def test_head_large_sigma_float_sums(dust, orc, T, d, V, K):
+    """sigma = 1.5: the largest possible sum of p 2^(sigma log2(e) a) no longer
+    fits the draw kernel's fixed-point range, so the CTA adds the sums as
+    floats in warp order; the 4096 and 6000 vocabularies take the 128- and
+    256-thread CTAs, 1000 the one-warp CTA, and K odd leaves a last draw pair
+    with one counted draw."""
+    x, z, y = _inputs(T, d, V, seed=V + K)
+    g, G = _run(dust, x, z, y, 1.5, K, 21, layer=2)
+    _check(orc, x, z, y, g, G, 1.5, K, 21, layer=2)
