@@ -14,7 +14,9 @@ import os
 import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libdust.so")
+# DUST_LIBRARY=debug loads the bounds-checked build (libdust_debug.so) instead.
+LIB_PATH = os.path.join(HERE, "libdust_debug.so" if os.environ.get("DUST_LIBRARY") == "debug"
+                        else "libdust.so")
 
 DUST_OK = 0
 STATUS_NAMES = {0: "DUST_OK", 1: "DUST_ERR_INVALID_ARG", 2: "DUST_ERR_UNSUPPORTED",
@@ -34,7 +36,8 @@ EXPORTS = ("dust_status_string", "dust_abi_version", "dust_workspace_status",
            "dust_block_workspace", "dust_block_job_offset", "dust_block_estimate",
            "dust_issue_probe", "dust_head_chunked_workspace",
            "dust_head_estimate_chunked", "dust_es_perturb", "dust_es_estimate",
-           "dust_box_muller_fast")
+           "dust_box_muller_fast", "dust_debug_build", "dust_debug_fault",
+           "dust_debug_check_index")
 BASELINE_MEAN, BASELINE_LEAVE_ONE_OUT, BASELINE_ANTITHETIC = 0, 1, 2
 
 
@@ -97,6 +100,9 @@ def lib():
         L.dust_embed_scatter_static.argtypes = [_P, _P, _I64, _I64, _I64, _P, _P, _P]
         L.dust_philox_fill.argtypes = [ctypes.c_uint64, _U32, _U32, _I64, _I64, _I64, _P, _P, _P]
         L.dust_box_muller_fast.argtypes = [_P, _I64, _P, _P]
+        L.dust_debug_build.restype = ctypes.c_int
+        L.dust_debug_fault.restype = ctypes.c_uint64
+        L.dust_debug_check_index.argtypes = [_I64, _I64, _P, _P]
         L.dust_gemm_bf16.argtypes = [_P, ctypes.c_int, _I64, _P, ctypes.c_int, _I64, _I64, _I64,
                                      _I64, _P, _I64, _P, _SZ, _P]
         L.dust_set_kernel_events.argtypes = [_P, _P, ctypes.c_int]
@@ -146,7 +152,7 @@ def lib():
                      "dust_attn_gate_estimate", "dust_attn_qk_estimate", "dust_block_estimate",
                      "dust_issue_probe",
                      "dust_head_estimate_chunked", "dust_es_perturb", "dust_es_estimate",
-           "dust_box_muller_fast"):
+                     "dust_box_muller_fast", "dust_debug_check_index"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -307,6 +313,32 @@ def box_muller_fast(words, stream=None):
     _check("dust_box_muller_fast",
            lib().dust_box_muller_fast(_ptr(words), words.numel() // 2, _ptr(out), _stream(stream)))
     return out
+
+
+def debug_build():
+    """True when the loaded library is the bounds-checked build."""
+    return bool(lib().dust_debug_build())
+
+
+def debug_fault():
+    """Synchronise the device and return the first out-of-range index the
+    debug build's checks met since the last call, as (file id, source line),
+    or None; always None for the release library."""
+    v = int(lib().dust_debug_fault())
+    if v == 0:
+        return None
+    if v == (1 << 64) - 1:
+        raise DustError("dust_debug_fault", 4)  # DUST_ERR_CUDA: the read itself failed
+    return (v >> 32, v & 0xFFFFFFFF)
+
+
+def debug_check_index(i, n, stream=None):
+    """The debug build's index check on its own (nothing is addressed with i):
+    True when 0 <= i < n; in the debug build a False also records a fault."""
+    out = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    _check("dust_debug_check_index",
+           lib().dust_debug_check_index(int(i), int(n), _ptr(out), _stream(stream)))
+    return bool(out.item())
 
 
 def wait_selftest(limit_ns, stream=None):

@@ -60,6 +60,14 @@ __global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
     __syncthreads();
 }
 
+// The debug build's index check on its own: one thread evaluates the check
+// of index i against extent n and writes whether it passed.  Nothing is
+// addressed with i, so an out-of-range i only records the fault (in the
+// debug build; the release check is the constant true).
+__global__ void debug_check_index_kernel(int64_t i, int64_t n, int* in_bounds) {
+    *in_bounds = DUST_IB(i, n) ? 1 : 0;
+}
+
 // Issue-rate probe: every thread runs `iters` rounds over eight independent
 // chains of one operation kind, so that throughput, not latency, bounds it.
 //   kind 0: the Philox step, a 32 x 32 -> 64-bit multiply and an xor of its
@@ -168,6 +176,13 @@ extern "C" dust_status dust_wait_selftest(void* ws, uint64_t limit_ns, void* str
     return launch_status();
 }
 
+extern "C" dust_status dust_debug_check_index(int64_t i, int64_t n, int* in_bounds,
+                                              void* stream) {
+    if (!in_bounds || !aligned(in_bounds, 4)) return DUST_ERR_INVALID_ARG;
+    debug_check_index_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(i, n, in_bounds);
+    return launch_status();
+}
+
 extern "C" int dust_abi_version(void) { return 100; }
 
 extern "C" const char* dust_status_string(dust_status s) {
@@ -238,3 +253,31 @@ extern "C" dust_status dust_issue_probe(int kind, int64_t iters, int64_t* thread
     return launch_status();
 }
 
+extern "C" int dust_debug_build(void) {
+#ifdef DUST_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+extern "C" uint64_t dust_debug_fault(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        (void)cudaGetLastError();
+        return ~0ull;
+    }
+    uint64_t (*const readers[])() = {debug_fault_file_1, debug_fault_file_2, debug_fault_file_3,
+                                     debug_fault_file_4, debug_fault_file_5, debug_fault_file_6,
+                                     debug_fault_file_7, debug_fault_file_8, debug_fault_file_9,
+                                     debug_fault_file_10};
+    uint64_t first = 0;
+    for (auto r : readers) {
+        const uint64_t v = r();
+        if (v && !first) first = v;
+    }
+    return first;
+}
+
+namespace dust {
+DUST_DEBUG_READER(10)
+}  // namespace dust

@@ -65,6 +65,7 @@ __global__ void attn_split_p_kernel(const float* __restrict__ P, int64_t rows, i
         const int64_t row = i / (L / 4);
         const int t0 = static_cast<int>(i - row * (L / 4)) * 4;
         const int s = static_cast<int>(row % L);
+        if (!DUST_IB(row * L + t0 + 3, rows * L)) continue;
         const float4 v = __ldg(reinterpret_cast<const float4*>(P + row * L + t0));
         float x[4] = {v.x, v.y, v.z, v.w};
         __nv_bfloat16 hi[4], lo[4];
@@ -114,6 +115,9 @@ __global__ void __launch_bounds__(256) attn_noise_kernel(const NoiseArgs a, cons
         }
         const float v0[4] = {n0.x, n0.y, n0.z, n0.w}, v1[4] = {n1.x, n1.y, n1.z, n1.w};
         const int64_t row0 = static_cast<int64_t>(y) * kDv + jb * 4;
+        const int64_t n2_ext =
+            static_cast<int64_t>(a.nseq) * a.H * kGroup * kDv * (2 * static_cast<int64_t>(a.L));
+        if (!DUST_IB((row0 + 3) * (2 * static_cast<int64_t>(a.L)) + a.L + t + 1, n2_ext)) continue;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             __nv_bfloat16* out = a.N2 + (row0 + k) * (2 * static_cast<int64_t>(a.L));
@@ -233,7 +237,9 @@ __global__ void __launch_bounds__(192, 1)
         bool ok = mbar_wait(acc_bar, 0, a.status);
         ok = __all_sync(0xFFFFFFFFu, ok);
         tc_fence_after();
-        if (ok) {
+        // (the TMEM loads below are warp-collective; the check skips the whole row set)
+        if (ok && DUST_IB(static_cast<int64_t>(tg) * (a.H * kDv) + h * kDv + kDv - 1,
+                          static_cast<int64_t>(a.T) * (a.H * kDv))) {
             const float* erow = a.E + static_cast<int64_t>(tg) * (a.H * kDv) + h * kDv;
             float acc[kGroup] = {0.f, 0.f, 0.f, 0.f};
             // accumulator columns: draw d, channels 32 half .. + 31
@@ -259,7 +265,8 @@ __global__ void __launch_bounds__(192, 1)
             }
 #pragma unroll
             for (int d = 0; d < kGroup; ++d)
-                if (d < a.nd)
+                if (d < a.nd && DUST_IB((static_cast<int64_t>(a.i0 + d) * a.H + h) * a.T + tg,
+                                        static_cast<int64_t>(a.i0 + a.nd) * a.H * a.T))
                     a.dlh[(static_cast<int64_t>(a.i0 + d) * a.H + h) * a.T + tg] = a.sigma * acc[d];
         }
     }
@@ -276,7 +283,8 @@ __global__ void attn_head_sum_kernel(const float* __restrict__ dlh, int K, int H
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t k = i / T, t = i - k * T;
         float s = 0.f;
-        for (int h = 0; h < H; ++h) s += dlh[(k * H + h) * T + t];
+        for (int h = 0; h < H; ++h)
+            if (DUST_IB((k * H + h) * T + t, n * H)) s += dlh[(k * H + h) * T + t];
         dl[i] = s;
     }
 }
@@ -454,6 +462,7 @@ __global__ void __launch_bounds__(256) attn_gate_dl_kernel(const GateArgs a, con
         const DrawHalf dh = philox_draw_half(a.draw0 + static_cast<uint32_t>(i), token, keys);
         float part = 0.f;
         for (int j = lane; j < nblk; j += 32) {
+            if (!DUST_IB(row + 4 * j + 3, static_cast<int64_t>(a.T) * a.C)) break;
             const float4 n = words_to_normals_fast(philox_rest(dh, philox_block_half(j, a.layer, keys), keys));
             const float4 z = __ldg(reinterpret_cast<const float4*>(a.z + row) + j);
             const float4 o = __ldg(reinterpret_cast<const float4*>(a.o + row) + j);
@@ -470,7 +479,8 @@ __global__ void __launch_bounds__(256) attn_gate_dl_kernel(const GateArgs a, con
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, off);
-        if (lane == 0) a.dl[static_cast<int64_t>(i) * a.T + t] = part;
+        if (lane == 0 && DUST_IB(static_cast<int64_t>(i) * a.T + t, static_cast<int64_t>(a.K) * a.T))
+            a.dl[static_cast<int64_t>(i) * a.T + t] = part;
     }
 }
 
@@ -567,3 +577,7 @@ extern "C" dust_status dust_attn_gate_estimate(const float* z, const float* o, c
     }
     return gemm_bf16_launch(gbf, true, C, xb, true, ldx, C, d_in, T, 0, 1, G_W, d_in, status, s);
 }
+
+namespace dust {
+DUST_DEBUG_READER(6)
+}  // namespace dust

@@ -307,8 +307,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int jb = h * (kHd / 4) + 2 * c8;
                     float4 n0, n1;
                     if (KEYS) {
-                        n0 = ld4(a.Q + (tok0 + row) * C + 4 * jb);
-                        n1 = ld4(a.Q + (tok0 + row) * C + 4 * jb + 4);
+                        const int64_t qe = static_cast<int64_t>(a.T) * C;
+                        n0 = ld4(a.Q + DUST_IDX((tok0 + row) * C + 4 * jb, 4, qe));
+                        n1 = ld4(a.Q + DUST_IDX((tok0 + row) * C + 4 * jb + 4, 4, qe));
                     } else {
                         n0 = words_to_normals_fast(philox_rest(
                             dh, philox_block_half(static_cast<uint32_t>(jb), a.layer, keys), keys));
@@ -336,8 +337,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (!ok) continue;
                 float4 pv[kTcCols / 4];
 #pragma unroll
-                for (int q = 0; q < kTcCols / 4; ++q)
-                    pv[q] = __ldg(reinterpret_cast<const float4*>(prow + j * kTcKeys) + q);
+                for (int q = 0; q < kTcCols / 4; ++q) {
+                    // prow's row of P: keys 0 .. L - 1 of query s of head h of sequence sq
+                    const int64_t pe = static_cast<int64_t>(a.T) * a.H * a.L;
+                    const int64_t pi = (prow - a.P) + j * kTcKeys + 4 * q;
+                    pv[q] = __ldg(reinterpret_cast<const float4*>(a.P + DUST_IDX(pi, 4, pe)));
+                }
                 ok = mbar_wait(ds_full(st), (g >> 1) & 1, a.status);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) continue;
@@ -411,7 +416,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 float eo = 0.f;
 #pragma unroll
                 for (int q = 0; q < kTcCols / 4; ++q) {
-                    const float4 o4 = ld4(a.O + off + 4 * q), e4 = ld4(a.E + off + 4 * q);
+                    const int64_t oi = DUST_IDX(off + 4 * q, 4, static_cast<int64_t>(a.T) * C);
+                    const float4 o4 = ld4(a.O + oi), e4 = ld4(a.E + oi);
                     eo = fmaf(e4.x, fmaf(-W, o4.x, __uint_as_float(r[4 * q])), eo);
                     eo = fmaf(e4.y, fmaf(-W, o4.y, __uint_as_float(r[4 * q + 1])), eo);
                     eo = fmaf(e4.z, fmaf(-W, o4.z, __uint_as_float(r[4 * q + 2])), eo);
@@ -423,7 +429,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         s_dl[grp][row] = dl;
         epi_sync();
-        if (ok && grp == 0) {
+        if (ok && grp == 0 && DUST_IB(tok0 + row, a.T)) {
             float sum = 0.f;
 #pragma unroll
             for (int q = 0; q < kTcGroups; ++q) sum += s_dl[q][row];
@@ -455,6 +461,7 @@ __global__ void qk_key_noise_kernel(int nd, int64_t T, int C, uint32_t draw_firs
         split_pair(v.x, v.y, hi0, lo0);
         split_pair(v.z, v.w, hi1, lo1);
         __nv_bfloat16* row = N2 + dt * 2 * C;
+        if (!DUST_IB(dt * 2 * C + C + 4 * jb + 3, n / nb * 2 * C)) continue;
         *reinterpret_cast<uint2*>(row + 4 * jb) = make_uint2(hi0, hi1);
         *reinterpret_cast<uint2*>(row + C + 4 * jb) = make_uint2(lo0, lo1);
     }
@@ -468,6 +475,7 @@ __global__ void qk_split_rows_kernel(const float* __restrict__ X, int64_t T, int
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t t = i / (C / 2);
         const int c = static_cast<int>(i - t * (C / 2)) * 2;
+        if (!DUST_IB(t * C + c + 1, T * C)) continue;
         const float2 v = *reinterpret_cast<const float2*>(X + t * C + c);
         uint32_t hi, lo;
         split_pair(v.x, v.y, hi, lo);
@@ -654,3 +662,7 @@ extern "C" dust_status dust_attn_qk_estimate(int which, const float* Q, const fl
     }
     return gemm_bf16_launch(gbf, true, C, xb, true, ldx, C, d_in, T, 0, 1, G_W, d_in, status, s);
 }
+
+namespace dust {
+DUST_DEBUG_READER(7)
+}  // namespace dust

@@ -26,6 +26,49 @@ __device__ __forceinline__ void record_status(uint32_t* status, uint32_t code) {
     if (status != nullptr) atomicCAS(status, 0u, code);
 }
 
+// ------------------------------------------------------------ debug build ----
+// In the debug build (-DDUST_DEBUG, libdust_debug.so) DUST_IB(i, n) checks a
+// computed index against the extent of the buffer it addresses before the
+// access it guards: an index outside [0, n) records the first such fault of
+// its source file (the line) and the access is skipped instead of reaching
+// memory.  In the release build DUST_IB is the constant true and compiles
+// away.  DUST_IDX(i, w, n) is the form for code whose control flow must stay
+// uniform across a warp (around warp-collective TMEM loads and barriers): for
+// an access of w elements from index i it checks i and i + w - 1, records a
+// fault the same way and yields index 0 in place of a bad i, so the access
+// still happens, at the buffer's start (every such buffer holds at least w
+// elements).  In release it is i.  DUST_DEBUG_READER(file_id) defines the host reader of a file's word.
+#ifdef DUST_DEBUG
+namespace {
+__device__ unsigned long long g_debug_fault;  // 0, or the faulting line
+}
+__device__ __forceinline__ bool debug_in_bounds(int64_t i, int64_t n, unsigned line) {
+    if (i >= 0 && i < n) return true;
+    atomicCAS(&g_debug_fault, 0ull, static_cast<unsigned long long>(line));
+    return false;
+}
+#define DUST_IB(i, n) \
+    (::dust::debug_in_bounds(static_cast<int64_t>(i), static_cast<int64_t>(n), __LINE__))
+#define DUST_IDX(i, w, n)                                                   \
+    (DUST_IB(i, n) && DUST_IB(static_cast<int64_t>(i) + (w) - 1, n) ? static_cast<int64_t>(i) \
+                                                                      : int64_t{0})
+#define DUST_DEBUG_READER(file_id)                                                     \
+    uint64_t debug_fault_file_##file_id() {                                            \
+        unsigned long long v = 0, zero = 0;                                            \
+        if (cudaMemcpyFromSymbol(&v, g_debug_fault, sizeof(v)) != cudaSuccess ||       \
+            cudaMemcpyToSymbol(g_debug_fault, &zero, sizeof(zero)) != cudaSuccess) {   \
+            (void)cudaGetLastError();                                                  \
+            return ~0ull;                                                              \
+        }                                                                              \
+        return v ? ((static_cast<uint64_t>(file_id) << 32) | v) : 0;                   \
+    }
+#else
+#define DUST_IB(i, n) true
+#define DUST_IDX(i, w, n) (i)
+#define DUST_DEBUG_READER(file_id) \
+    uint64_t debug_fault_file_##file_id() { return 0; }
+#endif
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

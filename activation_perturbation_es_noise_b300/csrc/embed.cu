@@ -196,7 +196,10 @@ __device__ void chunk_offsets(const uint32_t* hist, int nchunks, int c, uint32_t
         uint32_t t = 0;
         const uint32_t* row = hist + static_cast<int64_t>(tid) * nchunks;
         for (int k = 0; k < nchunks; ++k) {
-            const uint32_t h = __ldcg(row + k);
+            const uint32_t h =
+                DUST_IB(static_cast<int64_t>(tid) * nchunks + k, static_cast<int64_t>(256) * nchunks)
+                    ? __ldcg(row + k)
+                    : 0u;
             pre += k < c ? h : 0u;
             t += h;
         }
@@ -251,7 +254,7 @@ __global__ void __launch_bounds__(kChunk) embed_sort_kernel(const SortArgs a) {
         const int t = c * kChunk + tid;
         const bool valid = t < a.T;
         uint32_t key = 0xFFFFFFFFu;
-        if (valid) {
+        if (valid && DUST_IB(t, a.T)) {
             int id = __ldg(a.ids + t);
             if (id < 0 || id >= a.V) {
                 record_status(a.ctl, DUST_ERR_DEVICE_RANGE);
@@ -265,9 +268,11 @@ __global__ void __launch_bounds__(kChunk) embed_sort_kernel(const SortArgs a) {
         // one atomic per distinct id in the warp
         const bool counted = valid && key < static_cast<uint32_t>(a.V);
         const uint32_t peers = __match_any_sync(0xFFFFFFFFu, counted ? key : 0xFFFFFFFFu);
-        if (counted && (peers & lanemask_lt()) == 0) atomicAdd(a.cnt + key, __popc(peers));
+        if (counted && (peers & lanemask_lt()) == 0 && DUST_IB(key, a.V))
+            atomicAdd(a.cnt + key, __popc(peers));
         __syncthreads();
-        if (tid < 256) a.hist[static_cast<int64_t>(tid) * a.nchunks + c] = h[tid];
+        if (tid < 256 && DUST_IB(static_cast<int64_t>(tid) * a.nchunks + c, hist_words))
+            a.hist[static_cast<int64_t>(tid) * a.nchunks + c] = h[tid];
     }
 
     int cur = 0;
@@ -279,7 +284,8 @@ __global__ void __launch_bounds__(kChunk) embed_sort_kernel(const SortArgs a) {
             for (int64_t v = gtid; v < a.V; v += gthreads) {
                 const uint32_t n = __ldcg(a.cnt + v);
                 if (n == 0) {
-                    a.empty[__ldcg(a.eoff + v)] = static_cast<int32_t>(v);
+                    const uint32_t e = __ldcg(a.eoff + v);
+                    if (DUST_IB(e, a.V)) a.empty[e] = static_cast<int32_t>(v);
                     continue;
                 }
                 const uint32_t p0 = __ldcg(a.poff + v), s0 = __ldcg(a.seg + v);
@@ -290,7 +296,7 @@ __global__ void __launch_bounds__(kChunk) embed_sort_kernel(const SortArgs a) {
                     pc.start = static_cast<int32_t>(s0 + k * kPiece);
                     pc.len = static_cast<int32_t>(min(static_cast<uint32_t>(kPiece), n - k * kPiece));
                     pc.multi = np > 1;
-                    a.table[p0 + k] = pc;
+                    if (DUST_IB(p0 + k, a.np_max)) a.table[p0 + k] = pc;
                 }
             }
         }
@@ -312,7 +318,7 @@ __global__ void __launch_bounds__(kChunk) embed_sort_kernel(const SortArgs a) {
             __syncthreads();
             const int i = c * kChunk + tid;
             const bool valid = i < a.T;
-            const uint32_t key = valid ? __ldcg(keys_in + i) : 0u;
+            const uint32_t key = (valid && DUST_IB(i, a.T)) ? __ldcg(keys_in + i) : 0u;
             const uint32_t dig = valid ? (key >> shift) & 255u : 256u;  // 256: padding lane
             const uint32_t peers = __match_any_sync(0xFFFFFFFFu, dig);
             const uint32_t lrank = __popc(peers & lanemask_lt());
@@ -329,11 +335,14 @@ __global__ void __launch_bounds__(kChunk) embed_sort_kernel(const SortArgs a) {
             __syncthreads();
             if (valid) {
                 const uint32_t pos = choffs[dig] + wcnt[warp][dig] + lrank;
-                keys_out[pos] = key;
-                vals_out[pos] = __ldcg(vals_in + i);
+                if (DUST_IB(pos, a.T) && DUST_IB(i, a.T)) {
+                    keys_out[pos] = key;
+                    vals_out[pos] = __ldcg(vals_in + i);
+                }
                 if (hist_next) {
                     const uint32_t d2 = (key >> (shift + 8)) & 255u;
-                    atomicAdd(hist_next + static_cast<int64_t>(d2) * a.nchunks + pos / kChunk, 1u);
+                    const int64_t hi = static_cast<int64_t>(d2) * a.nchunks + pos / kChunk;
+                    if (DUST_IB(hi, hist_words)) atomicAdd(hist_next + hi, 1u);
                 }
             }
             __syncthreads();  // wcnt and choffs are reused by the next chunk
@@ -363,7 +372,8 @@ __global__ void __launch_bounds__(kChunk) embed_sort_kernel(const SortArgs a) {
         for (int64_t v = gtid; v < a.V; v += gthreads) {
             const uint32_t n = __ldcg(a.cnt + v);
             if (n == 0) {
-                a.empty[__ldcg(a.eoff + v)] = static_cast<int32_t>(v);
+                const uint32_t e = __ldcg(a.eoff + v);
+                if (DUST_IB(e, a.V)) a.empty[e] = static_cast<int32_t>(v);
                 continue;
             }
             const uint32_t p0 = __ldcg(a.poff + v), s0 = __ldcg(a.seg + v);
@@ -374,7 +384,7 @@ __global__ void __launch_bounds__(kChunk) embed_sort_kernel(const SortArgs a) {
                 pc.start = static_cast<int32_t>(s0 + k * kPiece);
                 pc.len = static_cast<int32_t>(min(static_cast<uint32_t>(kPiece), n - k * kPiece));
                 pc.multi = np > 1;
-                a.table[p0 + k] = pc;
+                if (DUST_IB(p0 + k, a.np_max)) a.table[p0 + k] = pc;
             }
         }
     }
@@ -393,6 +403,8 @@ struct RowArgs {
     int d, nslices;
     float* G_E;
     float* partial;  // npieces x d
+    int T, V;        // extents the debug build checks indices against
+    int64_t np_max;
 };
 
 // out[c] = sum_{q < n} rows[q * d + c], in order q = 0, 1, ..., for the warp's
@@ -477,11 +489,14 @@ __global__ void __launch_bounds__(kRowThreads) embed_rows_kernel(const RowArgs a
         if (u >= nunits) return;
         const int item = static_cast<int>(u / a.nslices);
         if (item >= npieces) {
-            pc.v = __ldg(a.empty + (item - npieces));
+            pc.v = DUST_IB(item - npieces, a.V) ? __ldg(a.empty + (item - npieces)) : 0;
             return;
         }
+        if (!DUST_IB(item, a.np_max)) return;
         pc = a.table[item];
-        myrow = lane < pc.len ? __ldg(a.perm + pc.start + lane) : 0;
+        myrow = (lane < pc.len && DUST_IB(pc.start + lane, a.T)) ? __ldg(a.perm + pc.start + lane)
+                                                                 : 0;
+        if (!DUST_IB(myrow, a.T)) myrow = 0;
     };
     Piece pc;
     int myrow;
@@ -498,13 +513,18 @@ __global__ void __launch_bounds__(kRowThreads) embed_rows_kernel(const RowArgs a
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int c = c0 + 32 * k;
-                if (c < w) {
+                if (c < w && DUST_IB(v, a.V)) {
                     if (VEC)
                         reinterpret_cast<float4*>(a.G_E + v * a.d)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
                     else
                         a.G_E[v * a.d + c] = 0.f;
                 }
             }
+            pc = pn;
+            myrow = rown;
+            continue;
+        }
+        if (!DUST_IB(pc.multi ? item : pc.v, pc.multi ? a.np_max : a.V)) {
             pc = pn;
             myrow = rown;
             continue;
@@ -559,6 +579,14 @@ __global__ void __launch_bounds__(kRowThreads) embed_rows_kernel(const RowArgs a
             __syncwarp();
             const uint32_t p0 = a.poff[pc.v], np = a.poff[pc.v + 1] - p0;
             const uint32_t k = static_cast<uint32_t>(item) - p0;  // piece within the row
+            const bool counters_ok =
+                DUST_IB(static_cast<int64_t>(p0) + np - 1, a.np_max) &&
+                DUST_IB(static_cast<int64_t>(pc.v) * a.nslices + s, static_cast<int64_t>(a.V) * a.nslices);
+            if (!counters_ok) {
+                pc = pn;
+                myrow = rown;
+                continue;
+            }
             const uint32_t gfirst = p0 + (k / kGroup) * kGroup;    // the group's first piece
             const uint32_t gsize = min(static_cast<uint32_t>(kGroup), p0 + np - gfirst);
             uint32_t fin = 0;
@@ -728,7 +756,8 @@ extern "C" dust_status dust_embed_scatter(const float* g_hat, const int32_t* ids
                reinterpret_cast<uint32_t*>(w + P.off_done),
                reinterpret_cast<uint32_t*>(w + P.off_gdone), static_cast<int>(d),
                static_cast<int>(vec ? ceil_div(d / 4, kSliceF4) : ceil_div(d, kSliceF)), G_E,
-               reinterpret_cast<float*>(w + P.off_part)};
+               reinterpret_cast<float*>(w + P.off_part), static_cast<int>(T), static_cast<int>(V),
+               P.np_max};
     const unsigned rgrid = 148 * 8;
     if (vec)
         embed_rows_kernel<true><<<rgrid, kRowThreads, 0, s>>>(ra);
@@ -737,3 +766,7 @@ extern "C" dust_status dust_embed_scatter(const float* g_hat, const int32_t* ids
     timer_end(s);
     return launch_status();
 }
+
+namespace dust {
+DUST_DEBUG_READER(3)
+}  // namespace dust

@@ -35,7 +35,7 @@ __global__ void es_perturb_kernel(const float* __restrict__ theta, int64_t n, in
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int64_t c = 4 * j + k;
-            if (c < n) out[static_cast<int64_t>(i) * n + c] = fmaf(sigma, ev[k], theta[c]);
+            if (c < n && DUST_IB(static_cast<int64_t>(i) * n + c, static_cast<int64_t>(K) * n)) out[static_cast<int64_t>(i) * n + c] = fmaf(sigma, ev[k], theta[c]);
         }
     }
 }
@@ -67,7 +67,7 @@ __global__ void es_estimate_kernel(const float* __restrict__ losses, int64_t n, 
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-        if (4 * j + k < n) g[4 * j + k] = acc[k] * scale;
+        if (4 * j + k < n && DUST_IB(4 * j + k, n)) g[4 * j + k] = acc[k] * scale;
 }
 
 bool es_args_ok(int64_t n, const dust_noise& nz) {
@@ -104,3 +104,7 @@ extern "C" dust_status dust_es_estimate(const float* losses, int64_t n, dust_noi
         philox_round_keys(nz.seed), g);
     return launch_status();
 }
+
+namespace dust {
+DUST_DEBUG_READER(9)
+}  // namespace dust

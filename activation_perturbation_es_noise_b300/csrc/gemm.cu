@@ -278,8 +278,10 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
                     if (EPI == EPI_STORE) {
                         if (row < sh.M) {
                             float* drow = es.D + static_cast<int64_t>(row) * es.ldd;
+                            const int64_t dext = static_cast<int64_t>(sh.M) * es.ldd;
                             if (((es.ldd & 3) == 0) && col0 + 32 <= sh.N &&
-                                ((reinterpret_cast<uintptr_t>(es.D) & 15) == 0)) {
+                                ((reinterpret_cast<uintptr_t>(es.D) & 15) == 0) &&
+                                DUST_IB(static_cast<int64_t>(row) * es.ldd + col0 + 31, dext)) {
 #pragma unroll
                                 for (int q = 0; q < 32; q += 4)
                                     *reinterpret_cast<float4*>(drow + col0 + q) = make_float4(
@@ -288,7 +290,9 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
                             } else {
 #pragma unroll
                                 for (int q = 0; q < 32; ++q)
-                                    if (col0 + q < sh.N) drow[col0 + q] = __uint_as_float(r[q]);
+                                    if (col0 + q < sh.N &&
+                                        DUST_IB(static_cast<int64_t>(row) * es.ldd + col0 + q, dext))
+                                        drow[col0 + q] = __uint_as_float(r[q]);
                             }
                         }
                     } else {
@@ -328,7 +332,10 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(buf));
         }
-        if (EPI == EPI_CE && ok && ce_valid)
+        // (the launch writes rows i0 .. i0 + ndraw - 1 of dl)
+        if (EPI == EPI_CE && ok && ce_valid &&
+            DUST_IB(static_cast<int64_t>(ec.i0 + ce_i) * ec.T + ce_t,
+                    static_cast<int64_t>(ec.i0 + ec.ndraw) * ec.T))
             ec.dl[static_cast<int64_t>(ec.i0 + ce_i) * ec.T + ce_t] = log1pf(ce_sum) - ce_zy;
     }
     tc_fence_before();
@@ -402,7 +409,8 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ in, int64_t rows, i
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t r = i / ld_out, c = i - r * ld_out;
-        out[i] = __float2bfloat16_rn(c < cols ? in[r * ld_in + c] : 0.0f);
+        const bool in_b = c < cols && DUST_IB(r * ld_in + c, (rows - 1) * ld_in + cols);
+        out[i] = __float2bfloat16_rn(in_b ? in[r * ld_in + c] : 0.0f);
     }
 }
 
@@ -412,7 +420,8 @@ __global__ void bf16_pad_kernel(const __nv_bfloat16* __restrict__ in, int64_t ro
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t r = i / ld_out, c = i - r * ld_out;
-        out[i] = c < cols ? in[r * ld_in + c] : __float2bfloat16_rn(0.0f);
+        const bool in_b = c < cols && DUST_IB(r * ld_in + c, (rows - 1) * ld_in + cols);
+        out[i] = in_b ? in[r * ld_in + c] : __float2bfloat16_rn(0.0f);
     }
 }
 
@@ -510,3 +519,7 @@ extern "C" dust_status dust_gemm_bf16(const void* A, int a_mn, int64_t lda, cons
     return gemm_bf16_launch(A, a_mn != 0, lda, B, b_mn != 0, ldb, M, N, K, 0, 1, G, ldg,
                             static_cast<uint32_t*>(ws), s);
 }
+
+namespace dust {
+DUST_DEBUG_READER(4)
+}  // namespace dust

@@ -135,7 +135,9 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
     const int i_end = min(A.K, i_begin + A.chunk);
     const int V = A.V;
     const bool vec = (V & 3) == 0;
-    const float* zrow = A.logits + static_cast<int64_t>(t) * (CH ? A.ldz : V) + (CH ? A.col0 : 0);
+    const int64_t zbase = static_cast<int64_t>(t) * (CH ? A.ldz : V) + (CH ? A.col0 : 0);
+    const int64_t zext = static_cast<int64_t>(A.T) * (CH ? A.ldz : V);  // logits, g_hat extent
+    const float* zrow = A.logits + zbase;
 
     // Cached logits of this token -> registers; softmax.
     float p[NB][4];
@@ -143,14 +145,15 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
         const int j = b * NT + tid;
-        if (vec && j < A.nblk) {
+        if (vec && j < A.nblk && DUST_IB(zbase + 4 * j + 3, zext)) {
             const float4 z4 = __ldg(reinterpret_cast<const float4*>(zrow) + j);
             p[b][0] = z4.x; p[b][1] = z4.y; p[b][2] = z4.z; p[b][3] = z4.w;
         } else {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int c = 4 * j + k;
-                p[b][k] = (j < A.nblk && c < V) ? __ldg(zrow + c) : -INFINITY;
+                p[b][k] = (j < A.nblk && c < V && DUST_IB(zbase + c, zext)) ? __ldg(zrow + c)
+                                                                            : -INFINITY;
             }
         }
 #pragma unroll
@@ -158,7 +161,7 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
     }
     float unpert = 0.f;  // CH: the probability mass outside the chunk
     if (CH) {
-        const float lse = __ldg(A.lse + t);
+        const float lse = DUST_IB(t, A.T) ? __ldg(A.lse + t) : 0.f;
         float pc = 0.f;
 #pragma unroll
         for (int b = 0; b < NB; ++b)
@@ -188,7 +191,7 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
 
     // Target channel: the thread that owns it supplies sigma a_y every draw
     // (in chunk mode only when the target lies in the chunk).
-    int y = __ldg(A.targets + t);
+    int y = DUST_IB(t, A.T) ? __ldg(A.targets + t) : -1;
     if (y < 0 || y >= (CH ? A.Vfull : V)) {
         if (tid == 0 && q == 0) record_status(A.status, DUST_ERR_DEVICE_RANGE);
         y = -1;
@@ -330,20 +333,23 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
 #pragma unroll
             for (int k = 0; k < 4; ++k) g[k] = (s1[b][k] - mean * s0[b][k]) * A.g_scale;
             if (vec) {
-                if (grow) *reinterpret_cast<float4*>(grow + 4 * j) = make_float4(g[0], g[1], g[2], g[3]);
+                if (grow && DUST_IB(zbase + 4 * j + 3, zext))
+                    *reinterpret_cast<float4*>(grow + 4 * j) = make_float4(g[0], g[1], g[2], g[3]);
                 __nv_bfloat162 lo = __floats2bfloat162_rn(g[0], g[1]);
                 __nv_bfloat162 hi = __floats2bfloat162_rn(g[2], g[3]);
                 uint2 pk;
                 pk.x = *reinterpret_cast<uint32_t*>(&lo);
                 pk.y = *reinterpret_cast<uint32_t*>(&hi);
-                *reinterpret_cast<uint2*>(brow + 4 * j) = pk;
+                if (DUST_IB((brow - A.gbf) + 4 * j + 3, static_cast<int64_t>(A.T) * A.ldg))
+                    *reinterpret_cast<uint2*>(brow + 4 * j) = pk;
             } else {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int c = 4 * j + k;
                     if (c < V) {
-                        if (grow) grow[c] = g[k];
-                        brow[c] = __float2bfloat16_rn(g[k]);
+                        if (grow && DUST_IB(zbase + c, zext)) grow[c] = g[k];
+                        if (DUST_IB((brow - A.gbf) + c, static_cast<int64_t>(A.T) * A.ldg))
+                            brow[c] = __float2bfloat16_rn(g[k]);
                     }
                 }
             }
@@ -357,13 +363,14 @@ __global__ void __launch_bounds__(ONE_WARP ? 32 : 256)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int c = 4 * j + k;
-                if (c < V) {
+                if (c < V && DUST_IB(off + c, static_cast<int64_t>(A.Q) * zext)) {
                     A.part_s1[off + c] = s1[b][k];
                     A.part_s0[off + c] = s0[b][k];
                 }
             }
         }
-        if (tid == 0) A.part_dl[static_cast<int64_t>(q) * A.T + t] = sdl;
+        if (tid == 0 && DUST_IB(static_cast<int64_t>(q) * A.T + t, static_cast<int64_t>(A.Q) * A.T))
+            A.part_dl[static_cast<int64_t>(q) * A.T + t] = sdl;
     }
 }
 
@@ -376,14 +383,19 @@ __global__ void head_finalize_kernel(const HeadArgs A) {
     float sdl = 0.f, s1 = 0.f, s0 = 0.f;
     for (int q = 0; q < A.Q; ++q) {
         const int64_t off = (static_cast<int64_t>(q) * A.T + t) * A.ldz + A.col0 + c;
+        if (!DUST_IB(off, static_cast<int64_t>(A.Q) * A.T * A.ldz) ||
+            !DUST_IB(static_cast<int64_t>(q) * A.T + t, static_cast<int64_t>(A.Q) * A.T))
+            continue;
         sdl += A.part_dl[static_cast<int64_t>(q) * A.T + t];
         s1 += A.part_s1[off];
         s0 += A.part_s0[off];
     }
     const float mean = sdl / static_cast<float>(A.K);
     const float g = (s1 - mean * s0) * A.g_scale;
-    if (A.g_hat) A.g_hat[static_cast<int64_t>(t) * A.ldz + A.col0 + c] = g;
-    A.gbf[static_cast<int64_t>(t) * A.ldg + A.col0 + c] = __float2bfloat16_rn(g);
+    const int64_t gi = static_cast<int64_t>(t) * A.ldz + A.col0 + c;
+    if (A.g_hat && DUST_IB(gi, static_cast<int64_t>(A.T) * A.ldz)) A.g_hat[gi] = g;
+    const int64_t bi = static_cast<int64_t>(t) * A.ldg + A.col0 + c;
+    if (DUST_IB(bi, static_cast<int64_t>(A.T) * A.ldg)) A.gbf[bi] = __float2bfloat16_rn(g);
 }
 
 // The mean-baseline draws, two per pass (leave-one-out is the same kernel
@@ -434,7 +446,9 @@ __global__ void __launch_bounds__(NTC == 0 ? 256 : NTC, NTC == 32 ? 16 : (NTC ==
     const int i_end = min(A.K, i_begin + A.chunk);
     const int V = A.V;
     const bool vec = (V & 3) == 0;
-    const float* zrow = A.logits + static_cast<int64_t>(t) * V;
+    const int64_t zbase = static_cast<int64_t>(t) * V;
+    const int64_t zext = static_cast<int64_t>(A.T) * V;  // logits, g_hat extent
+    const float* zrow = A.logits + zbase;
 
     // Cached logits of this token -> softmax -> shared memory.
     float p[NB][4];
@@ -442,14 +456,15 @@ __global__ void __launch_bounds__(NTC == 0 ? 256 : NTC, NTC == 32 ? 16 : (NTC ==
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
         const int j = b * NT + tid;
-        if (vec && j < A.nblk) {
+        if (vec && j < A.nblk && DUST_IB(zbase + 4 * j + 3, zext)) {
             const float4 z4 = __ldg(reinterpret_cast<const float4*>(zrow) + j);
             p[b][0] = z4.x; p[b][1] = z4.y; p[b][2] = z4.z; p[b][3] = z4.w;
         } else {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int c = 4 * j + k;
-                p[b][k] = (j < A.nblk && c < V) ? __ldg(zrow + c) : -INFINITY;
+                p[b][k] = (j < A.nblk && c < V && DUST_IB(zbase + c, zext)) ? __ldg(zrow + c)
+                                                                            : -INFINITY;
             }
         }
 #pragma unroll
@@ -471,7 +486,7 @@ __global__ void __launch_bounds__(NTC == 0 ? 256 : NTC, NTC == 32 ? 16 : (NTC ==
         psm[b * NT + tid] = make_float4(p[b][0] * zinv, p[b][1] * zinv, p[b][2] * zinv,
                                         p[b][3] * zinv);
 
-    int y = __ldg(A.targets + t);
+    int y = DUST_IB(t, A.T) ? __ldg(A.targets + t) : -1;
     if (y < 0 || y >= V) {
         if (tid == 0 && q == 0) record_status(A.status, DUST_ERR_DEVICE_RANGE);
         y = -1;
@@ -612,20 +627,23 @@ __global__ void __launch_bounds__(NTC == 0 ? 256 : NTC, NTC == 32 ? 16 : (NTC ==
 #pragma unroll
             for (int k = 0; k < 4; ++k) g[k] = (s1[b][k] - mean * s0[b][k]) * A.g_scale;
             if (vec) {
-                if (grow) *reinterpret_cast<float4*>(grow + 4 * j) = make_float4(g[0], g[1], g[2], g[3]);
+                if (grow && DUST_IB(zbase + 4 * j + 3, zext))
+                    *reinterpret_cast<float4*>(grow + 4 * j) = make_float4(g[0], g[1], g[2], g[3]);
                 __nv_bfloat162 lo = __floats2bfloat162_rn(g[0], g[1]);
                 __nv_bfloat162 hi = __floats2bfloat162_rn(g[2], g[3]);
                 uint2 pk;
                 pk.x = *reinterpret_cast<uint32_t*>(&lo);
                 pk.y = *reinterpret_cast<uint32_t*>(&hi);
-                *reinterpret_cast<uint2*>(brow + 4 * j) = pk;
+                if (DUST_IB((brow - A.gbf) + 4 * j + 3, static_cast<int64_t>(A.T) * A.ldg))
+                    *reinterpret_cast<uint2*>(brow + 4 * j) = pk;
             } else {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int c = 4 * j + k;
                     if (c < V) {
-                        if (grow) grow[c] = g[k];
-                        brow[c] = __float2bfloat16_rn(g[k]);
+                        if (grow && DUST_IB(zbase + c, zext)) grow[c] = g[k];
+                        if (DUST_IB((brow - A.gbf) + c, static_cast<int64_t>(A.T) * A.ldg))
+                            brow[c] = __float2bfloat16_rn(g[k]);
                     }
                 }
             }
@@ -639,13 +657,14 @@ __global__ void __launch_bounds__(NTC == 0 ? 256 : NTC, NTC == 32 ? 16 : (NTC ==
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int c = 4 * j + k;
-                if (c < V) {
+                if (c < V && DUST_IB(off + c, static_cast<int64_t>(A.Q) * zext)) {
                     A.part_s1[off + c] = s1[b][k];
                     A.part_s0[off + c] = s0[b][k];
                 }
             }
         }
-        if (tid == 0) A.part_dl[static_cast<int64_t>(q) * A.T + t] = sdl;
+        if (tid == 0 && DUST_IB(static_cast<int64_t>(q) * A.T + t, static_cast<int64_t>(A.Q) * A.T))
+            A.part_dl[static_cast<int64_t>(q) * A.T + t] = sdl;
     }
 }
 
@@ -946,8 +965,9 @@ __global__ void __launch_bounds__(256)
     }
     for (int v = threadIdx.x; v < V; v += blockDim.x) {
         const float g = expf(zr[v] - m) * inv - (v == y ? 1.0f : 0.0f);
-        if (g_out) g_out[t * V + v] = g;
-        gbf[t * ldg + v] = __float2bfloat16_rn(g);
+        if (g_out && DUST_IB(t * V + v, static_cast<int64_t>(gridDim.x) * V)) g_out[t * V + v] = g;
+        if (DUST_IB(t * ldg + v, static_cast<int64_t>(gridDim.x) * ldg))
+            gbf[t * ldg + v] = __float2bfloat16_rn(g);
     }
 }
 
@@ -1168,3 +1188,7 @@ extern "C" dust_status dust_head_estimate_chunked(const float* logits, const int
     return gemm_bf16_launch(A.gbf, true, P.ldg, xb, true, ldx, V, d, T, 0, 1, G_W, d,
                             static_cast<uint32_t*>(ws), s);
 }
+
+namespace dust {
+DUST_DEBUG_READER(1)
+}  // namespace dust

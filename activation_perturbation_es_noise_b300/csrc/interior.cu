@@ -72,7 +72,9 @@ __global__ void softmax_rows_kernel(const float* __restrict__ z, int V, int ldp,
     float* pr = p + t * ldp;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     float m = -INFINITY;
-    for (int v = threadIdx.x; v < V; v += blockDim.x) m = fmaxf(m, zr[v]);
+    const int64_t zext = static_cast<int64_t>(gridDim.x) * V;  // rows of z and p: gridDim.x
+    for (int v = threadIdx.x; v < V; v += blockDim.x)
+        if (DUST_IB(t * V + v, zext)) m = fmaxf(m, zr[v]);
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
     if (lane == 0) red[warp] = m;
     __syncthreads();
@@ -80,14 +82,17 @@ __global__ void softmax_rows_kernel(const float* __restrict__ z, int V, int ldp,
     for (int w = 0; w < nw; ++w) m = fmaxf(m, red[w]);
     __syncthreads();
     float s = 0.f;
-    for (int v = threadIdx.x; v < V; v += blockDim.x) s += expf(zr[v] - m);
+    for (int v = threadIdx.x; v < V; v += blockDim.x)
+        if (DUST_IB(t * V + v, zext)) s += expf(zr[v] - m);
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
     if (lane == 0) red[warp] = s;
     __syncthreads();
     s = 0.f;
     for (int w = 0; w < nw; ++w) s += red[w];
     const float inv = 1.0f / s;
-    for (int v = threadIdx.x; v < ldp; v += blockDim.x) pr[v] = v < V ? expf(zr[v] - m) * inv : 0.f;
+    for (int v = threadIdx.x; v < ldp; v += blockDim.x)
+        if (DUST_IB(t * ldp + v, static_cast<int64_t>(gridDim.x) * ldp))
+            pr[v] = (v < V && DUST_IB(t * V + v, zext)) ? expf(zr[v] - m) * inv : 0.f;
 }
 
 struct DhArgs {
@@ -115,7 +120,7 @@ __global__ void interior_dh_kernel(const DhArgs a, const PhiloxKeys keys) {
         const bool valid = t < a.T;
         const int64_t e4 = static_cast<int64_t>(valid ? t : 0) * (a.C / 4) + j;
         float4 y = make_float4(0.f, 0.f, 0.f, 0.f), g = y, c1 = y, c2 = y, c3 = y, c4 = y;
-        if (valid) {
+        if (valid && DUST_IB(e4, static_cast<int64_t>(a.T) * (a.C / 4))) {
             if (a.taylor) {
                 const float4* cp = a.coef + e4 * 4;
                 c1 = __ldg(cp); c2 = __ldg(cp + 1); c3 = __ldg(cp + 2); c4 = __ldg(cp + 3);
@@ -151,8 +156,12 @@ __global__ void interior_dh_kernel(const DhArgs a, const PhiloxKeys keys) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) h[k] = l[k] = __float2bfloat16_rn(0.f);
             }
-            *reinterpret_cast<uint2*>(row + 4 * j) = pack4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint2*>(row + a.C + 4 * j) = pack4(l[0], l[1], l[2], l[3]);
+            const int64_t ri = chunk_row(t, i, a.nd) * (2 * static_cast<int64_t>(a.C));
+            const int64_t rext = static_cast<int64_t>(a.nd) * a.Tp * 2 * a.C;
+            if (DUST_IB(ri + 4 * j + 3, rext))
+                *reinterpret_cast<uint2*>(row + 4 * j) = pack4(h[0], h[1], h[2], h[3]);
+            if (DUST_IB(ri + a.C + 4 * j + 3, rext))
+                *reinterpret_cast<uint2*>(row + a.C + 4 * j) = pack4(l[0], l[1], l[2], l[3]);
         }
     }
 }
@@ -185,6 +194,9 @@ __global__ void __launch_bounds__(32 * kEmaWarps)
     const int t0 = s * seq_len + min(seq_len, w * clen);
     const int t1 = s * seq_len + min(seq_len, (w + 1) * clen);
     const float one_m = 1.0f - lam;
+    // du and A2 hold nd x round_up(T, 128) rows
+    const int64_t rows_ext = static_cast<int64_t>(nd) * (((nseq * seq_len) + 127) / 128 * 128);
+    const int64_t du_ext = rows_ext * dm, a2_ext = rows_ext * 2 * dm;
 
     float e = 0.f, pw = 1.f;
     if (ok) {
@@ -193,7 +205,10 @@ __global__ void __launch_bounds__(32 * kEmaWarps)
         for (; t + 8 <= t1; t += 8) {
             float u[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) u[q] = __ldg(du + chunk_row(t + q, i, nd) * dm + k);
+            for (int q = 0; q < 8; ++q) {
+                const int64_t di = chunk_row(t + q, i, nd) * dm + k;
+                u[q] = DUST_IB(di, du_ext) ? __ldg(du + di) : 0.f;
+            }
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 e = fmaf(lam, e, one_m * u[q]);
@@ -201,7 +216,8 @@ __global__ void __launch_bounds__(32 * kEmaWarps)
             }
         }
         for (; t < t1; ++t) {
-            e = fmaf(lam, e, one_m * __ldg(du + chunk_row(t, i, nd) * dm + k));
+            const int64_t di = chunk_row(t, i, nd) * dm + k;
+            e = fmaf(lam, e, one_m * (DUST_IB(di, du_ext) ? __ldg(du + di) : 0.f));
             pw *= lam;
         }
     }
@@ -222,24 +238,31 @@ __global__ void __launch_bounds__(32 * kEmaWarps)
         for (; t + 8 <= t1; t += 8) {
             float u[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) u[q] = __ldg(du + chunk_row(t + q, i, nd) * dm + k);
+            for (int q = 0; q < 8; ++q) {
+                const int64_t di = chunk_row(t + q, i, nd) * dm + k;
+                u[q] = DUST_IB(di, du_ext) ? __ldg(du + di) : 0.f;
+            }
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const int64_t r = chunk_row(t + q, i, nd);
                 e = fmaf(lam, e, one_m * u[q]);
                 __nv_bfloat16 h, l;
                 split_bf16(e, h, l);
-                A2[r * 2 * dm + k] = h;
-                A2[r * 2 * dm + dm + k] = l;
+                if (DUST_IB(r * 2 * dm + dm + k, a2_ext)) {
+                    A2[r * 2 * dm + k] = h;
+                    A2[r * 2 * dm + dm + k] = l;
+                }
             }
         }
         for (; t < t1; ++t) {
             const int64_t r = chunk_row(t, i, nd);
-            e = fmaf(lam, e, one_m * __ldg(du + r * dm + k));
+            e = fmaf(lam, e, one_m * (DUST_IB(r * dm + k, du_ext) ? __ldg(du + r * dm + k) : 0.f));
             __nv_bfloat16 h, l;
             split_bf16(e, h, l);
-            A2[r * 2 * dm + k] = h;
-            A2[r * 2 * dm + dm + k] = l;
+            if (DUST_IB(r * 2 * dm + dm + k, a2_ext)) {
+                A2[r * 2 * dm + k] = h;
+                A2[r * 2 * dm + dm + k] = l;
+            }
         }
     }
 }
@@ -248,8 +271,10 @@ __global__ void draw_mean_kernel(const float* __restrict__ dl, int K, int T, flo
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= T) return;
     float s = 0.f;
-    for (int i = 0; i < K; ++i) s += dl[static_cast<int64_t>(i) * T + t];
-    m[t] = s / static_cast<float>(K);
+    for (int i = 0; i < K; ++i)
+        if (DUST_IB(static_cast<int64_t>(i) * T + t, static_cast<int64_t>(K) * T))
+            s += dl[static_cast<int64_t>(i) * T + t];
+    if (DUST_IB(t, T)) m[t] = s / static_cast<float>(K);
 }
 
 // r_{i,t} = c_{i,t} + gamma r_{i,t+1} inside each sequence, c = -(dl - m).
@@ -270,7 +295,9 @@ __global__ void reward_scan_kernel(const float* __restrict__ dl, const float* __
     const int t0 = s * seq_len + min(seq_len, lane * chunk);
     const int t1 = s * seq_len + min(seq_len, (lane + 1) * chunk);
     float A = 0.f, P = 1.f;
+    const int64_t kt = static_cast<int64_t>(K) * T;
     for (int t = t1 - 1; t >= t0; --t) {
+        if (!DUST_IB(rowoff + t, kt) || !DUST_IB(t, T)) continue;
         A = fmaf(gamma, A, -(dl[rowoff + t] - m[t]));
         P *= gamma;
     }
@@ -289,6 +316,7 @@ __global__ void reward_scan_kernel(const float* __restrict__ dl, const float* __
     float acc = __shfl_down_sync(0xFFFFFFFFu, A, 1);
     if (lane == 31) acc = 0.f;
     for (int t = t1 - 1; t >= t0; --t) {
+        if (!DUST_IB(rowoff + t, kt) || !DUST_IB(t, T)) continue;
         acc = fmaf(gamma, acc, -(dl[rowoff + t] - m[t]));
         r[rowoff + t] = acc;
     }
@@ -324,7 +352,9 @@ __global__ void interior_ghat_kernel(const GhatArgs a, const PhiloxKeys keys) {
         const float* rcol = a.r + t;
 #pragma unroll 2
         for (int i = 0; i < a.K; ++i) {
-            const float ri = __ldg(rcol + static_cast<int64_t>(i) * a.T);
+            const float ri = DUST_IB(t + static_cast<int64_t>(i) * a.T, static_cast<int64_t>(a.K) * a.T)
+                                 ? __ldg(rcol + static_cast<int64_t>(i) * a.T)
+                                 : 0.f;
             const DrawHalf dh = philox_draw_half(a.draw0 + i, a.token0 + t, keys);
             uint4 w[2];
 #pragma unroll
@@ -343,6 +373,7 @@ __global__ void interior_ghat_kernel(const GhatArgs a, const PhiloxKeys keys) {
             const float4 g = make_float4(acc[u].x * a.neg_inv_ks, acc[u].y * a.neg_inv_ks,
                                          acc[u].z * a.neg_inv_ks, acc[u].w * a.neg_inv_ks);
             const int64_t off = static_cast<int64_t>(t) * a.C + 4 * jb[u];
+            if (!DUST_IB(off + 3, static_cast<int64_t>(a.T) * a.C)) continue;
             if (a.g_hat) *reinterpret_cast<float4*>(a.g_hat + off) = g;
             *reinterpret_cast<uint2*>(a.gbf + off) =
                 pack4(__float2bfloat16_rn(g.x), __float2bfloat16_rn(g.y),
@@ -559,3 +590,7 @@ extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, cons
     }
     return gemm_bf16_launch(gbf, true, C, xb, true, ldx, C, d_in, T, 0, 1, G_W1, d_in, status, s);
 }
+
+namespace dust {
+DUST_DEBUG_READER(2)
+}  // namespace dust

@@ -65,6 +65,22 @@ inline dust_status launch_status() {
     return e == cudaSuccess ? DUST_OK : DUST_ERR_CUDA;
 }
 
+// Debug build: the first out-of-bounds index each source file's kernels met
+// since the last read, as (file id << 32) | line, or 0 (always 0 in the
+// release build); reading clears it.  File ids: 1 head, 2 interior,
+// 3 embed, 4 gemm, 5 reforward, 6 attention, 7 attention_qk, 8 optim, 9 es,
+// 10 abi (the index self-check).
+uint64_t debug_fault_file_1();
+uint64_t debug_fault_file_2();
+uint64_t debug_fault_file_3();
+uint64_t debug_fault_file_4();
+uint64_t debug_fault_file_5();
+uint64_t debug_fault_file_6();
+uint64_t debug_fault_file_7();
+uint64_t debug_fault_file_8();
+uint64_t debug_fault_file_9();
+uint64_t debug_fault_file_10();
+
 // Optional event pairs around the dominant kernel of each entry point (the
 // benchmark hook of dust_set_kernel_events).
 struct KernelTimer {

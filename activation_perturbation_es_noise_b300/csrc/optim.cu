@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(256) optim_kernel(const OptArgs a) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t t0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
     for (int64_t i = t0; i < a.n4; i += stride) {
+        if (!DUST_IB(4 * i + 3, a.n)) break;
         float4 w = reinterpret_cast<const float4*>(a.W)[i];
         const float4 g = __ldcs(reinterpret_cast<const float4*>(a.G) + i);
         float4 m = reinterpret_cast<const float4*>(a.m)[i];
@@ -169,3 +170,7 @@ extern "C" dust_status dust_adam_step(float* W, const float* G, float* m, float*
     a.inv_bc2 = inv_bias_correction(beta2, step);
     return launch_optim(a, true, static_cast<cudaStream_t>(stream));
 }
+
+namespace dust {
+DUST_DEBUG_READER(8)
+}  // namespace dust

@@ -42,6 +42,7 @@ struct RefArgs {
     float* du;        // rows x dm (plain epilogue)
     __nv_bfloat16* A2;  // rows x 2 dm: [hi | lo] of the EMA output (EMA epilogue)
     int T, C, dm, nd;
+    int64_t rows;  // rows of du / A2: nd x the token count rounded up to a tile
     int ema;    // 1: work item = (sequence, draw), EMA in the epilogue
     int tiles;  // token blocks per sequence (EMA epilogue)
     float lam;  // EMA decay
@@ -241,6 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (t < a.T) {
                             const float4* cp =
                                 a.coef + (static_cast<int64_t>(t) * (a.C / 4) + j) * 4;
+                            if (!DUST_IB((static_cast<int64_t>(t) * (a.C / 4) + j) * 4 + 3,
+                                         static_cast<int64_t>(a.T) * a.C))
+                                continue;
                             const float4 c1 = __ldg(cp), c2 = __ldg(cp + 1);
                             const float4 c3 = __ldg(cp + 2), c4 = __ldg(cp + 3);
                             const float4 nrm =
@@ -271,7 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int m = 0; m < kRows; ++m) {
                         const int t = tb * kBM + r0 + 2 * kProducerWarps * m;
-                        if (t < a.T) {
+                        if (t < a.T && DUST_IB(static_cast<int64_t>(t) * (a.C / 4) + j,
+                                               static_cast<int64_t>(a.T) * (a.C / 4))) {
                             const int64_t e4 = static_cast<int64_t>(t) * (a.C / 4) + j;
                             yv[m] = __ldg(reinterpret_cast<const float4*>(a.y1) + e4);
                             gv[m] = __ldg(reinterpret_cast<const float4*>(a.h0) + e4);
@@ -368,8 +373,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         f = fmaf(a.lam, f, sc[r * 32 + off[r & 7]]);
                         const float e = one_m * f;
                         const __nv_bfloat16 hi = __float2bfloat16_rn(e);
-                        out[0] = hi;
-                        out[a.dm] = __float2bfloat16_rn(e - __bfloat162float(hi));
+                        if (DUST_IB((row0 + r) * (2 * a.dm) + col0 + lane + a.dm,
+                                    a.rows * (2 * a.dm))) {
+                            out[0] = hi;
+                            out[a.dm] = __float2bfloat16_rn(e - __bfloat162float(hi));
+                        }
                         out += 2 * a.dm;
                     }
                     __syncwarp();
@@ -387,6 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t v[32];
                         tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + col0, v);
                         tmem_wait_ld();
+                        // (the TMEM load above is warp-collective; only the stores are checked)
+                        if (!DUST_IB(row * a.dm + col0 + 31, a.rows * a.dm)) continue;
 #pragma unroll
                         for (int q = 0; q < 32; q += 4)
                             *reinterpret_cast<float4*>(drow + col0 + q) =
@@ -491,6 +501,7 @@ dust_status reforward1_launch(const float* y1, const float* h0, const void* coef
     a.C = static_cast<int>(C);
     a.dm = static_cast<int>(dm);
     a.nd = nd;
+    a.rows = static_cast<int64_t>(nd) * Tp;
     a.ema = ema ? 1 : 0;
     a.tiles = ema ? static_cast<int>(seq_len / kBM) : 1;
     a.lam = lam;
@@ -504,4 +515,8 @@ dust_status reforward1_launch(const float* y1, const float* h0, const void* coef
     return launch_status();
 }
 
+}  // namespace dust
+
+namespace dust {
+DUST_DEBUG_READER(5)
 }  // namespace dust

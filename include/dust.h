@@ -294,6 +294,30 @@ dust_status dust_box_muller_fast(const uint32_t* words, int64_t npairs, float* n
                                  void* stream);
 
 /*
+ * The debug build.  libdust_debug.so is the same library compiled with every
+ * computed global-memory index of the CUDA-core code checked against the
+ * extent of the buffer it addresses: an index out of range skips its access
+ * (nothing outside the caller's buffers is read or written) and records the
+ * first such fault per source file.  dust_debug_build returns 1 for that
+ * library, 0 for libdust.so.  dust_debug_fault synchronises the device,
+ * returns the first recorded fault as (file id << 32) | source line, or 0 if
+ * no checked access failed since the last call (always 0 in libdust.so), and
+ * clears the record.
+ */
+int dust_debug_build(void);
+uint64_t dust_debug_fault(void);
+
+/*
+ * The debug build's index check by itself: one device thread checks index i
+ * against extent n and writes 1 (in range) or 0 to the device int
+ * `in_bounds`, addressing nothing with i.  In libdust_debug.so an i outside
+ * [0, n) also records a fault that dust_debug_fault then returns (file id
+ * 10); libdust.so always writes 1.  Asynchronous on `stream`.  Returns
+ * DUST_ERR_INVALID_ARG for a null or unaligned `in_bounds`.
+ */
+dust_status dust_debug_check_index(int64_t i, int64_t n, int* in_bounds, void* stream);
+
+/*
  * The outer-product GEMM alone: G[m][n] = sum_k A(m, k) B(n, k) in fp32 from
  * bf16 operands on the tensor cores.  A is stored M-major (k rows of M
  * elements, row stride lda elements) when a_mn != 0, else K-major (M rows of

@@ -53,3 +53,15 @@ def to_dev(a, dtype=None):
     if dtype is not None:
         t = t.to(dtype)
     return t.cuda()
+
+
+@pytest.fixture(autouse=True)
+def _debug_build_faults(request):
+    """Under DUST_LIBRARY=debug (the bounds-checked library) every GPU test
+    also fails if a checked index went out of range while it ran."""
+    yield
+    if os.environ.get("DUST_LIBRARY") == "debug" and request.node.get_closest_marker("gpu"):
+        import activation_perturbation_es_noise_b300 as d
+        if d._lib is not None:
+            fault = d.debug_fault()
+            assert fault is None, "index out of range in csrc file id %d, line %d" % fault
