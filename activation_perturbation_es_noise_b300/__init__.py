@@ -653,12 +653,13 @@ def sum_over_ranks(G, group=None):
 
 
 # ---------------------------------------------------------------- probes ----
-PROBE_OPS_PER_ROUND = {0: 16, 1: 8, 2: 8, 3: 16, 4: 16}  # per thread and round
+PROBE_OPS_PER_ROUND = {0: 16, 1: 8, 2: 8, 3: 16, 4: 16, 5: 16}  # per thread and round
 
 
 def issue_probe(kind, iters, stream=None):
     """Operations per second of one probe kind (0: Philox multiply/xor,
-    1: ex2, 2: fp32 fma), timed with events on the stream: (ops/s, ms)."""
+    1: ex2, 2: fp32 fma, 3 and 4: Philox with split multiplies, 5: packed fp32
+    fma, two operations each), timed with events on the stream: (ops/s, ms)."""
     sink = torch.zeros(256, dtype=torch.int32, device="cuda")
     n = _I64(0)
     s = stream if stream is not None else torch.cuda.current_stream()

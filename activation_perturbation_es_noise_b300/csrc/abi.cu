@@ -73,7 +73,8 @@ __global__ void debug_check_index_kernel(int64_t i, int64_t n, int* in_bounds) {
 //   kind 0: the Philox step, a 32 x 32 -> 64-bit multiply and an xor of its
 //           halves (2 operations per chain and round);
 //   kind 1: ex2.approx (1 XU operation per chain and round);
-//   kind 2: fp32 fma (1 operation per chain and round).
+//   kind 2: fp32 fma (1 operation per chain and round);
+//   kind 5: packed fp32 fma, fma.rn.f32x2 (2 operations per chain and round).
 // The chains' results go to `sink` so that nothing is optimised away.
 __global__ void __launch_bounds__(256) issue_probe_kernel(int kind, int64_t iters,
                                                           uint32_t* sink) {
@@ -114,6 +115,19 @@ __global__ void __launch_bounds__(256) issue_probe_kernel(int kind, int64_t iter
         }
 #pragma unroll
         for (int c = 0; c < 8; ++c) acc ^= x[c];
+    } else if (kind == 5) {
+        float2 f[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            f[c] = make_float2(0.001f * static_cast<float>((tid + c) & 255),
+                               0.002f * static_cast<float>((tid + c) & 127));
+        const float2 m = make_float2(0.999f, 0.998f), k = make_float2(0.0001f, 0.0002f);
+        for (int64_t i = 0; i < iters; ++i) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) f[c] = fma2(f[c], m, k);
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc ^= __float_as_uint(f[c].x) ^ __float_as_uint(f[c].y);
     } else if (kind == 1) {
         float f[8];
 #pragma unroll
@@ -243,7 +257,7 @@ extern "C" dust_status dust_box_muller_fast(const uint32_t* words, int64_t npair
 
 extern "C" dust_status dust_issue_probe(int kind, int64_t iters, int64_t* threads_out,
                                         void* sink, void* stream) {
-    if (kind < 0 || kind > 4 || iters < 1 || iters > (1LL << 32) || !threads_out || !sink ||
+    if (kind < 0 || kind > 5 || iters < 1 || iters > (1LL << 32) || !threads_out || !sink ||
         !aligned(sink, 4))
         return DUST_ERR_INVALID_ARG;
     constexpr int kBlocks = 148 * 8, kThreads = 256;

@@ -516,7 +516,10 @@ __global__ void __launch_bounds__(NTC == 0 ? 256 : NTC, NTC == 32 ? 16 : (NTC ==
         const float w1 = (i + 1 < i_end) ? 1.f : 0.f;
         const DrawHalf dh0 = philox_draw_half(A.draw0 + static_cast<uint32_t>(i), token, keys);
         const DrawHalf dh1 = philox_draw_half(A.draw0 + static_cast<uint32_t>(i + 1), token, keys);
-        float pt0 = 0.f, pt1 = 0.f, ay0 = 0.f, ay1 = 0.f;
+        float ay0 = 0.f, ay1 = 0.f;
+        // sum_v p_v 2^b_v of each draw as two interleaved partial sums (even
+        // and odd channels of the thread's blocks), on packed pairs
+        float2 pe0 = make_float2(0.f, 0.f), pe1 = pe0;
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             // Blocks past the vocabulary (only in the last block row) carry
@@ -525,19 +528,14 @@ __global__ void __launch_bounds__(NTC == 0 ? 256 : NTC, NTC == 32 ? 16 : (NTC ==
             const BlockHalf hb = philox_block_half(b * NT + tid, A.layer, keys);
             const uint4 wd0 = philox_rest(dh0, hb, keys);
             const uint4 wd1 = philox_rest(dh1, hb, keys);
-            const float4 n0 = words_to_normals_fast(wd0, A.clog);
-            const float4 n1 = words_to_normals_fast(wd1, A.clog);
+            const float4 n0 = words_to_normals_fast2(wd0, A.clog);
+            const float4 n1 = words_to_normals_fast2(wd1, A.clog);
             const float4 pb = psm[b * NT + tid];
-            float e = pb.x * ex2_approx(n0.x);
-            e = fmaf(pb.y, ex2_approx(n0.y), e);
-            e = fmaf(pb.z, ex2_approx(n0.z), e);
-            e = fmaf(pb.w, ex2_approx(n0.w), e);
-            float f = pb.x * ex2_approx(n1.x);
-            f = fmaf(pb.y, ex2_approx(n1.y), f);
-            f = fmaf(pb.z, ex2_approx(n1.z), f);
-            f = fmaf(pb.w, ex2_approx(n1.w), f);
-            pt0 = b == 0 ? e : pt0 + e;
-            pt1 = b == 0 ? f : pt1 + f;
+            const float2 plo = make_float2(pb.x, pb.y), phi = make_float2(pb.z, pb.w);
+            pe0 = fma2(plo, make_float2(ex2_approx(n0.x), ex2_approx(n0.y)), pe0);
+            pe0 = fma2(phi, make_float2(ex2_approx(n0.z), ex2_approx(n0.w)), pe0);
+            pe1 = fma2(plo, make_float2(ex2_approx(n1.x), ex2_approx(n1.y)), pe1);
+            pe1 = fma2(phi, make_float2(ex2_approx(n1.z), ex2_approx(n1.w)), pe1);
             nsm[b * NT + tid] = n0;
             nsm[(NB + b) * NT + tid] = n1;
             if (ywarp && b == yb) {  // warp-uniform
@@ -545,6 +543,7 @@ __global__ void __launch_bounds__(NTC == 0 ? 256 : NTC, NTC == 32 ? 16 : (NTC ==
                 ay1 = yc == 0 ? n1.x : yc == 1 ? n1.y : yc == 2 ? n1.z : n1.w;
             }
         }
+        const float pt0 = pe0.x + pe0.y, pt1 = pe1.x + pe1.y;
         const int slot = pass % 3, buf = pass & 1;
         float S0, S1;
         if (fixed) {
@@ -600,18 +599,23 @@ __global__ void __launch_bounds__(NTC == 0 ? 256 : NTC, NTC == 32 ? 16 : (NTC ==
         const float dl0 = (lg2_approx(S0) - ay0) * 0.69314718055994531f;
         const float dl1 = (lg2_approx(S1) - ay1) * 0.69314718055994531f * w1;
         sdl += dl0 + dl1;
+        const float2 d0 = make_float2(dl0, dl0), d1 = make_float2(dl1, dl1);
+        const float2 ww = make_float2(w1, w1);
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             const float4 n0 = nsm[b * NT + tid];
             const float4 n1 = nsm[(NB + b) * NT + tid];
-            s1[b][0] = fmaf(dl1, n1.x, fmaf(dl0, n0.x, s1[b][0]));
-            s1[b][1] = fmaf(dl1, n1.y, fmaf(dl0, n0.y, s1[b][1]));
-            s1[b][2] = fmaf(dl1, n1.z, fmaf(dl0, n0.z, s1[b][2]));
-            s1[b][3] = fmaf(dl1, n1.w, fmaf(dl0, n0.w, s1[b][3]));
-            s0[b][0] = fmaf(n1.x, w1, s0[b][0] + n0.x);
-            s0[b][1] = fmaf(n1.y, w1, s0[b][1] + n0.y);
-            s0[b][2] = fmaf(n1.z, w1, s0[b][2] + n0.z);
-            s0[b][3] = fmaf(n1.w, w1, s0[b][3] + n0.w);
+            // s1 += dl0 n0 + dl1 n1; s0 += n0 + w1 n1, channel pairs (0, 1), (2, 3)
+            float2 u = fma2(d1, make_float2(n1.x, n1.y),
+                            fma2(d0, make_float2(n0.x, n0.y), make_float2(s1[b][0], s1[b][1])));
+            float2 v = fma2(d1, make_float2(n1.z, n1.w),
+                            fma2(d0, make_float2(n0.z, n0.w), make_float2(s1[b][2], s1[b][3])));
+            s1[b][0] = u.x; s1[b][1] = u.y; s1[b][2] = v.x; s1[b][3] = v.y;
+            u = fma2(make_float2(n1.x, n1.y), ww,
+                     add2(make_float2(s0[b][0], s0[b][1]), make_float2(n0.x, n0.y)));
+            v = fma2(make_float2(n1.z, n1.w), ww,
+                     add2(make_float2(s0[b][2], s0[b][3]), make_float2(n0.z, n0.w)));
+            s0[b][0] = u.x; s0[b][1] = u.y; s0[b][2] = v.x; s0[b][3] = v.y;
         }
     }
 

@@ -230,4 +230,51 @@ __device__ __forceinline__ float4 words_to_normals_fast(uint4 w, float clog = kC
     return a;
 }
 
+// Packed fp32 pairs (the f32x2 forms of add, mul and fma, sm_100 and later):
+// one instruction does the operation on both lanes of the pair, each rounded
+// exactly as the scalar operation (round to nearest even, no flush), so a
+// computation moved onto pairs gives the same bits as its scalar form.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n .reg .b64 pa, pb, pc, pd;\n mov.b64 pa, {%2, %3};\n mov.b64 pb, {%4, %5};\n"
+        " mov.b64 pc, {%6, %7};\n fma.rn.f32x2 pd, pa, pb, pc;\n mov.b64 {%0, %1}, pd;\n}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n .reg .b64 pa, pb, pd;\n mov.b64 pa, {%2, %3};\n mov.b64 pb, {%4, %5};\n"
+        " mul.rn.f32x2 pd, pa, pb;\n mov.b64 {%0, %1}, pd;\n}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n .reg .b64 pa, pb, pd;\n mov.b64 pa, {%2, %3};\n mov.b64 pb, {%4, %5};\n"
+        " add.rn.f32x2 pd, pa, pb;\n mov.b64 {%0, %1}, pd;\n}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// words_to_normals_fast with its two Box-Muller pairs side by side on packed
+// pairs: the same operations in the same order, so the same bits.
+__device__ __forceinline__ float4 words_to_normals_fast2(uint4 w, float clog = kClogUnit) {
+    const float2 u = add2(make_float2(unit_float(w.x), unit_float(w.z)),
+                          make_float2(-0x1.fffffep-1f, -0x1.fffffep-1f));
+    const float2 x = mul2(make_float2(lg2_approx(u.x), lg2_approx(u.y)), make_float2(clog, clog));
+    const float r0 = sqrt_approx(x.x), r1 = sqrt_approx(x.y);
+    const float2 th = fma2(make_float2(unit_float(w.y), unit_float(w.w)),
+                           make_float2(6.2831853071795865f, 6.2831853071795865f),
+                           make_float2(-9.4247779f, -9.4247779f));
+    float s0, c0, s1, c1;
+    __sincosf(th.x, &s0, &c0);
+    __sincosf(th.y, &s1, &c1);
+    const float2 a01 = mul2(make_float2(-r0, -r0), make_float2(c0, s0));
+    const float2 a23 = mul2(make_float2(-r1, -r1), make_float2(c1, s1));
+    return make_float4(a01.x, a01.y, a23.x, a23.y);
+}
+
 }  // namespace dust

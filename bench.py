@@ -255,7 +255,8 @@ def issue_probes(dust):
     """Measured issue rates (T operations/s) of the library's probe kernel:
     Philox's multiply/xor step, ex2 on the XU pipe, and fp32 fma."""
     out = {}
-    for kind, name, iters in ((0, "philox_mul_xor", 10000), (1, "ex2", 4000), (2, "ffma", 40000)):
+    for kind, name, iters in ((0, "philox_mul_xor", 10000), (1, "ex2", 4000), (2, "ffma", 40000),
+                              (5, "ffma2_ops", 40000)):
         dust.issue_probe(kind, 16)  # warm-up
         rate, _ = dust.issue_probe(kind, iters)
         out[name] = rate / 1e12
@@ -321,7 +322,7 @@ def roofline(wl, kernel_ms, traffic, probes=None, split=None):
         peak = peaks["hbm_gbs"]
         ach = nbytes / (kernel_ms * 1e-3) / 1e9
         return {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-                "traffic": traffic, "kernel": "the whole embedding call (prep, 2 radix scatters, rows)",
+                "traffic": traffic, "kernel": "the whole embedding call (memset, sort, rows)",
                 "kernel_ms": kernel_ms, "bytes_per_call": nbytes,
                 "peak_source": "hbm_gbs (%s)" % which}
     return None
@@ -483,8 +484,11 @@ ATTN = dict(nseq=8, H=8, L=2048, d_in=512, K=64, sigma=0.02, gamma=0.99)
 def run_attn_value(args):
     """The value projection inside attention (8 x 2048 tokens, 8 heads of 64,
     d_in 512, K = 64, gamma 0.99), inputs resident: token-evals/s, and the
-    re-forward kernel against the sustained bf16 tensor peak, counting the
-    three split-bf16 passes over the causal keys the kernel covers."""
+    re-forward kernel against the sustained bf16 tensor peak on the method's
+    own flops: per (sequence, head, draw), the causal product
+    sum_{t <= s} P[s, t] a_t, 64 multiply-adds for each of the L (L + 1) / 2
+    (query, key) pairs.  The kernel executes three split-bf16 passes over whole
+    128-key tiles up to the diagonal (the line's `executed_tflop`)."""
     import torch
 
     import activation_perturbation_es_noise_b300 as dust
@@ -529,7 +533,8 @@ def run_attn_value(args):
     # covered key slices per (sequence, head): sum over query tiles of 128 x 128 (qb + 1)
     nt = L // 128
     pairs = 128 * 128 * nt * (nt + 1) // 2
-    flops = 3 * 2.0 * pairs * 64 * 4 * (K // 4) * nseq * H
+    executed = 3 * 2.0 * pairs * 64 * 4 * (K // 4) * nseq * H
+    flops = 2.0 * 64 * (L * (L + 1) // 2) * K * nseq * H
     peaks, which = _peaks()
     ach = flops / (kernel_ms * 1e-3) / 1e12
     print(json.dumps({
@@ -542,7 +547,8 @@ def run_attn_value(args):
         "roofline": {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"],
                      "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops_sustained"],
                      "traffic": load_traffic({"name": "attn_value"}), "kernel": "attn_v_kernel",
-                     "kernel_ms": kernel_ms,
+                     "kernel_ms": kernel_ms, "flops": "algorithmic",
+                     "algorithmic_tflop": flops / 1e12, "executed_tflop": executed / 1e12,
                      "peak_source": "bf16_tflops_sustained (%s)" % which},
         "cpu_baseline": None, "e2e": None, "gpu_launches": args.steps * (2 * (K // 4) + 6),
         "clocks": clocks.summary()}), flush=True)
@@ -552,9 +558,11 @@ def run_attn_value(args):
 def run_attn_qk(args):
     """The query projection inside attention (which 0; 8 x 2048 tokens, 8
     heads of 64, d_in 512, K = 64, gamma 0.99), inputs resident: token-evals/s,
-    and the tensor-core kernel against the sustained bf16 peak, counting the
-    flops it executes: per 64-key slice of the causal range, two 128 x 64 x 64
-    products (score shifts, weighted values), each as three split-bf16 passes."""
+    and the tensor-core kernel against the sustained bf16 peak on the method's
+    own flops: per (sequence, head, draw) and causal (query, key) pair, two
+    64-long dot products (the score shift and the weighted value).  The kernel
+    executes each over whole 64-key slices up to the diagonal as three
+    split-bf16 passes (the line's `executed_tflop`)."""
     import torch
 
     import activation_perturbation_es_noise_b300 as dust
@@ -602,7 +610,8 @@ def run_attn_qk(args):
     kernel_ms = timer.total_ms() / args.steps
     nt = L // 128
     slices = 2 * nt * (nt + 1) // 2  # 64-key slices per (sequence, head, draw)
-    flops = 3 * 2 * (2.0 * 128 * 64 * 64) * slices * nseq * H * K
+    executed = 3 * 2 * (2.0 * 128 * 64 * 64) * slices * nseq * H * K
+    flops = 2 * 2.0 * 64 * (L * (L + 1) // 2) * nseq * H * K
     peaks, which = _peaks()
     peak = peaks["bf16_tflops_sustained"]
     ach = flops / (kernel_ms * 1e-3) / 1e12
@@ -616,6 +625,8 @@ def run_attn_qk(args):
         "roofline": {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                      "frac": ach / peak, "traffic": load_traffic({"name": "attn_qk"}),
                      "kernel": "attn_qk_tc_kernel<queries>", "kernel_ms": kernel_ms,
+                     "flops": "algorithmic", "algorithmic_tflop": flops / 1e12,
+                     "executed_tflop": executed / 1e12,
                      "peak_source": "bf16_tflops_sustained (%s)" % which},
         "cpu_baseline": None, "e2e": None, "gpu_launches": args.steps * 7,
         "clocks": clocks.summary()}), flush=True)

@@ -528,7 +528,9 @@ dust_status dust_wait_selftest(void* ws, uint64_t limit_ns, void* stream);
  *   kind 1: ex2.approx (8 XU operations per thread and round),
  *   kind 2: fp32 fma (8 operations per thread and round),
  *   kind 3, 4: kind 0's step with the product's halves as two 32-bit
- *           multiplies, written as PTX (3) or as C (4) (16 per round).
+ *           multiplies, written as PTX (3) or as C (4) (16 per round),
+ *   kind 5: packed fp32 fma, fma.rn.f32x2 (2 operations per instruction; 16
+ *           operations per thread and round).
  * The caller times it with events on `stream`.  `sink` (device, >= 1 KB) only
  * keeps the results alive.  INVALID_ARG for another kind, iters outside
  * [1, 2^32], or a NULL pointer.

@@ -18,6 +18,14 @@ def test_probe_rates_are_physical(dust):
     assert rates[1] < rates[2] and rates[0] < 1.05 * NOMINAL_LANE_OPS, rates
 
 
+def test_packed_fma_probe_counts_two_operations_per_instruction(dust):
+    dust.issue_probe(5, 16)
+    packed, ms = dust.issue_probe(5, 20000)
+    assert ms > 0.1
+    # at most two fp32 operations per lane and clock
+    assert 0.25 * NOMINAL_LANE_OPS < packed < 2.1 * NOMINAL_LANE_OPS, packed
+
+
 def test_probe_rejects_bad_kind(dust):
     with pytest.raises(dust.DustError):
-        dust.issue_probe(5, 10)
+        dust.issue_probe(6, 10)
