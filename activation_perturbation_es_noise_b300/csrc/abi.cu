@@ -33,15 +33,26 @@ __global__ void philox_fill_kernel(PhiloxKeys keys, uint32_t layer, uint32_t dra
     }
 }
 
-// One thread per pair of words: the kernels' fast Box-Muller at scale 1.
+// The kernels' fast Box-Muller at scale 1: one thread per two pairs of words
+// through words_to_normals_fast (the packed form every estimator kernel
+// runs), and the last pair of an odd count through box_muller_fast (the
+// scalar form it must equal bit for bit).
 __global__ void box_muller_fast_kernel(const uint2* __restrict__ words, int64_t npairs,
                                        float2* __restrict__ normals) {
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < npairs;
+    const int64_t nquads = npairs / 2;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i <= nquads;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const uint2 w = words[i];
-        float2 a;
-        box_muller_fast(w.x, w.y, a.x, a.y, -2.0f * 0.69314718055994531f);
-        normals[i] = a;
+        if (i < nquads) {
+            const uint2 w0 = words[2 * i], w1 = words[2 * i + 1];
+            const float4 a = words_to_normals_fast(make_uint4(w0.x, w0.y, w1.x, w1.y), kClogUnit);
+            normals[2 * i] = make_float2(a.x, a.y);
+            normals[2 * i + 1] = make_float2(a.z, a.w);
+        } else if (2 * nquads < npairs) {
+            const uint2 w = words[2 * nquads];
+            float2 a;
+            box_muller_fast(w.x, w.y, a.x, a.y, kClogUnit);
+            normals[2 * nquads] = a;
+        }
     }
 }
 

@@ -39,20 +39,10 @@ namespace {
 constexpr int kHd = 64;       // channels per head
 constexpr int kQKRows = 128;  // query rows per CTA
 
-// e^x - 1 for the score shifts: x (1 + x/2 + x^2/6 + x^3/24) for |x| < 1/8
-// (truncation about 2e-6 relative at x = 1/8 and 2.2e-6 at x = -1/8, under
-// the 2^-16 of the bf16 split the result goes through next, and no
-// cancellation), else expm1f.
-__device__ __forceinline__ float expm1_shift(float x) {
-    if (fabsf(x) < 0.125f) {
-        float q = fmaf(x, 1.0f / 24.0f, 1.0f / 6.0f);
-        q = fmaf(x, q, 0.5f);
-        q = fmaf(x, q, 1.0f);
-        return x * q;
-    }
-    return expm1f(x);
-}
-
+// e^x - 1 for the score shifts (in the slice loop below, on channel pairs):
+// x (1 + x/2 + x^2/6 + x^3/24) for |x| < 1/8 (truncation about 2e-6 relative
+// at x = 1/8 and 2.2e-6 at x = -1/8, under the 2^-16 of the bf16 split the
+// result goes through next, and no cancellation), else expm1f.
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
 // ------------------------------------------------------------------------
@@ -328,21 +318,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_fence_async_shared();
             }
             mbar_arrive(a_full);
-            float wsum = 0.f;
+            float2 wsum2 = make_float2(0.f, 0.f);
             const float* prow =
                 a.P + ((static_cast<int64_t>(sq) * a.H + h) * a.L + s) * a.L + kTcCols * grp;
+            // P of slice j is loaded one slice ahead of its use
+            const int64_t pe = static_cast<int64_t>(a.T) * a.H * a.L;
+            auto load_p = [&](int jj, float4 (&dst)[kTcCols / 4]) {
+#pragma unroll
+                for (int q = 0; q < kTcCols / 4; ++q) {
+                    const int64_t pi = (prow - a.P) + jj * kTcKeys + 4 * q;
+                    dst[q] = __ldg(reinterpret_cast<const float4*>(a.P + DUST_IDX(pi, 4, pe)));
+                }
+            };
+            float4 pn[kTcCols / 4];
+            if (ok) load_p(0, pn);
             for (int j = 0; j < ns; ++j, ++g) {
                 const int st = g & 1;
                 const int k0 = j * kTcKeys + kTcCols * grp;  // this thread's first key
                 if (!ok) continue;
                 float4 pv[kTcCols / 4];
 #pragma unroll
-                for (int q = 0; q < kTcCols / 4; ++q) {
-                    // prow's row of P: keys 0 .. L - 1 of query s of head h of sequence sq
-                    const int64_t pe = static_cast<int64_t>(a.T) * a.H * a.L;
-                    const int64_t pi = (prow - a.P) + j * kTcKeys + 4 * q;
-                    pv[q] = __ldg(reinterpret_cast<const float4*>(a.P + DUST_IDX(pi, 4, pe)));
-                }
+                for (int q = 0; q < kTcCols / 4; ++q) pv[q] = pn[q];
+                if (j + 1 < ns) load_p(j + 1, pn);
                 ok = mbar_wait(ds_full(st), (g >> 1) & 1, a.status);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) continue;
@@ -352,32 +349,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(ds_empty(st));
-                float w[kTcCols];
-                if ((j + 1) * kTcKeys <= qb * kQKRows) {  // below the tile's diagonal: no mask
+                // e^x - 1 on channel pairs: x (1 + x/2 + x^2/6 + x^3/24) for |x| < 1/8;
+                // a warp with any larger x redoes those with expm1f.
+                float2 ex[kTcCols / 2];
+                bool big = false;
 #pragma unroll
-                    for (int q = 0; q < kTcCols / 4; ++q) {
-                        const float pr[4] = {pv[q].x, pv[q].y, pv[q].z, pv[q].w};
+                for (int m = 0; m < kTcCols / 2; ++m) {
+                    const float2 x = make_float2(__uint_as_float(r[2 * m]), __uint_as_float(r[2 * m + 1]));
+                    big |= fabsf(x.x) >= 0.125f || fabsf(x.y) >= 0.125f;
+                    float2 q = fma2(x, make_float2(1.0f / 24.0f, 1.0f / 24.0f),
+                                    make_float2(1.0f / 6.0f, 1.0f / 6.0f));
+                    q = fma2(x, q, make_float2(0.5f, 0.5f));
+                    q = fma2(x, q, make_float2(1.0f, 1.0f));
+                    ex[m] = mul2(x, q);
+                }
+                if (__any_sync(0xffffffffu, big)) {
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const float x = pr[u] * expm1_shift(__uint_as_float(r[4 * q + u]));
-                            w[4 * q + u] = x;
-                            wsum += x;
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int q = 0; q < kTcCols / 4; ++q) {
-                        const float pr[4] = {pv[q].x, pv[q].y, pv[q].z, pv[q].w};
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int t = k0 + 4 * q + u;
-                            const float x =
-                                t <= s ? pr[u] * expm1_shift(__uint_as_float(r[4 * q + u])) : 0.f;
-                            w[4 * q + u] = x;
-                            wsum += x;
-                        }
+                    for (int m = 0; m < kTcCols / 2; ++m) {
+                        const float x0 = __uint_as_float(r[2 * m]), x1 = __uint_as_float(r[2 * m + 1]);
+                        if (fabsf(x0) >= 0.125f) ex[m].x = expm1f(x0);
+                        if (fabsf(x1) >= 0.125f) ex[m].y = expm1f(x1);
                     }
                 }
+                // w = P (e^ds - 1), zero after the query (only the tile's diagonal slices)
+                float2 w[kTcCols / 2];
+#pragma unroll
+                for (int q = 0; q < kTcCols / 4; ++q) {
+                    w[2 * q] = mul2(make_float2(pv[q].x, pv[q].y), ex[2 * q]);
+                    w[2 * q + 1] = mul2(make_float2(pv[q].z, pv[q].w), ex[2 * q + 1]);
+                }
+                if ((j + 1) * kTcKeys > qb * kQKRows) {
+#pragma unroll
+                    for (int m = 0; m < kTcCols / 2; ++m) {
+                        if (k0 + 2 * m > s) w[m].x = 0.f;
+                        if (k0 + 2 * m + 1 > s) w[m].y = 0.f;
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < kTcCols / 2; ++m) wsum2 = add2(wsum2, w[m]);
                 if (g >= 2) {
                     ok = mbar_wait(w_empty(st), ((g >> 1) & 1) ^ 1u, a.status);
                     ok = __all_sync(0xffffffffu, ok);
@@ -388,7 +397,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int m = 0; m < kTcCols / 8; ++m) {
                     uint32_t hi[4], lo[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) split_pair(w[8 * m + 2 * u], w[8 * m + 2 * u + 1], hi[u], lo[u]);
+                    for (int u = 0; u < 4; ++u) split_pair2(w[4 * m + u], hi[u], lo[u]);
                     const uint32_t off = sw128(row, (kTcCols / 8) * grp + m);
                     st_shared_v4(wh + off, hi[0], hi[1], hi[2], hi[3]);
                     st_shared_v4(wl + off, lo[0], lo[1], lo[2], lo[3]);
@@ -396,6 +405,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_fence_async_shared();
                 mbar_arrive(w_full(st));
             }
+            const float wsum = wsum2.x + wsum2.y;
             // end of the head: W_s, then <E, dO> over this thread's channels
             s_w[h & 1][grp][row] = wsum;
             ok = epi_all(ok);

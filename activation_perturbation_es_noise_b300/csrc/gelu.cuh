@@ -35,4 +35,66 @@ __device__ __forceinline__ float gelu_as(float u) {
     return u * fmaf(0.5f, erf_as(u * 0.70710678118654752f), 0.5f);
 }
 
+// gelu_as on a packed pair, the same operations in the same order (so the
+// same bits as two gelu_as calls).  Two rewrites keep it free of sign
+// operations: x (x c) equals |x| (|x| c) exactly, and 1 - q t e is formed
+// as q t e - 1, whose magnitude copysign takes.
+__device__ __forceinline__ float2 gelu_as2(float2 u) {
+    const float2 x = mul2(u, make_float2(0.70710678118654752f, 0.70710678118654752f));
+    const float2 den = fma2(make_float2(0.3275911f, 0.3275911f),
+                            make_float2(fabsf(x.x), fabsf(x.y)), make_float2(1.0f, 1.0f));
+    const float2 t = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+    float2 q = fma2(t, make_float2(1.061405429f, 1.061405429f),
+                    make_float2(-1.453152027f, -1.453152027f));
+    q = fma2(t, q, make_float2(1.421413741f, 1.421413741f));
+    q = fma2(t, q, make_float2(-0.284496736f, -0.284496736f));
+    q = fma2(t, q, make_float2(0.254829592f, 0.254829592f));
+    const float2 m = mul2(x, mul2(x, make_float2(-1.4426950408889634f, -1.4426950408889634f)));
+    const float2 e = make_float2(ex2a(m.x), ex2a(m.y));
+    const float2 r = fma2(mul2(q, t), e, make_float2(-1.0f, -1.0f));
+    const float2 erf = make_float2(copysignf(r.x, x.x), copysignf(r.y, x.y));
+    return mul2(u, fma2(make_float2(0.5f, 0.5f), erf, make_float2(0.5f, 0.5f)));
+}
+
+// Taylor coefficients of d -> GELU(y + d) - GELU(y) about d = 0 for small
+// perturbations (the coefficient kernel in reforward.cu states them), for
+// blocks of four channels, in two arrays of nblk entries laid out one after
+// the other: c1 (float4) and c2, c3 as fp16 pairs (c2.x c2.y | c2.z c2.w |
+// c3.x c3.y | c3.z c3.w, first lane in the low half); 8 bytes per channel,
+// read once per draw by the on-chip producers.  With |d| <= 5.77 sigma <=
+// 0.15 the cubic drops d^4 G(y)/24 (|G|/24 < 0.07: under 1e-8 at a
+// typical draw, |d| = sigma = 0.02, and 3.4e-5 at the largest), and the fp16
+// rounding of c2 and c3 (|c2| <= 0.4, |c3| <= 0.13, both in fp16's normal
+// range but for values whose terms are negligible) moves the difference by
+// under 2^-11 of its d^2 and d^3 terms.  The first error is even in d, so it
+// does not bias the estimate, which weights each draw by its own a; the
+// estimator's parity tests bound what is left.  (bf16, with 2^-9, measured
+// five times the ĝ error of fp32 coefficients; fp16 is below their noise.)
+struct GeluCoefs {
+    const float4* c1;
+    const uint4* c23;
+};
+
+__host__ __device__ inline GeluCoefs gelu_coefs(const void* base, int64_t nblk) {
+    const float4* f = static_cast<const float4*>(base);
+    return GeluCoefs{f, reinterpret_cast<const uint4*>(f + nblk)};
+}
+
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t u) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&u));
+}
+
+// GELU(y + d) - GELU(y) = d (c1 + d (c2 + d c3)) for channel pairs (0, 1)
+// and (2, 3) of one block, d = e per channel.
+__device__ __forceinline__ void gelu_taylor_pairs(float4 c1, uint4 c23, float4 e, float2& d01,
+                                                  float2& d23) {
+    const float2 e01 = make_float2(e.x, e.y), e23 = make_float2(e.z, e.w);
+    float2 q01 = fma2(e01, f16x2_to_float2(c23.z), f16x2_to_float2(c23.x));
+    float2 q23 = fma2(e23, f16x2_to_float2(c23.w), f16x2_to_float2(c23.y));
+    q01 = fma2(e01, q01, make_float2(c1.x, c1.y));
+    q23 = fma2(e23, q23, make_float2(c1.z, c1.w));
+    d01 = mul2(e01, q01);
+    d23 = mul2(e23, q23);
+}
+
 }  // namespace dust

@@ -528,8 +528,8 @@ __global__ void __launch_bounds__(NTC == 0 ? 256 : NTC, NTC == 32 ? 16 : (NTC ==
             const BlockHalf hb = philox_block_half(b * NT + tid, A.layer, keys);
             const uint4 wd0 = philox_rest(dh0, hb, keys);
             const uint4 wd1 = philox_rest(dh1, hb, keys);
-            const float4 n0 = words_to_normals_fast2(wd0, A.clog);
-            const float4 n1 = words_to_normals_fast2(wd1, A.clog);
+            const float4 n0 = words_to_normals_fast(wd0, A.clog);
+            const float4 n1 = words_to_normals_fast(wd1, A.clog);
             const float4 pb = psm[b * NT + tid];
             const float2 plo = make_float2(pb.x, pb.y), phi = make_float2(pb.z, pb.w);
             pe0 = fma2(plo, make_float2(ex2_approx(n0.x), ex2_approx(n0.y)), pe0);

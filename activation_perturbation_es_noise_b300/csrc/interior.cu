@@ -98,7 +98,7 @@ __global__ void softmax_rows_kernel(const float* __restrict__ z, int V, int ldp,
 struct DhArgs {
     const float* y1;
     const float* h0;      // GELU(y1), same function as below
-    const float4* coef;   // Taylor coefficients of the GELU difference
+    const void* coef;     // Taylor coefficients of the GELU difference (GeluCoefs layout)
     int taylor;
     int T, Tp, C, nd;
     uint32_t draw_first, token0, layer;  // draw_first = draw0 + i0
@@ -119,11 +119,13 @@ __global__ void interior_dh_kernel(const DhArgs a, const PhiloxKeys keys) {
         const int t = static_cast<int>(idx / nblk);
         const bool valid = t < a.T;
         const int64_t e4 = static_cast<int64_t>(valid ? t : 0) * (a.C / 4) + j;
-        float4 y = make_float4(0.f, 0.f, 0.f, 0.f), g = y, c1 = y, c2 = y, c3 = y, c4 = y;
+        float4 y = make_float4(0.f, 0.f, 0.f, 0.f), g = y, c1 = y;
+        uint4 c23 = make_uint4(0u, 0u, 0u, 0u);
         if (valid && DUST_IB(e4, static_cast<int64_t>(a.T) * (a.C / 4))) {
             if (a.taylor) {
-                const float4* cp = a.coef + e4 * 4;
-                c1 = __ldg(cp); c2 = __ldg(cp + 1); c3 = __ldg(cp + 2); c4 = __ldg(cp + 3);
+                const GeluCoefs cf = gelu_coefs(a.coef, static_cast<int64_t>(a.T) * (a.C / 4));
+                c1 = __ldg(cf.c1 + e4);
+                c23 = __ldg(cf.c23 + e4);
             } else {
                 y = __ldg(reinterpret_cast<const float4*>(a.y1) + e4);
                 g = __ldg(reinterpret_cast<const float4*>(a.h0) + e4);
@@ -138,17 +140,22 @@ __global__ void interior_dh_kernel(const DhArgs a, const PhiloxKeys keys) {
                     philox_rest(philox_draw_half(a.draw_first + i, a.token0 + t, keys), bh, keys));
                 float d[4];
                 if (a.taylor) {
-                    const float e[4] = {a.sigma * nrm.x, a.sigma * nrm.y, a.sigma * nrm.z,
-                                        a.sigma * nrm.w};
-                    d[0] = e[0] * fmaf(e[0], fmaf(e[0], fmaf(e[0], c4.x, c3.x), c2.x), c1.x);
-                    d[1] = e[1] * fmaf(e[1], fmaf(e[1], fmaf(e[1], c4.y, c3.y), c2.y), c1.y);
-                    d[2] = e[2] * fmaf(e[2], fmaf(e[2], fmaf(e[2], c4.z, c3.z), c2.z), c1.z);
-                    d[3] = e[3] * fmaf(e[3], fmaf(e[3], fmaf(e[3], c4.w, c3.w), c2.w), c1.w);
+                    const float2 sg = make_float2(a.sigma, a.sigma);
+                    const float2 e01 = mul2(sg, make_float2(nrm.x, nrm.y));
+                    const float2 e23 = mul2(sg, make_float2(nrm.z, nrm.w));
+                    float2 d01, d23;
+                    gelu_taylor_pairs(c1, c23, make_float4(e01.x, e01.y, e23.x, e23.y), d01, d23);
+                    d[0] = d01.x; d[1] = d01.y; d[2] = d23.x; d[3] = d23.y;
                 } else {
-                    d[0] = gelu_as(fmaf(a.sigma, nrm.x, y.x)) - g.x;
-                    d[1] = gelu_as(fmaf(a.sigma, nrm.y, y.y)) - g.y;
-                    d[2] = gelu_as(fmaf(a.sigma, nrm.z, y.z)) - g.z;
-                    d[3] = gelu_as(fmaf(a.sigma, nrm.w, y.w)) - g.w;
+                    // the GEMM 1 producers' arithmetic, on packed pairs (same bits)
+                    const float2 sg = make_float2(a.sigma, a.sigma);
+                    const float2 d01 = sub2(
+                        gelu_as2(fma2(sg, make_float2(nrm.x, nrm.y), make_float2(y.x, y.y))),
+                        make_float2(g.x, g.y));
+                    const float2 d23 = sub2(
+                        gelu_as2(fma2(sg, make_float2(nrm.z, nrm.w), make_float2(y.z, y.w))),
+                        make_float2(g.z, g.w));
+                    d[0] = d01.x; d[1] = d01.y; d[2] = d23.x; d[3] = d23.y;
                 }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) split_bf16(d[k], h[k], l[k]);
@@ -362,10 +369,10 @@ __global__ void interior_ghat_kernel(const GhatArgs a, const PhiloxKeys keys) {
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const float4 nrm = words_to_normals_fast(w[u]);
-                acc[u].x = fmaf(ri, nrm.x, acc[u].x);
-                acc[u].y = fmaf(ri, nrm.y, acc[u].y);
-                acc[u].z = fmaf(ri, nrm.z, acc[u].z);
-                acc[u].w = fmaf(ri, nrm.w, acc[u].w);
+                const float2 r2 = make_float2(ri, ri);
+                const float2 lo = fma2(r2, make_float2(nrm.x, nrm.y), make_float2(acc[u].x, acc[u].y));
+                const float2 hi = fma2(r2, make_float2(nrm.z, nrm.w), make_float2(acc[u].z, acc[u].w));
+                acc[u] = make_float4(lo.x, lo.y, hi.x, hi.y);
             }
         }
 #pragma unroll
@@ -411,7 +418,7 @@ InteriorPlan interior_plan(int64_t T, int64_t d_in, int64_t C, int64_t dm, int64
     w.take(kCtlBytes);
     P.off_p = w.take(static_cast<size_t>(T * round_up(V, 4)) * 4);
     P.off_h0 = w.take(static_cast<size_t>(T * C) * 4);
-    P.off_coef = w.take(P.fused ? 0 : static_cast<size_t>(T * C) * 16);
+    P.off_coef = w.take(static_cast<size_t>(T * C) * 8);  // GeluCoefs
     P.off_a1 = w.take(P.fused ? 0 : rows * static_cast<size_t>(2 * C) * 2);
     P.off_du = w.take(rows * static_cast<size_t>(dm) * 4);
     P.off_a2 = w.take(rows * static_cast<size_t>(2 * dm) * 2);
@@ -521,13 +528,12 @@ extern "C" dust_status dust_linear_estimate(const void* x, const float* y1, cons
     if ((st = launch_status()) != DUST_OK) return st;
     float* h0 = reinterpret_cast<float*>(w + P.off_h0);
     if ((st = gelu_launch(y1, T * C, h0, s)) != DUST_OK) return st;
-    // Staged A operand (d_model > 512), small sigma: GELU(y1 + d) - GELU(y1)
-    // by its fourth-order Taylor polynomial in d, coefficients once per call
-    // and read once per element for all draws of a chunk.  GEMM 1 with the A
-    // operand on chip evaluates the difference directly: there the
-    // coefficients would be read once per draw, which costs more than the
-    // GELU (measured).
-    const bool taylor = !P.fused && 5.77 * nz.sigma <= 0.15;
+    // Small sigma: GELU(y1 + d) - GELU(y1) by its third-order Taylor
+    // polynomial in d, coefficients once per call (8 bytes per channel),
+    // read once per draw by GEMM 1's on-chip producers and once per chunk by
+    // the staged path; a few packed fmas replace the GELU's erf, reciprocal
+    // and exponential.
+    const bool taylor = 5.77 * nz.sigma <= 0.15;
     void* coef = w + P.off_coef;
     if (taylor && (st = gelu_taylor_launch(y1, T * C, coef, s)) != DUST_OK) return st;
 

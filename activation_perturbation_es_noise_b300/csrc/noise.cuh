@@ -21,6 +21,8 @@
 
 #include <stdint.h>
 
+#include "pairs.cuh"
+
 namespace dust {
 
 constexpr uint32_t kPhiloxM0 = 0xD2511F53u;
@@ -223,45 +225,10 @@ __device__ __forceinline__ void box_muller_fast(uint32_t w_even, uint32_t w_odd,
 // its error estimate is weighted by are the same numbers.
 constexpr float kClogUnit = -1.3862943611198906f;
 
+// The four normals of a word quadruple by box_muller_fast, its two pairs side
+// by side on packed fp32 pairs: the same operations in the same order as two
+// box_muller_fast calls, so the same bits, in fewer instructions.
 __device__ __forceinline__ float4 words_to_normals_fast(uint4 w, float clog = kClogUnit) {
-    float4 a;
-    box_muller_fast(w.x, w.y, a.x, a.y, clog);
-    box_muller_fast(w.z, w.w, a.z, a.w, clog);
-    return a;
-}
-
-// Packed fp32 pairs (the f32x2 forms of add, mul and fma, sm_100 and later):
-// one instruction does the operation on both lanes of the pair, each rounded
-// exactly as the scalar operation (round to nearest even, no flush), so a
-// computation moved onto pairs gives the same bits as its scalar form.
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-    float2 d;
-    asm("{\n .reg .b64 pa, pb, pc, pd;\n mov.b64 pa, {%2, %3};\n mov.b64 pb, {%4, %5};\n"
-        " mov.b64 pc, {%6, %7};\n fma.rn.f32x2 pd, pa, pb, pc;\n mov.b64 {%0, %1}, pd;\n}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return d;
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-    float2 d;
-    asm("{\n .reg .b64 pa, pb, pd;\n mov.b64 pa, {%2, %3};\n mov.b64 pb, {%4, %5};\n"
-        " mul.rn.f32x2 pd, pa, pb;\n mov.b64 {%0, %1}, pd;\n}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-    float2 d;
-    asm("{\n .reg .b64 pa, pb, pd;\n mov.b64 pa, {%2, %3};\n mov.b64 pb, {%4, %5};\n"
-        " add.rn.f32x2 pd, pa, pb;\n mov.b64 {%0, %1}, pd;\n}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-
-// words_to_normals_fast with its two Box-Muller pairs side by side on packed
-// pairs: the same operations in the same order, so the same bits.
-__device__ __forceinline__ float4 words_to_normals_fast2(uint4 w, float clog = kClogUnit) {
     const float2 u = add2(make_float2(unit_float(w.x), unit_float(w.z)),
                           make_float2(-0x1.fffffep-1f, -0x1.fffffep-1f));
     const float2 x = mul2(make_float2(lg2_approx(u.x), lg2_approx(u.y)), make_float2(clog, clog));

@@ -286,9 +286,11 @@ dust_status dust_philox_fill(uint64_t seed, uint32_t layer, uint32_t draw, int64
  * normals[2k+1] = rho sin theta with rho = sqrt(-2 ln u(w_even)),
  * theta = 2 pi u(w_odd) and u(w) = ((w >> 9) + 0.5) 2^-23, computed with the
  * hardware log2, square root and sin/cos (the map of dust_noise, to within
- * the error those approximations leave).  words and normals are device
- * arrays of 2 npairs elements, 8-byte aligned.  INVALID_ARG for a negative
- * count or a NULL or misaligned array.
+ * the error those approximations leave).  Pairs are taken two at a time by
+ * the packed-pair form the estimator kernels run and the last pair of an odd
+ * count by the scalar form; both give the same bits.  words and normals are
+ * device arrays of 2 npairs elements, 8-byte aligned.  INVALID_ARG for a
+ * negative count or a NULL or misaligned array.
  */
 dust_status dust_box_muller_fast(const uint32_t* words, int64_t npairs, float* normals,
                                  void* stream);

@@ -45,6 +45,23 @@ def test_attn_qk_matches_oracle(dust, orc, which, nseq, H, L, d_in, K, gamma):
 
 
 @pytest.mark.parametrize("which", [0, 1])
+def test_attn_qk_large_score_shifts(dust, orc, which):
+    """sigma 0.6: most score shifts are beyond the short e^x - 1 series'
+    range (|x| >= 1/8), so the warps take the expm1f fallback, and the
+    perturbed softmax is far from linear in the noise."""
+    nseq, H, L, d_in, K = 1, 2, 256, 24, 6
+    Q, Kk, V, E, x, P, O = _case(orc, nseq, H, L, d_in, seed=91 + which)
+    dQ, dK, dV, dE, dx, dP, dO = _dev(Q, Kk, V, E, x, P, O)
+    g, G, ws = dust.attn_qk_estimate(which, dQ, dK, dV, dO, dP, dE, dx, L, 0.6, 0.97, K, 5)
+    torch.cuda.synchronize()
+    assert dust.workspace_status(ws) == 0
+    ref = orc.attn_qk_estimate(which, Q, Kk, V, E, x, L, H, 0.6, 0.97, K, 5, 4 + which)
+    eg, eG = rel_l2(g.cpu().numpy(), ref["g"]), rel_l2(G.cpu().numpy(), ref["G"])
+    assert eg <= G_TOL and eG <= GW_TOL, (eg, eG)
+    parity(g=eg, G_W=eG)
+
+
+@pytest.mark.parametrize("which", [0, 1])
 def test_attn_qk_full_size_first_sequence(dust, orc, which):
     """8 x 2048 tokens, 8 heads of 64, d_in 512 (the bench's shapes) with 4
     draws: sequence 0's rows of g against the oracle run on that sequence

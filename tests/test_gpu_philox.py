@@ -77,6 +77,23 @@ def test_fast_box_muller_on_every_uniform(dust, orc):
     assert rms <= 1e-6
 
 
+def test_packed_box_muller_equals_the_scalar_form(dust):
+    """The estimator kernels run the fast map on packed fp32 pairs
+    (words_to_normals_fast); the hook applies that form to pairs taken two at
+    a time and the scalar box_muller_fast to the last pair of an odd count.
+    The same pair through both forms must give the same bits."""
+    import torch
+    rng = np.random.default_rng(11)
+    words = rng.integers(0, 2**32, (64, 2), dtype=np.uint64).astype(np.uint32)
+    words[0] = (0xFFFFFFFF, 0)          # u closest to 1: the smallest radius
+    words[1] = (0, 0xFFFFFFFF)          # u = 2^-24: the largest radius
+    dev = torch.from_numpy(words.view(np.int32)).cuda()
+    packed = dust.box_muller_fast(dev).cpu().numpy()          # 64 pairs: all packed
+    for k in range(64):
+        one = dust.box_muller_fast(dev[k:k + 1].contiguous()).cpu().numpy()  # scalar
+        assert one[0].view(np.uint32).tolist() == packed[k].view(np.uint32).tolist(), k
+
+
 def test_fast_box_muller_matches_counter_normals(dust, orc):
     """On Philox words of real counters, the fast map agrees with the oracle's
     normals of the same counters (the map the estimators' noise follows)."""
