@@ -68,8 +68,19 @@ constexpr int kTcEpi = 128 * kTcGroups;
 constexpr int kTcThreads = 64 + kTcEpi;      // TMA, MMA, epilogue
 constexpr uint32_t kT8 = 64u * 128u;         // 64 rows x 128 bytes
 constexpr uint32_t kT16 = 128u * 128u;       // 128 rows x 128 bytes
-constexpr uint32_t kTcStage = 4u * kT8;      // K_hi, K_lo, Vt_hi, Vt_lo
-constexpr uint32_t kTcOffA = 2u * kTcStage;  // A_hi, A_lo
+// K slices ([hi | lo], 16 KB), V^T slices ([hi | lo], 16 KB) and the tile's
+// P (128 queries x 32 keys fp32, 16 KB: a slice in two halves) come by TMA in
+// rings of their own, so each is loaded ahead of the product or the epilogue
+// step that needs it.  P arrives 128-byte swizzled: a thread reads its query's
+// row as 16-byte pieces spread over the banks, where reading it from global
+// memory would touch a different line per lane.
+constexpr int kNK = 2;                       // K ring stages
+constexpr int kNV = 2;                       // V ring stages
+constexpr int kNP = 3;                       // P ring stages (half slices)
+constexpr uint32_t kTcHalf = 2u * kT8;       // one K or V stage: hi and lo
+constexpr uint32_t kTcOffV = kNK * kTcHalf;
+constexpr uint32_t kTcOffP = kTcOffV + kNV * kTcHalf;
+constexpr uint32_t kTcOffA = kTcOffP + kNP * kT16;  // A_hi, A_lo
 constexpr uint32_t kTcOffW = kTcOffA + 2u * kT16;  // W[2] = {hi, lo} each
 constexpr uint32_t kTcOffBar = kTcOffW + 4u * kT16;
 constexpr uint32_t kTcSmem = kTcOffBar + 256u + 1024u;
@@ -141,7 +152,8 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
 template <bool KEYS>
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_qk_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                      const QKTcArgs a, const PhiloxKeys keys) {
+                      const __grid_constant__ CUtensorMap tp, const QKTcArgs a,
+                      const PhiloxKeys keys) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ float s_w[2][kTcGroups][kQKRows];  // row sums of w per head parity and key group
     __shared__ float s_dl[kTcGroups][kQKRows];
@@ -149,14 +161,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_gen = smem_raw + (base - raw);
     const uint32_t bars = base + kTcOffBar;
-    auto kv_full = [&](int s) { return bars + 8u * s; };
-    auto kv_empty = [&](int s) { return bars + 16u + 8u * s; };
-    auto ds_full = [&](int b) { return bars + 32u + 8u * b; };
-    auto ds_empty = [&](int b) { return bars + 48u + 8u * b; };
-    auto w_full = [&](int b) { return bars + 64u + 8u * b; };
-    auto w_empty = [&](int b) { return bars + 80u + 8u * b; };
-    const uint32_t a_full = bars + 96u, acc_full = bars + 104u, acc_empty = bars + 112u;
-    const uint32_t tmem_slot = bars + 120u;
+    auto k_full = [&](int s) { return bars + 8u * s; };
+    auto k_empty = [&](int s) { return bars + 8u * (kNK + s); };
+    auto v_full = [&](int s) { return bars + 8u * (2 * kNK + s); };
+    auto v_empty = [&](int s) { return bars + 8u * (2 * kNK + kNV + s); };
+    auto p_full = [&](int s) { return bars + 8u * (2 * kNK + 2 * kNV + s); };
+    auto p_empty = [&](int s) { return bars + 8u * (2 * kNK + 2 * kNV + kNP + s); };
+    const uint32_t bars2 = bars + 8u * (2 * kNK + 2 * kNV + 2 * kNP);
+    auto ds_full = [&](int b) { return bars2 + 8u * b; };
+    auto ds_empty = [&](int b) { return bars2 + 16u + 8u * b; };
+    auto w_full = [&](int b) { return bars2 + 32u + 8u * b; };
+    auto w_empty = [&](int b) { return bars2 + 48u + 8u * b; };
+    const uint32_t a_full = bars2 + 64u, acc_full = bars2 + 72u, acc_empty = bars2 + 80u;
+    const uint32_t tmem_slot = bars2 + 88u;
     volatile uint32_t* tmem_slot_gen =
         reinterpret_cast<volatile uint32_t*>(base_gen + (tmem_slot - base));
 
@@ -171,9 +188,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int64_t tok0 = static_cast<int64_t>(sq) * a.L + qb * kQKRows;
 
     if (threadIdx.x == 0) {
+        for (int b = 0; b < kNK; ++b) {
+            mbar_init(k_full(b), 1);
+            mbar_init(k_empty(b), 1);
+        }
+        for (int b = 0; b < kNV; ++b) {
+            mbar_init(v_full(b), 1);
+            mbar_init(v_empty(b), 1);
+        }
+        for (int b = 0; b < kNP; ++b) {
+            mbar_init(p_full(b), 1);
+            mbar_init(p_empty(b), kTcEpi / 2);  // the threads of one half of the keys
+        }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(kv_full(b), 1);
-            mbar_init(kv_empty(b), 1);
             mbar_init(ds_full(b), 1);
             mbar_init(ds_empty(b), kTcEpi);
             mbar_init(w_full(b), kTcEpi);
@@ -185,6 +212,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_fence_init();
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
+        tma_prefetch_desc(&tp);
     }
     if (warp == 1) tmem_alloc(tmem_slot, 256);
     tc_fence_before();
@@ -197,20 +225,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool ok = true;
             for (int h = 0, g = 0; h < a.H && ok; ++h) {
                 for (int j = 0; j < ns; ++j, ++g) {
-                    const int st = g & 1;
-                    if (g >= 2 && !mbar_wait(kv_empty(st), ((g >> 1) & 1) ^ 1u, a.status)) {
+                    const int sk = g % kNK, sv = g % kNV;
+                    const uint32_t uk = static_cast<uint32_t>(g / kNK), uv = static_cast<uint32_t>(g / kNV);
+                    const int key0 = j * kTcKeys;
+                    const int C = a.H * kHd;
+                    if (g >= kNK && !mbar_wait(k_empty(sk), (uk & 1u) ^ 1u, a.status)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t dst = base + st * kTcStage;
-                    const int key0 = j * kTcKeys;
-                    mbar_arrive_expect_tx(kv_full(st), kTcStage);
-                    const int C = a.H * kHd;
-                    tma_load_2d(dst, &tk, h * kHd, krow0 + key0, kv_full(st));               // K_hi
-                    tma_load_2d(dst + kT8, &tk, C + h * kHd, krow0 + key0, kv_full(st));     // K_lo
-                    tma_load_2d(dst + 2 * kT8, &tv, key0, (sq * a.H + h) * kHd, kv_full(st));   // Vt_hi
-                    tma_load_2d(dst + 3 * kT8, &tv, a.L + key0, (sq * a.H + h) * kHd,          // Vt_lo
-                                kv_full(st));
+                    const uint32_t kd = base + sk * kTcHalf;
+                    mbar_arrive_expect_tx(k_full(sk), kTcHalf);
+                    tma_load_2d(kd, &tk, h * kHd, krow0 + key0, k_full(sk));               // K_hi
+                    tma_load_2d(kd + kT8, &tk, C + h * kHd, krow0 + key0, k_full(sk));     // K_lo
+                    if (g >= kNV && !mbar_wait(v_empty(sv), (uv & 1u) ^ 1u, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t vd = base + kTcOffV + sv * kTcHalf;
+                    mbar_arrive_expect_tx(v_full(sv), kTcHalf);
+                    tma_load_2d(vd, &tv, key0, (sq * a.H + h) * kHd, v_full(sv));           // Vt_hi
+                    tma_load_2d(vd + kT8, &tv, a.L + key0, (sq * a.H + h) * kHd, v_full(sv));  // Vt_lo
+                    // P of the slice: keys key0 .. + 31, then + 32 .. + 63, of the tile's queries
+                    for (int half = 0; half < 2 && ok; ++half) {
+                        const int gp = 2 * g + half, sp = gp % kNP;
+                        const uint32_t up = static_cast<uint32_t>(gp / kNP);
+                        if (gp >= kNP && !mbar_wait(p_empty(sp), (up & 1u) ^ 1u, a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(p_full(sp), kT16);
+                        tma_load_2d(base + kTcOffP + sp * kT16, &tp, key0 + 32 * half,
+                                    (sq * a.H + h) * a.L + qb * kQKRows, p_full(sp));
+                    }
+                    if (!ok) break;
                 }
             }
         }
@@ -221,11 +268,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool ok = true;
             // score product of slice g into ds buffer g & 1
             auto g1 = [&](int g) -> bool {
-                const int st = g & 1;
-                if (!mbar_wait(kv_full(st), (g >> 1) & 1, a.status)) return false;
+                const int st = g & 1, sk = g % kNK;
+                if (!mbar_wait(k_full(sk), static_cast<uint32_t>(g / kNK) & 1u, a.status)) return false;
                 if (g >= 2 && !mbar_wait(ds_empty(st), ((g >> 1) & 1) ^ 1u, a.status)) return false;
                 tc_fence_after();
-                const uint32_t kh = base + st * kTcStage, kl = kh + kT8;
+                const uint32_t kh = base + sk * kTcHalf, kl = kh + kT8;
                 const uint32_t d = tmem + kTcKeys * st;
 #pragma unroll
                 for (int kk = 0; kk < kHd / 16; ++kk) {
@@ -238,15 +285,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     umma_bf16(d, al, bh, idesc, 1u);
                 }
                 umma_commit(ds_full(st));
+                umma_commit(k_empty(sk));
                 return true;
             };
             // value product of slice g (j-th of its head) into acc
             auto g2 = [&](int g, int j) -> bool {
-                const int st = g & 1;
+                const int st = g & 1, sv = g % kNV;
+                if (!mbar_wait(v_full(sv), static_cast<uint32_t>(g / kNV) & 1u, a.status)) return false;
                 if (!mbar_wait(w_full(st), (g >> 1) & 1, a.status)) return false;
                 tc_fence_after();
                 const uint32_t wh = base + kTcOffW + st * 2u * kT16, wl = wh + kT16;
-                const uint32_t vh = base + st * kTcStage + 2 * kT8, vl = vh + kT8;
+                const uint32_t vh = base + kTcOffV + sv * kTcHalf, vl = vh + kT8;
 #pragma unroll
                 for (int kk = 0; kk < kTcKeys / 16; ++kk) {
                     const uint64_t ah = sdesc_sw128(wh + kk * 32u, 16u, 1024u);
@@ -258,7 +307,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     umma_bf16(tmem + 128, al, bh, idesc, 1u);
                 }
                 umma_commit(w_empty(st));
-                umma_commit(kv_empty(st));
+                umma_commit(v_empty(sv));
                 return true;
             };
             for (int h = 0, g0 = 0; h < a.H && ok; ++h, g0 += ns) {
@@ -319,27 +368,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             mbar_arrive(a_full);
             float2 wsum2 = make_float2(0.f, 0.f);
-            const float* prow =
-                a.P + ((static_cast<int64_t>(sq) * a.H + h) * a.L + s) * a.L + kTcCols * grp;
-            // P of slice j is loaded one slice ahead of its use
-            const int64_t pe = static_cast<int64_t>(a.T) * a.H * a.L;
-            auto load_p = [&](int jj, float4 (&dst)[kTcCols / 4]) {
-#pragma unroll
-                for (int q = 0; q < kTcCols / 4; ++q) {
-                    const int64_t pi = (prow - a.P) + jj * kTcKeys + 4 * q;
-                    dst[q] = __ldg(reinterpret_cast<const float4*>(a.P + DUST_IDX(pi, 4, pe)));
-                }
-            };
-            float4 pn[kTcCols / 4];
-            if (ok) load_p(0, pn);
             for (int j = 0; j < ns; ++j, ++g) {
                 const int st = g & 1;
                 const int k0 = j * kTcKeys + kTcCols * grp;  // this thread's first key
                 if (!ok) continue;
+                // this thread's 16 keys of P: half grp / 2 of the slice, 16-byte
+                // pieces 4 (grp % 2) .. + 3 of its row, swizzled
                 float4 pv[kTcCols / 4];
+                {
+                    const int gp = 2 * g + (grp >> 1), sp = gp % kNP;
+                    ok = mbar_wait(p_full(sp), static_cast<uint32_t>(gp / kNP) & 1u, a.status);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) continue;
+                    const uint32_t prow = base + kTcOffP + sp * kT16 + static_cast<uint32_t>(row) * 128u;
 #pragma unroll
-                for (int q = 0; q < kTcCols / 4; ++q) pv[q] = pn[q];
-                if (j + 1 < ns) load_p(j + 1, pn);
+                    for (int q = 0; q < kTcCols / 4; ++q) {
+                        const uint32_t c = static_cast<uint32_t>(((grp & 1) * 4 + q) ^ (row & 7));
+                        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                     : "=f"(pv[q].x), "=f"(pv[q].y), "=f"(pv[q].z), "=f"(pv[q].w)
+                                     : "r"(prow + (c << 4))
+                                     : "memory");
+                    }
+                    // the reads above before the TMA's next write to the stage (a
+                    // generic-proxy read, then an async-proxy write)
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_arrive(p_empty(sp));
+                }
                 ok = mbar_wait(ds_full(st), (g >> 1) & 1, a.status);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) continue;
@@ -622,11 +676,12 @@ extern "C" dust_status dust_attn_qk_estimate(int which, const float* Q, const fl
         if ((st = launch_status()) != DUST_OK) return st;
         const int group = which == 0 ? static_cast<int>(nz.num_draws)
                                      : std::min(static_cast<int>(nz.num_draws), kKeyGroup);
-        CUtensorMap tk, tv;
+        CUtensorMap tk, tv, tp;
         if (!encode_bf16_2d(&tk, which == 0 ? K2 : N2, 2 * C, which == 0 ? T : group * T, 2 * C,
                             kTcKeys, kTcKeys) ||
             !encode_bf16_2d(&tv, V2, 2 * seq_len, T / seq_len * H * kHd, 2 * seq_len, kTcKeys,
-                            kHd))
+                            kHd) ||
+            !encode_f32_2d(&tp, P, seq_len, T * H, seq_len, 32, kQKRows))
             return DUST_ERR_CUDA;
         if (which == 0)
             DUST_CUDA_TRY(set_smem_once(attn_qk_tc_kernel<false>, static_cast<int>(kTcSmem), qk_tc_smem_set[0]));
@@ -648,9 +703,9 @@ extern "C" dust_status dust_attn_qk_estimate(int which, const float* Q, const fl
             const dim3 grid(static_cast<unsigned>(nd), static_cast<unsigned>(T / kQKRows));
             timer_begin(s);
             if (which == 0)
-                attn_qk_tc_kernel<false><<<grid, kTcThreads, kTcSmem, s>>>(tk, tv, ta, keys);
+                attn_qk_tc_kernel<false><<<grid, kTcThreads, kTcSmem, s>>>(tk, tv, tp, ta, keys);
             else
-                attn_qk_tc_kernel<true><<<grid, kTcThreads, kTcSmem, s>>>(tk, tv, ta, keys);
+                attn_qk_tc_kernel<true><<<grid, kTcThreads, kTcSmem, s>>>(tk, tv, tp, ta, keys);
             timer_end(s);
             if ((st = launch_status()) != DUST_OK) return st;
         }

@@ -308,7 +308,8 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
                                 float4 p4;
                                 asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                                              : "=f"(p4.x), "=f"(p4.y), "=f"(p4.z), "=f"(p4.w)
-                                             : "r"(prow + (((g4 ^ (rit & 7)) & 7u) << 4)));
+                                             : "r"(prow + (((g4 ^ (rit & 7)) & 7u) << 4))
+                                             : "memory");
                                 const int qq = 4 * g4;
                                 ce_sum = fmaf(p4.x, expm1_small(__uint_as_float(r[qq])), ce_sum);
                                 ce_sum = fmaf(p4.y, expm1_small(__uint_as_float(r[qq + 1])), ce_sum);
@@ -316,6 +317,9 @@ __global__ void __launch_bounds__(threads_of<EPI>(), 1)
                                 ce_sum = fmaf(p4.w, expm1_small(__uint_as_float(r[qq + 3])), ce_sum);
                             }
                         }
+                        // the reads above before the TMA's next write to the buffer (a
+                        // generic-proxy read, then an async-proxy write)
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                         __syncwarp();
                         if (lane == 0) mbar_arrive(pempty_bar(pb));
                         if (!ce_valid) continue;
@@ -396,6 +400,23 @@ bool encode_bf16_2d(CUtensorMap* map, const void* ptr, int64_t inner, int64_t ou
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 2-D fp32 tensor (inner x outer elements, row stride in elements) with a
+// 128-byte-swizzled box of box_inner (32) x box_outer; out-of-range reads are 0.
+bool encode_f32_2d(CUtensorMap* map, const void* ptr, int64_t inner, int64_t outer,
+                   int64_t stride_elems, uint32_t box_inner, uint32_t box_outer) {
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(stride_elems) * 4};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -126,6 +126,9 @@ dust_status gemm_ce_launch(const void* A, int64_t lda, const void* B, int64_t ld
 // 128-byte swizzle, box box_inner x box_outer, zero fill out of range.
 bool encode_bf16_2d(CUtensorMap* map, const void* ptr, int64_t inner, int64_t outer,
                     int64_t stride_elems, uint32_t box_inner, uint32_t box_outer);
+// The same for fp32 (box_inner 32: one 128-byte row of the box).
+bool encode_f32_2d(CUtensorMap* map, const void* ptr, int64_t inner, int64_t outer,
+                   int64_t stride_elems, uint32_t box_inner, uint32_t box_outer);
 
 struct PhiloxKeys;
 
