@@ -3,9 +3,13 @@
 // id_t (Dust translation, hn.213312.xyz, §2.2 信用分配, last sentences).
 //
 // Done without floating-point atomics so that the result is bitwise
-// reproducible, in two launches:
-//   1. sort (one cooperative launch after a memset of its counters; a
-//      bounded grid-wide barrier between radix passes): per 1024-token chunk
+// reproducible, in two launches after one memset (the control words, every
+// counter and the rows kernel's completion counters):
+//   1. sort, one cooperative launch.  For up to 8190 ids and 64 chunks of
+//      1024 tokens (the pages' 4096-token vocabulary over a batch) it is the
+//      counting pass of embed_count_sort_kernel below: one grid barrier.
+//      Otherwise (a bounded grid-wide barrier between radix passes): per
+//      1024-token chunk
 //      the sort keys (an id outside [0, V) becomes V, sorted last and left
 //      out), the first pass's digit counts and every id's token count
 //      (integer atomics, warp-aggregated: the same sums in any order); then
@@ -41,6 +45,16 @@ constexpr int kSliceF4 = 128;  // float4 columns (512 floats) per row work unit
 constexpr int kSliceF = 128;   // float columns per work unit without float4 rows
 constexpr int kRowThreads = 256;
 constexpr int64_t kMaxT = 1LL << 26;
+// The counting pass, for few ids and few tokens (the pages' 4096-token
+// vocabulary over one batch): every CTA takes one chunk, sorts it stably in
+// shared memory and counts its ids; after one grid barrier every CTA finds
+// each id's place from all chunks' counts.  Keys are below 8192 (13 bits; 8191
+// pads a chunk's tail).
+constexpr int kCountV = 8190;       // largest V the counting pass takes
+constexpr int kCountBins = 8192;
+constexpr int kCountChunks = 64;    // largest chunk count it takes
+constexpr uint32_t kPadKey = 8191u;
+constexpr size_t kCountSmem = (4 * kCountBins + 8 + 4 * 1024 + 32 * 128 + 128 + 4 * 32 + 32) * 4;
 constexpr int64_t kMaxV = 1LL << 24;
 
 // Control words after the status word (word 0) of the workspace.
@@ -179,10 +193,13 @@ struct SortArgs {
     uint32_t* eoff;     // V empty ids before every id
     Piece* table;
     int32_t* empty;     // ids with no token, in order
-    uint32_t* row_done; // V x nslices counters of the rows kernel
-    uint32_t* group_done;  // np_max x nslices counters of the rows kernel
+    uint32_t* row_done; // V x nslices counters of the rows kernel (zeroed by the caller)
+    uint32_t* group_done;  // np_max x nslices counters of the rows kernel (zeroed by the caller)
     int64_t np_max;
     uint32_t* ctl;      // workspace control words (status word 0)
+    uint32_t* chist;    // counting pass: (V + 1) x nchp tokens per id and chunk (zeroed)
+    int nchp;
+    int32_t* perm_dst;  // counting pass: where the permutation goes
 };
 
 // offs[d] for chunk c: tokens of every chunk with a smaller digit, plus
@@ -239,10 +256,6 @@ __global__ void __launch_bounds__(kChunk) embed_sort_kernel(const SortArgs a) {
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid;
     const int64_t hist_words = static_cast<int64_t>(256) * a.nchunks;
 
-    // The rows kernel's counters (nothing here uses them).
-    for (int64_t k = gtid; k < static_cast<int64_t>(a.V) * a.nslices; k += gthreads)
-        a.row_done[k] = 0;
-    for (int64_t k = gtid; k < a.np_max * a.nslices; k += gthreads) a.group_done[k] = 0;
 
     // Keys, the first digit's counts per chunk, tokens per id (cnt and the
     // later passes' digit counts were cleared by the caller's memset).
@@ -390,6 +403,280 @@ __global__ void __launch_bounds__(kChunk) embed_sort_kernel(const SortArgs a) {
     }
 }
 
+// Exclusive prefix sums of four per-thread values over the CTA's 1024 threads
+// (in thread order); tot receives the four totals.  Every thread must call it.
+__device__ void block_exclusive_scan4(const uint32_t (&x)[4], uint32_t (&pre)[4],
+                                      uint32_t (&tot)[4], uint32_t* wsum /* [4][32] */) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t incl[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        incl[c] = x[c];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl[c], o);
+            if (lane >= o) incl[c] += y;
+        }
+        if (lane == 31) wsum[c * 32 + warp] = incl[c];
+    }
+    __syncthreads();
+    if (warp < 4) {
+        const uint32_t w = wsum[warp * 32 + lane];
+        uint32_t wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+            if (lane >= o) wi += y;
+        }
+        wsum[warp * 32 + lane] = wi - w;  // exclusive prefix of the warp totals
+        if (lane == 31) wsum[128 + warp] = wi;  // the CTA total
+    }
+    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        pre[c] = wsum[c * 32 + warp] + incl[c] - x[c];
+        tot[c] = wsum[128 + c];
+    }
+    __syncthreads();  // wsum is free again
+}
+
+// Piece k of id v's n sorted tokens, which start at s0.
+__device__ __forceinline__ Piece make_piece(uint32_t v, uint32_t s0, uint32_t n, uint32_t k) {
+    Piece pc;
+    pc.v = static_cast<int32_t>(v);
+    pc.start = static_cast<int32_t>(s0 + k * kPiece);
+    pc.len = static_cast<int32_t>(min(static_cast<uint32_t>(kPiece), n - k * kPiece));
+    pc.multi = n > static_cast<uint32_t>(kPiece);
+    return pc;
+}
+
+// The counting pass (V <= kCountV, nchunks <= kCountChunks, one CTA per chunk,
+// cooperative launch with kCountSmem bytes of dynamic shared memory).
+//   1. The chunk's sort keys (an id outside [0, V) becomes V, counted and
+//      sorted last, then left out), its count per key (warp-aggregated
+//      shared-memory atomics: exact in any order), and the chunk's (key,
+//      token) pairs sorted stably by key in shared memory (two passes of
+//      7-bit digits, ranks from per-warp digit counts as in the radix sort).
+//      The counts go to chist[chunk][key].
+//   2. After one grid barrier, thread i of every CTA owns keys 8i .. 8i + 7:
+//      their totals over all chunks and over the chunks before this one, and
+//      this chunk's counts, scanned over the keys give each key's first
+//      sorted position seg, its first piece and its place among the ids no
+//      token hits.  A token at place p of the chunk's sorted list with key v
+//      lands at seg[v] + (tokens of v in earlier chunks) + (p - first place
+//      of v in this chunk).  Every CTA scans all keys; CTA b writes the piece
+//      table, the empty ids and poff of the keys owned by its threads
+//      i = b, b + grid, ...
+__global__ void __launch_bounds__(kChunk) embed_count_sort_kernel(const SortArgs a) {
+    extern __shared__ uint32_t csm[];
+    uint32_t* bins = csm;              // this chunk's counts per key, then the scatter bases
+    uint32_t* tot_s = bins + kCountBins;           // tokens per key, all chunks
+    uint32_t* pre_s = tot_s + kCountBins;          // ... in earlier chunks, then each key's seg
+    uint32_t* poff_s = pre_s + kCountBins;         // first piece of each key (kCountBins + 8)
+    uint32_t* lk0 = poff_s + kCountBins + 8;
+    uint32_t* lk1 = lk0 + kChunk;
+    int32_t* lv0 = reinterpret_cast<int32_t*>(lk1 + kChunk);
+    int32_t* lv1 = lv0 + kChunk;
+    uint32_t* wc = reinterpret_cast<uint32_t*>(lv1 + kChunk);  // [32 warps][128 digits]
+    uint32_t* dt = wc + 32 * 128;                              // [128] digit starts
+    uint32_t* wsum = dt + 128;                                 // [4][32] + [4]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = blockIdx.x;
+    const int V1 = a.V + 1;
+
+    for (int v = tid; v < kCountBins; v += kChunk) bins[v] = 0;
+    __syncthreads();
+    const int t = c * kChunk + tid;
+    uint32_t key = kPadKey;
+    if (t < a.T && DUST_IB(t, a.T)) {
+        int id = __ldg(a.ids + t);
+        if (id < 0 || id >= a.V) {
+            record_status(a.ctl, DUST_ERR_DEVICE_RANGE);
+            id = a.V;
+        }
+        key = static_cast<uint32_t>(id);
+    }
+    {
+        // this chunk's count per key, and every chunk's total in cnt (integer
+        // atomics, one per distinct key of a warp: the same sums in any order)
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, key);
+        if (key != kPadKey && (peers & lanemask_lt()) == 0 && DUST_IB(key, kCountBins)) {
+            atomicAdd(&bins[key], static_cast<uint32_t>(__popc(peers)));
+            if (DUST_IB(key, a.V + 1)) atomicAdd(a.cnt + key, static_cast<uint32_t>(__popc(peers)));
+        }
+    }
+    lk0[tid] = key;
+    lv0[tid] = t;
+    for (int pass = 0; pass < 2; ++pass) {
+        const uint32_t* ki = pass ? lk1 : lk0;
+        const int32_t* vi = pass ? lv1 : lv0;
+        uint32_t* ko = pass ? lk0 : lk1;
+        int32_t* vo = pass ? lv0 : lv1;
+        for (int k = tid; k < 32 * 128; k += kChunk) wc[k] = 0;
+        __syncthreads();
+        const uint32_t k = ki[tid];
+        const int32_t val = vi[tid];
+        const uint32_t dig = (k >> (7 * pass)) & 127u;
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, dig);
+        const uint32_t lrank = __popc(peers & lanemask_lt());
+        if (lrank == 0) wc[warp * 128 + dig] = __popc(peers);
+        __syncthreads();
+        if (tid < 128) {  // digit tid: prefix over the warps, then the digit's total
+            uint32_t acc = 0;
+            for (int w = 0; w < 32; ++w) {
+                const uint32_t x = wc[w * 128 + tid];
+                wc[w * 128 + tid] = acc;
+                acc += x;
+            }
+            dt[tid] = acc;
+        }
+        __syncthreads();
+        if (warp == 0) {  // exclusive prefix of the 128 digit totals, four per lane
+            uint32_t x[4], sum = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                x[q] = dt[4 * lane + q];
+                sum += x[q];
+            }
+            uint32_t incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            uint32_t run = incl - sum;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                dt[4 * lane + q] = run;
+                run += x[q];
+            }
+        }
+        __syncthreads();
+        const uint32_t pos = dt[dig] + wc[warp * 128 + dig] + lrank;
+        if (DUST_IB(pos, kChunk)) {
+            ko[pos] = k;
+            vo[pos] = val;
+        }
+    }
+    __syncthreads();  // lk0/lv0: the chunk sorted by key, ties by token
+    // this chunk's counts into column c of chist (zeroed by the caller: only the
+    // keys the chunk holds are written)
+    const int64_t ch_words = static_cast<int64_t>(V1) * a.nchp;
+    for (int v = tid; v < V1; v += kChunk) {
+        const uint32_t n = bins[v];
+        if (n != 0 && DUST_IB(static_cast<int64_t>(v) * a.nchp + c, ch_words))
+            a.chist[static_cast<int64_t>(v) * a.nchp + c] = n;
+    }
+    if (!grid_barrier(a.ctl)) return;
+
+    // For the keys this chunk holds, their counts in the earlier chunks: a
+    // key's row of chist is nchp words, 16-byte aligned, so four chunks per
+    // load; thread i takes keys i + 1024 k, which spreads the keys that every
+    // chunk holds (the frequent ids) over the threads.
+    for (int k = 0; k < kCountBins / kChunk; ++k) {
+        const int v = tid + kChunk * k;
+        uint32_t acc = 0;
+        if (v < V1 && c > 0 && bins[v] != 0) {
+            const int64_t r0 = static_cast<int64_t>(v) * a.nchp;
+            if (a.nchp <= 16) {
+                uint4 q[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    q[u] = (4 * u < c && DUST_IB(r0 + 4 * u + 3, ch_words))
+                               ? __ldcg(reinterpret_cast<const uint4*>(a.chist + r0 + 4 * u))
+                               : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int cc = 4 * u;
+                    acc += (cc < c ? q[u].x : 0u) + (cc + 1 < c ? q[u].y : 0u) +
+                           (cc + 2 < c ? q[u].z : 0u) + (cc + 3 < c ? q[u].w : 0u);
+                }
+            } else {
+                for (int c4 = 0; c4 < c; c4 += 4) {
+                    if (!DUST_IB(r0 + c4 + 3, ch_words)) break;
+                    const uint4 q = __ldcg(reinterpret_cast<const uint4*>(a.chist + r0 + c4));
+                    acc += q.x + (c4 + 1 < c ? q.y : 0u) + (c4 + 2 < c ? q.z : 0u) +
+                           (c4 + 3 < c ? q.w : 0u);
+                }
+            }
+        }
+        pre_s[v] = acc;
+    }
+    __syncthreads();
+    // Keys v0 .. v0 + 7 of this thread, in order, for the scans: totals (cnt),
+    // this chunk's counts, the earlier chunks' counts.
+    const int v0 = 8 * tid;
+    uint32_t tot[8], pre[8], own[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int v = v0 + k;
+        tot[k] = (v < V1 && DUST_IB(v, a.V + 1)) ? __ldcg(a.cnt + v) : 0u;
+        own[k] = v < V1 ? bins[v] : 0u;
+        pre[k] = pre_s[v];
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tot_s[v0 + k] = tot[k];
+    // per-thread sums: tokens, pieces, ids no token hits (v < V), this chunk's tokens
+    uint32_t x4[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int v = v0 + k;
+        x4[0] += tot[k];
+        if (v < a.V) {
+            x4[1] += (tot[k] + kPiece - 1) / kPiece;
+            x4[2] += tot[k] == 0 ? 1u : 0u;
+        }
+        x4[3] += own[k];
+    }
+    uint32_t p4[4], t4[4];
+    block_exclusive_scan4(x4, p4, t4, wsum);  // (its barriers also order the reads of bins above)
+    const bool writer = (tid % static_cast<int>(gridDim.x)) == c;
+    uint32_t seg = p4[0], pof = p4[1], eof = p4[2], lst = p4[3];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int v = v0 + k;
+        if (v >= V1) break;
+        bins[v] = seg + pre[k] - lst;  // scatter base: position = base + place in the chunk
+        pre_s[v] = seg;
+        poff_s[v] = v < a.V ? pof : t4[1];
+        if (writer && v < a.V) {
+            if (DUST_IB(v, a.V + 1)) a.poff[v] = pof;
+            if (tot[k] == 0 && DUST_IB(eof, a.V)) a.empty[eof] = v;
+        }
+        seg += tot[k];
+        if (v < a.V) {
+            pof += (tot[k] + kPiece - 1) / kPiece;
+            eof += tot[k] == 0 ? 1u : 0u;
+        }
+        lst += own[k];
+    }
+    if (c == 0 && tid == 0) {
+        a.poff[a.V] = t4[1];
+        a.ctl[kNPieces] = t4[1];
+        a.ctl[kNEmpty] = t4[2];
+    }
+    __syncthreads();
+    // The piece table, pieces q = c, c + grid, ... of this CTA: q's key is the
+    // last v < V with poff[v] <= q (binary search), k = q - poff[v] its place.
+    const uint32_t npieces = t4[1];
+    for (uint32_t q = static_cast<uint32_t>(c) + static_cast<uint32_t>(gridDim.x) * tid; q < npieces;
+         q += static_cast<uint32_t>(gridDim.x) * kChunk) {
+        int lo = 0, hi = a.V - 1;  // poff_s[lo] <= q < poff_s[hi + 1]
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (poff_s[mid] <= q) lo = mid;
+            else hi = mid - 1;
+        }
+        if (DUST_IB(q, a.np_max))
+            a.table[q] = make_piece(static_cast<uint32_t>(lo), pre_s[lo], tot_s[lo], q - poff_s[lo]);
+    }
+    const uint32_t kk = lk0[tid];
+    if (kk != kPadKey && DUST_IB(kk, kCountBins)) {
+        const uint32_t pos = bins[kk] + static_cast<uint32_t>(tid);
+        if (DUST_IB(pos, a.T)) a.perm_dst[pos] = lv0[tid];
+    }
+}
+
 struct RowArgs {
     const float* g;
     const int32_t* perm;
@@ -397,9 +684,9 @@ struct RowArgs {
     const uint32_t* poff;
     const int32_t* empty;
     const uint32_t* ctl;
-    uint32_t* row_done;    // V x nslices counters of finished groups (cleared by the sort)
+    uint32_t* row_done;    // V x nslices counters of finished groups (zeroed by the caller)
     uint32_t* group_done;  // pieces x nslices counters of finished pieces, at a group's
-                           // first piece (cleared by the sort)
+                           // first piece (zeroed by the caller)
     int d, nslices;
     float* G_E;
     float* partial;  // npieces x d
@@ -619,10 +906,13 @@ __global__ void __launch_bounds__(kRowThreads) embed_rows_kernel(const RowArgs a
 
 struct EmbedPlan {
     int nchunks, passes, nslices;
+    int nchp;           // counting pass: chunk counts per key, padded to 4 words
+    bool counting;      // the counting pass (one grid barrier) instead of the radix sort
     int64_t np_max;
-    size_t zero_bytes;  // [ctl | digit counts | id counts]: cleared before the sort
+    size_t zero_bytes;  // [ctl | digit counts | id counts | chunk counts | the rows kernel's
+                        // counters]: cleared before the sort
     size_t off_hist, off_cnt, off_eoff, off_done, off_gdone, off_k0, off_v0, off_k1, off_v1, off_offs,
-        off_seg, off_poff, off_table, off_empty, off_part, bytes;
+        off_seg, off_poff, off_table, off_empty, off_part, off_chist, bytes;
 };
 
 EmbedPlan embed_plan(int64_t T, int64_t d, int64_t V) {
@@ -641,11 +931,14 @@ EmbedPlan embed_plan(int64_t T, int64_t d, int64_t V) {
     WsLayout w;
     w.take(kCtlBytes);
     P.off_hist = w.take(static_cast<size_t>(P.passes) * hist_words * 4);
-    P.off_cnt = w.take(Vn * 4);
-    P.zero_bytes = w.used;
-    P.off_eoff = w.take(Vn * 4);
+    P.off_cnt = w.take((Vn + 1) * 4);  // (the counting pass counts the invalid key V too)
+    P.counting = V <= kCountV && P.nchunks <= kCountChunks;
+    P.nchp = static_cast<int>(round_up(P.nchunks, 4));
+    P.off_chist = w.take(P.counting ? (Vn + 1) * static_cast<size_t>(P.nchp) * 4 : 0);
     P.off_done = w.take(Vn * static_cast<size_t>(P.nslices) * 4);
     P.off_gdone = w.take(static_cast<size_t>(P.np_max) * static_cast<size_t>(P.nslices) * 4);
+    P.zero_bytes = w.used;
+    P.off_eoff = w.take(Vn * 4);
     P.off_k0 = w.take(Tn * 4);
     P.off_v0 = w.take(Tn * 4);
     P.off_k1 = w.take(Tn * 4);
@@ -660,10 +953,12 @@ EmbedPlan embed_plan(int64_t T, int64_t d, int64_t V) {
     return P;
 }
 
-// CTAs of the sort kernel that fit on the current device at once (the grid
-// of its cooperative launch is at most this), looked up once per device.
-int sort_grid_limit() {
-    static std::atomic<int> limit[64];
+// CTAs of a sort kernel that fit on the current device at once (the grid of
+// its cooperative launch is at most this), looked up once per device: the
+// radix sort (counting = false) or the counting pass with its shared memory.
+int sort_grid_limit(bool counting) {
+    static std::atomic<int> limits[2][64];
+    std::atomic<int>* limit = limits[counting ? 1 : 0];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -673,8 +968,12 @@ int sort_grid_limit() {
     int cached = limit[dev].load(std::memory_order_acquire);
     if (cached > 0) return cached;
     int per_sm = 0, sms = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, embed_sort_kernel, kChunk, 0) !=
-            cudaSuccess ||
+    const cudaError_t occ =
+        counting ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                       &per_sm, embed_count_sort_kernel, kChunk, static_cast<size_t>(kCountSmem))
+                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, embed_sort_kernel,
+                                                                 kChunk, 0);
+    if (occ != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
@@ -710,7 +1009,11 @@ extern "C" dust_status dust_embed_scatter(const float* g_hat, const int32_t* ids
         DUST_CUDA_TRY(cudaMemsetAsync(G_E, 0, static_cast<size_t>(V * d) * 4, s));
         return DUST_OK;
     }
-    const int limit = sort_grid_limit();
+    if (P.counting) {
+        static std::atomic<uint64_t> smem_set{0};
+        DUST_CUDA_TRY(set_smem_once(embed_count_sort_kernel, static_cast<int>(kCountSmem), smem_set));
+    }
+    const int limit = sort_grid_limit(P.counting);
     if (limit < 1) return DUST_ERR_CUDA;
     const bool vec = (d % 4 == 0) && aligned(g_hat, 16) && aligned(G_E, 16);
 
@@ -738,13 +1041,22 @@ extern "C" dust_status dust_embed_scatter(const float* g_hat, const int32_t* ids
     sa.group_done = reinterpret_cast<uint32_t*>(w + P.off_gdone);
     sa.np_max = P.np_max;
     sa.ctl = ctl;
+    sa.chist = reinterpret_cast<uint32_t*>(w + P.off_chist);
+    sa.nchp = P.nchp;
     // the last pass's values: perm_out, or the ping-pong buffer it lands in
-    const int32_t* perm = perm_out ? perm_out : sa.vals[P.passes & 1];
+    sa.perm_dst = perm_out ? perm_out : sa.vals[0];
+    const int32_t* perm = P.counting ? sa.perm_dst : perm_out ? perm_out : sa.vals[P.passes & 1];
+    if (P.counting && P.nchunks > limit) return DUST_ERR_CUDA;
 
     timer_begin(s);  // the benchmark hook times the whole call
     // status and barrier words, the later passes' digit counts, the id counts
     DUST_CUDA_TRY(cudaMemsetAsync(ws, 0, P.zero_bytes, s));
-    {
+    if (P.counting) {
+        void* args[] = {&sa};
+        DUST_CUDA_TRY(cudaLaunchCooperativeKernel(
+            reinterpret_cast<const void*>(embed_count_sort_kernel), dim3(P.nchunks), dim3(kChunk),
+            args, kCountSmem, s));
+    } else {
         const unsigned grid = static_cast<unsigned>(std::min(P.nchunks, limit));
         void* args[] = {&sa};
         DUST_CUDA_TRY(cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(embed_sort_kernel),
