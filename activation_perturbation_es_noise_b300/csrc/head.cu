@@ -514,8 +514,10 @@ __global__ void __launch_bounds__(NTC == 0 ? 256 : NTC, NTC == 32 ? 16 : (NTC ==
         // The second draw of an odd count's last pass is generated but not
         // counted (w1 = 0).
         const float w1 = (i + 1 < i_end) ? 1.f : 0.f;
-        const DrawHalf dh0 = philox_draw_half(A.draw0 + static_cast<uint32_t>(i), token, keys);
-        const DrawHalf dh1 = philox_draw_half(A.draw0 + static_cast<uint32_t>(i + 1), token, keys);
+        const DrawHalf2 dh0 =
+            philox_draw_half2(philox_draw_half(A.draw0 + static_cast<uint32_t>(i), token, keys));
+        const DrawHalf2 dh1 =
+            philox_draw_half2(philox_draw_half(A.draw0 + static_cast<uint32_t>(i + 1), token, keys));
         float ay0 = 0.f, ay1 = 0.f;
         // sum_v p_v 2^b_v of each draw as two interleaved partial sums (even
         // and odd channels of the thread's blocks), on packed pairs
@@ -525,9 +527,9 @@ __global__ void __launch_bounds__(NTC == 0 ? 256 : NTC, NTC == 32 ? 16 : (NTC ==
             // Blocks past the vocabulary (only in the last block row) carry
             // real noise of unused counters; their probabilities are zero and
             // their accumulators are never written.
-            const BlockHalf hb = philox_block_half(b * NT + tid, A.layer, keys);
-            const uint4 wd0 = philox_rest(dh0, hb, keys);
-            const uint4 wd1 = philox_rest(dh1, hb, keys);
+            const BlockHalf2 hb = philox_block_half2(philox_block_half(b * NT + tid, A.layer, keys), keys);
+            const uint4 wd0 = philox_rest2(dh0, hb, keys);
+            const uint4 wd1 = philox_rest2(dh1, hb, keys);
             const float4 n0 = words_to_normals_fast(wd0, A.clog);
             const float4 n1 = words_to_normals_fast(wd1, A.clog);
             const float4 pb = psm[b * NT + tid];

@@ -93,6 +93,35 @@ __device__ __forceinline__ uint4 philox_rest(DrawHalf d, BlockHalf b, const Phil
     return make_uint4(x0, x1, x2, x3);
 }
 
+// The second round splits too: from the state after round 1, its product of
+// word 2 depends only on the block half and its product of word 0 only on
+// the draw half.  Kernels that pair every block with several draws (and
+// every draw with several blocks) compute each side once.
+struct BlockHalf2 {  // hi(M1 x2) ^ k0[1], lo(M1 x2), x3 ^ k1[1] after round 1
+    uint32_t bh, bl, b3;
+};
+struct DrawHalf2 {  // hi(M0 x0), lo(M0 x0), x1 after round 1
+    uint32_t dh, dl, d1;
+};
+
+__device__ __forceinline__ BlockHalf2 philox_block_half2(BlockHalf b, const PhiloxKeys& k) {
+    const uint64_t p1 = static_cast<uint64_t>(b.x2) * kPhiloxM1;
+    return {static_cast<uint32_t>(p1 >> 32) ^ k.k0[1], static_cast<uint32_t>(p1), b.x3 ^ k.k1[1]};
+}
+
+__device__ __forceinline__ DrawHalf2 philox_draw_half2(DrawHalf d) {
+    const uint64_t p0 = static_cast<uint64_t>(d.x0) * kPhiloxM0;
+    return {static_cast<uint32_t>(p0 >> 32), static_cast<uint32_t>(p0), d.x1};
+}
+
+// Rounds 3..10 from the two halves of round 2 (the same words as philox_rest).
+__device__ __forceinline__ uint4 philox_rest2(DrawHalf2 d, BlockHalf2 b, const PhiloxKeys& k) {
+    uint32_t x0 = b.bh ^ d.d1, x1 = b.bl, x2 = d.dh ^ b.b3, x3 = d.dl;
+#pragma unroll
+    for (int r = 2; r < 10; ++r) philox_round(x0, x1, x2, x3, k.k0[r], k.k1[r]);
+    return make_uint4(x0, x1, x2, x3);
+}
+
 __device__ __forceinline__ uint4 philox4x32_10(uint32_t j, uint32_t token, uint32_t draw,
                                                uint32_t layer, const PhiloxKeys& k) {
     return philox_rest(philox_draw_half(draw, token, k), philox_block_half(j, layer, k), k);

@@ -289,7 +289,10 @@ def roofline(wl, kernel_ms, traffic, probes=None, split=None):
         peak = N_SM * 128 * peaks.get("sm_max_mhz", SM_MAX_MHZ) * 1e6 / 1e12
         ach = ops / (kernel_ms * 1e-3) / 1e12
         return {"bound": "alu", "achieved": ach, "peak": peak, "unit": "Tops/s",
-                "frac": ach / peak, "traffic": traffic, "kernel": "head_draws_kernel",
+                "frac": ach / peak, "traffic": traffic,
+                "kernel": ("head_draws_kernel<antithetic>" if wl.get("baseline") == 2 else
+                           "head_draws_kernel<vocabulary chunks>" if wl.get("vchunk") else
+                           "head_pair_kernel"),
                 "kernel_ms": kernel_ms, "peak_source": "148 SMs x 128 lanes x %.0f MHz (%s clocks)"
                 % (peaks.get("sm_max_mhz", SM_MAX_MHZ), which),
                 "issue_probe": probes}

@@ -1,4 +1,6 @@
-"""Embedding scatter-add: CUDA path against the oracle (GPU).
+"""Embedding scatter-add: CUDA path against the oracle (GPU), through both
+sorts: the counting pass (at most 8190 ids and 64 chunks of 1024 tokens) and
+the LSD radix sort (everything else).
 
 perm is bit-exact (the stable order of the ids is unique); G_E within
 rel-L2 1e-5 (fp32 sums in a fixed order against float64).
@@ -26,6 +28,9 @@ def _run(dust, g, ids, V):
     (3000, 33, 300, "same"),      # every token has the same id: one long run
     (1, 4, 1, "uniform"),
     (2500, 16, 70000, "uniform"), # three radix passes
+    (65536, 8, 8190, "uniform"),  # the counting pass at its limits: 64 chunks, 8190 ids
+    (70000, 8, 300, "zipf"),      # 69 chunks: the radix sort with few ids
+    (5000, 8, 8191, "uniform"),   # one id more than the counting pass takes
 ])
 def test_embed_shapes(dust, orc, T, d, V, kind):
     rng = np.random.default_rng(T + d)
@@ -72,6 +77,17 @@ def test_embed_bad_id_sets_status(dust):
     G, perm, st = _run(dust, g, ids, 10)
     assert st == 6
     assert G[3].sum() == 0 and G[4].sum() == 4
+
+
+def test_embed_bad_id_sets_status_radix(dust):
+    """The same through the radix sort (more ids than the counting pass takes)."""
+    g = np.ones((10, 4), np.float32)
+    ids = np.arange(10, dtype=np.int32) * 900
+    ids[3] = 9999
+    G, perm, st = _run(dust, g, ids, 9000)
+    assert st == 6
+    assert G[2700].sum() == 0 and G[3600].sum() == 4
+    assert perm[-1] == 3  # the bad id sorts last
 
 
 def test_embed_without_perm_output(dust):
