@@ -131,13 +131,14 @@ __global__ void interior_dh_kernel(const DhArgs a, const PhiloxKeys keys) {
                 g = __ldg(reinterpret_cast<const float4*>(a.h0) + e4);
             }
         }
-        const BlockHalf bh = philox_block_half(j, a.layer, keys);
+        const BlockHalf2 bh = philox_block_half2(philox_block_half(j, a.layer, keys), keys);
         for (int i = 0; i < a.nd; ++i) {
             __nv_bfloat16* row = a.A1 + chunk_row(t, i, a.nd) * (2 * static_cast<int64_t>(a.C));
             __nv_bfloat16 h[4], l[4];
             if (valid) {
                 const float4 nrm = words_to_normals_fast(
-                    philox_rest(philox_draw_half(a.draw_first + i, a.token0 + t, keys), bh, keys));
+                    philox_rest2(philox_draw_half2(philox_draw_half(a.draw_first + i, a.token0 + t, keys)),
+                                 bh, keys));
                 float d[4];
                 if (a.taylor) {
                     const float2 sg = make_float2(a.sigma, a.sigma);
@@ -349,11 +350,11 @@ __global__ void interior_ghat_kernel(const GhatArgs a, const PhiloxKeys keys) {
         const int j0 = static_cast<int>(idx % half);
         const int t = static_cast<int>(idx / half);
         const int jb[2] = {j0, j0 + half};
-        BlockHalf bh[2];
+        BlockHalf2 bh[2];
         float4 acc[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-            bh[u] = philox_block_half(jb[u], a.layer, keys);
+            bh[u] = philox_block_half2(philox_block_half(jb[u], a.layer, keys), keys);
             acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         const float* rcol = a.r + t;
@@ -362,10 +363,10 @@ __global__ void interior_ghat_kernel(const GhatArgs a, const PhiloxKeys keys) {
             const float ri = DUST_IB(t + static_cast<int64_t>(i) * a.T, static_cast<int64_t>(a.K) * a.T)
                                  ? __ldg(rcol + static_cast<int64_t>(i) * a.T)
                                  : 0.f;
-            const DrawHalf dh = philox_draw_half(a.draw0 + i, a.token0 + t, keys);
+            const DrawHalf2 dh = philox_draw_half2(philox_draw_half(a.draw0 + i, a.token0 + t, keys));
             uint4 w[2];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) w[u] = philox_rest(dh, bh[u], keys);
+            for (int u = 0; u < 2; ++u) w[u] = philox_rest2(dh, bh[u], keys);
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const float4 nrm = words_to_normals_fast(w[u]);

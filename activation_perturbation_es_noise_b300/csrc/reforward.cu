@@ -215,13 +215,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < ntiles; ++k) {
             const int tb = tb0 + k;
             const int mt = tb * a.nd + di;
-            // The (draw, token) half of Philox's first round is the same for
-            // every slice of a row: computed once per tile.
-            DrawHalf dhalf[kRows];
+            // The (draw, token) halves of Philox's first two rounds are the same
+            // for every slice of a row: computed once per tile.
+            DrawHalf2 dhalf[kRows];
 #pragma unroll
             for (int m = 0; m < kRows; ++m)
-                dhalf[m] = philox_draw_half(a.draw_first + di,
-                                            a.token0 + tb * kBM + r0 + 2 * kProducerWarps * m, keys);
+                dhalf[m] = philox_draw_half2(philox_draw_half(
+                    a.draw_first + di, a.token0 + tb * kBM + r0 + 2 * kProducerWarps * m, keys));
             for (int kb = 0; kb < nk; ++kb, ++it) {
                 if (!ok) continue;
                 const int s = it % kStages;
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint32_t st = base + s * kStageBytes;
                 const int j = kb * (kBK / 4) + jj;  // global channel block
-                const BlockHalf bhalf = philox_block_half(j, a.layer, keys);
+                const BlockHalf2 bhalf = philox_block_half2(philox_block_half(j, a.layer, keys), keys);
                 if (a.taylor) {
                     // dh = d (c1 + d (c2 + d c3)), d = sigma a per channel (the noise
                     // comes out scaled by sigma); the coefficients' loads of every row
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float4 ev[kRows];
 #pragma unroll
                     for (int m = 0; m < kRows; ++m)
-                        ev[m] = words_to_normals_fast(philox_rest(dhalf[m], bhalf, keys), a.clog);
+                        ev[m] = words_to_normals_fast(philox_rest2(dhalf[m], bhalf, keys), a.clog);
 #pragma unroll
                     for (int m = 0; m < kRows; ++m) {
                         const int r = r0 + 2 * kProducerWarps * m;
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float4 nv[kRows];  // the noise of every row first, as above
 #pragma unroll
                     for (int m = 0; m < kRows; ++m)
-                        nv[m] = words_to_normals_fast(philox_rest(dhalf[m], bhalf, keys));
+                        nv[m] = words_to_normals_fast(philox_rest2(dhalf[m], bhalf, keys));
 #pragma unroll
                     for (int m = 0; m < kRows; ++m) {
                         const int r = r0 + 2 * kProducerWarps * m;
