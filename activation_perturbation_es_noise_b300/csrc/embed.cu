@@ -41,8 +41,11 @@ namespace {
 constexpr int kChunk = 1024;   // tokens per radix-sort chunk (one CTA's threads)
 constexpr int kPiece = 32;     // tokens per partial row sum
 constexpr int kGroup = 8;      // partials added together at the first level
+// (wider slices, 256 and 384 float4 columns, measured slower: more registers, fewer warps)
 constexpr int kSliceF4 = 128;  // float4 columns (512 floats) per row work unit
 constexpr int kSliceF = 128;   // float columns per work unit without float4 rows
+constexpr int kLaneF4 = kSliceF4 / 32;  // float4 columns of a lane
+constexpr int kLaneF = kSliceF / 32;    // float columns of a lane
 constexpr int kRowThreads = 256;
 constexpr int64_t kMaxT = 1LL << 26;
 // The counting pass, for few ids and few tokens (the pages' 4096-token
@@ -700,15 +703,15 @@ template <bool VEC>
 __device__ __forceinline__ void add_rows_in_order(const float* rows, uint32_t n, int64_t d,
                                                   int c0, int w, float* out) {
     if (VEC) {
-        float4 acc[4];
+        float4 acc[kLaneF4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < kLaneF4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         for (uint32_t q = 0; q < n; q += 2) {
-            float4 x[2][4];
+            float4 x[2][kLaneF4];
 #pragma unroll
             for (int j = 0; j < 2; ++j)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < kLaneF4; ++k) {
                     const int c = c0 + 32 * k;
                     x[j][k] = (q + j < n && c < w)
                                   ? __ldcg(reinterpret_cast<const float4*>(rows + (q + j) * d) + c)
@@ -718,24 +721,24 @@ __device__ __forceinline__ void add_rows_in_order(const float* rows, uint32_t n,
             for (int j = 0; j < 2; ++j)
                 if (q + j < n)
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
+                    for (int k = 0; k < kLaneF4; ++k) {
                         acc[k].x += x[j][k].x; acc[k].y += x[j][k].y;
                         acc[k].z += x[j][k].z; acc[k].w += x[j][k].w;
                     }
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kLaneF4; ++k) {
             const int c = c0 + 32 * k;
             if (c < w) reinterpret_cast<float4*>(out)[c] = acc[k];
         }
     } else {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float acc[kLaneF] = {};
         for (uint32_t q = 0; q < n; q += 2) {
-            float x[2][4];
+            float x[2][kLaneF];
 #pragma unroll
             for (int j = 0; j < 2; ++j)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < kLaneF; ++k) {
                     const int c = c0 + 32 * k;
                     x[j][k] = (q + j < n && c < w) ? __ldcg(rows + (q + j) * d + c) : 0.f;
                 }
@@ -743,10 +746,10 @@ __device__ __forceinline__ void add_rows_in_order(const float* rows, uint32_t n,
             for (int j = 0; j < 2; ++j)
                 if (q + j < n)
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) acc[k] += x[j][k];
+                    for (int k = 0; k < kLaneF; ++k) acc[k] += x[j][k];
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kLaneF; ++k) {
             const int c = c0 + 32 * k;
             if (c < w) out[c] = acc[k];
         }
@@ -798,7 +801,7 @@ __global__ void __launch_bounds__(kRowThreads) embed_rows_kernel(const RowArgs a
         if (item >= npieces) {  // an id no token hits: zeros
             const int64_t v = pc.v;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < (VEC ? kLaneF4 : kLaneF); ++k) {
                 const int c = c0 + 32 * k;
                 if (c < w && DUST_IB(v, a.V)) {
                     if (VEC)
@@ -819,15 +822,15 @@ __global__ void __launch_bounds__(kRowThreads) embed_rows_kernel(const RowArgs a
         float* dst = pc.multi ? a.partial + static_cast<int64_t>(item) * a.d
                               : a.G_E + static_cast<int64_t>(pc.v) * a.d;
         if (VEC) {
-            float4 acc[4];
+            float4 acc[kLaneF4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k = 0; k < kLaneF4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
             for (int r = 0; r < pc.len; ++r) {
                 const float4* src = reinterpret_cast<const float4*>(
                     a.g + static_cast<int64_t>(__shfl_sync(0xFFFFFFFFu, myrow, r)) * a.d);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < kLaneF4; ++k) {
                     const int c = c0 + 32 * k;
                     if (c < w) {
                         const float4 x = __ldg(src + c);
@@ -836,24 +839,24 @@ __global__ void __launch_bounds__(kRowThreads) embed_rows_kernel(const RowArgs a
                 }
             }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < kLaneF4; ++k) {
                 const int c = c0 + 32 * k;
                 if (c < w) reinterpret_cast<float4*>(dst)[c] = acc[k];
             }
         } else {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            float acc[kLaneF] = {};
 #pragma unroll 4
             for (int r = 0; r < pc.len; ++r) {
                 const float* src =
                     a.g + static_cast<int64_t>(__shfl_sync(0xFFFFFFFFu, myrow, r)) * a.d;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < kLaneF; ++k) {
                     const int c = c0 + 32 * k;
                     if (c < w) acc[k] += __ldg(src + c);
                 }
             }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < kLaneF; ++k) {
                 const int c = c0 + 32 * k;
                 if (c < w) dst[c] = acc[k];
             }
