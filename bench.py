@@ -180,8 +180,10 @@ def make_workload(name, device, rank):
         }
     if name == "embed_scale":
         wl = W.embed_workload()
+        # g (101 MB) is smaller than L2: the steps rotate over three copies of
+        # the inputs, so a step's inputs were last read two steps (200 MB) ago
         return {"kind": "embed", "name": name, "T": wl["T"], "d": wl["d"], "V": wl["V"], "K": 1,
-                "host": {"g": wl["g"], "ids": wl["ids"]},
+                "host": {"g": wl["g"], "ids": wl["ids"]}, "rotate": 3,
                 "dev": {"g": dev(wl["g"]), "ids": dev(wl["ids"])}}
     raise SystemExit("unknown workload " + name)
 
@@ -244,9 +246,13 @@ def make_step(wl, dust):
         G = torch.empty((V, dd), dtype=torch.float32, device=d["g"].device)
         perm = torch.empty(T, dtype=torch.int32, device=G.device)
         ws = dust._workspace(dust.embed_workspace_bytes(T, dd, V), G.device)
+        sets = [d] + [{k: v.clone() for k, v in d.items()} for _ in range(wl.get("rotate", 1) - 1)]
+        cur = [0]
 
         def step():
-            dust.embed_scatter(d["g"], d["ids"], V, out=(G, perm), ws=ws)
+            s_ = sets[cur[0]]
+            cur[0] = (cur[0] + 1) % len(sets)
+            dust.embed_scatter(s_["g"], s_["ids"], V, out=(G, perm), ws=ws)
         return step, T, 4, ws, G
     raise SystemExit("bad workload")
 
@@ -400,9 +406,75 @@ def oracle_sample(wl, budget_s=12.0):
     return None, ""
 
 
+L2_BYTES = 126 << 20
+FLUSH_BYTES = 256 << 20
+
+
+def input_bytes(wl):
+    return sum(np.asarray(v).nbytes for v in wl["host"].values())
+
+
+def l2_mode(wl):
+    """How a step's inputs are kept out of L2: "large" (the inputs are larger
+    than L2), "rotate" (the steps rotate over copies of the inputs) or "flush"
+    (a 256 MB write before every step, outside the step's events)."""
+    if wl.get("rotate", 1) > 1:
+        return "rotate"
+    return "large" if input_bytes(wl) > L2_BYTES else "flush"
+
+
+def l2_label(wl):
+    mode = l2_mode(wl)
+    if mode == "rotate":
+        n = wl["rotate"]
+        return "%d input sets of %.0f MB rotated (%.0f MB > L2)" % (
+            n, input_bytes(wl) / 1e6, n * input_bytes(wl) / 1e6)
+    if mode == "flush":
+        return "L2 flushed before every step (a 256 MB write outside the step's events)"
+    return "inputs larger than L2 (no flush)"
+
+
+class StepTimer:
+    """Device time of n calls of fn on a stream.  Without a flush, one pair of
+    events brackets all the calls; with one, a 256 MB write precedes every
+    call and a pair of events brackets each call alone (their sum)."""
+
+    def __init__(self, stream, flush):
+        import torch
+        self.stream = stream
+        self.scrub = (torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=stream.device)
+                      if flush else None)
+
+    def flush(self):
+        if self.scrub is not None:
+            self.scrub.fill_(1)
+
+    def time(self, n, fn):
+        import torch
+        ev = lambda: torch.cuda.Event(enable_timing=True)
+        if self.scrub is None:
+            e0, e1 = ev(), ev()
+            e0.record(self.stream)
+            for _ in range(n):
+                fn()
+            e1.record(self.stream)
+            e1.synchronize()
+            return e0.elapsed_time(e1)
+        pairs = []
+        for _ in range(n):
+            self.flush()
+            a, b = ev(), ev()
+            a.record(self.stream)
+            fn()
+            b.record(self.stream)
+            pairs.append((a, b))
+        pairs[-1][1].synchronize()
+        return sum(a.elapsed_time(b) for a, b in pairs)
+
+
 def config_of(wl, n_gpus):
     c = {"workload": wl["name"], "tokens": wl["T"], "draws": wl["K"],
-         "l2": "inputs larger than L2 (no flush)", "parallelism": "dp%d" % n_gpus}
+         "l2": l2_label(wl), "parallelism": "dp%d" % n_gpus}
     if n_gpus > 1:
         c["tokens_per_rank"] = wl["T"]
         c["exchange"] = "G_W summed over ranks (all-reduce) every step"
@@ -449,6 +521,9 @@ def run_optim(args):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(0) as clocks:
+        for _ in range(max(3, args.warmup)):  # clocks back up after the sampler's start
+            step()
+        torch.cuda.synchronize()
         e0.record()
         for _ in range(args.steps):
             step()
@@ -520,6 +595,9 @@ def run_attn_value(args):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(0) as clocks:
+        for _ in range(max(3, args.warmup)):  # clocks back up after the sampler's start
+            step()
+        torch.cuda.synchronize()
         e0.record()
         for _ in range(args.steps):
             step()
@@ -598,6 +676,9 @@ def run_attn_qk(args):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(0) as clocks:
+        for _ in range(max(3, args.warmup)):  # clocks back up after the sampler's start
+            step()
+        torch.cuda.synchronize()
         e0.record()
         for _ in range(args.steps):
             step()
@@ -670,14 +751,8 @@ def run_head_sweep(args):
         for _ in range(max(3, args.warmup)):
             step()
         torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(args.steps):
-            step()
-        e1.record()
-        e1.synchronize()
-        ms = e0.elapsed_time(e1) / args.steps
+        # the inputs are far smaller than L2: flushed before every step
+        ms = StepTimer(torch.cuda.current_stream(), True).time(args.steps, step) / args.steps
         Gk = Gw.double().cpu().numpy()
         cos = float((Gk * G).sum() / np.linalg.norm(Gk) / np.linalg.norm(G))
         print(json.dumps({"metric": METRIC, "value": K * p["T"] / (ms * 1e-3), "unit": UNIT,
@@ -754,17 +829,16 @@ def run_dust(args):
         raise SystemExit("kernel status word set during warm-up")
 
     stream = torch.cuda.current_stream()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
+    timed = StepTimer(stream, l2_mode(wl) == "flush")
     barrier()
     with ClockSampler(local) as clocks:
-        e0.record(stream)
-        for _ in range(args.steps):
+        # the sampler's start leaves the GPU idle for 0.3 s: a few untimed steps
+        # bring the clocks back up before the timed region
+        for _ in range(max(3, args.warmup)):
             step()
-        e1.record(stream)
-        e1.synchronize()
+        barrier()
+        ms = timed.time(args.steps, step)
     barrier()
-    ms = e0.elapsed_time(e1)
     # The dominant kernel's launches, timed in a second pass of the same steps
     # by events the library records around them on their stream (kept out of
     # the timed region above, where they would add host work per launch).
@@ -775,6 +849,7 @@ def run_dust(args):
         # then bracket the kernel alone, not host gaps between small launches.
         torch.cuda._sleep(1_000_000 * max(1, args.steps))
         for _ in range(args.steps):
+            timed.flush()
             step()
     torch.cuda.synchronize()
     kernel_ms = timer.total_ms() / max(args.steps, 1)
@@ -799,19 +874,21 @@ def run_dust(args):
         with torch.cuda.stream(side):
             step()
         stream.wait_stream(side)
-        cg = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(cg):
-            step()
-        cg.replay()
-        torch.cuda.synchronize()
-        g0 = torch.cuda.Event(enable_timing=True)
-        g1 = torch.cuda.Event(enable_timing=True)
-        g0.record(stream)
-        for _ in range(args.steps):
+        # one graph per input set when the steps rotate over copies
+        graphs = []
+        for _ in range(wl.get("rotate", 1)):
+            graphs.append(torch.cuda.CUDAGraph())
+            with torch.cuda.graph(graphs[-1]):
+                step()
+        for cg in graphs:
             cg.replay()
-        g1.record(stream)
-        g1.synchronize()
-        gms = g0.elapsed_time(g1) / args.steps
+        torch.cuda.synchronize()
+        nxt = [0]
+
+        def replay():
+            graphs[nxt[0]].replay()
+            nxt[0] = (nxt[0] + 1) % len(graphs)
+        gms = timed.time(args.steps, replay) / args.steps
         graph = {"ms_per_step": gms, "value": evals * world / (gms * 1e-3), "unit": UNIT}
     value = evals * world * args.steps / (ms_max * 1e-3)
 
