@@ -62,6 +62,35 @@ def test_attn_qk_large_score_shifts(dust, orc, which):
 
 
 @pytest.mark.parametrize("which", [0, 1])
+def test_attn_qk_repeats_bit_for_bit(dust, which):
+    """The same call four times gives the same bits: 4 sequences of 1024,
+    4 heads, K = 16, sigma 0.3 (some warps take the expm1f fallback and some
+    do not, so the epilogue warps drift apart in time), the workspace reused."""
+    nseq, H, L, d_in, K = 4, 4, 1024, 64, 16
+    T, C = nseq * L, H * 64
+    gen = torch.Generator(device="cuda").manual_seed(17 + which)
+    Q, Kk, V = (torch.randn((T, C), generator=gen, device="cuda") for _ in range(3))
+    E = torch.randn((T, C), generator=gen, device="cuda") * 0.1
+    x = torch.randn((T, d_in), generator=gen, device="cuda")
+    q4, k4, v4 = (t.view(nseq, L, H, 64).transpose(1, 2) for t in (Q, Kk, V))
+    s = (q4 @ k4.transpose(-1, -2)) / 8.0
+    s = s.masked_fill(torch.triu(torch.ones(L, L, dtype=torch.bool, device="cuda"), 1),
+                      float("-inf"))
+    P = torch.softmax(s, dim=-1).contiguous()
+    O = (P @ v4).transpose(1, 2).reshape(T, C).contiguous()
+    ws = dust._workspace(dust.lib().dust_attn_qk_workspace(T, L, H, 64, d_in, K), Q.device)
+    outs = []
+    for _ in range(4):
+        g, G, _ = dust.attn_qk_estimate(which, Q, Kk, V, O, P, E, x, L, 0.3, 0.99, K, 99,
+                                        ws=ws)
+        torch.cuda.synchronize()
+        assert dust.workspace_status(ws) == 0
+        outs.append((g.clone(), G.clone()))
+    for g, G in outs[1:]:
+        assert torch.equal(g, outs[0][0]) and torch.equal(G, outs[0][1])
+
+
+@pytest.mark.parametrize("which", [0, 1])
 def test_attn_qk_full_size_first_sequence(dust, orc, which):
     """8 x 2048 tokens, 8 heads of 64, d_in 512 (the bench's shapes) with 4
     draws: sequence 0's rows of g against the oracle run on that sequence
